@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Throughput of the masked post-LN encoder stack forward on GB300.
+
+One step = one forward of the whole stack (every layer: fused QKV, masked
+attention, out-projection + residual + LayerNorm, FFN with exact GELU,
+residual + LayerNorm) over one batch of synthetic inputs already resident in
+HBM.  The default workload is the 4-layer d_model=128 encoder on 4096
+sequences of 64 tokens, fp16 I/O.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 is launched by torch.distributed.run, one rank per GPU; every rank runs
+its own batch (sequences are independent: weak scaling, no collective on the
+data path) and the step time is the max over ranks.  ``--impl reference``
+times the fp64 CPU oracle on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "encoder forward tokens/s on 1 GB300 (masked); % of tensor/HBM roofline"
+DEFAULT_WORKLOAD = "short_d128_L64_B4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def sum_visible_keys(valid_len, L):
+    """sum over sequences and query rows of min(i + 1, valid_len)."""
+    tot = 0
+    for v in np.asarray(valid_len, dtype=np.int64):
+        v = int(v)
+        tot += v * (v + 1) // 2 + (L - v) * v
+    return tot
+
+
+def algorithmic_counts(shape, valid_len):
+    """Flops and minimal HBM bytes of one forward (what the method must do)."""
+    T, d, dff, nl = shape.tokens, shape.d_model, shape.d_ff, shape.n_layers
+    es = 4 if shape.dtype == "f32" else 2
+    keys = sum_visible_keys(valid_len, shape.seq_len)
+    per_layer = {
+        "qkv": 2.0 * T * 3 * d * d,
+        "attention": 4.0 * d * keys,
+        "out": 2.0 * T * d * d,
+        "ffn1": 2.0 * T * d * dff,
+        "ffn2": 2.0 * T * dff * d,
+    }
+    weights = nl * ((4 * d * d + 2 * d * dff) * es + (3 * d + d + 4 * d + dff + d) * es)
+    return {
+        "flops_per_layer": per_layer,
+        "flops": nl * sum(per_layer.values()),
+        "hbm_bytes": 2 * T * d * es + weights + 4 * shape.batch,
+        "visible_keys": keys,
+    }
+
+
+# Kernel class -> (bound, algorithmic work per launch) for the roofline line.
+def kernel_work(cls, shape, counts):
+    pl = counts["flops_per_layer"]
+    T, d = shape.tokens, shape.d_model
+    table = {
+        "simt_gemm_qkv": ("alu", pl["qkv"]), "simt_attention": ("alu", pl["attention"]),
+        "simt_gemm_out": ("alu", pl["out"]), "simt_gemm_ffn1": ("alu", pl["ffn1"]),
+        "simt_gemm_ffn2": ("alu", pl["ffn2"]),
+        "simt_layernorm": ("hbm", 2.0 * T * d * 4),
+        "tc_gemm_qkv": ("tensor", pl["qkv"]), "tc_attention": ("tensor", pl["attention"]),
+        "tc_gemm_out_ln": ("tensor", pl["out"]), "tc_gemm_ffn1": ("tensor", pl["ffn1"]),
+        "tc_gemm_ffn2_ln": ("tensor", pl["ffn2"]),
+        "megakernel": ("tensor", counts["flops"]),
+    }
+    return table.get(cls)
+
+
+def traffic_from_profiles(cls):
+    """DRAM bytes per launch of kernel class `cls` from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    e = t.get(cls)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "transformer_encoder_layer_gb300", "csrc", e["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return e["dram_bytes_per_launch"] if sha == e["source_sha"] else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, shape):
+    """The fp64 CPU oracle as the reference arm: each step is a bounded
+    sample of the same workload (the first `ref_seqs` sequences)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from transformer_encoder_layer_gb300.inputs import make_inputs
+    n = min(args.ref_seqs, shape.batch)
+    inp = make_inputs(shape, seed=0, input_scale=1.0, batch=n)
+    for _ in range(args.warmup):
+        oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, shape.n_heads, check=False)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, shape.n_heads, check=False)
+        times.append(time.perf_counter() - t0)
+    tok = n * shape.seq_len
+    value = tok * len(times) / sum(times)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "sample_sequences": n, "seq_len": shape.seq_len},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {shape.batch} sequences ({tok} tokens) per step, "
+                                   f"numpy fp64 oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(shape, n_seqs):
+    import oracle
+    from transformer_encoder_layer_gb300.inputs import make_inputs
+    n = min(n_seqs, shape.batch)
+    inp = make_inputs(shape, seed=0, input_scale=1.0, batch=n)
+    t0 = time.perf_counter()
+    oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, shape.n_heads, check=False)
+    dt = time.perf_counter() - t0
+    tok = n * shape.seq_len
+    return {"value": tok / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} of {shape.batch} sequences ({tok} tokens), numpy fp64 oracle, "
+                      f"{dt:.1f} s"}
+
+
+def run_ours(args, shape):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from transformer_encoder_layer_gb300 import binding, build
+    from transformer_encoder_layer_gb300.inputs import make_inputs, to_storage
+
+    if rank == 0 or not os.path.exists(binding.LIB_PATH):
+        build.build()
+    if dist:
+        dist.barrier()
+    inp = make_inputs(shape, seed=rank, input_scale=1.0)
+    counts = algorithmic_counts(shape, inp.valid_len)
+    enc = binding.Encoder(inp.layers, shape.d_model, shape.n_heads, shape.d_ff, shape.dtype)
+    if args.path != "auto":
+        enc.set_path(args.path)
+    path = enc.plan(shape.batch, shape.seq_len)
+    xs = to_storage(inp.x, shape.dtype)
+    tdt = binding.torch_dtype(shape.dtype)
+    if shape.dtype == "bf16":
+        x_host = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16)
+    else:
+        x_host = torch.from_numpy(xs)
+    x_host = x_host.contiguous().pin_memory()
+    vl_host = torch.from_numpy(inp.valid_len.astype(np.int32)).pin_memory()
+    x = x_host.to(dev)
+    vl = vl_host.to(dev)
+    out = torch.empty_like(x)
+    wsz = enc.workspace_size(shape.batch, shape.seq_len)
+    work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        enc.forward(x, vl, out=out, workspace=work, stream=stream, check=False)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if enc.get_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    enc.enable_timing(True, capacity=max(4096, 64 * args.steps * shape.n_layers))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the events)
+            starts[i].record(stream)
+            step()
+            stops[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        if dist:
+            dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    per_kernel = enc.read_timing()
+    enc.enable_timing(False)
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if enc.get_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    ms_per_step = total_ms / args.steps
+    value = ws * shape.tokens / (ms_per_step / 1e3)
+    launches = sum(n for _, n in per_kernel.values())
+
+    # End to end: the C-ABI host-buffer call (H2D of x and valid_len, the
+    # forward, D2H of out, stream sync) timed by the host clock.
+    out_host = torch.empty_like(x_host).pin_memory()
+    hws = torch.empty(enc.host_workspace_size(shape.batch, shape.seq_len), dtype=torch.uint8, device=dev)
+    enc.forward_host(x_host, vl_host, out_host, workspace=hws)
+    e2e_t = []
+    for _ in range(max(3, min(args.steps, 10))):
+        t0 = time.perf_counter()
+        enc.forward_host(x_host, vl_host, out_host, workspace=hws)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_t)
+    if not torch.equal(out_host, out.cpu()):
+        raise RuntimeError("host-buffer forward disagrees with the device forward")
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    roof = None
+    if per_kernel:
+        dom = max(per_kernel, key=lambda k: per_kernel[k][0])
+        ms, n = per_kernel[dom]
+        bound, work_per_launch = kernel_work(dom, shape, counts) or ("tensor", counts["flops"])
+        if dom == "megakernel":
+            n_launch_work = work_per_launch
+        else:
+            n_launch_work = work_per_launch
+        avg_s = ms / n / 1e3
+        if bound == "hbm":
+            achieved, peak, unit = n_launch_work / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        elif bound == "alu":
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            achieved, unit = n_launch_work / avg_s / 1e12, "TFLOP/s"
+        else:
+            achieved, peak, unit = (n_launch_work / avg_s / 1e12,
+                                    peaks["bf16_tflops_sustained"], "TFLOP/s")
+        roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic_from_profiles(dom),
+                "peak_source": peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max clock)"
+                                                  if bound == "alu" else ""),
+                "share_of_step": ms / total_ms if total_ms else None,
+                "launches": n, "avg_launch_ms": ms / n}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if path == "simt" else shape.dtype, "data": "synthetic",
+        "config": {"workload": shape.name, "n_layers": shape.n_layers, "d_model": shape.d_model,
+                   "n_heads": shape.n_heads, "d_ff": shape.d_ff, "batch_per_gpu": shape.batch,
+                   "global_batch": ws * shape.batch, "seq_len": shape.seq_len,
+                   "io_dtype": shape.dtype, "valid_len": f"U[{shape.vl_lo},{shape.vl_hi}]",
+                   "input_scale": 1.0, "path": path, "parallelism": f"dp{ws}" if ws > 1 else "single",
+                   "l2": "flushed between timed steps (256 MB write)"},
+        "valid_tokens_per_s": ws * int(inp.valid_len.sum()) / (ms_per_step / 1e3),
+        "algorithmic_tflop_per_s": counts["flops"] / (ms_per_step / 1e3) / 1e12,
+        "roofline": roof,
+        "per_kernel_ms": {k: v[0] / args.steps for k, v in per_kernel.items()},
+        "gpu_launches": launches,
+        "wall_s_timed_region": t_wall,
+        "e2e": {"value": ws * shape.tokens / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size() + vl_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "clocks": clk.summary(),
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, args.cpu_seqs)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "layered", "mega"])
+    ap.add_argument("--cpu-seqs", type=int, default=1024,
+                    help="sequences in the bounded CPU-oracle sample")
+    ap.add_argument("--ref-seqs", type=int, default=64,
+                    help="sequences per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from transformer_encoder_layer_gb300.inputs import SHAPES
+    shape = SHAPES[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape)
+    else:
+        run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+/*
+ * tl_encoder.h -- C ABI of the GB300 (sm_103a) masked post-LN encoder stack.
+ *
+ * What it computes.  The forward pass of a stack of transformer encoder
+ * layers, as the three source pages describe the task ("Hyper-optimized
+ * megakernel-hybrid transformer inference", "KernelForge", "Implement a GPU
+ * Kernel for a Transformer Layer").  For every layer, in order:
+ *
+ *   qkv = x W_qkv^T + b_qkv                    fused QKV projection
+ *   ctx = MHA(q, k, v)                         causal + key-padding mask
+ *   y   = LayerNorm1(x + ctx W_o^T + b_o)      post-LN, eps 1e-5
+ *   x'  = LayerNorm2(y + gelu(y W_1^T + b_1) W_2^T + b_2)   exact-erf GELU
+ *
+ * with no dropout.  Attention uses the scale 1/sqrt(dh); key j is visible to
+ * query row i of sequence b iff j <= i and j < valid_len[b]; padded query rows
+ * (i >= valid_len[b]) are computed by the same rule and returned.  The single
+ * entry point that handles every shape follows the megakernel page's section
+ * "Appendix" (one callable for all cases) and KernelForge's "What it does"
+ * (a frozen per-shape plan chosen at run time with no autotuning).
+ *
+ * Numbers.  Inputs, weights and outputs use one I/O dtype (fp32, fp16 or
+ * bf16).  The residual stream, LayerNorm, softmax and every accumulator are
+ * fp32; 16-bit tensor-core operands that are activations are carried as a
+ * (hi, lo) pair so that products keep about fp32 accuracy.  Results meet the
+ * pages' per-element gate |err| <= 0.002 OR |err| <= 0.02 |ref| against an
+ * fp64 evaluation of the same function.
+ *
+ * Conventions for every call.
+ *  - Device pointers are plain CUDA device addresses of the current device;
+ *    "stream" is a cudaStream_t passed as void* (NULL = the legacy stream).
+ *  - Synchronous argument checks return a status before anything is launched.
+ *    Errors that depend on device data (a valid_len outside [1, L], a device
+ *    wait that timed out) are recorded in a per-handle device status word and
+ *    reported by tl_encoder_get_status().
+ *  - No call is thread-safe on one handle; distinct handles are independent.
+ */
+#ifndef TL_ENCODER_H
+#define TL_ENCODER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TL_F32 = 0, TL_F16 = 1, TL_BF16 = 2 } tl_dtype;
+
+typedef enum {
+  TL_OK = 0,
+  TL_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, misaligned buffer   */
+  TL_ERR_UNSUPPORTED_SHAPE = 2,  /* d_model % n_heads != 0, head_dim too large, path n/a  */
+  TL_ERR_CUDA = 3,               /* a CUDA runtime call failed                           */
+  TL_ERR_OUT_OF_MEMORY = 4,      /* create could not allocate the packed weights         */
+  TL_ERR_WORKSPACE_TOO_SMALL = 5,
+  TL_ERR_BAD_VALID_LEN = 6,      /* some valid_len[b] was outside [1, L]; it was clamped */
+  TL_ERR_DEVICE_TIMEOUT = 7      /* a bounded device-side wait gave up                   */
+} tl_status;
+
+/* Execution paths.  TL_PATH_AUTO picks by shape (the frozen dispatch table).
+ * The others force one path, for cross-checks; a forced path that cannot run
+ * the shape makes forward return TL_ERR_UNSUPPORTED_SHAPE.
+ *   SIMT      generic fp32 CUDA-core kernels, every shape (head_dim <= 128)
+ *   LAYERED   tcgen05/TMEM GEMMs fed by TMA with fused epilogues, plus the
+ *             flash-attention kernel; one launch per step per layer
+ *   MEGA      sequence-resident megakernel: every layer of a 128-row tile of
+ *             whole sequences in one CTA, activations kept on chip          */
+typedef enum {
+  TL_PATH_AUTO = 0,
+  TL_PATH_SIMT = 1,
+  TL_PATH_LAYERED = 2,
+  TL_PATH_MEGA = 3
+} tl_path;
+
+typedef struct tl_encoder tl_encoder; /* opaque handle */
+
+/* One layer's parameters, every array in the handle's dtype, PyTorch's
+ * [out, in] row-major weight layout:
+ *   w_qkv [3d, d], b_qkv [3d]  rows 0..d-1 are Q, d..2d-1 K, 2d..3d-1 V; within
+ *                              each block head h owns rows h*dh .. (h+1)*dh-1
+ *   w_o [d, d], b_o [d]; ln1_g, ln1_b [d]
+ *   w_1 [d_ff, d], b_1 [d_ff]; w_2 [d, d_ff], b_2 [d]; ln2_g, ln2_b [d]      */
+typedef struct {
+  const void *w_qkv, *b_qkv;
+  const void *w_o, *b_o;
+  const void *ln1_g, *ln1_b;
+  const void *w_1, *b_1;
+  const void *w_2, *b_2;
+  const void *ln2_g, *ln2_b;
+} tl_layer_weights;
+
+/* Create a handle.  weights points to n_layers structs; their arrays may be
+ * host or device memory (detected per pointer) and are copied and packed into
+ * library-owned device memory, so the caller may free them on return.
+ * Requires n_layers >= 1, d_model >= 16 and a multiple of 16, d_model %
+ * n_heads == 0, head_dim = d_model / n_heads in [1, 128], d_ff >= 16 and a
+ * multiple of 16.  Allocates (cudaMalloc) and synchronises the device once.
+ * On error *out is set to NULL. */
+tl_status tl_encoder_create(const tl_layer_weights *weights, int n_layers, int d_model,
+                            int n_heads, int d_ff, tl_dtype dtype, tl_encoder **out);
+
+/* Force an execution path (default TL_PATH_AUTO).  Host-only, no device work. */
+tl_status tl_encoder_set_path(tl_encoder *h, tl_path path);
+
+/* The path forward() would run for a batch of B sequences of length L. */
+tl_status tl_encoder_plan(const tl_encoder *h, int B, int L, tl_path *path);
+
+/* Bytes of scratch device memory forward() needs for B sequences of length
+ * L on the path it would choose.  0 is possible (then workspace may be NULL). */
+tl_status tl_encoder_workspace_size(const tl_encoder *h, int B, int L, size_t *bytes);
+
+/* The forward pass.  x [B, L, d_model] and out [B, L, d_model] are device
+ * arrays in the handle's dtype, row-major, batch first, 16-byte aligned, and
+ * must not overlap.  valid_len is a device int32 [B], each in [1, L]
+ * (right padding: tokens valid_len[b] .. L-1 of sequence b are padding).
+ * workspace is caller-owned device scratch of at least
+ * tl_encoder_workspace_size() bytes, 256-byte aligned.  The call only
+ * enqueues work on stream: it neither allocates nor synchronises. */
+tl_status tl_encoder_forward(tl_encoder *h, const void *x, int B, int L,
+                             const int32_t *valid_len, void *out, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace tl_encoder_forward_host() needs: the forward's
+ * own scratch plus device copies of x, valid_len and out. */
+tl_status tl_encoder_host_workspace_size(const tl_encoder *h, int B, int L, size_t *bytes);
+
+/* The forward pass on HOST buffers: copies x [B, L, d] and valid_len [B] from
+ * host memory to the workspace, runs tl_encoder_forward on stream, copies the
+ * result to out (host), and synchronises stream before returning.  Pinned
+ * host memory makes the copies asynchronous DMA; pageable memory also works. */
+tl_status tl_encoder_forward_host(tl_encoder *h, const void *x_host, int B, int L,
+                                  const int32_t *valid_len_host, void *out_host,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise stream, then read and clear the handle's device status word:
+ * TL_OK, TL_ERR_BAD_VALID_LEN or TL_ERR_DEVICE_TIMEOUT (the first error seen
+ * since the last call). */
+tl_status tl_encoder_get_status(tl_encoder *h, void *stream);
+
+/* Free the packed weights and the handle (synchronises the device).  NULL is
+ * accepted. */
+tl_status tl_encoder_destroy(tl_encoder *h);
+
+/* Per-kernel timing.  While enabled, forward() records a CUDA event pair
+ * around each of its kernel launches on the launch stream (capacity pairs at
+ * most; later launches are not timed).  tl_encoder_read_timing() synchronises
+ * the device, then returns for kernel class k (0 <= k < TL_KERNEL_CLASSES)
+ * the summed device time in ms and the number of timed launches, and
+ * tl_encoder_reset_timing() forgets everything recorded so far.  Enabling
+ * creates events (host allocation); disabling destroys them. */
+#define TL_KERNEL_CLASSES 16
+tl_status tl_encoder_enable_timing(tl_encoder *h, int enable, int capacity);
+tl_status tl_encoder_read_timing(tl_encoder *h, int k, float *total_ms, int *launches);
+tl_status tl_encoder_reset_timing(tl_encoder *h);
+/* Name of kernel class k ("" past the last class). */
+const char *tl_kernel_class_name(int k);
+
+/* Static description of a status code. */
+const char *tl_status_string(tl_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_ENCODER_H */

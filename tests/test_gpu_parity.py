@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every comparison is element by element under the pages' gate
+(|err| <= 0.002 OR |err| <= 0.02 |ref|, NaN/Inf fail), on seeded inputs, over
+seeds and the input-scale sweep 1e-3 .. 1e3.  Sizes the oracle finishes in
+seconds are checked in full; full-size workloads are checked on sampled
+sequences (sequences are independent) or, for the 100k-token workload, on a
+causal prefix (rows < P depend only on tokens < P when P <= valid_len).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from transformer_encoder_layer_gb300.gate import gate
+from transformer_encoder_layer_gb300.inputs import (
+    INPUT_SCALES, SHAPES, make_inputs, tiny_shape, to_storage, from_storage)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transformer_encoder_layer_gb300 import binding, build
+    build.build()
+    binding.load()
+
+
+def _paths_for(shape):
+    from transformer_encoder_layer_gb300 import binding
+    enc = binding.Encoder(make_inputs(shape.with_(batch=1, seq_len=1, vl_lo=1, vl_hi=1)).layers,
+                          shape.d_model, shape.n_heads, shape.d_ff, shape.dtype)
+    out = []
+    for p in ("simt", "layered", "mega"):
+        enc.set_path(p)
+        try:
+            enc.plan(shape.batch, shape.seq_len)
+            out.append(p)
+        except binding.TLError:
+            pass
+    enc.close()
+    return out
+
+
+def _run(inp, path="auto"):
+    from transformer_encoder_layer_gb300 import binding
+    return binding.run_forward(inp, path=path)
+
+
+def _check(inp, path="auto", rows=None):
+    got = _run(inp, path)
+    ref = oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, inp.shape.n_heads)
+    if rows is not None:
+        got, ref = got[:, rows], ref[:, rows]
+    ok, util, idx = gate(got, ref)
+    assert ok, f"{inp.shape.name} scale={inp.input_scale} seed={inp.seed} path={path}: " \
+               f"envelope {util:.3f} at {idx}: gpu={got[idx]} ref={ref[idx]}"
+    return util
+
+
+# ----------------------------------------------------------- small, in full
+@pytest.mark.parametrize("scale", INPUT_SCALES)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_d32_full(seed, scale):
+    s = SHAPES["tiny_d32_L32"]
+    for p in _paths_for(s):
+        _check(make_inputs(s, seed=seed, input_scale=scale), p)
+
+
+@pytest.mark.parametrize("scale", INPUT_SCALES)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_batch1_d256_full(seed, scale):
+    s = SHAPES["batch1_d256_L512"]
+    for p in _paths_for(s):
+        _check(make_inputs(s, seed=seed, input_scale=scale), p)
+
+
+@pytest.mark.parametrize("scale", INPUT_SCALES)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_short_d128_subsample(seed, scale):
+    s = SHAPES["short_d128_L64_B4096"]
+    for p in _paths_for(s.with_(batch=32)):
+        _check(make_inputs(s, seed=seed, input_scale=scale, batch=32), p)
+
+
+@pytest.mark.parametrize("scale", INPUT_SCALES)
+def test_wide_d1024_subsample(scale):
+    s = SHAPES["wide_d1024_L1024_B32"]
+    for p in _paths_for(s.with_(batch=2)):
+        _check(make_inputs(s, seed=0, input_scale=scale, batch=2), p)
+
+
+@pytest.mark.parametrize("scale", INPUT_SCALES)
+def test_long_d64_reduced_length(scale):
+    # Same layer as the 100k-token workload, 3000 tokens (ragged tail) so the
+    # whole output is checked, valid_len spanning the same 90-100% range.
+    s = SHAPES["long_d64_L100k_B8"].with_(batch=2, seq_len=3000, vl_lo=2700, vl_hi=3000)
+    for p in _paths_for(s):
+        _check(make_inputs(s, seed=0, input_scale=scale), p)
+
+
+# ----------------------------------------------------- full size, sampled
+def _sampled_sequences(shape_name, n_sample, scale=1.0, seed=0):
+    s = SHAPES[shape_name]
+    inp = make_inputs(s, seed=seed, input_scale=scale)
+    got = _run(inp)
+    idx = np.sort(np.random.default_rng(123).choice(s.batch, size=n_sample, replace=False))
+    ref = oracle.encoder_forward(inp.x[idx], inp.valid_len[idx], inp.layers, s.n_heads)
+    ok, util, where = gate(got[idx], ref)
+    assert ok, f"{shape_name}: envelope {util:.3f} at {where}"
+    # Row 0 of every sequence has a closed form (it sees only itself).
+    r0 = oracle.first_row_closed_form(inp.x[:, 0], inp.layers)
+    ok0, util0, where0 = gate(got[:, 0], r0)
+    assert ok0, f"{shape_name} row 0: envelope {util0:.3f} at {where0}"
+    return max(util, util0)
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_short_d128_full_size_sampled(scale):
+    _sampled_sequences("short_d128_L64_B4096", 48, scale=scale)
+
+
+def test_wide_d1024_full_size_sampled():
+    _sampled_sequences("wide_d1024_L1024_B32", 2)
+
+
+def test_long_d64_full_size_prefix_and_first_row():
+    s = SHAPES["long_d64_L100k_B8"]
+    inp = make_inputs(s, seed=0)
+    got = _run(inp)
+    P = 2048  # every valid_len >= 90000 > P, so rows < P see only tokens < P
+    ref = oracle.encoder_forward(inp.x[:, :P], inp.valid_len * 0 + P, inp.layers, s.n_heads)
+    ok, util, where = gate(got[:, :P], ref)
+    assert ok, f"prefix: envelope {util:.3f} at {where}"
+    r0 = oracle.first_row_closed_form(inp.x[:, 0], inp.layers)
+    ok0, util0, where0 = gate(got[:, 0], r0)
+    assert ok0
+    assert np.all(np.isfinite(got))
+
+
+# ------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("L,vl_lo,vl_hi", [(1, 1, 1), (37, 1, 37), (129, 1, 3), (130, 129, 130)])
+def test_edge_lengths(dtype, L, vl_lo, vl_hi):
+    s = tiny_shape(dtype=dtype, batch=3, seq_len=L, vl_lo=vl_lo, vl_hi=vl_hi,
+                   d_model=64, n_heads=4, d_ff=256)
+    for p in _paths_for(s):
+        _check(make_inputs(s, seed=5, input_scale=1.0), p)
+
+
+@pytest.mark.parametrize("dh", [16, 32, 64, 128])
+def test_head_dims(dh):
+    s = tiny_shape(dtype="f16", batch=2, seq_len=70, vl_lo=5, vl_hi=70,
+                   d_model=dh * 2, n_heads=2, d_ff=4 * dh * 2)
+    for p in _paths_for(s):
+        _check(make_inputs(s, seed=6, input_scale=1.0), p)
+
+
+# ------------------------------------------------------- GPU invariances
+def test_causal_and_padding_invariance_bitwise():
+    s = SHAPES["short_d128_L64_B4096"].with_(batch=8)
+    inp = make_inputs(s, seed=1)
+    base = _run(inp)
+    x2 = inp.x.copy()
+    t = 20
+    x2[:, t + 1:] = -x2[:, t + 1:]
+    inp2 = make_inputs(s, seed=1)
+    inp2.x = x2
+    out = _run(inp2)
+    assert np.array_equal(out[:, :t + 1], base[:, :t + 1])
+    # A padded position p changes only row p.
+    b = 0
+    vl = int(inp.valid_len[b])
+    if vl < s.seq_len:
+        x3 = inp.x.copy()
+        x3[b, s.seq_len - 1] = -x3[b, s.seq_len - 1]
+        inp3 = make_inputs(s, seed=1)
+        inp3.x = x3
+        out3 = _run(inp3)
+        changed = np.any(out3 != base, axis=-1)
+        assert changed[b, s.seq_len - 1] and changed.sum() == 1
+
+
+def test_bad_valid_len_is_reported_and_clamped():
+    from transformer_encoder_layer_gb300 import binding
+    s = tiny_shape(dtype="f16", batch=2, seq_len=16, vl_lo=16, vl_hi=16, d_model=32)
+    inp = make_inputs(s, seed=0)
+    enc = binding.Encoder(inp.layers, 32, 2, 128, "f16")
+    x = torch.from_numpy(to_storage(inp.x, "f16")).cuda()
+    vl = torch.tensor([0, 17], dtype=torch.int32, device="cuda")
+    out = enc.forward(x, vl, check=False)
+    assert enc.get_status() == 6  # TL_ERR_BAD_VALID_LEN
+    assert enc.get_status() == 0  # cleared by the read
+    # Clamped to [1, L]: equal to running with valid_len = [1, 16].
+    ref = enc.forward(x, torch.tensor([1, 16], dtype=torch.int32, device="cuda"))
+    assert torch.equal(out, ref)
+    enc.close()
+
+
+def test_forward_host_matches_device_forward():
+    from transformer_encoder_layer_gb300 import binding
+    s = SHAPES["short_d128_L64_B4096"].with_(batch=16)
+    inp = make_inputs(s, seed=2)
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    xh = torch.from_numpy(to_storage(inp.x, "f16")).pin_memory()
+    vh = torch.from_numpy(inp.valid_len.astype(np.int32)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    enc.forward_host(xh, vh, oh)
+    od = enc.forward(xh.cuda(), vh.cuda()).cpu()
+    assert torch.equal(oh, od)
+    enc.close()

@@ -1,0 +1,298 @@
+// The C ABI (include/tl_encoder.h): handle creation and weight packing,
+// workspace sizing, shape dispatch and the per-layer launch sequence.
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "paths.h"
+
+using namespace tl;
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+float host_half_to_float(uint16_t h) {
+  uint32_t sign = (uint32_t)(h >> 15) << 31, exp = (h >> 10) & 0x1f, man = h & 0x3ff;
+  uint32_t bits;
+  if (exp == 0) {
+    if (man == 0) {
+      bits = sign;
+    } else {  // subnormal: renormalise
+      int e = -1;
+      do { ++e; man <<= 1; } while ((man & 0x400) == 0);
+      bits = sign | (uint32_t)(127 - 15 - e) << 23 | (man & 0x3ff) << 13;
+    }
+  } else if (exp == 31) {
+    bits = sign | 0x7f800000u | man << 13;
+  } else {
+    bits = sign | (exp - 15 + 127) << 23 | man << 13;
+  }
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return f;
+}
+
+float host_to_float(const void* p, size_t i, tl_dtype t) {
+  if (t == TL_F32) return reinterpret_cast<const float*>(p)[i];
+  uint16_t u = reinterpret_cast<const uint16_t*>(p)[i];
+  if (t == TL_F16) return host_half_to_float(u);
+  uint32_t bits = (uint32_t)u << 16;
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return f;
+}
+
+// Byte offsets of one layer's parameters inside the packed buffer.
+struct LayerOffsets {
+  size_t w_qkv, w_o, w_1, w_2, b_qkv, b_o, ln1_g, ln1_b, b_1, b_2, ln2_g, ln2_b, end;
+};
+
+LayerOffsets layer_offsets(size_t start, int d, int dff, size_t es) {
+  LayerOffsets o;
+  size_t p = start;
+  auto take = [&](size_t bytes) { size_t at = p; p = align_up(p + bytes, 256); return at; };
+  o.w_qkv = take((size_t)3 * d * d * es);
+  o.w_o = take((size_t)d * d * es);
+  o.w_1 = take((size_t)dff * d * es);
+  o.w_2 = take((size_t)d * dff * es);
+  o.b_qkv = take((size_t)3 * d * 4);
+  o.b_o = take((size_t)d * 4);
+  o.ln1_g = take((size_t)d * 4);
+  o.ln1_b = take((size_t)d * 4);
+  o.b_1 = take((size_t)dff * 4);
+  o.b_2 = take((size_t)d * 4);
+  o.ln2_g = take((size_t)d * 4);
+  o.ln2_b = take((size_t)d * 4);
+  o.end = p;
+  return o;
+}
+
+// Copy n elements of a caller array (host or device) to host memory.
+bool fetch(const void* src, size_t bytes, std::vector<unsigned char>& dst) {
+  dst.resize(bytes);
+  return cudaMemcpy(dst.data(), src, bytes, cudaMemcpyDefault) == cudaSuccess;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tl_status_string(tl_status s) {
+  switch (s) {
+    case TL_OK: return "ok";
+    case TL_ERR_INVALID_ARG: return "invalid argument";
+    case TL_ERR_UNSUPPORTED_SHAPE: return "unsupported shape for this path";
+    case TL_ERR_CUDA: return "CUDA runtime error";
+    case TL_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case TL_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case TL_ERR_BAD_VALID_LEN: return "valid_len outside [1, L] (clamped)";
+    case TL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d_model,
+                            int n_heads, int d_ff, tl_dtype dtype, tl_encoder** out) {
+  if (!out) return TL_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!weights || n_layers < 1 || d_model < 16 || n_heads < 1 || d_ff < 16)
+    return TL_ERR_INVALID_ARG;
+  if (dtype != TL_F32 && dtype != TL_F16 && dtype != TL_BF16) return TL_ERR_INVALID_ARG;
+  if (d_model % 16 || d_ff % 16 || d_model % n_heads || d_model > 1024 || d_ff > 16384)
+    return TL_ERR_UNSUPPORTED_SHAPE;
+  const int dh = d_model / n_heads;
+  if (dh > 128) return TL_ERR_UNSUPPORTED_SHAPE;
+  for (int l = 0; l < n_layers; ++l) {
+    const tl_layer_weights& w = weights[l];
+    const void* ps[] = {w.w_qkv, w.b_qkv, w.w_o, w.b_o, w.ln1_g, w.ln1_b,
+                        w.w_1, w.b_1, w.w_2, w.b_2, w.ln2_g, w.ln2_b};
+    for (const void* p : ps)
+      if (!p) return TL_ERR_INVALID_ARG;
+  }
+
+  tl_encoder* h = new (std::nothrow) tl_encoder();
+  if (!h) return TL_ERR_OUT_OF_MEMORY;
+  h->n_layers = n_layers; h->d = d_model; h->H = n_heads; h->dh = dh; h->dff = d_ff;
+  h->dtype = dtype;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return TL_ERR_CUDA;
+  }
+  const size_t es = dtype_size(dtype);
+  std::vector<LayerOffsets> offs;
+  size_t total = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    offs.push_back(layer_offsets(total, d_model, d_ff, es));
+    total = offs.back().end;
+  }
+  size_t extra = packed_extra_bytes(h);
+  size_t extra_off = total;
+  total += extra;
+  std::vector<unsigned char> stage(total, 0), tmp;
+  const int d = d_model;
+  for (int l = 0; l < n_layers; ++l) {
+    const tl_layer_weights& w = weights[l];
+    const LayerOffsets& o = offs[l];
+    struct { const void* src; size_t off; size_t n; } mats[] = {
+        {w.w_qkv, o.w_qkv, (size_t)3 * d * d}, {w.w_o, o.w_o, (size_t)d * d},
+        {w.w_1, o.w_1, (size_t)d_ff * d}, {w.w_2, o.w_2, (size_t)d * d_ff}};
+    for (auto& m : mats) {
+      if (!fetch(m.src, m.n * es, tmp)) { delete h; return TL_ERR_INVALID_ARG; }
+      std::memcpy(stage.data() + m.off, tmp.data(), m.n * es);
+    }
+    struct { const void* src; size_t off; size_t n; } vecs[] = {
+        {w.b_qkv, o.b_qkv, (size_t)3 * d}, {w.b_o, o.b_o, (size_t)d},
+        {w.ln1_g, o.ln1_g, (size_t)d}, {w.ln1_b, o.ln1_b, (size_t)d},
+        {w.b_1, o.b_1, (size_t)d_ff}, {w.b_2, o.b_2, (size_t)d},
+        {w.ln2_g, o.ln2_g, (size_t)d}, {w.ln2_b, o.ln2_b, (size_t)d}};
+    for (auto& v : vecs) {
+      if (!fetch(v.src, v.n * es, tmp)) { delete h; return TL_ERR_INVALID_ARG; }
+      float* dst = reinterpret_cast<float*>(stage.data() + v.off);
+      for (size_t i = 0; i < v.n; ++i) dst[i] = host_to_float(tmp.data(), i, dtype);
+    }
+  }
+  if (cudaMalloc(&h->wbuf, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return TL_ERR_OUT_OF_MEMORY;
+  }
+  if (cudaMalloc((void**)&h->status, 256) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->wbuf);
+    delete h;
+    return TL_ERR_OUT_OF_MEMORY;
+  }
+  h->wbuf_bytes = total;
+  h->layers = new (std::nothrow) tl_layer_dev[n_layers];
+  unsigned char* base = reinterpret_cast<unsigned char*>(h->wbuf);
+  for (int l = 0; l < n_layers && h->layers; ++l) {
+    const LayerOffsets& o = offs[l];
+    tl_layer_dev& L = h->layers[l];
+    L.w_qkv = base + o.w_qkv; L.w_o = base + o.w_o; L.w_1 = base + o.w_1; L.w_2 = base + o.w_2;
+    L.b_qkv = (const float*)(base + o.b_qkv); L.b_o = (const float*)(base + o.b_o);
+    L.ln1_g = (const float*)(base + o.ln1_g); L.ln1_b = (const float*)(base + o.ln1_b);
+    L.b_1 = (const float*)(base + o.b_1); L.b_2 = (const float*)(base + o.b_2);
+    L.ln2_g = (const float*)(base + o.ln2_g); L.ln2_b = (const float*)(base + o.ln2_b);
+  }
+  bool ok = h->layers != nullptr &&
+            cudaMemcpy(h->wbuf, stage.data(), total - extra, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemset(h->status, 0, 256) == cudaSuccess &&
+            pack_extra(h, base + extra_off, extra) == cudaSuccess &&
+            cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    tl_encoder_destroy(h);
+    return TL_ERR_CUDA;
+  }
+  *out = h;
+  return TL_OK;
+}
+
+tl_status tl_encoder_set_path(tl_encoder* h, tl_path path) {
+  if (!h || path < TL_PATH_AUTO || path > TL_PATH_MEGA) return TL_ERR_INVALID_ARG;
+  h->path = path;
+  return TL_OK;
+}
+
+tl_status tl_encoder_plan(const tl_encoder* h, int B, int L, tl_path* path) {
+  if (!h || !path || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  *path = p;
+  return TL_OK;
+}
+
+tl_status tl_encoder_workspace_size(const tl_encoder* h, int B, int L, size_t* bytes) {
+  if (!h || !bytes || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  *bytes = path_workspace_bytes(h, p, B, L);
+  return TL_OK;
+}
+
+tl_status tl_encoder_forward(tl_encoder* h, const void* x, int B, int L, const int32_t* valid_len,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !x || !out || !valid_len || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(valid_len, 4)) return TL_ERR_INVALID_ARG;
+  const size_t io_bytes = (size_t)B * L * h->d * dtype_size(h->dtype);
+  const char* xb = (const char*)x; const char* ob = (const char*)out;
+  if (xb < ob + io_bytes && ob < xb + io_bytes) return TL_ERR_INVALID_ARG;  // overlap
+  tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  size_t need = path_workspace_bytes(h, p, B, L);
+  if (workspace_bytes < need) return TL_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && (!workspace || !aligned(workspace, 256))) return TL_ERR_INVALID_ARG;
+  cudaError_t e = run_path(h, p, x, B, L, valid_len, out, workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
+tl_status tl_encoder_host_workspace_size(const tl_encoder* h, int B, int L, size_t* bytes) {
+  size_t fw = 0;
+  tl_status s = tl_encoder_workspace_size(h, B, L, &fw);
+  if (s != TL_OK) return s;
+  const size_t io = align_up((size_t)B * L * h->d * dtype_size(h->dtype), 256);
+  *bytes = 2 * io + align_up((size_t)B * 4, 256) + fw;
+  return TL_OK;
+}
+
+tl_status tl_encoder_forward_host(tl_encoder* h, const void* x_host, int B, int L,
+                                  const int32_t* valid_len_host, void* out_host, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!h || !x_host || !valid_len_host || !out_host || !workspace || B < 1 || L < 1)
+    return TL_ERR_INVALID_ARG;
+  size_t need = 0;
+  tl_status s = tl_encoder_host_workspace_size(h, B, L, &need);
+  if (s != TL_OK) return s;
+  if (workspace_bytes < need) return TL_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return TL_ERR_INVALID_ARG;
+  const size_t raw = (size_t)B * L * h->d * dtype_size(h->dtype);
+  const size_t io = align_up(raw, 256);
+  char* w = (char*)workspace;
+  void* xd = w;
+  void* od = w + io;
+  int32_t* vld = (int32_t*)(w + 2 * io);
+  char* fw = w + 2 * io + align_up((size_t)B * 4, 256);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(xd, x_host, raw, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(vld, valid_len_host, (size_t)B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return TL_ERR_CUDA;
+  s = tl_encoder_forward(h, xd, B, L, vld, od, fw, workspace_bytes - (fw - w), stream);
+  if (s != TL_OK) return s;
+  if (cudaMemcpyAsync(out_host, od, raw, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return TL_ERR_CUDA;
+  return TL_OK;
+}
+
+tl_status tl_encoder_get_status(tl_encoder* h, void* stream) {
+  if (!h) return TL_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TL_ERR_CUDA;
+  if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess)
+    return TL_ERR_CUDA;
+  return (tl_status)v;
+}
+
+tl_status tl_encoder_destroy(tl_encoder* h) {
+  if (!h) return TL_OK;
+  cudaDeviceSynchronize();
+  timing_destroy(h);
+  if (h->wbuf) cudaFree(h->wbuf);
+  if (h->status) cudaFree(h->status);
+  delete[] h->layers;
+  delete h;
+  return TL_OK;
+}
+
+}  // extern "C"

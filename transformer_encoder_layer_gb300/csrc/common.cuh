@@ -1,0 +1,65 @@
+// Shared device/host helpers of the encoder library: dtype conversion,
+// the device status word, and small warp reductions.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tl_encoder.h"
+
+namespace tl {
+
+// ---------------------------------------------------------------- dtypes
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+inline size_t dtype_size(tl_dtype t) { return t == TL_F32 ? 4 : 2; }
+
+// ------------------------------------------------------- device status
+// One int per handle.  Kernels record the first error with atomicCAS from 0;
+// the host reads and clears it in tl_encoder_get_status().
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// valid_len clamped to [1, L]; an out-of-range value is recorded.
+__device__ __forceinline__ int load_valid_len(const int32_t* vl, int b, int L, int* status) {
+  int v = vl[b];
+  if (v < 1 || v > L) {
+    set_status(status, TL_ERR_BAD_VALID_LEN);
+    v = v < 1 ? 1 : L;
+  }
+  return v;
+}
+
+// ------------------------------------------------------ warp reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Exact GELU on fp32: 0.5 u (1 + erf(u / sqrt 2)), with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float u) {
+  return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+}
+
+}  // namespace tl

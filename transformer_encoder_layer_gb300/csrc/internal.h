@@ -1,0 +1,94 @@
+// Internal (C++) interface between the C ABI and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tl_encoder.h"
+#include "neartie.cuh"
+
+// Device pointers of one layer's packed parameters.  Weights stay in the I/O
+// dtype ([out, in] row-major, exactly the caller's values); biases and
+// LayerNorm parameters are also kept as fp32 copies for the epilogues.
+struct tl_layer_dev {
+  const void* w_qkv;  // [3d, d]  dtype
+  const void* w_o;    // [d, d]
+  const void* w_1;    // [d_ff, d]
+  const void* w_2;    // [d, d_ff]
+  const float* b_qkv; // [3d]     fp32
+  const float* b_o;   // [d]
+  const float* ln1_g; const float* ln1_b;
+  const float* b_1;   // [d_ff]
+  const float* b_2;   // [d]
+  const float* ln2_g; const float* ln2_b;
+};
+
+// Kernel classes for per-kernel timing (names in timing.cu).
+enum tl_kernel_class {
+  KC_SIMT_GEMM_QKV = 0, KC_SIMT_ATTENTION, KC_SIMT_GEMM_OUT, KC_SIMT_LAYERNORM,
+  KC_SIMT_GEMM_FFN1, KC_SIMT_GEMM_FFN2, KC_TC_GEMM_QKV, KC_TC_ATTENTION,
+  KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX,
+  KC_COUNT
+};
+
+struct tl_timing;  // event pool, defined in timing.cu
+
+struct tl_encoder {
+  int n_layers = 0, d = 0, H = 0, dh = 0, dff = 0;
+  tl_dtype dtype = TL_F32;
+  tl_path path = TL_PATH_AUTO;
+  int device = 0;
+  int num_sms = 0;
+  void* wbuf = nullptr;      // one allocation holding every packed parameter
+  size_t wbuf_bytes = 0;
+  int* status = nullptr;     // device status word
+  tl_layer_dev* layers = nullptr;  // host array of n_layers
+  tl_timing* timing = nullptr;     // non-null while per-kernel timing is on
+};
+
+namespace tl {
+// Records an event pair around one launch when timing is enabled.
+struct KernelTimer {
+  KernelTimer(tl_encoder* h, int kernel_class, cudaStream_t s);
+  ~KernelTimer();
+  tl_encoder* h; int k; cudaStream_t s; int slot;
+};
+void timing_destroy(tl_encoder* h);
+}  // namespace tl
+
+namespace tl {
+
+// ---- generic fp32 CUDA-core (SIMT) kernels -------------------------------
+enum SimtEpi { EPI_QKV_HEADMAJOR = 0, EPI_BIAS_GELU = 1, EPI_BIAS_RESID = 2 };
+
+// C[M, N] = A[M, K] . W[N, K]^T with a fused epilogue.
+//  a_dtype: TL_F32 for fp32 activations, else the I/O dtype of x.
+//  EPI_QKV_HEADMAJOR: out is fp32 q|k|v, each [B, H, L, dh] (N = 3d).
+//  EPI_BIAS_GELU:     out fp32 [M, N] = gelu(acc + bias).
+//  EPI_BIAS_RESID:    out fp32 [M, N] = acc + bias + resid (resid in r_dtype).
+struct SimtGemmArgs {
+  const void* A; tl_dtype a_dtype;
+  const void* W; tl_dtype w_dtype;
+  const float* bias;
+  const void* resid; tl_dtype r_dtype;
+  float* out;
+  int M, N, K;
+  int B, L, H, dh;  // for the head-major epilogue
+  int epi;
+};
+cudaError_t simt_gemm(const SimtGemmArgs& a, cudaStream_t s);
+
+// Causal + key-padding attention, fp32.  q, k, v [B, H, L, dh] fp32 ->
+// ctx [B, L, H*dh] fp32.  dh <= 128.  Near-tie rows are queued on `ties`.
+cudaError_t simt_attention(const float* q, const float* k, const float* v, const int32_t* vl,
+                           float* ctx, int B, int H, int L, int dh, int* status,
+                           NearTieList ties, cudaStream_t s);
+
+// Row LayerNorm over d (<= 1024): y = (r - mean)/sqrt(var + 1e-5) g + b,
+// two-pass in fp32.  Writes y32 (fp32, may be null) and/or yout (I/O dtype,
+// may be null).
+cudaError_t simt_layernorm(const float* r, const float* g, const float* b, float* y32,
+                           void* yout, tl_dtype out_dtype, int M, int d, cudaStream_t s);
+
+}  // namespace tl
