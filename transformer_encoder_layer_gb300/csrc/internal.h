@@ -79,11 +79,17 @@ struct SimtGemmArgs {
 };
 cudaError_t simt_gemm(const SimtGemmArgs& a, cudaStream_t s);
 
-// Causal + key-padding attention, fp32.  q, k, v [B, H, L, dh] fp32 ->
-// ctx [B, L, H*dh] fp32.  dh <= 128.  Near-tie rows are queued on `ties`.
-cudaError_t simt_attention(const float* q, const float* k, const float* v, const int32_t* vl,
-                           float* ctx, int B, int H, int L, int dh, int* status,
-                           NearTieList ties, cudaStream_t s);
+// Causal + key-padding attention on CUDA cores, fp32 arithmetic.
+// mode 0: fp32 q, k, v [B, H, L, dh] and fp32 ctx [B, L, H*dh];
+// mode 1/2: fp16/bf16 (hi, lo) planes, v given transposed [B, H, dh, Lp],
+// ctx written as (hi, lo) planes.  dh <= 128.  Near-tie rows are queued.
+struct AttnIO {
+  const void *q_hi, *q_lo, *k_hi, *k_lo, *v_hi, *v_lo;
+  int v_transposed, Lp;
+  void *ctx_hi, *ctx_lo;
+};
+cudaError_t simt_attention(const AttnIO& io, int mode, const int32_t* vl, int B, int H, int L,
+                           int dh, int* status, NearTieList ties, cudaStream_t s);
 
 // Row LayerNorm over d (<= 1024): y = (r - mean)/sqrt(var + 1e-5) g + b,
 // two-pass in fp32.  Writes y32 (fp32, may be null) and/or yout (I/O dtype,

@@ -2,6 +2,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "paths.h"
+#include "tc_gemm.h"
 
 namespace tl {
 namespace {
@@ -52,8 +53,9 @@ cudaError_t run_simt(tl_encoder* h, const void* x, int B, int L, const int32_t* 
     NearTieList ties{w.ties, w.ties + 1, M * h->H};
     if ((e = cudaMemsetAsync(w.ties, 0, sizeof(int), s)) != cudaSuccess) break;
     { KernelTimer t(h, KC_SIMT_ATTENTION, s);
-      e = simt_attention(w.qkv, w.qkv + plane, w.qkv + 2 * plane, vl, w.ctx, B, h->H, L, h->dh,
-                         h->status, ties, s); }
+      AttnIO io{w.qkv, nullptr, w.qkv + plane, nullptr, w.qkv + 2 * plane, nullptr, 0, L,
+                w.ctx, nullptr};
+      e = simt_attention(io, 0, vl, B, h->H, L, h->dh, h->status, ties, s); }
     if (e != cudaSuccess) break;
     {
       FixupArgs fa{};
@@ -94,6 +96,153 @@ cudaError_t run_simt(tl_encoder* h, const void* x, int B, int L, const int32_t* 
   return e;
 }
 
+// ---------------------------------------------------------------- LAYERED
+// tcgen05 GEMMs with fused epilogues; activations between steps are (hi, lo)
+// 16-bit planes so every GEMM operand keeps about fp32 accuracy.
+bool layered_supported(const tl_encoder* h) {
+  if (h->dtype == TL_F32) return false;
+  const int d = h->d, dh = h->dh;
+  // K of every GEMM a multiple of the 64-wide TMA box; N tiles of 32 columns.
+  if (d % 64 || h->dff % 64) return false;
+  if (!(dh % 32 == 0 || 32 % dh == 0)) return false;
+  return true;
+}
+
+// Largest N tile (a multiple of 32, at most 256) that divides n.
+int pick_bn(int n) {
+  for (int bn = 256; bn >= 32; bn -= 32)
+    if (n % bn == 0) return bn;
+  return 0;
+}
+
+struct LayeredWs {
+  void *xh, *xl, *qh, *ql, *kh, *kl, *vth, *vtl, *ch, *cl, *yh, *yl, *hh, *hl;
+  float *x32, *y32, *rs;
+  int* ties;
+  int Lp;
+  size_t bytes;
+};
+
+LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
+  const size_t T = (size_t)B * L, d = h->d;
+  const int Lp = (L + 7) / 8 * 8;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align256(off + bytes); return at; };
+  char* b = (char*)base;
+  LayeredWs w;
+  w.Lp = Lp;
+  const size_t e = 2;
+  size_t o[17];
+  o[0] = take(T * d * e); o[1] = take(T * d * e);                          // x hi/lo
+  o[2] = take(T * d * e); o[3] = take(T * d * e);                          // q
+  o[4] = take(T * d * e); o[5] = take(T * d * e);                          // k
+  o[6] = take((size_t)B * d * Lp * e); o[7] = take((size_t)B * d * Lp * e);  // v^T
+  o[8] = take(T * d * e); o[9] = take(T * d * e);                          // ctx
+  o[10] = take(T * d * e); o[11] = take(T * d * e);                        // y
+  o[12] = take(T * h->dff * e); o[13] = take(T * h->dff * e);              // ffn hidden
+  o[14] = take(T * d * 4); o[15] = take(T * d * 4);                        // x32, y32
+  o[16] = take(d > 256 ? T * d * 4 : 4);                                   // LN scratch
+  size_t ot = take((1 + T * h->H) * 4);
+  void** p[14] = {&w.xh, &w.xl, &w.qh, &w.ql, &w.kh, &w.kl, &w.vth, &w.vtl, &w.ch, &w.cl,
+                  &w.yh, &w.yl, &w.hh, &w.hl};
+  for (int i = 0; i < 14; ++i) *p[i] = b + o[i];
+  w.x32 = (float*)(b + o[14]); w.y32 = (float*)(b + o[15]); w.rs = (float*)(b + o[16]);
+  w.ties = (int*)(b + ot);
+  w.bytes = off;
+  return w;
+}
+
+cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_t* vl, void* out,
+                        void* ws, cudaStream_t s) {
+  LayeredWs w = layered_layout(h, B, L, ws);
+  const int M = B * L, d = h->d, dff = h->dff, H = h->H, dh = h->dh;
+  const bool bf = h->dtype == TL_BF16;
+  const int pk = bf ? 4 : 3;  // (hi, lo) plane kind for the fix-up
+  cudaError_t e = cudaSuccess;
+  CUtensorMap ma0, ma1, mw;
+  auto amaps = [&](const void* p0, const void* p1, int rows, int K) {
+    bool ok = make_tmap_2d(&ma0, p0, bf, rows, K, K, 64, 128, 128);
+    ok = ok && make_tmap_2d(&ma1, p1 ? p1 : p0, bf, rows, K, K, 64, 128, 128);
+    return ok;
+  };
+  for (int l = 0; l < h->n_layers; ++l) {
+    const tl_layer_dev& P = h->layers[l];
+    const bool first = l == 0, last = l == h->n_layers - 1;
+    // a1: fused QKV projection, head-major (hi, lo) epilogue.
+    {
+      TcGemmArgs g{};
+      g.M = M; g.N = 3 * d; g.K = d; g.BN = pick_bn(3 * d); g.n_parts = first ? 1 : 2;
+      g.bias = P.b_qkv;
+      g.q_hi = w.qh; g.q_lo = w.ql; g.k_hi = w.kh; g.k_lo = w.kl; g.vt_hi = w.vth; g.vt_lo = w.vtl;
+      g.B = B; g.L = L; g.H = H; g.dh = dh; g.Lp = w.Lp; g.status = h->status;
+      if (!amaps(first ? x : w.xh, first ? nullptr : w.xl, M, d) ||
+          !make_tmap_2d(&mw, P.w_qkv, bf, 3 * d, d, d, 64, g.BN, 128))
+        return cudaErrorInvalidValue;
+      KernelTimer t(h, KC_TC_GEMM_QKV, s);
+      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_QKV, h->num_sms, s)) != cudaSuccess) return e;
+    }
+    // a2: masked attention (ctx as (hi, lo) planes), then the near-tie fix-up.
+    NearTieList ties{w.ties, w.ties + 1, M * H};
+    if ((e = cudaMemsetAsync(w.ties, 0, sizeof(int), s)) != cudaSuccess) return e;
+    {
+      AttnIO io{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, 1, w.Lp, w.ch, w.cl};
+      KernelTimer t(h, KC_TC_ATTENTION, s);
+      if ((e = simt_attention(io, bf ? 2 : 1, vl, B, H, L, dh, h->status, ties, s)) != cudaSuccess) return e;
+    }
+    {
+      FixupArgs fa{};
+      fa.ties = ties;
+      fa.x = first ? Plane{x, nullptr, bf ? 2 : 1} : Plane{w.xh, w.xl, pk};
+      fa.w_qkv = P.w_qkv; fa.w_kind = (int)h->dtype; fa.b_qkv = P.b_qkv;
+      fa.q = Plane{w.qh, w.ql, pk}; fa.k = Plane{w.kh, w.kl, pk}; fa.v = Plane{w.vth, w.vtl, pk};
+      fa.v_transposed = 1; fa.Lp = w.Lp;
+      fa.ctx_hi = w.ch; fa.ctx_lo = w.cl; fa.ctx_kind = pk; fa.valid_len = vl;
+      fa.B = B; fa.H = H; fa.L = L; fa.dh = dh; fa.d = d;
+      KernelTimer t(h, KC_AUX, s);
+      if ((e = neartie_fixup(fa, s)) != cudaSuccess) return e;
+    }
+    // a3: out-projection + bias + residual + LayerNorm 1.
+    {
+      TcGemmArgs g{};
+      g.M = M; g.N = d; g.K = d; g.BN = pick_bn(d); g.n_parts = 2; g.bias = P.b_o;
+      g.resid = first ? x : (const void*)w.x32; g.resid_kind = first ? 1 : 0;
+      g.gamma = P.ln1_g; g.beta = P.ln1_b; g.o32 = w.y32; g.o_hi = w.yh; g.o_lo = w.yl;
+      g.rscratch = w.rs; g.status = h->status;
+      if (!amaps(w.ch, w.cl, M, d) || !make_tmap_2d(&mw, P.w_o, bf, d, d, d, 64, g.BN, 128))
+        return cudaErrorInvalidValue;
+      KernelTimer t(h, KC_TC_GEMM_OUT_LN, s);
+      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+    }
+    // a4: FFN1 + bias + exact GELU.
+    {
+      TcGemmArgs g{};
+      g.M = M; g.N = dff; g.K = d; g.BN = pick_bn(dff); g.n_parts = 2; g.bias = P.b_1;
+      g.o_hi = w.hh; g.o_lo = w.hl; g.status = h->status;
+      if (!amaps(w.yh, w.yl, M, d) || !make_tmap_2d(&mw, P.w_1, bf, dff, d, d, 64, g.BN, 128))
+        return cudaErrorInvalidValue;
+      KernelTimer t(h, KC_TC_GEMM_FFN1, s);
+      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_GELU, h->num_sms, s)) != cudaSuccess) return e;
+    }
+    // a5: FFN2 + bias + residual + LayerNorm 2.
+    {
+      TcGemmArgs g{};
+      g.M = M; g.N = d; g.K = dff; g.BN = pick_bn(d); g.n_parts = 2; g.bias = P.b_2;
+      g.resid = w.y32; g.resid_kind = 0; g.gamma = P.ln2_g; g.beta = P.ln2_b;
+      if (last) {
+        g.o_final = out;
+      } else {
+        g.o32 = w.x32; g.o_hi = w.xh; g.o_lo = w.xl;
+      }
+      g.rscratch = w.rs; g.status = h->status;
+      if (!amaps(w.hh, w.hl, M, dff) || !make_tmap_2d(&mw, P.w_2, bf, d, dff, dff, 64, g.BN, 128))
+        return cudaErrorInvalidValue;
+      KernelTimer t(h, KC_TC_GEMM_FFN2_LN, s);
+      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+    }
+  }
+  return e;
+}
+
 }  // namespace
 
 size_t packed_extra_bytes(const tl_encoder*) { return 0; }
@@ -103,8 +252,14 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
   (void)B; (void)L;
   switch (h->path) {
     case TL_PATH_SIMT:
-    case TL_PATH_AUTO:
       return TL_PATH_SIMT;
+    case TL_PATH_LAYERED:
+      return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_AUTO;
+    case TL_PATH_AUTO:
+      // The frozen plan table: 16-bit I/O runs on the tensor cores; fp32
+      // I/O keeps fp32 weights, which the 16-bit MMAs cannot hold exactly,
+      // and runs on the CUDA cores.
+      return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_SIMT;
     default:
       return TL_PATH_AUTO;  // not built for this shape
   }
@@ -112,12 +267,14 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
 
 size_t path_workspace_bytes(const tl_encoder* h, tl_path p, int B, int L) {
   if (p == TL_PATH_SIMT) return simt_layout(h, B, L, nullptr).bytes;
+  if (p == TL_PATH_LAYERED) return layered_layout(h, B, L, nullptr).bytes;
   return 0;
 }
 
 cudaError_t run_path(tl_encoder* h, tl_path p, const void* x, int B, int L, const int32_t* vl,
                      void* out, void* ws, cudaStream_t s) {
   if (p == TL_PATH_SIMT) return run_simt(h, x, B, L, vl, out, ws, s);
+  if (p == TL_PATH_LAYERED) return run_layered(h, x, B, L, vl, out, ws, s);
   return cudaErrorInvalidValue;
 }
 

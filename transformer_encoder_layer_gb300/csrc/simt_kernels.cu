@@ -109,25 +109,50 @@ cudaError_t gemm_w(const SimtGemmArgs& a, cudaStream_t s) {
 // within that error could move the softmax (see neartie.cuh).
 constexpr int AQ = 128;
 
+// Where the attention reads Q/K/V and writes the context:
+//  MODE 0  fp32 q, k, v [B, H, L, dh]; fp32 ctx [T, d]
+//  MODE 1/2  fp16/bf16 (hi, lo) planes, q, k [B, H, L, dh], v^T [B, H, dh, Lp];
+//            ctx as (hi, lo) planes [T, d]
+template <int MODE> struct AttnAcc;
+template <> struct AttnAcc<0> {
+  __device__ static float ld(const void* hi, const void*, size_t i) {
+    return reinterpret_cast<const float*>(hi)[i];
+  }
+  __device__ static void st(void* hi, void*, size_t i, float v) { reinterpret_cast<float*>(hi)[i] = v; }
+};
+template <typename T> struct AttnAccPair {
+  __device__ static float ld(const void* hi, const void* lo, size_t i) {
+    return to_f32<T>(reinterpret_cast<const T*>(hi)[i]) + to_f32<T>(reinterpret_cast<const T*>(lo)[i]);
+  }
+  __device__ static void st(void* hi, void* lo, size_t i, float v) {
+    T h = from_f32<T>(v);
+    reinterpret_cast<T*>(hi)[i] = h;
+    reinterpret_cast<T*>(lo)[i] = from_f32<T>(v - to_f32<T>(h));
+  }
+};
+template <> struct AttnAcc<1> : AttnAccPair<__half> {};
+template <> struct AttnAcc<2> : AttnAccPair<__nv_bfloat16> {};
+
 // Key-tile size shrinks as head_dim grows to bound registers.
-template <int DH, int AK = (DH <= 32 ? 32 : DH == 64 ? 16 : 8)>
-__global__ void __launch_bounds__(AQ) simt_attention_kernel(
-    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
-    const int32_t* __restrict__ vlp, float* __restrict__ ctx, int B, int H, int L, int dh,
-    int* status, NearTieList ties) {
+template <int DH, int MODE, int AK = (DH <= 32 ? 32 : DH == 64 ? 16 : 8)>
+__global__ void __launch_bounds__(AQ) simt_attention_kernel(AttnIO io, const int32_t* __restrict__ vlp,
+                                                            int B, int H, int L, int dh, int* status,
+                                                            NearTieList ties) {
+  using Acc = AttnAcc<MODE>;
   __shared__ float Ks[AK][DH];
   __shared__ float Vs[AK][DH];
   __shared__ float Kn[AK];
   const int b = blockIdx.z, h = blockIdx.y;
   const int i0 = blockIdx.x * AQ, i = i0 + threadIdx.x;
   const int vl = load_valid_len(vlp, b, L, threadIdx.x == 0 && blockIdx.x == 0 && h == 0 ? status : nullptr);
-  const size_t base = ((size_t)b * H + h) * L * dh;
+  const size_t bh = (size_t)b * H + h;
+  const size_t base = bh * L * dh;
   const float scale_log2 = rsqrtf((float)dh) * 1.4426950408889634f;
   float qr[DH], acc[DH];
   float qn2 = 0.f;
 #pragma unroll
   for (int c = 0; c < DH; ++c) {
-    float qv = (i < L && c < dh) ? q[base + (size_t)i * dh + c] : 0.f;
+    float qv = (i < L && c < dh) ? Acc::ld(io.q_hi, io.q_lo, base + (size_t)i * dh + c) : 0.f;
     qn2 = fmaf(qv, qv, qn2);
     qr[c] = qv * scale_log2;
     acc[c] = 0.f;
@@ -139,8 +164,9 @@ __global__ void __launch_bounds__(AQ) simt_attention_kernel(
     for (int e = threadIdx.x; e < AK * DH; e += AQ) {
       int jj = e / DH, c = e % DH, j = j0 + jj;
       bool ok = j < block_keys && c < dh;
-      Ks[jj][c] = ok ? k[base + (size_t)j * dh + c] : 0.f;
-      Vs[jj][c] = ok ? v[base + (size_t)j * dh + c] : 0.f;
+      Ks[jj][c] = ok ? Acc::ld(io.k_hi, io.k_lo, base + (size_t)j * dh + c) : 0.f;
+      size_t vi = io.v_transposed ? (bh * dh + c) * io.Lp + j : base + (size_t)j * dh + c;
+      Vs[jj][c] = ok ? Acc::ld(io.v_hi, io.v_lo, vi) : 0.f;
     }
     __syncthreads();
     if (threadIdx.x < AK) {
@@ -182,13 +208,13 @@ __global__ void __launch_bounds__(AQ) simt_attention_kernel(
   }
   if (i < L) {
     float inv = 1.f / l;
-    float* dst = ctx + ((size_t)b * L + i) * H * dh + (size_t)h * dh;
+    const size_t o = ((size_t)b * L + i) * H * dh + (size_t)h * dh;
 #pragma unroll
     for (int c = 0; c < DH; ++c)
-      if (c < dh) dst[c] = acc[c] * inv;
+      if (c < dh) Acc::st(io.ctx_hi, io.ctx_lo, o + c, acc[c] * inv);
     // scores are in log2 units here; the test takes natural-log gaps
     if (neartie_flag((m - m2) * 0.69314718055994531f, sqrtf(qn2), kmax, dh))
-      neartie_push(ties, ((b * H + h) * L) + i);
+      neartie_push(ties, (int)(bh * L) + i);
   }
 }
 
@@ -242,15 +268,22 @@ cudaError_t simt_gemm(const SimtGemmArgs& a, cudaStream_t s) {
   }
 }
 
-cudaError_t simt_attention(const float* q, const float* k, const float* v, const int32_t* vl,
-                           float* ctx, int B, int H, int L, int dh, int* status,
-                           NearTieList ties, cudaStream_t s) {
+template <int MODE>
+static cudaError_t attn_mode(const AttnIO& io, const int32_t* vl, int B, int H, int L, int dh,
+                             int* status, NearTieList ties, cudaStream_t s) {
   dim3 grid((L + AQ - 1) / AQ, H, B);
-  if (dh <= 16) simt_attention_kernel<16><<<grid, AQ, 0, s>>>(q, k, v, vl, ctx, B, H, L, dh, status, ties);
-  else if (dh <= 32) simt_attention_kernel<32><<<grid, AQ, 0, s>>>(q, k, v, vl, ctx, B, H, L, dh, status, ties);
-  else if (dh <= 64) simt_attention_kernel<64><<<grid, AQ, 0, s>>>(q, k, v, vl, ctx, B, H, L, dh, status, ties);
-  else simt_attention_kernel<128><<<grid, AQ, 0, s>>>(q, k, v, vl, ctx, B, H, L, dh, status, ties);
+  if (dh <= 16) simt_attention_kernel<16, MODE><<<grid, AQ, 0, s>>>(io, vl, B, H, L, dh, status, ties);
+  else if (dh <= 32) simt_attention_kernel<32, MODE><<<grid, AQ, 0, s>>>(io, vl, B, H, L, dh, status, ties);
+  else if (dh <= 64) simt_attention_kernel<64, MODE><<<grid, AQ, 0, s>>>(io, vl, B, H, L, dh, status, ties);
+  else simt_attention_kernel<128, MODE><<<grid, AQ, 0, s>>>(io, vl, B, H, L, dh, status, ties);
   return cudaGetLastError();
+}
+
+cudaError_t simt_attention(const AttnIO& io, int mode, const int32_t* vl, int B, int H, int L,
+                           int dh, int* status, NearTieList ties, cudaStream_t s) {
+  if (mode == 0) return attn_mode<0>(io, vl, B, H, L, dh, status, ties, s);
+  if (mode == 1) return attn_mode<1>(io, vl, B, H, L, dh, status, ties, s);
+  return attn_mode<2>(io, vl, B, H, L, dh, status, ties, s);
 }
 
 cudaError_t simt_layernorm(const float* r, const float* g, const float* b, float* y32,

@@ -73,6 +73,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait that ignores the abort flag: used when draining work already
+// in flight (TMA loads, issued MMAs) before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      set_status(status, TL_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map,
                                             uint64_t* bar, int x, int y) {

@@ -1,0 +1,482 @@
+// tcgen05 GEMM with fused epilogues: C[M, N] = A[M, K] . W[N, K]^T.
+//
+// A is an activation carried as one or two 16-bit planes (hi, lo: the value
+// is hi + lo, about fp32 accuracy); W is a weight in the same 16-bit type,
+// exact.  Both are K-major.  Per 128 x BN output tile the MMA issues, per
+// 64-wide K block, 4 x n_parts tcgen05.mma (K = 16 each) into an fp32 TMEM
+// accumulator; the product hi.W + lo.W is accumulated in the same TMEM
+// columns.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer: A planes and the W tile of each K block into a
+//              `stages`-deep shared-memory ring (128-byte swizzle)
+//   warp 1     TMEM allocation; one elected thread issues the MMAs
+//   warps 2-5  epilogue: thread = output row (TMEM lane), 32 columns at a
+//              time with tcgen05.ld; two TMEM accumulators let the epilogue
+//              of one tile overlap the main loop of the next
+// Epilogues (the pages' fused steps: "KernelForge", section "What we
+// built" -- fused QKV projection, fused add + LayerNorm; the megakernel
+// page, section "Hybrid" -- QKV GEMM with the head-major transpose fused):
+//   QKV   + bias, scattered head-major: Q and K as [B, H, L, dh] and V as
+//         V^T [B, H, dh, Lp], each as (hi, lo) planes
+//   GELU  + bias, exact-erf GELU, (hi, lo) planes [M, N]
+//   LN    + bias + residual, LayerNorm over the full row (the CTA owns all
+//         N columns of its rows; per-32-column (mean, M2) merged with Chan's
+//         formula), written as fp32 and/or (hi, lo) planes, or as the final
+//         output in the I/O dtype.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+#include "tc_gemm.h"
+
+namespace tl {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128, kBK = 64;
+constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+
+struct Smem {
+  // carved from dynamic shared memory: [stages x stage bytes] then barriers
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* acc_full;   // [2]
+  uint64_t* acc_empty;  // [2]
+  uint64_t* mma_done;   // [1]
+  uint32_t* tmem_base;
+  int* abort;
+};
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T* hi, T* lo, size_t i, float v) {
+  T h, l;
+  Split<T>::go(v, h, l);
+  hi[i] = h;
+  lo[i] = l;
+}
+
+// 32 consecutive values of one row as (hi, lo) 16-bit planes, 16-byte stores.
+template <typename T>
+__device__ __forceinline__ void store_row32_pair(T* hi, T* lo, size_t at, const float (&v)[32]) {
+  uint4 hv[4], lv[4];
+  T* hp = reinterpret_cast<T*>(hv);
+  T* lp = reinterpret_cast<T*>(lv);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) Split<T>::go(v[j], hp[j], lp[j]);
+  uint4* hd = reinterpret_cast<uint4*>(hi + at);
+  uint4* ld = reinterpret_cast<uint4*>(lo + at);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    hd[j] = hv[j];
+    ld[j] = lv[j];
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, size_t at, const float (&v)[32]) {
+  uint4 hv[4];
+  T* hp = reinterpret_cast<T*>(hv);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) hp[j] = from_f32<T>(v[j]);
+  uint4* hd = reinterpret_cast<uint4*>(dst + at);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) hd[j] = hv[j];
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <typename T, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                   const __grid_constant__ CUtensorMap map_w, const TcGemmArgs args) {
+  extern __shared__ __align__(1024) unsigned char dyn_smem[];
+  const TcGemmArgs& a = args;
+  // 1024-byte align the operand ring (the 128-byte swizzle atom).
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const int BN = a.BN;
+  const int stage_bytes = a.n_parts * kATileBytes + BN * kBK * 2;
+  unsigned char* bar_base = base + (size_t)a.stages * stage_bytes;
+  Smem sm;
+  sm.full = reinterpret_cast<uint64_t*>(bar_base);
+  sm.empty = sm.full + a.stages;
+  sm.acc_full = sm.empty + a.stages;
+  sm.acc_empty = sm.acc_full + 2;
+  sm.mma_done = sm.acc_empty + 2;
+  sm.tmem_base = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
+  sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
+
+  T* const q_hi = reinterpret_cast<T*>(a.q_hi);
+  T* const q_lo = reinterpret_cast<T*>(a.q_lo);
+  T* const k_hi = reinterpret_cast<T*>(a.k_hi);
+  T* const k_lo = reinterpret_cast<T*>(a.k_lo);
+  T* const vt_hi = reinterpret_cast<T*>(a.vt_hi);
+  T* const vt_lo = reinterpret_cast<T*>(a.vt_lo);
+  T* const o_hi = reinterpret_cast<T*>(a.o_hi);
+  T* const o_lo = reinterpret_cast<T*>(a.o_lo);
+  T* const o_final = reinterpret_cast<T*>(a.o_final);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const bool ln_rows = (EPI == TC_EPI_LN);
+  // Work units: LN -> one 128-row block with all its N tiles; else one tile.
+  const int n_units = ln_rows ? a.m_blocks : a.m_blocks * a.n_tiles;
+  const int tiles_per_unit = ln_rows ? a.n_tiles : 1;
+  const int k_blocks = (a.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.acc_full[s], 1);
+      mbar_init(&sm.acc_empty[s], 128);
+    }
+    mbar_init(sm.mma_done, 1);
+    *sm.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a0);
+    if (a.n_parts > 1) tma_prefetch_desc(&map_a1);
+    tma_prefetch_desc(&map_w);
+  }
+  if (warp == 1) tmem_alloc(sm.tmem_base, a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_base;
+  volatile int* abort = sm.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      const uint32_t tx = (uint32_t)stage_bytes;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int t = 0; t < tiles_per_unit && ok; ++t) {
+          const int m_blk = ln_rows ? u : u / a.n_tiles;
+          const int n_tile = ln_rows ? t : u % a.n_tiles;
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort, a.status)) { ok = false; break; }
+            unsigned char* st = base + (size_t)stage * stage_bytes;
+            mbar_arrive_expect_tx(&sm.full[stage], tx);
+            tma_load_2d(st, &map_a0, &sm.full[stage], kb * kBK, m_blk * kBM);
+            if (a.n_parts > 1) tma_load_2d(st + kATileBytes, &map_a1, &sm.full[stage], kb * kBK, m_blk * kBM);
+            tma_load_2d(st + a.n_parts * kATileBytes, &map_w, &sm.full[stage], kb * kBK, n_tile * BN);
+            ++issued;
+            if (++stage == a.stages) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+      // Every load issued must have landed before the CTA exits: wait (with
+      // a bound, ignoring the abort flag) on the last `stages` full phases.
+      for (long long r = 1; r <= issued && r <= a.stages; ++r) {
+        const long long idx = issued - r;
+        mbar_wait_bounded(&sm.full[idx % a.stages], (uint32_t)((idx / a.stages) & 1), a.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int t = 0; t < tiles_per_unit && ok; ++t) {
+        if (!mbar_wait(&sm.acc_empty[acc], acc_phase ^ 1, abort, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, abort, a.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            unsigned char* st = base + (size_t)stage * stage_bytes;
+            const uint32_t w_addr = smem_u32(st + a.n_parts * kATileBytes);
+            for (int p = 0; p < a.n_parts; ++p) {
+              const uint32_t a_addr = smem_u32(st + p * kATileBytes);
+#pragma unroll
+              for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                mma_f16(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
+                        a.idesc, (kb | p | k16) != 0);
+              }
+            }
+            mma_commit(&sm.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == a.stages) { stage = 0; phase ^= 1; }
+        }
+        if (lane == 0) mma_commit(&sm.acc_full[acc]);
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+    // All issued MMAs complete before TMEM is released.
+    if (lane == 0) mma_commit(sm.mma_done);
+    __syncwarp();
+    mbar_wait_bounded(sm.mma_done, 0, a.status);
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int qd = warp & 3;
+    const int row_in_tile = qd * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int n_chunks = BN / 32;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int m_blk = ln_rows ? u : u / a.n_tiles;
+      const int row = m_blk * kBM + row_in_tile;
+      const bool row_ok = row < a.M;
+      // LayerNorm running statistics over the row (Chan's parallel merge).
+      float ln_n = 0.f, ln_mean = 0.f, ln_m2 = 0.f;
+      for (int t = 0; t < tiles_per_unit; ++t) {
+        const int n_tile = ln_rows ? t : u % a.n_tiles;
+        if (!mbar_wait(&sm.acc_full[acc], acc_phase, abort, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tbase = tmem + lane_addr + (uint32_t)(acc * BN);
+        for (int c = 0; c < n_chunks; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int n0 = n_tile * BN + c * 32;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += __ldg(a.bias + n0 + j);
+          if (EPI == TC_EPI_QKV) {
+            if (row_ok) {
+              const int d = a.H * a.dh;
+              const int b = row / a.L, i = row % a.L;
+              // a 32-column chunk covers whole heads (dh = 16) or part of one
+              for (int j0 = 0; j0 < 32; j0 += (a.dh < 32 ? a.dh : 32)) {
+                const int n = n0 + j0;
+                const int which = n / d, h = (n % d) / a.dh, c0 = n % a.dh;
+                const int w = a.dh < 32 ? a.dh : 32;
+                const size_t bh = (size_t)b * a.H + h;
+                if (which < 2) {
+                  T* hi = which == 0 ? q_hi : k_hi;
+                  T* lo = which == 0 ? q_lo : k_lo;
+                  const size_t at = (bh * a.L + i) * a.dh + c0;
+                  if (w == 32) {
+                    store_row32_pair(hi, lo, at, v);
+                  } else {
+                    for (int j = 0; j < w; ++j) store_pair(hi, lo, at + j, v[j0 + j]);
+                  }
+                } else {
+                  for (int j = 0; j < w; ++j)
+                    store_pair(vt_hi, vt_lo, (bh * a.dh + c0 + j) * a.Lp + i, v[j0 + j]);
+                }
+              }
+            }
+          } else if (EPI == TC_EPI_GELU) {
+            if (row_ok) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+              store_row32_pair(o_hi, o_lo, (size_t)row * a.N + n0, v);
+            }
+          } else {  // LN pass 1: r = acc + bias + residual, chunk stats
+            if (row_ok) {
+              const size_t at = (size_t)row * a.N + n0;
+              if (a.resid_kind == 0) {
+                const float4* r4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.resid) + at);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float4 r = r4[j];
+                  v[4 * j] += r.x; v[4 * j + 1] += r.y; v[4 * j + 2] += r.z; v[4 * j + 3] += r.w;
+                }
+              } else {
+                const uint4* r4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.resid) + at);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 r = r4[j];
+                  const T* rt = reinterpret_cast<const T*>(&r);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[8 * j + e] += to_f32<T>(rt[e]);
+                }
+              }
+            }
+            float cm = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cm += v[j];
+            cm *= (1.f / 32.f);
+            float c2 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) c2 = fmaf(v[j] - cm, v[j] - cm, c2);
+            const float nn = ln_n + 32.f, delta = cm - ln_mean;
+            ln_mean += delta * (32.f / nn);
+            ln_m2 += c2 + delta * delta * (ln_n * 32.f / nn);
+            ln_n = nn;
+            if (a.n_tiles == 1) {
+              tmem_st32(tbase + c * 32, v);  // keep r on chip
+            } else if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(a.rscratch + (size_t)row * a.N + n0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          }
+        }
+        if (EPI == TC_EPI_LN && t == tiles_per_unit - 1) {
+          // LN pass 2: normalise and write.
+          const float mean = ln_mean;
+          const float rstd = rsqrtf(ln_m2 / ln_n + 1e-5f);
+          for (int tt = 0; tt < a.n_tiles; ++tt) {
+            for (int c = 0; c < n_chunks; ++c) {
+              float v[32];
+              const int n0 = tt * BN + c * 32;
+              if (a.n_tiles == 1) {
+                tmem_ld32(tbase + c * 32, v);
+              } else if (row_ok) {
+                const float4* src = reinterpret_cast<const float4*>(a.rscratch + (size_t)row * a.N + n0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float4 r = src[j];
+                  v[4 * j] = r.x; v[4 * j + 1] = r.y; v[4 * j + 2] = r.z; v[4 * j + 3] = r.w;
+                }
+              }
+              if (!row_ok) continue;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = (v[j] - mean) * rstd * __ldg(a.gamma + n0 + j) + __ldg(a.beta + n0 + j);
+              const size_t at = (size_t)row * a.N + n0;
+              if (a.o32) {
+                float4* dst = reinterpret_cast<float4*>(a.o32 + at);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              }
+              if (o_hi) store_row32_pair(o_hi, o_lo, at, v);
+              if (o_final) store_row32(o_final, at, v);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.acc_empty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+template <typename T, int EPI>
+cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& mw,
+                   const TcGemmArgs& a, int grid, size_t smem, cudaStream_t s) {
+  auto k = tc_gemm_kernel<T, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, s>>>(m0, m1, mw, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_gemm_stages(int BN, int n_parts) {
+  const int stage = n_parts * kATileBytes + BN * kBK * 2;
+  int st = (kTcGemmSmemBudget - 2048) / stage;
+  return st > 6 ? 6 : st;
+}
+
+size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages) {
+  const int stage = n_parts * kATileBytes + BN * kBK * 2;
+  return 1024 + (size_t)stages * stage + 256;
+}
+
+cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const CUtensorMap& map_w,
+                    TcGemmArgs a, bool bf16, int epi, int num_sms, cudaStream_t s) {
+  // Reject shapes this kernel does not handle (a host-side check, so a bad
+  // call never reaches the GPU).
+  if (a.BN % 32 || a.BN < 32 || a.BN > 256 || a.N % a.BN || a.K < 16 || a.K % 8 ||
+      a.n_parts < 1 || a.n_parts > 2 || a.M < 1)
+    return cudaErrorInvalidValue;
+  a.n_tiles = a.N / a.BN;
+  a.m_blocks = (a.M + kBM - 1) / kBM;
+  a.stages = tc_gemm_stages(a.BN, a.n_parts);
+  int cols = 32;
+  while (cols < 2 * a.BN) cols <<= 1;
+  a.tmem_cols = cols;
+  a.idesc = idesc_f16(kBM, a.BN, bf16);
+  const int units = epi == TC_EPI_LN ? a.m_blocks : a.m_blocks * a.n_tiles;
+  const int grid = units < num_sms ? units : num_sms;
+  const size_t smem = tc_gemm_smem_bytes(a.BN, a.n_parts, a.stages);
+  if (bf16) {
+    switch (epi) {
+      case TC_EPI_QKV: return launch<__nv_bfloat16, TC_EPI_QKV>(map_a0, map_a1, map_w, a, grid, smem, s);
+      case TC_EPI_GELU: return launch<__nv_bfloat16, TC_EPI_GELU>(map_a0, map_a1, map_w, a, grid, smem, s);
+      default: return launch<__nv_bfloat16, TC_EPI_LN>(map_a0, map_a1, map_w, a, grid, smem, s);
+    }
+  }
+  switch (epi) {
+    case TC_EPI_QKV: return launch<__half, TC_EPI_QKV>(map_a0, map_a1, map_w, a, grid, smem, s);
+    case TC_EPI_GELU: return launch<__half, TC_EPI_GELU>(map_a0, map_a1, map_w, a, grid, smem, s);
+    default: return launch<__half, TC_EPI_LN>(map_a0, map_a1, map_w, a, grid, smem, s);
+  }
+}
+
+}  // namespace tl
+
+// ------------------------------------------------------------ tensor maps
+namespace tl {
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* map, const void* ptr, bool bf16, uint64_t rows, uint64_t cols,
+                  uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace tl
