@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -124,6 +125,8 @@ tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d
   if (!h) return TL_ERR_OUT_OF_MEMORY;
   h->n_layers = n_layers; h->d = d_model; h->H = n_heads; h->dh = dh; h->dff = d_ff;
   h->dtype = dtype;
+  // Debug switch: CUDA-core attention inside the layered path (cross-checks).
+  if (const char* e = getenv("TL_SIMT_ATTENTION")) h->simt_attention = e[0] == '1';
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     delete h;

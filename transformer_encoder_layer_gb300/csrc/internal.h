@@ -38,6 +38,7 @@ struct tl_encoder {
   int n_layers = 0, d = 0, H = 0, dh = 0, dff = 0;
   tl_dtype dtype = TL_F32;
   tl_path path = TL_PATH_AUTO;
+  bool simt_attention = false;  // layered path: CUDA-core attention instead of tcgen05
   int device = 0;
   int num_sms = 0;
   void* wbuf = nullptr;      // one allocation holding every packed parameter

@@ -2,6 +2,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "paths.h"
+#include "tc_attention.h"
 #include "tc_gemm.h"
 
 namespace tl {
@@ -99,26 +100,28 @@ cudaError_t run_simt(tl_encoder* h, const void* x, int B, int L, const int32_t* 
 // ---------------------------------------------------------------- LAYERED
 // tcgen05 GEMMs with fused epilogues; activations between steps are (hi, lo)
 // 16-bit planes so every GEMM operand keeps about fp32 accuracy.
+// Largest N tile (a multiple of 32 and of `unit`, at most 256) dividing n.
+int pick_bn(int n, int unit = 32) {
+  for (int bn = 256; bn >= 32; bn -= 32)
+    if (n % bn == 0 && bn % unit == 0) return bn;
+  return 0;
+}
+
 bool layered_supported(const tl_encoder* h) {
   if (h->dtype == TL_F32) return false;
   const int d = h->d, dh = h->dh;
   // K of every GEMM a multiple of the 64-wide TMA box; N tiles of 32 columns.
   if (d % 64 || h->dff % 64) return false;
   if (!(dh % 32 == 0 || 32 % dh == 0)) return false;
-  return true;
+  return pick_bn(3 * d, dh > 32 ? dh : 32) > 0;
 }
 
-// Largest N tile (a multiple of 32, at most 256) that divides n.
-int pick_bn(int n) {
-  for (int bn = 256; bn >= 32; bn -= 32)
-    if (n % bn == 0) return bn;
-  return 0;
-}
 
 struct LayeredWs {
   void *xh, *xl, *qh, *ql, *kh, *kl, *vth, *vtl, *ch, *cl, *yh, *yl, *hh, *hl;
   float *x32, *y32, *rs;
   int* ties;
+  int* kmax;
   int Lp;
   size_t bytes;
 };
@@ -143,11 +146,13 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   o[14] = take(T * d * 4); o[15] = take(T * d * 4);                        // x32, y32
   o[16] = take(d > 256 ? T * d * 4 : 4);                                   // LN scratch
   size_t ot = take((1 + T * h->H) * 4);
+  size_t ok_ = take((size_t)B * h->H * 4);
   void** p[14] = {&w.xh, &w.xl, &w.qh, &w.ql, &w.kh, &w.kl, &w.vth, &w.vtl, &w.ch, &w.cl,
                   &w.yh, &w.yl, &w.hh, &w.hl};
   for (int i = 0; i < 14; ++i) *p[i] = b + o[i];
   w.x32 = (float*)(b + o[14]); w.y32 = (float*)(b + o[15]); w.rs = (float*)(b + o[16]);
   w.ties = (int*)(b + ot);
+  w.kmax = (int*)(b + ok_);
   w.bytes = off;
   return w;
 }
@@ -171,10 +176,12 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
     // a1: fused QKV projection, head-major (hi, lo) epilogue.
     {
       TcGemmArgs g{};
-      g.M = M; g.N = 3 * d; g.K = d; g.BN = pick_bn(3 * d); g.n_parts = first ? 1 : 2;
+      g.M = M; g.N = 3 * d; g.K = d; g.BN = pick_bn(3 * d, dh > 32 ? dh : 32); g.n_parts = first ? 1 : 2;
       g.bias = P.b_qkv;
       g.q_hi = w.qh; g.q_lo = w.ql; g.k_hi = w.kh; g.k_lo = w.kl; g.vt_hi = w.vth; g.vt_lo = w.vtl;
       g.B = B; g.L = L; g.H = H; g.dh = dh; g.Lp = w.Lp; g.status = h->status;
+      g.kmax = w.kmax;
+      if ((e = cudaMemsetAsync(w.kmax, 0, (size_t)B * H * 4, s)) != cudaSuccess) return e;
       if (!amaps(first ? x : w.xh, first ? nullptr : w.xl, M, d) ||
           !make_tmap_2d(&mw, P.w_qkv, bf, 3 * d, d, d, 64, g.BN, 128))
         return cudaErrorInvalidValue;
@@ -184,9 +191,14 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
     // a2: masked attention (ctx as (hi, lo) planes), then the near-tie fix-up.
     NearTieList ties{w.ties, w.ties + 1, M * H};
     if ((e = cudaMemsetAsync(w.ties, 0, sizeof(int), s)) != cudaSuccess) return e;
-    {
-      AttnIO io{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, 1, w.Lp, w.ch, w.cl};
+    if (tc_attention_supported(dh) && !h->simt_attention) {
+      TcAttnArgs ta{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, w.ch, w.cl, vl, w.kmax, ties,
+                    B, H, L, w.Lp, dh, d, h->status};
       KernelTimer t(h, KC_TC_ATTENTION, s);
+      if ((e = tc_attention(ta, bf, h->num_sms, s)) != cudaSuccess) return e;
+    } else {
+      AttnIO io{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, 1, w.Lp, w.ch, w.cl};
+      KernelTimer t(h, KC_SIMT_ATTENTION, s);
       if ((e = simt_attention(io, bf ? 2 : 1, vl, B, H, L, dh, h->status, ties, s)) != cudaSuccess) return e;
     }
     {

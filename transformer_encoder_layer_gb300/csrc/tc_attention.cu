@@ -1,0 +1,453 @@
+// Flash attention on tcgen05 with the causal and key-padding masks applied
+// in registers ("KernelForge", section "What we built": both masks inside
+// the kernel; section "Challenges": only key tiles that cross a row's limit
+// need the per-element predicate).  The L x L scores never leave the chip.
+//
+// One CTA per SM, persistent over (plane, 128-query tile) work items taken
+// heaviest first (the causal triangle makes late query tiles longest).
+// Q, K and V arrive as (hi, lo) 16-bit planes; scores and probabilities are
+// products of split operands, S = Qh.Kh + Qh.Kl + Ql.Kh and O = Ph.Vh +
+// Ph.Vl + Pl.Vh (the lo.lo term is below fp32 rounding), accumulated in
+// fp32 in TMEM.
+//
+// Warp roles (192 threads):
+//   warp 0     TMA: Q (once per work item) and K/V^T tiles of 64 keys into a
+//              3-deep ring
+//   warp 1     TMEM owner; one thread issues S = Q K^T into one of two TMEM
+//              score buffers, then O_j = P_j V_j into one of two TMEM output
+//              buffers once the softmax warps have written P_j
+//   warps 2-5  softmax: thread = query row.  Reads its 64 scores, masks,
+//              updates the running max/sum, writes P_j as (hi, lo) into the
+//              swizzled shared-memory operand, and folds the previous tile's
+//              O_{j-1} into its fp32 register accumulator with the
+//              online-softmax correction.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "neartie.cuh"
+#include "tc_attention.h"
+#include "tc_common.cuh"
+#include "tc_gemm.h"
+
+namespace tl {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kBQ = 128, kBKV = 64, kStages = 3;
+
+// Shared-memory descriptor for a K-major operand whose rows are `row_bytes`
+// (32, 64 or 128) long, swizzled at the same width: 8-row atoms of
+// 8*row_bytes bytes.
+__device__ __forceinline__ uint64_t sdesc_rows(uint32_t saddr, int row_bytes) {
+  const uint64_t mode = row_bytes == 128 ? 2 : (row_bytes == 64 ? 4 : 6);
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)((8 * row_bytes) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= mode << 61;
+  return d;
+}
+
+// Byte offset of element (r, c) of a K-major tile with `row_bytes`-long
+// rows written with the swizzle of the same width: the 16-byte chunk index
+// (address bits 4..) is XORed with the 128-byte line index (bits 7..),
+// masked to the chunks of one row.
+__device__ __forceinline__ int swz_offset(int r, int c_bytes, int row_bytes) {
+  const int o = r * row_bytes + c_bytes;
+  return o ^ (((o >> 7) & ((row_bytes >> 4) - 1)) << 4);
+}
+
+template <typename T, int DH>
+struct Layout {
+  static constexpr int kQBytes = kBQ * DH * 2;      // one Q plane
+  static constexpr int kKBytes = kBKV * DH * 2;     // one K plane tile
+  static constexpr int kVBytes = DH * kBKV * 2;     // one V^T plane tile
+  static constexpr int kPBytes = kBQ * kBKV * 2;    // one P plane (16 KB)
+  static constexpr int kStageBytes = 2 * kKBytes + 2 * kVBytes;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
+  static constexpr int kPOff = kKVOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kPOff + 2 * 2 * kPBytes;
+  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kRowBytes = DH * 2;          // Q/K rows: 32, 64, 128
+};
+
+template <typename T, int DH>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_attention_kernel(const __grid_constant__ CUtensorMap mqh, const __grid_constant__ CUtensorMap mql,
+                        const __grid_constant__ CUtensorMap mkh, const __grid_constant__ CUtensorMap mkl,
+                        const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
+                        const TcAttnArgs a) {
+  using Lay = Layout<T, DH>;
+  extern __shared__ __align__(1024) unsigned char dyn_smem[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Lay::kBarOff);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;            // [kStages]
+  uint64_t* kv_empty = kv_full + kStages;  // [kStages]
+  uint64_t* s_full = kv_empty + kStages;   // [2]
+  uint64_t* s_empty = s_full + 2;          // [2]
+  uint64_t* p_full = s_empty + 2;          // [2]
+  uint64_t* p_empty = p_full + 2;          // [2]
+  uint64_t* o_full = p_empty + 2;          // [2]
+  uint64_t* o_empty = o_full + 2;          // [2]
+  uint64_t* mma_done = o_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int planes = a.B * a.H;
+  const int nqt = (a.L + kBQ - 1) / kBQ;
+  const int n_items = planes * nqt;
+  constexpr uint32_t kTmemCols = 256;  // S: 2 x 64, O: 2 x DH (<= 128)
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1 + 128);  // the MMA's last S commit + every softmax thread
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 128);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&p_empty[s], 1);
+      mbar_init(&o_full[s], 1);
+      mbar_init(&o_empty[s], 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  volatile int* abort = abort_flag;
+  const uint32_t tS = tmem, tO = tmem + 2 * kBKV;
+
+  // Work item w -> (plane, query tile), heaviest query tiles first.
+  auto item = [&](int w, int& plane, int& qt) {
+    qt = nqt - 1 - w / planes;
+    plane = w % planes;
+  };
+  auto key_tiles = [&](int plane, int qt, int& vl) {
+    vl = a.valid_len[plane / a.H];
+    vl = vl < 1 ? 1 : (vl > a.L ? a.L : vl);
+    const int kend = min(qt * kBQ + kBQ, vl);  // keys any row of the tile sees
+    return (kend + kBKV - 1) / kBKV;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      long long kv_it = 0, n_items_done = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_items_done) {
+        int plane, qt, vl;
+        item(w, plane, qt);
+        const int nkt = key_tiles(plane, qt, vl);
+        if (!mbar_wait(q_empty, (uint32_t)(n_items_done & 1) ^ 1, abort, a.status)) break;
+        mbar_arrive_expect_tx(q_full, 2 * Lay::kQBytes);
+        const int qrow = plane * a.L + qt * kBQ;
+        tma_load_2d(base + Lay::kQOff, &mqh, q_full, 0, qrow);
+        tma_load_2d(base + Lay::kQOff + Lay::kQBytes, &mql, q_full, 0, qrow);
+        for (int j = 0; j < nkt; ++j, ++kv_it) {
+          const int st = (int)(kv_it % kStages);
+          const uint32_t ph = (uint32_t)((kv_it / kStages) & 1);
+          if (!mbar_wait(&kv_empty[st], ph ^ 1, abort, a.status)) { ok = false; break; }
+          unsigned char* sb = base + Lay::kKVOff + st * Lay::kStageBytes;
+          mbar_arrive_expect_tx(&kv_full[st], Lay::kStageBytes);
+          const int krow = plane * a.L + j * kBKV;
+          tma_load_2d(sb, &mkh, &kv_full[st], 0, krow);
+          tma_load_2d(sb + Lay::kKBytes, &mkl, &kv_full[st], 0, krow);
+          tma_load_2d(sb + 2 * Lay::kKBytes, &mvh, &kv_full[st], j * kBKV, plane * DH);
+          tma_load_2d(sb + 2 * Lay::kKBytes + Lay::kVBytes, &mvl, &kv_full[st], j * kBKV, plane * DH);
+        }
+      }
+      // Drain: wait for the last loads issued into each ring slot and Q.
+      for (long long r = 1; r <= kv_it && r <= kStages; ++r) {
+        const long long it = kv_it - r;
+        mbar_wait_bounded(&kv_full[it % kStages], (uint32_t)((it / kStages) & 1), a.status);
+      }
+      if (n_items_done > 0) mbar_wait_bounded(q_full, (uint32_t)((n_items_done - 1) & 1), a.status);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t idesc_s = idesc_f16(kBQ, kBKV, kBf);
+    const uint32_t idesc_o = idesc_f16(kBQ, DH, kBf);
+    long long kv_it = 0, s_it = 0, o_it = 0, n_done = 0;
+    bool ok = true;
+    const uint32_t q_addr = smem_u32(base + Lay::kQOff);
+    auto issue_pv = [&](long long it_kv, long long it_o) -> bool {
+      const int pb = (int)(it_o & 1);
+      const uint32_t ph = (uint32_t)((it_o >> 1) & 1);
+      if (!mbar_wait(&p_full[pb], ph, abort, a.status)) return false;
+      if (!mbar_wait(&o_empty[pb], ph ^ 1, abort, a.status)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const int st = (int)(it_kv % kStages);
+        const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
+        const uint32_t vh = sb + 2 * Lay::kKBytes, vl_ = vh + Lay::kVBytes;
+        const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * 2 * Lay::kPBytes);
+        const uint32_t pl_ = ph_ + Lay::kPBytes;
+        const uint32_t d = tO + (uint32_t)(pb * DH);
+        // O = Ph.Vh + Ph.Vl + Pl.Vh over 64 keys (4 steps of K = 16)
+        const uint32_t as[3] = {ph_, ph_, pl_};
+        const uint32_t bs[3] = {vh, vl_, vh};
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+#pragma unroll
+          for (int k = 0; k < kBKV / 16; ++k)
+            mma_f16(d, sdesc_rows(as[t] + k * 32, 128), sdesc_rows(bs[t] + k * 32, 128), idesc_o,
+                    (t | k) != 0);
+        mma_commit(&o_full[pb]);
+        mma_commit(&p_empty[pb]);
+        mma_commit(&kv_empty[st]);
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_done) {
+      int plane, qt, vl;
+      item(w, plane, qt);
+      const int nkt = key_tiles(plane, qt, vl);
+      if (!mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) break;
+      tc_fence_after();
+      for (int j = 0; j < nkt; ++j) {
+        const long long it = kv_it + j;
+        const int st = (int)(it % kStages);
+        if (!mbar_wait(&kv_full[st], (uint32_t)((it / kStages) & 1), abort, a.status)) { ok = false; break; }
+        const int sbuf = (int)(s_it & 1);
+        if (!mbar_wait(&s_empty[sbuf], (uint32_t)(((s_it >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
+          const uint32_t kh = sb, kl = sb + Lay::kKBytes;
+          const uint32_t qh = q_addr, ql = q_addr + Lay::kQBytes;
+          const uint32_t d = tS + (uint32_t)(sbuf * kBKV);
+          const uint32_t as[3] = {qh, qh, ql};
+          const uint32_t bs[3] = {kh, kl, kh};
+#pragma unroll
+          for (int t = 0; t < 3; ++t)
+#pragma unroll
+            for (int k = 0; k < DH / 16; ++k)
+              mma_f16(d, sdesc_rows(as[t] + k * 32, Lay::kRowBytes),
+                      sdesc_rows(bs[t] + k * 32, Lay::kRowBytes), idesc_s, (t | k) != 0);
+          mma_commit(&s_full[sbuf]);
+          if (j == nkt - 1) mma_commit(q_empty);  // Q no longer read
+        }
+        __syncwarp();
+        ++s_it;
+        if (j > 0) {
+          if (!issue_pv(kv_it + j - 1, o_it)) { ok = false; break; }
+          ++o_it;
+        }
+      }
+      if (!ok) break;
+      if (!issue_pv(kv_it + nkt - 1, o_it)) { ok = false; break; }
+      ++o_it;
+      kv_it += nkt;
+    }
+    if (lane == 0) mma_commit(mma_done);
+    __syncwarp();
+    mbar_wait_bounded(mma_done, 0, a.status);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;  // row of the query tile == TMEM lane
+    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    T* const ctx_hi = reinterpret_cast<T*>(a.ctx_hi);
+    T* const ctx_lo = reinterpret_cast<T*>(a.ctx_lo);
+    const float scale_log2 = rsqrtf((float)DH) * 1.4426950408889634f;
+    long long s_it = 0, o_it = 0, n_done = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_done) {
+      int plane, qt, vl;
+      item(w, plane, qt);
+      const int nkt = key_tiles(plane, qt, vl);
+      const int i = qt * kBQ + r;                    // query position in the sequence
+      const int limit = min(i + 1, vl);              // keys [0, limit) visible
+      const int full_keys = min(qt * kBQ + 1, vl);   // keys every row of the tile sees
+      float acc[DH];
+#pragma unroll
+      for (int c = 0; c < DH; ++c) acc[c] = 0.f;
+      float m = -INFINITY, m2 = -INFINITY, l = 0.f, m_prev_o = -INFINITY;
+      float m_hist[2] = {-INFINITY, -INFINITY};     // running max after tile j (by parity)
+      // |q_i| for the near-tie test, from the (hi, lo) Q tile in shared memory.
+      float qn2 = 0.f;
+      if (mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) {
+        const unsigned char* qh = base + Lay::kQOff;
+#pragma unroll
+        for (int c = 0; c < DH; ++c) {
+          const int off = swz_offset(r, c * 2, Lay::kRowBytes);
+          float qv = to_f32<T>(*reinterpret_cast<const T*>(qh + off)) +
+                     to_f32<T>(*reinterpret_cast<const T*>(qh + Lay::kQBytes + off));
+          qn2 = fmaf(qv, qv, qn2);
+        }
+        mbar_arrive(q_empty);  // this thread no longer reads Q
+      } else {
+        ok = false;
+        break;
+      }
+      // Fold O_{jo} (computed against the running max after tile jo) into acc.
+      auto fold_o = [&](int jo) -> bool {
+        const int ob = (int)(o_it & 1);
+        const uint32_t ph = (uint32_t)((o_it >> 1) & 1);
+        if (!mbar_wait(&o_full[ob], ph, abort, a.status)) return false;
+        tc_fence_after();
+        const float mj = m_hist[jo & 1];
+        const float corr = exp2f(m_prev_o - mj);   // 0 on the first fold
+        const uint32_t ta = tO + lane_addr + (uint32_t)(ob * DH);
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t rr[16];
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+              "%13,%14,%15}, [%16];"
+              : "=r"(rr[0]), "=r"(rr[1]), "=r"(rr[2]), "=r"(rr[3]), "=r"(rr[4]), "=r"(rr[5]),
+                "=r"(rr[6]), "=r"(rr[7]), "=r"(rr[8]), "=r"(rr[9]), "=r"(rr[10]), "=r"(rr[11]),
+                "=r"(rr[12]), "=r"(rr[13]), "=r"(rr[14]), "=r"(rr[15])
+              : "r"(ta + c0));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(acc[c0 + c], corr, __uint_as_float(rr[c]));
+        }
+        m_prev_o = mj;
+        tc_fence_before();
+        mbar_arrive(&o_empty[ob]);
+        ++o_it;
+        return true;
+      };
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int sbuf = (int)(s_it & 1);
+        if (!mbar_wait(&s_full[sbuf], (uint32_t)((s_it >> 1) & 1), abort, a.status)) { ok = false; break; }
+        tc_fence_after();
+        float s[kBKV];
+        tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV), *reinterpret_cast<float(*)[32]>(&s[0]));
+        tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV + 32), *reinterpret_cast<float(*)[32]>(&s[32]));
+        tc_fence_before();
+        mbar_arrive(&s_empty[sbuf]);
+        ++s_it;
+        const int k0 = j * kBKV;
+        const bool needs_mask = k0 + kBKV > full_keys;
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBKV; ++c) {
+          float v = s[c] * scale_log2;
+          if (needs_mask && k0 + c >= limit) v = -INFINITY;
+          s[c] = v;
+          m2 = fmaxf(m2, fminf(fmaxf(m, tmax), v));
+          tmax = fmaxf(tmax, v);
+        }
+        const float mn = fmaxf(m, tmax);
+        // A row with no visible key in this tile keeps its max; its
+        // probabilities are exactly 0 below.
+        const float mref = mn == -INFINITY ? 0.f : mn;
+        l *= exp2f(m - mref);
+        m = mn;
+        m_hist[j & 1] = mref;
+        // P_j into the (hi, lo) swizzled operand buffer.
+        const int pb = (int)((s_it - 1) & 1);
+        if (!mbar_wait(&p_empty[pb], (uint32_t)((((s_it - 1) >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
+        unsigned char* ph = base + Lay::kPOff + pb * 2 * Lay::kPBytes;
+        unsigned char* pl = ph + Lay::kPBytes;
+#pragma unroll
+        for (int c8 = 0; c8 < kBKV / 8; ++c8) {
+          uint4 hv, lv;
+          T* hp = reinterpret_cast<T*>(&hv);
+          T* lp = reinterpret_cast<T*>(&lv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p = exp2f(s[c8 * 8 + e] - mref);
+            l += p;
+            Split<T>::go(p, hp[e], lp[e]);
+          }
+          const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(ph + off) = hv;
+          *reinterpret_cast<uint4*>(pl + off) = lv;
+        }
+        fence_proxy_async();
+        mbar_arrive(&p_full[pb]);
+        if (j > 0 && !fold_o(j - 1)) { ok = false; break; }
+      }
+      if (!ok) break;
+      if (!fold_o(nkt - 1)) { ok = false; break; }
+      if (i < a.L) {
+        const float inv = 1.f / l;
+        const size_t at = ((size_t)(plane / a.H) * a.L + i) * a.d + (size_t)(plane % a.H) * DH;
+#pragma unroll
+        for (int c8 = 0; c8 < DH / 8; ++c8) {
+          uint4 hv, lv;
+          T* hp = reinterpret_cast<T*>(&hv);
+          T* lp = reinterpret_cast<T*>(&lv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) Split<T>::go(acc[c8 * 8 + e] * inv, hp[e], lp[e]);
+          *reinterpret_cast<uint4*>(ctx_hi + at + c8 * 8) = hv;
+          *reinterpret_cast<uint4*>(ctx_lo + at + c8 * 8) = lv;
+        }
+        const float kmax = __int_as_float(a.kmax[plane]);
+        if (neartie_flag((m - m2) * 0.69314718055994531f, sqrtf(qn2), kmax, DH))
+          neartie_push(a.ties, plane * a.L + i);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename T, int DH>
+cudaError_t launch_dh(const TcAttnArgs& a, const CUtensorMap* maps, int grid, cudaStream_t s) {
+  using Lay = Layout<T, DH>;
+  auto k = tc_attention_kernel<T, DH>;
+  const size_t smem = Lay::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_attention_supported(int dh) { return dh == 16 || dh == 32 || dh == 64; }
+
+cudaError_t tc_attention(const TcAttnArgs& a, bool bf16, int num_sms, cudaStream_t s) {
+  const int dh = a.dh;
+  if (!tc_attention_supported(dh) || a.L < 1 || a.Lp % 8 || a.Lp < a.L) return cudaErrorInvalidValue;
+  const uint64_t rows = (uint64_t)a.B * a.H * a.L;
+  CUtensorMap maps[6];
+  bool ok = make_tmap_2d(&maps[0], a.q_hi, bf16, rows, dh, dh, dh, kBQ, dh * 2) &&
+            make_tmap_2d(&maps[1], a.q_lo, bf16, rows, dh, dh, dh, kBQ, dh * 2) &&
+            make_tmap_2d(&maps[2], a.k_hi, bf16, rows, dh, dh, dh, kBKV, dh * 2) &&
+            make_tmap_2d(&maps[3], a.k_lo, bf16, rows, dh, dh, dh, kBKV, dh * 2) &&
+            make_tmap_2d(&maps[4], a.vt_hi, bf16, (uint64_t)a.B * a.H * dh, a.Lp, a.Lp, kBKV, dh, 128) &&
+            make_tmap_2d(&maps[5], a.vt_lo, bf16, (uint64_t)a.B * a.H * dh, a.Lp, a.Lp, kBKV, dh, 128);
+  if (!ok) return cudaErrorInvalidValue;
+  const int items = a.B * a.H * ((a.L + kBQ - 1) / kBQ);
+  const int grid = items < num_sms ? items : num_sms;
+  if (bf16) {
+    if (dh == 16) return launch_dh<__nv_bfloat16, 16>(a, maps, grid, s);
+    if (dh == 32) return launch_dh<__nv_bfloat16, 32>(a, maps, grid, s);
+    return launch_dh<__nv_bfloat16, 64>(a, maps, grid, s);
+  }
+  if (dh == 16) return launch_dh<__half, 16>(a, maps, grid, s);
+  if (dh == 32) return launch_dh<__half, 32>(a, maps, grid, s);
+  return launch_dh<__half, 64>(a, maps, grid, s);
+}
+
+}  // namespace tl

@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sm.acc_full[acc], acc_phase, abort, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tbase = tmem + lane_addr + (uint32_t)(acc * BN);
+        float kn2 = 0.f;  // running |k|^2 of the head being written (QKV)
         for (int c = 0; c < n_chunks; ++c) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
@@ -280,9 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   } else {
                     for (int j = 0; j < w; ++j) store_pair(hi, lo, at + j, v[j0 + j]);
                   }
+                  if (which == 1 && a.kmax) {  // |k_j| of this head, for the near-tie test
+                    for (int j = 0; j < w; ++j) kn2 = fmaf(v[j0 + j], v[j0 + j], kn2);
+                    if (c0 + w == a.dh) {
+                      atomicMax(a.kmax + bh, __float_as_int(sqrtf(kn2)));
+                      kn2 = 0.f;
+                    }
+                  }
                 } else {
-                  for (int j = 0; j < w; ++j)
-                    store_pair(vt_hi, vt_lo, (bh * a.dh + c0 + j) * a.Lp + i, v[j0 + j]);
+                  for (int j = 0; j < w; ++j) {
+                    const size_t vr = (bh * a.dh + c0 + j) * a.Lp;
+                    store_pair(vt_hi, vt_lo, vr + i, v[j0 + j]);
+                    if (i == a.L - 1)  // zero the pitch padding: keys beyond L read as 0
+                      for (int z = a.L; z < a.Lp; ++z) store_pair(vt_hi, vt_lo, vr + z, 0.f);
+                  }
                 }
               }
             }

@@ -23,6 +23,7 @@ struct TcGemmArgs {
   // TC_EPI_QKV: head-major (hi, lo) planes; V transposed with row pitch Lp.
   void *q_hi, *q_lo, *k_hi, *k_lo, *vt_hi, *vt_lo;
   int B, L, H, dh, Lp;
+  int* kmax;     // [B*H] max |k_j| per plane as float bits (atomicMax), or null
   // TC_EPI_GELU: (hi, lo) planes [M, N].  TC_EPI_LN: optional (hi, lo) out.
   void *o_hi, *o_lo;
   // TC_EPI_LN
