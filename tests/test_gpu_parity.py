@@ -211,3 +211,31 @@ def test_forward_host_matches_device_forward():
     od = enc.forward(xh.cuda(), vh.cuda()).cpu()
     assert torch.equal(oh, od)
     enc.close()
+
+
+# ------------------------------------------------- sequence-resident path
+@pytest.mark.parametrize("dtype,L,dff,n_layers,batch", [
+    ("f16", 64, 512, 4, 37),     # the d128 workload's layer, ragged last tile
+    ("bf16", 64, 512, 2, 6),
+    ("f16", 32, 256, 2, 9),      # four sequences per tile
+    ("f16", 128, 128, 1, 3),     # one sequence per tile, d_ff = d
+    ("bf16", 128, 384, 3, 2),
+])
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_mega_shapes(dtype, L, dff, n_layers, batch, scale):
+    from transformer_encoder_layer_gb300 import binding
+    s = tiny_shape(dtype=dtype, batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=128,
+                   n_heads=4, d_ff=dff, n_layers=n_layers)
+    inp = make_inputs(s, seed=3, input_scale=scale)
+    assert "mega" in _paths_for(s)
+    _check(inp, "mega")
+
+
+def test_mega_matches_layered_closely():
+    # Two tensor-core paths over the same split-operand arithmetic: they
+    # differ only in summation order, so their difference is far inside the gate.
+    s = SHAPES["short_d128_L64_B4096"].with_(batch=64)
+    inp = make_inputs(s, seed=4)
+    a = _run(inp, "mega")
+    b = _run(inp, "layered")
+    assert np.max(np.abs(a - b)) < 2e-3

@@ -46,6 +46,7 @@ struct tl_encoder {
   int* status = nullptr;     // device status word
   tl_layer_dev* layers = nullptr;  // host array of n_layers
   tl_timing* timing = nullptr;     // non-null while per-kernel timing is on
+  const void* mega_layers = nullptr;  // device array of MegaLayer (megakernel path)
 };
 
 namespace tl {

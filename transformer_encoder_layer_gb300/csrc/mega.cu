@@ -1,0 +1,782 @@
+// Sequence-resident megakernel: every layer of the stack for a 128-row tile
+// of whole sequences in one CTA, activations kept on chip from the input
+// load to the output store ("Hyper-optimized megakernel-hybrid transformer
+// inference", section "Problem decomposition": short sequences fit in
+// shared memory, one CTA owns them across all layers).
+//
+// Shape: d_model = 128, head_dim = 32 (4 heads), d_ff a multiple of 128,
+// sequence length L in {32, 64, 128}: a tile holds 128 / L sequences, which
+// are rows [128 t, 128 t + 128) of the [B*L, d] input.  16-bit I/O (fp16 or
+// bf16); activations are carried as (hi, lo) 16-bit pairs wherever they feed
+// a tensor-core product.
+//
+// One CTA per SM, persistent over tiles.  320 threads:
+//   warp 0      TMA: the input tile (once per tile) and 128 x 64 weight boxes
+//               from L2 into a 2-deep ring, in the order the MMAs use them
+//   warp 1      TMEM (all 512 columns); one thread issues every tcgen05.mma
+//   warps 2-9   two groups of 4 warps ("halves" h = 0, 1); both groups cover
+//               all 128 rows (TMEM lanes), half h takes columns/keys
+//               [64h, 64h + 64) of each row
+//
+// Per layer (TMEM columns in brackets):
+//   QKV   acc[0, 384) = X . W_qkv^T      X = (hi, lo) of the layer input
+//   per head h: Q_h, K_h, V_h^T -> shared memory as (hi, lo);
+//         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
+//         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32)
+//   ctx = O / l -> shared memory (hi, lo)
+//   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> X buffer
+//   FFN   per 128-wide chunk c of d_ff: acc1[256 + 128 (c % 2)] = y . W_1c^T,
+//         h_c = gelu(acc1 + b_1c) -> shared memory, acc2[0, 128) += h_c . W_2c^T
+//         (chunk c + 1's first product overlaps chunk c's GELU)
+//   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
+//
+// Near ties (see neartie.cuh) are corrected in place: a flagged (row, head)
+// has its probabilities recomputed in fp64 from the layer input and the
+// weights before the P . V product.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "mega.h"
+#include "neartie.cuh"
+#include "tc_common.cuh"
+#include "tc_gemm.h"
+
+namespace tl {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;
+constexpr int kD = 128, kDH = 32, kH = 4;
+constexpr int kNW = 2;  // weight ring depth
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16-bit
+constexpr int kXA = 0;                                // [part][khalf] x 16 KB = 64 KB
+constexpr int kPB = kXA + 4 * kTile16;                // [part][khalf] x 16 KB = 64 KB
+constexpr int kQB = kPB + 4 * kTile16;                // [part] 128 x 32, 8 KB each
+constexpr int kKB = kQB + 2 * 8192;                   // [part] 128 x 32
+constexpr int kVB = kKB + 2 * 8192;                   // [part][khalf] 32 x 64, 4 KB each
+constexpr int kWR = kVB + 4 * 4096;                   // [kNW] x 16 KB
+constexpr int kMisc = kWR + kNW * kTile16;
+// misc (floats unless noted)
+constexpr int kQn2 = kMisc;                           // [2][128] partial |q|^2
+constexpr int kKn2 = kQn2 + 2 * 128 * 4;              // [2][128] partial |k|^2
+constexpr int kXch = kKn2 + 2 * 128 * 4;              // [2][128] exchange 0
+constexpr int kXch2 = kXch + 2 * 128 * 4;             // [2][128] exchange 1
+constexpr int kXch3 = kXch2 + 2 * 128 * 4;            // [2][128] exchange 2
+constexpr int kLs = kXch3 + 2 * 128 * 4;              // [4][128] softmax sums per head
+constexpr int kKmax = kLs + 4 * 128 * 4;              // [4] int (float bits)
+constexpr int kFlags = kKmax + 16;                    // int count + [128] row list
+constexpr int kBars = ((kFlags + 4 + 128 * 4 + 7) / 8) * 8;
+constexpr int kNumBars = 32;
+constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
+
+// mbarrier indices
+enum {
+  B_X_FULL = 0, B_W_FULL, B_W_FULL1, B_W_EMPTY, B_W_EMPTY1, B_A_READY, B_QKV_DONE, B_QKVH_READY,
+  B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
+  B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_F2_DONE, B_XA_FREE, B_MMA_DONE,
+  B_SYNC, B_COUNT
+};
+static_assert(B_COUNT <= kNumBars, "barrier slots");
+static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget");
+
+__device__ __forceinline__ int sw128(int r, int c8) { return r * 128 + ((c8 ^ (r & 7)) << 4); }
+__device__ __forceinline__ int sw64(int r, int c_bytes) {
+  const int o = r * 64 + c_bytes;
+  return o ^ (((o >> 7) & 3) << 4);
+}
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
+
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* v) {
+  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(v));
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
+template <typename T>
+__device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int off, const float* v) {
+  uint4 hv, lv;
+  T* hp = reinterpret_cast<T*>(&hv);
+  T* lp = reinterpret_cast<T*>(&lv);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) Split<T>::go(v[e], hp[e], lp[e]);
+  *reinterpret_cast<uint4*>(hi + off) = hv;
+  *reinterpret_cast<uint4*>(lo + off) = lv;
+}
+template <typename T>
+__device__ __forceinline__ void get8(const unsigned char* hi, const unsigned char* lo, int off,
+                                     bool use_lo, float* v) {
+  uint4 hv = *reinterpret_cast<const uint4*>(hi + off);
+  const T* hp = reinterpret_cast<const T*>(&hv);
+  if (use_lo) {
+    uint4 lv = *reinterpret_cast<const uint4*>(lo + off);
+    const T* lp = reinterpret_cast<const T*>(&lv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]) + to_f32<T>(lp[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
+  }
+}
+
+template <typename T, int L>
+__global__ void __launch_bounds__(kThreads, 1)
+    mega_kernel(const __grid_constant__ CUtensorMap map_x, const MegaArgs a) {
+  extern __shared__ __align__(1024) unsigned char dyn_smem[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBars);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + kBars + kNumBars * 8);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+  constexpr int S = 128 / L;  // sequences per tile
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_tiles = (a.B + S - 1) / S;
+  const int n_chunks = a.dff / 128;
+  const int T_rows = a.B * L;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      switch (i) {
+        case B_A_READY: case B_QKVH_READY: case B_S_FREE: case B_P_READY: case B_CTX_READY:
+        case B_Y_READY: case B_F1_FREE: case B_F1_FREE1: case B_H_READY: case B_XA_FREE:
+        case B_SYNC:
+          cnt = kCompute;
+          break;
+        default: break;
+      }
+      mbar_init(bar + i, cnt);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  volatile int* abort = abort_flag;
+  int* status = a.status;
+
+  if (warp == 0) {
+    // ================================================================ TMA
+    if (lane == 0) {
+      long long w_it = 0, tiles_done = 0;
+      bool ok = true;
+      auto wload = [&](const CUtensorMap* m, int x, int y) -> bool {
+        const int st = (int)(w_it % kNW);
+        const uint32_t ph = (uint32_t)((w_it / kNW) & 1);
+        if (!mbar_wait(bar + B_W_EMPTY + st, ph ^ 1, abort, status)) return false;
+        mbar_arrive_expect_tx(bar + B_W_FULL + st, kTile16);
+        tma_load_2d(sm + kWR + st * kTile16, m, bar + B_W_FULL + st, x, y);
+        ++w_it;
+        return true;
+      };
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles_done) {
+        if (!mbar_wait(bar + B_XA_FREE, (uint32_t)(tiles_done & 1) ^ 1, abort, status)) break;
+        mbar_arrive_expect_tx(bar + B_X_FULL, 2 * kTile16);
+        tma_load_2d(sm + kXA, &map_x, bar + B_X_FULL, 0, t * 128);
+        tma_load_2d(sm + kXA + kTile16, &map_x, bar + B_X_FULL, 64, t * 128);
+        for (int l = 0; l < a.n_layers && ok; ++l) {
+          const MegaLayer& P = a.layers[l];
+          for (int nb = 0; nb < 3 && ok; ++nb)
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb);
+          for (int kh = 0; kh < 2 && ok; ++kh) ok = ok && wload(P.map_o, 64 * kh, 0);
+          for (int c = 0; c <= n_chunks && ok; ++c) {
+            if (c < n_chunks)
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 128 * c);
+            if (c >= 1)
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = ok && wload(P.map_2, 128 * (c - 1) + 64 * kh, 0);
+          }
+        }
+      }
+      // Drain the loads in flight.
+      for (long long r = 1; r <= w_it && r <= kNW; ++r) {
+        const long long it = w_it - r;
+        mbar_wait_bounded(bar + B_W_FULL + (int)(it % kNW), (uint32_t)((it / kNW) & 1), status);
+      }
+      if (tiles_done > 0) mbar_wait_bounded(bar + B_X_FULL, (uint32_t)((tiles_done - 1) & 1), status);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA
+    long long w_it = 0;
+    long long n_a = 0, n_x = 0, n_head = 0, n_layer = 0;
+    const uint32_t id128 = idesc_f16(128, 128, kBf);
+    const uint32_t id32 = idesc_f16(128, 32, kBf);
+    bool ok = true;
+    const uint32_t xa = smem_u32(sm + kXA), pb = smem_u32(sm + kPB);
+    const uint32_t qb = smem_u32(sm + kQB), kb = smem_u32(sm + kKB), vb = smem_u32(sm + kVB);
+    // One 128 x 64 weight box against A (parts x 4 k16 steps) into d.
+    auto wbox = [&](uint32_t d, uint32_t a_base, int parts, bool first) -> bool {
+      const int st = (int)(w_it % kNW);
+      if (!mbar_wait(bar + B_W_FULL + st, (uint32_t)((w_it / kNW) & 1), abort, status)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t w = smem_u32(sm + kWR + st * kTile16);
+        for (int p = 0; p < parts; ++p)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(d, sdesc_sw128(a_base + p * 2 * kTile16 + k * 32), sdesc_sw128(w + k * 32), id128,
+                    (first && p == 0 && k == 0) ? 0u : 1u);
+        mma_commit(bar + B_W_EMPTY + st);
+      }
+      __syncwarp();
+      ++w_it;
+      return true;
+    };
+    auto commit = [&](int b) {
+      if (lane == 0) mma_commit(bar + b);
+      __syncwarp();
+    };
+    auto wait = [&](int b, long long& n, bool is_free = false) -> bool {
+      const uint32_t par = (uint32_t)(n & 1) ^ (is_free ? 1u : 0u);
+      ++n;
+      if (!mbar_wait(bar + b, par, abort, status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    long long c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0, c_f1free0 = 0, c_f1free1 = 0,
+              c_hr = 0;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      for (int l = 0; l < a.n_layers && ok; ++l, ++n_layer) {
+        // ---- QKV
+        if (l == 0) ok = wait(B_X_FULL, n_x);
+        else ok = wait(B_A_READY, n_a);
+        const int parts = l == 0 ? 1 : 2;
+        for (int nb = 0; nb < 3 && ok; ++nb)
+          for (int kh = 0; kh < 2 && ok; ++kh)
+            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, parts, kh == 0);
+        if (!ok) break;
+        commit(B_QKV_DONE);
+        // ---- attention, head by head
+        for (int h = 0; h < kH && ok; ++h, ++n_head) {
+          ok = wait(B_QKVH_READY, c_qkvh) && wait(B_S_FREE, c_sfree, true);
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t as[3] = {qb, qb, qb + 8192};
+            const uint32_t bs[3] = {kb, kb + 8192, kb};
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+              for (int k = 0; k < 2; ++k)
+                mma_f16(tmem + 384, desc_sw64(as[c] + k * 32), desc_sw64(bs[c] + k * 32), id128,
+                        (c | k) != 0);
+          }
+          commit(B_S_DONE);
+          ok = wait(B_P_READY, c_p);
+          if (!ok) break;
+          if (lane == 0) {
+            // O_h = Ph.Vh + Ph.Vl + Pl.Vh over 128 keys (2 halves x 4 steps)
+            const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+              for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_f16(tmem + 32 * h,
+                          sdesc_sw128(pb + (ap[c] * 2 + kh) * kTile16 + k * 32),
+                          sdesc_sw128(vb + (bp[c] * 2 + kh) * 4096 + k * 32), id32,
+                          (c | kh | k) != 0);
+          }
+          commit(B_O_DONE);
+        }
+        if (!ok) break;
+        // ---- out-projection
+        ok = wait(B_CTX_READY, c_ctx);
+        for (int kh = 0; kh < 2 && ok; ++kh) ok = wbox(tmem + 128, pb + kh * kTile16, 2, kh == 0);
+        if (!ok) break;
+        commit(B_OUT_DONE);
+        // ---- FFN
+        ok = wait(B_Y_READY, c_y);
+        for (int c = 0; c <= n_chunks && ok; ++c) {
+          if (c < n_chunks) {
+            const int buf = c & 1;
+            ok = buf == 0 ? wait(B_F1_FREE, c_f1free0, true) : wait(B_F1_FREE1, c_f1free1, true);
+            for (int kh = 0; kh < 2 && ok; ++kh)
+              ok = wbox(tmem + 256 + 128 * buf, xa + kh * kTile16, 2, kh == 0);
+            if (!ok) break;
+            commit(B_F1_DONE + buf);
+          }
+          if (c >= 1) {
+            ok = wait(B_H_READY, c_hr);
+            for (int kh = 0; kh < 2 && ok; ++kh)
+              ok = wbox(tmem, pb + kh * kTile16, 2, c == 1 && kh == 0);
+            if (!ok) break;
+            commit(B_H_FREE);
+          }
+        }
+        if (!ok) break;
+        commit(B_F2_DONE);
+      }
+    }
+    commit(B_MMA_DONE);
+    mbar_wait_bounded(bar + B_MMA_DONE, 0, status);
+  } else {
+    // ======================================================== compute warps
+    const int cw = warp - 2;               // 0..7
+    const int half = cw >> 2;              // column / key half
+    const int qd = warp & 3;               // TMEM lane quarter
+    const int r = qd * 32 + lane;          // row in the tile
+    const int sq = r / L;                  // sequence within the tile
+    const int i = r % L;                   // position in the sequence
+    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    float* qn2_s = reinterpret_cast<float*>(sm + kQn2);
+    float* kn2_s = reinterpret_cast<float*>(sm + kKn2);
+    float* xch = reinterpret_cast<float*>(sm + kXch);
+    float* xch2 = reinterpret_cast<float*>(sm + kXch2);
+    float* xch3 = reinterpret_cast<float*>(sm + kXch3);
+    float* l_s = reinterpret_cast<float*>(sm + kLs);
+    int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
+    int* flag_cnt = reinterpret_cast<int*>(sm + kFlags);
+    int* flag_rows = flag_cnt + 1;
+    unsigned char* xa = sm + kXA;
+    unsigned char* pbuf = sm + kPB;
+    const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
+    long long c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1_0 = 0, c_f1_1 = 0, c_hfree = 0,
+              c_f2 = 0;
+    bool ok = true;
+    auto wait = [&](int b, long long& n) -> bool {
+      const uint32_t par = (uint32_t)(n & 1);
+      ++n;
+      if (!mbar_wait(bar + b, par, abort, status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    auto arrive = [&](int b) {
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar + b);
+    };
+    // Barrier of the 256 compute threads on an mbarrier, so that the wait is
+    // bounded like every other wait (a bar.sync could not give up).
+    long long c_sync = 0;
+    auto bar_compute = [&]() {
+      mbar_arrive(bar + B_SYNC);
+      const uint32_t par = (uint32_t)(c_sync & 1);
+      ++c_sync;
+      mbar_wait(bar + B_SYNC, par, abort, status);
+    };
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const int seq = t * S + sq;
+      const bool row_valid = seq < a.B;
+      int vl = row_valid ? a.valid_len[seq] : 1;
+      if (vl < 1 || vl > L) {
+        if (row_valid) set_status(status, TL_ERR_BAD_VALID_LEN);
+        vl = vl < 1 ? 1 : L;
+      }
+      const int limit = min(i + 1, vl);   // visible keys of this row: [sq*L, sq*L + limit)
+      const size_t grow = (size_t)t * 128 + r;
+      for (int l = 0; l < a.n_layers && ok; ++l) {
+        const MegaLayer& P = a.layers[l];
+        const bool first = l == 0;
+        if (!wait(B_QKV_DONE, c_qkv)) { ok = false; break; }
+        if (threadIdx.x == 64) {
+          for (int h = 0; h < kH; ++h) kmax_s[h] = 0;
+        }
+        for (int h = 0; h < kH && ok; ++h) {
+          // ---- Q_h, K_h, V_h^T into shared memory as (hi, lo); columns [16 half, +16)
+          if (h > 0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+          float qv[16], kv[16], vv[16];
+          tmem_ld<16>(tmem + lane_addr + 32 * h + 16 * half, qv);
+          tmem_ld<16>(tmem + lane_addr + 128 + 32 * h + 16 * half, kv);
+          tmem_ld<16>(tmem + lane_addr + 256 + 32 * h + 16 * half, vv);
+          float q2 = 0.f, k2 = 0.f;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int col = 32 * h + 16 * half + c;
+            qv[c] += __ldg(P.b_qkv + col);
+            kv[c] += __ldg(P.b_qkv + 128 + col);
+            vv[c] += __ldg(P.b_qkv + 256 + col);
+            q2 = fmaf(qv[c], qv[c], q2);
+            k2 = fmaf(kv[c], kv[c], k2);
+          }
+          qn2_s[half * 128 + r] = q2;
+          kn2_s[half * 128 + r] = k2;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int off = sw64(r, (2 * half + cc) * 16);
+            put8<T>(sm + kQB, sm + kQB + 8192, off, qv + 8 * cc);
+            put8<T>(sm + kKB, sm + kKB + 8192, off, kv + 8 * cc);
+          }
+          {
+            // V^T [dim][key]: this thread's key r, dims [16 half, +16)
+            const int kh = r >> 6, kc = r & 63;
+            unsigned char* vh = sm + kVB + kh * 4096;
+            unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int dim = 16 * half + c;
+              const int off = dim * 128 + ((((kc >> 3) ^ (dim & 7))) << 4) + (kc & 7) * 2;
+              T hv, lv;
+              Split<T>::go(vv[c], hv, lv);
+              *reinterpret_cast<T*>(vh + off) = hv;
+              *reinterpret_cast<T*>(vlo + off) = lv;
+            }
+          }
+          arrive(B_QKVH_READY);
+          // ---- softmax over this row's keys in key half `half`
+          if (!wait(B_S_DONE, c_s)) { ok = false; break; }
+          const int k0 = 64 * half;                    // first key of my half
+          const int vis_lo = sq * L, vis_hi = sq * L + limit;
+          const bool any = (k0 < sq * L + L) && (k0 + 64 > sq * L);  // warp-uniform
+          float s[64];
+          float m1 = -INFINITY, m2 = -INFINITY;
+          if (any) {
+            tmem_ld<32>(tmem + lane_addr + 384 + k0, s);
+            tmem_ld<32>(tmem + lane_addr + 384 + k0 + 32, s + 32);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int key = k0 + c;
+              float v = (key >= vis_lo && key < vis_hi) ? s[c] * scale_log2 : -INFINITY;
+              s[c] = v;
+              m2 = fmaxf(m2, fminf(m1, v));
+              m1 = fmaxf(m1, v);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(bar + B_S_FREE);
+          xch[half * 128 + r] = m1;
+          xch2[half * 128 + r] = m2;
+          bar_compute();
+          const float o1 = xch[(1 - half) * 128 + r], o2 = xch2[(1 - half) * 128 + r];
+          const float M = fmaxf(m1, o1);
+          const float M2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+          // per-key |k| of this thread's key r, maxed over the tile
+          {
+            float kn = sqrtf(kn2_s[r] + kn2_s[128 + r]);
+            kn = warp_max(kn);
+            if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
+          }
+          float lsum = 0.f;
+          {
+            unsigned char* ph = pbuf + half * kTile16;
+            unsigned char* pl = pbuf + (2 + half) * kTile16;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              float p[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                p[e] = any ? exp2f(s[c8 * 8 + e] - M) : 0.f;
+                lsum += p[e];
+              }
+              put8<T>(ph, pl, sw128(r, c8), p);
+            }
+          }
+          xch3[half * 128 + r] = lsum;
+          bar_compute();
+          const float lt = xch3[r] + xch3[128 + r];
+          if (half == 0) l_s[h * 128 + r] = lt;
+          if (threadIdx.x == 64) *flag_cnt = 0;
+          // near-tie test (natural-log gap); half 0 decides for the row
+          const float qn = sqrtf(qn2_s[r] + qn2_s[128 + r]);
+          const float kmx = __int_as_float(kmax_s[h]);
+          bar_compute();
+          if (half == 0 && row_valid && neartie_flag((M - M2) * 0.69314718055994531f, qn, kmx, kDH)) {
+            int at = atomicAdd(flag_cnt, 1);
+            flag_rows[at] = r;
+          }
+          bar_compute();
+          const int nflag = *flag_cnt;
+          if (nflag > 0) {
+            // fp64 correction of the flagged rows' probabilities (rare).
+            for (int e = cw; e < nflag; e += 8) {
+              const int rr = flag_rows[e];
+              const int rs = rr / L, ri = rr % L;
+              int rvl = a.valid_len[t * S + rs];
+              rvl = rvl < 1 ? 1 : (rvl > L ? L : rvl);
+              const int nk = min(ri + 1, rvl);
+              const int kb0 = rs * L;
+              // x_j = the layer input (hi + lo; the first layer's input is exact in hi)
+              auto xval = [&](int row, int col) -> double {
+                const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
+                const int off = sw128(row, c8) + e8 * 2;
+                double v = (double)to_f32<T>(*reinterpret_cast<const T*>(xa + kh * kTile16 + off));
+                if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
+                return v;
+              };
+              const T* W = reinterpret_cast<const T*>(P.w_qkv);
+              // q_i (fp64), lane c owns dim c
+              double q64 = (double)P.b_qkv[32 * h + lane];
+              for (int tt = 0; tt < kD; ++tt)
+                q64 = fma((double)to_f32<T>(W[(size_t)(32 * h + lane) * kD + tt]), xval(rr, tt), q64);
+              // u = W_k,h^T q_i (lane owns tt = lane + 32 m), u0 = b_k,h . q_i
+              double u[4] = {0, 0, 0, 0};
+              double u0 = 0.0, qn2 = 0.0;
+              for (int c = 0; c < kDH; ++c) {
+                const double qc = __shfl_sync(0xffffffffu, q64, c);
+                u0 = fma(qc, (double)P.b_qkv[128 + 32 * h + c], u0);
+                qn2 = fma(qc, qc, qn2);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                  u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
+              }
+              // screening scores (fp32 q and k from shared memory), best score
+              auto qk32 = [&](int key) -> float {
+                float acc = 0.f;
+                for (int c = 0; c < kDH; ++c) {
+                  const int off = sw64(rr, c * 2), ko = sw64(key, c * 2);
+                  const float qf = to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + off)) +
+                                   to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + 8192 + off));
+                  const float kf = to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + ko)) +
+                                   to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + 8192 + ko));
+                  acc = fmaf(qf, kf, acc);
+                }
+                return acc * rsqrtf((float)kDH);
+              };
+              float best = -INFINITY;
+              for (int j = lane; j < nk; j += 32) best = fmaxf(best, qk32(kb0 + j));
+              best = warp_max(best);
+              const float err = neartie_err((float)sqrt(qn2), kmx, kDH);
+              const float thr = best - kTieGap - 2.f * err;
+              // Scores of keys kb0 + j (lane j % 32, slot j / 32): exact in fp64
+              // for candidates (x_j . u + u0, all lanes cooperating per key),
+              // the screening fp32 value otherwise.
+              double sc_own[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+              double Mx = -INFINITY;
+              for (int j0 = 0; j0 < nk; j0 += 32) {
+                const int j = j0 + lane;
+                const float sc = j < nk ? qk32(kb0 + j) : -INFINITY;
+                unsigned need = __ballot_sync(0xffffffffu, j < nk && sc >= thr);
+                double val = (double)sc;
+                while (need) {
+                  const int src = __ffs(need) - 1;
+                  need &= need - 1;
+                  const int key = kb0 + j0 + src;
+                  double part = 0.0;
+#pragma unroll
+                  for (int m = 0; m < 4; ++m) part = fma(xval(key, lane + 32 * m), u[m], part);
+#pragma unroll
+                  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                  if (lane == src) val = (part + u0) * (1.0 / sqrt((double)kDH));
+                }
+                sc_own[j0 / 32] = j < nk ? val : -INFINITY;
+                Mx = fmax(Mx, sc_own[j0 / 32]);
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+              double wsum = 0.0;
+              float w_own[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const double w = sc_own[m] == -INFINITY ? 0.0 : exp(sc_own[m] - Mx);
+                w_own[m] = (float)w;
+                wsum += w;
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+              // Rewrite this row's probabilities for the keys of its sequence
+              // (keys of other sequences already hold 0).
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int j = lane + 32 * m;
+                if (j >= L) continue;
+                const int key = kb0 + j;
+                const float w = j < nk ? w_own[m] : 0.f;
+                const int kh = key >> 6, c8 = (key & 63) >> 3, e8 = key & 7;
+                const int off = sw128(rr, c8) + e8 * 2;
+                T hv, lv;
+                Split<T>::go(w, hv, lv);
+                *reinterpret_cast<T*>(pbuf + kh * kTile16 + off) = hv;
+                *reinterpret_cast<T*>(pbuf + (2 + kh) * kTile16 + off) = lv;
+              }
+              if (lane == 0) l_s[h * 128 + rr] = (float)wsum;
+              __syncwarp();
+            }
+            bar_compute();
+          }
+          arrive(B_P_READY);
+        }
+        if (!ok) break;
+        // ---- ctx = O / l -> PB (hi, lo); half h takes heads 2 half, 2 half + 1
+        if (!wait(B_O_DONE, c_o)) { ok = false; break; }
+        {
+          float o[64];
+          tmem_ld<32>(tmem + lane_addr + 64 * half, o);
+          tmem_ld<32>(tmem + lane_addr + 64 * half + 32, o + 32);
+          const float inv0 = 1.f / l_s[(2 * half) * 128 + r];
+          const float inv1 = 1.f / l_s[(2 * half + 1) * 128 + r];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] *= inv0;
+#pragma unroll
+          for (int c = 32; c < 64; ++c) o[c] *= inv1;
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), o + 8 * c8);
+        }
+        arrive(B_CTX_READY);
+        // ---- out-projection + b_o + residual, LayerNorm 1 -> y in XA
+        if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
+        auto layernorm = [&](uint32_t tcol, const float* bias, const float* g, const float* be,
+                             bool resid_lo, float* outv) {
+          float v[64];
+          tmem_ld<32>(tmem + lane_addr + tcol + 64 * half, v);
+          tmem_ld<32>(tmem + lane_addr + tcol + 64 * half + 32, v + 32);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            float x8[8];
+            get8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), resid_lo, x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[c8 * 8 + e] += x8[e] + __ldg(bias + 64 * half + c8 * 8 + e);
+          }
+          float mean = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mean += v[c];
+          mean *= (1.f / 64.f);
+          float m2v = 0.f;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
+          xch[half * 128 + r] = mean;
+          xch2[half * 128 + r] = m2v;
+          bar_compute();
+          const float om = xch[(1 - half) * 128 + r], om2 = xch2[(1 - half) * 128 + r];
+          bar_compute();
+          // Chan's merge of two 64-column halves (same order on both threads)
+          const float ma = half == 0 ? mean : om, mb = half == 0 ? om : mean;
+          const float qa = half == 0 ? m2v : om2, qb = half == 0 ? om2 : m2v;
+          const float delta = mb - ma;
+          const float mu = ma + 0.5f * delta;
+          const float var = (qa + qb + delta * delta * 32.f) * (1.f / 128.f);
+          const float rstd = rsqrtf(var + 1e-5f);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int col = 64 * half + c;
+            outv[c] = (v[c] - mu) * rstd * __ldg(g + col) + __ldg(be + col);
+          }
+        };
+        {
+          float y[64];
+          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, y);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), y + 8 * c8);
+        }
+        arrive(B_Y_READY);
+        // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB
+        for (int c = 0; c < n_chunks && ok; ++c) {
+          const int buf = c & 1;
+          if (!(buf == 0 ? wait(B_F1_DONE, c_f1_0) : wait(B_F1_DONE1, c_f1_1))) { ok = false; break; }
+          float hv[64];
+          tmem_ld<32>(tmem + lane_addr + 256 + 128 * buf + 64 * half, hv);
+          tmem_ld<32>(tmem + lane_addr + 256 + 128 * buf + 64 * half + 32, hv + 32);
+          tc_fence_before();
+          mbar_arrive(bar + (buf == 0 ? B_F1_FREE : B_F1_FREE1));
+#pragma unroll
+          for (int e = 0; e < 64; ++e) hv[e] = gelu_erf(hv[e] + __ldg(P.b_1 + 128 * c + 64 * half + e));
+          if (c > 0) {
+            // PB still feeds the previous chunk's second product
+            const uint32_t par = (uint32_t)(c_hfree & 1);
+            ++c_hfree;
+            if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), hv + 8 * c8);
+          arrive(B_H_READY);
+        }
+        if (!ok) break;
+        // ---- FFN2 + b_2 + residual y, LayerNorm 2
+        if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
+        {
+          // the last chunk's h_free completes with f2_done: keep the count in step
+          const uint32_t par = (uint32_t)(c_hfree & 1);
+          ++c_hfree;
+          if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
+          float xo[64];
+          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, xo);
+          if (l + 1 < a.n_layers) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), xo + 8 * c8);
+            arrive(B_A_READY);
+          } else if (row_valid && grow < (size_t)T_rows) {
+            T* dst = reinterpret_cast<T*>(a.out) + grow * kD + 64 * half;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              uint4 u;
+              T* up = reinterpret_cast<T*>(&u);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) up[e] = from_f32<T>(xo[c8 * 8 + e]);
+              *reinterpret_cast<uint4*>(dst + c8 * 8) = u;
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(bar + B_XA_FREE);  // the next tile's input may overwrite XA
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename T, int L>
+cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStream_t s) {
+  auto k = mega_kernel<T, L>;
+  const size_t smem = kSmemBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, s>>>(mx, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
+  return d == kD && H == kH && dff % 128 == 0 && dff >= 128 && (L == 32 || L == 64 || L == 128) &&
+         dt != TL_F32;
+}
+
+cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int num_sms, cudaStream_t s) {
+  CUtensorMap mx;
+  if (!make_tmap_2d(&mx, x, bf16, (uint64_t)a.B * L, kD, kD, 64, 128, 128)) return cudaErrorInvalidValue;
+  const int S = 128 / L;
+  const int tiles = (a.B + S - 1) / S;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  if (bf16) {
+    if (L == 32) return launch_l<__nv_bfloat16, 32>(mx, a, grid, s);
+    if (L == 64) return launch_l<__nv_bfloat16, 64>(mx, a, grid, s);
+    return launch_l<__nv_bfloat16, 128>(mx, a, grid, s);
+  }
+  if (L == 32) return launch_l<__half, 32>(mx, a, grid, s);
+  if (L == 64) return launch_l<__half, 64>(mx, a, grid, s);
+  return launch_l<__half, 128>(mx, a, grid, s);
+}
+
+}  // namespace tl

@@ -2,6 +2,9 @@
 #include "common.cuh"
 #include "internal.h"
 #include "paths.h"
+
+#include <vector>
+#include "mega.h"
 #include "tc_attention.h"
 #include "tc_gemm.h"
 
@@ -257,8 +260,44 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
 
 }  // namespace
 
-size_t packed_extra_bytes(const tl_encoder*) { return 0; }
-cudaError_t pack_extra(tl_encoder*, void*, size_t) { return cudaSuccess; }
+// Packed extras: per layer four weight tensor maps (for the megakernel's TMA
+// loads, which need them in device memory) followed by the MegaLayer array.
+size_t packed_extra_bytes(const tl_encoder* h) {
+  if (h->dtype == TL_F32 || h->d != 128) return 0;
+  return (size_t)h->n_layers * (4 * sizeof(CUtensorMap) + sizeof(MegaLayer)) + 128;
+}
+
+cudaError_t pack_extra(tl_encoder* h, void* dst, size_t bytes) {
+  if (bytes == 0) return cudaSuccess;
+  const bool bf = h->dtype == TL_BF16;
+  const int d = h->d, dff = h->dff, nl = h->n_layers;
+  char* base = (char*)(((uintptr_t)dst + 63) & ~(uintptr_t)63);
+  CUtensorMap* maps_dev = (CUtensorMap*)base;
+  MegaLayer* layers_dev = (MegaLayer*)(base + (size_t)nl * 4 * sizeof(CUtensorMap));
+  std::vector<CUtensorMap> maps(4 * (size_t)nl);
+  std::vector<MegaLayer> ml(nl);
+  for (int l = 0; l < nl; ++l) {
+    const tl_layer_dev& P = h->layers[l];
+    bool ok = make_tmap_2d(&maps[4 * l + 0], P.w_qkv, bf, 3 * d, d, d, 64, 128, 128) &&
+              make_tmap_2d(&maps[4 * l + 1], P.w_o, bf, d, d, d, 64, 128, 128) &&
+              make_tmap_2d(&maps[4 * l + 2], P.w_1, bf, dff, d, d, 64, 128, 128) &&
+              make_tmap_2d(&maps[4 * l + 3], P.w_2, bf, d, dff, dff, 64, 128, 128);
+    if (!ok) return cudaSuccess;  // the megakernel path stays unavailable
+    MegaLayer& m = ml[l];
+    m.map_qkv = maps_dev + 4 * l + 0; m.map_o = maps_dev + 4 * l + 1;
+    m.map_1 = maps_dev + 4 * l + 2; m.map_2 = maps_dev + 4 * l + 3;
+    m.w_qkv = P.w_qkv; m.b_qkv = P.b_qkv; m.b_o = P.b_o; m.ln1_g = P.ln1_g; m.ln1_b = P.ln1_b;
+    m.b_1 = P.b_1; m.b_2 = P.b_2; m.ln2_g = P.ln2_g; m.ln2_b = P.ln2_b;
+  }
+  cudaError_t e = cudaMemcpy(maps_dev, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(layers_dev, ml.data(), ml.size() * sizeof(MegaLayer), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) h->mega_layers = layers_dev;
+  return e;
+}
+
+bool mega_ok(const tl_encoder* h, int L) {
+  return h->mega_layers != nullptr && mega_supported(h->d, h->H, h->dff, L, h->dtype);
+}
 
 tl_path choose_path(const tl_encoder* h, int B, int L) {
   (void)B; (void)L;
@@ -267,10 +306,14 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
       return TL_PATH_SIMT;
     case TL_PATH_LAYERED:
       return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_AUTO;
+    case TL_PATH_MEGA:
+      return mega_ok(h, L) ? TL_PATH_MEGA : TL_PATH_AUTO;
     case TL_PATH_AUTO:
-      // The frozen plan table: 16-bit I/O runs on the tensor cores; fp32
-      // I/O keeps fp32 weights, which the 16-bit MMAs cannot hold exactly,
-      // and runs on the CUDA cores.
+      // The frozen plan table: short sequences of the d_model = 128 family
+      // stay resident in one CTA for the whole stack; other 16-bit shapes
+      // run the layered tensor-core path; fp32 I/O keeps fp32 weights, which
+      // the 16-bit MMAs cannot hold exactly, and runs on the CUDA cores.
+      if (mega_ok(h, L)) return TL_PATH_MEGA;
       return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_SIMT;
     default:
       return TL_PATH_AUTO;  // not built for this shape
@@ -280,13 +323,18 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
 size_t path_workspace_bytes(const tl_encoder* h, tl_path p, int B, int L) {
   if (p == TL_PATH_SIMT) return simt_layout(h, B, L, nullptr).bytes;
   if (p == TL_PATH_LAYERED) return layered_layout(h, B, L, nullptr).bytes;
-  return 0;
+  return 0;  // the megakernel needs no scratch memory
 }
 
 cudaError_t run_path(tl_encoder* h, tl_path p, const void* x, int B, int L, const int32_t* vl,
                      void* out, void* ws, cudaStream_t s) {
   if (p == TL_PATH_SIMT) return run_simt(h, x, B, L, vl, out, ws, s);
   if (p == TL_PATH_LAYERED) return run_layered(h, x, B, L, vl, out, ws, s);
+  if (p == TL_PATH_MEGA) {
+    MegaArgs a{(const MegaLayer*)h->mega_layers, h->n_layers, B, h->dff, vl, out, h->status};
+    KernelTimer t(h, KC_MEGA, s);
+    return mega_forward(x, a, L, h->dtype == TL_BF16, h->num_sms, s);
+  }
   return cudaErrorInvalidValue;
 }
 
