@@ -141,6 +141,32 @@ tl_status tl_encoder_get_status(tl_encoder *h, void *stream);
  * accepted. */
 tl_status tl_encoder_destroy(tl_encoder *h);
 
+/* The forward pass with no caller-supplied workspace and no allocation of
+ * any kind, for callers that cannot call cudaMalloc (or any allocating
+ * routine) where they run the forward: a host that has handed out its whole
+ * device-memory budget in advance, a plugin or real-time loop that is not
+ * allowed the implicit synchronisation an allocation may bring, code whose
+ * allocator owns every device pointer and offers no scratch.  The source
+ * pages have no counterpart; this is a property of the library, not of the
+ * method.
+ *
+ * Scratch comes from one array of TL_STATIC_SCRATCH_BYTES of device memory
+ * that the library declares statically: every GPU that loads the library
+ * holds it until the process exits.  A shape whose workspace
+ * (tl_encoder_workspace_size) exceeds it is rejected with
+ * TL_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current and caches it, so make that first call before any
+ * stream capture.  Every call on a device shares the one array and it keeps
+ * the last call's contents (the forward zeroes what it needs zeroed itself);
+ * calls that overlap on the GPU -- on two streams, or from two handles --
+ * race on it, so serialise them.  Otherwise as tl_encoder_forward (x, out,
+ * valid_len are the caller's device buffers; h must belong to the current
+ * device). */
+#define TL_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+tl_status tl_encoder_forward_static(tl_encoder *h, const void *x, int B, int L,
+                                    const int32_t *valid_len, void *out, void *stream);
+
 /* Per-kernel timing.  While enabled, forward() records a CUDA event pair
  * around each of its kernel launches on the launch stream (capacity pairs at
  * most; later launches are not timed).  tl_encoder_read_timing() synchronises

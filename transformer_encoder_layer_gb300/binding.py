@@ -37,6 +37,7 @@ SIGNATURES = {
     "tl_encoder_get_status": (_i, [_vp, _vp]),
     "tl_encoder_destroy": (_i, [_vp]),
     "tl_status_string": (ctypes.c_char_p, [_i]),
+    "tl_encoder_forward_static": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "tl_encoder_enable_timing": (_i, [_vp, _i, _i]),
     "tl_encoder_read_timing": (_i, [_vp, _i, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i)]),
     "tl_encoder_reset_timing": (_i, [_vp]),
@@ -183,6 +184,21 @@ class Encoder:
         _check(self.lib.tl_encoder_forward(self.handle, x.data_ptr(), B, L, valid_len.data_ptr(),
                                            out.data_ptr(), ws.data_ptr() if nbytes else None,
                                            ws.numel() if nbytes else 0, sp), "tl_encoder_forward")
+        if check:
+            _check(self.lib.tl_encoder_get_status(self.handle, sp), "device status")
+        return out
+
+    def forward_static(self, x, valid_len, out=None, stream=None, check: bool = True):
+        """The forward with the library's static scratch array instead of a
+        caller workspace (allocates nothing; see tl_encoder_forward_static)."""
+        torch = _torch()
+        B, L, d = x.shape
+        if out is None:
+            out = torch.empty_like(x)
+        sp = _stream_ptr(stream)
+        _check(self.lib.tl_encoder_forward_static(self.handle, x.data_ptr(), B, L,
+                                                  valid_len.data_ptr(), out.data_ptr(), sp),
+               "tl_encoder_forward_static")
         if check:
             _check(self.lib.tl_encoder_get_status(self.handle, sp), "device status")
         return out
