@@ -128,7 +128,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -379,7 +379,7 @@ def run_ours(args, shape):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -389,11 +389,15 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=64,
                     help="sequences per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (small cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from transformer_encoder_layer_gb300.inputs import SHAPES
     shape = SHAPES[args.workload]
+    if args.batch:
+        shape = shape.with_(batch=args.batch)
     if args.impl == "reference":
         run_reference(args, shape)
     else:

@@ -49,7 +49,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups: control (TMA, MMA, 2 idle), compute x 2
 constexpr int kCompute = 256;
 constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kNW = 2;  // weight ring depth
@@ -64,15 +64,18 @@ constexpr int kVB = kKB + 2 * 8192;                   // [part][khalf] 32 x 64, 
 constexpr int kWR = kVB + 4 * 4096;                   // [kNW] x 16 KB
 constexpr int kMisc = kWR + kNW * kTile16;
 // misc (floats unless noted)
-constexpr int kQn2 = kMisc;                           // [2][128] partial |q|^2
-constexpr int kKn2 = kQn2 + 2 * 128 * 4;              // [2][128] partial |k|^2
-constexpr int kXch = kKn2 + 2 * 128 * 4;              // [2][128] exchange 0
+constexpr int kQn2 = kMisc;                           // [128] |q_r|^2 of the current head
+constexpr int kXch = kQn2 + 128 * 4;                  // [2][128] exchange 0
 constexpr int kXch2 = kXch + 2 * 128 * 4;             // [2][128] exchange 1
 constexpr int kXch3 = kXch2 + 2 * 128 * 4;            // [2][128] exchange 2
 constexpr int kLs = kXch3 + 2 * 128 * 4;              // [4][128] softmax sums per head
 constexpr int kKmax = kLs + 4 * 128 * 4;              // [4] int (float bits)
-constexpr int kFlags = kKmax + 16;                    // int count + [128] row list
-constexpr int kBars = ((kFlags + 4 + 128 * 4 + 7) / 8) * 8;
+constexpr int kVec = kKmax + 16;                      // the layer's bias / LayerNorm vectors
+constexpr int kMaxDff = 512;
+// offsets (floats) inside the vector block
+constexpr int V_BQKV = 0, V_BO = 384, V_G1 = 512, V_BE1 = 640, V_B2 = 768, V_G2 = 896,
+              V_BE2 = 1024, V_B1 = 1152, V_COUNT = 1152 + kMaxDff;
+constexpr int kBars = ((kVec + V_COUNT * 4 + 7) / 8) * 8;
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
@@ -122,14 +125,27 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 columns without waiting; call tmem_wait_ld() before using any of them.
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
 template <typename T>
 __device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int off, const float* v) {
   uint4 hv, lv;
-  T* hp = reinterpret_cast<T*>(&hv);
-  T* lp = reinterpret_cast<T*>(&lv);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) Split<T>::go(v[e], hp[e], lp[e]);
+  split8(v, hv, lv, T());
   *reinterpret_cast<uint4*>(hi + off) = hv;
   *reinterpret_cast<uint4*>(lo + off) = lv;
 }
@@ -147,6 +163,114 @@ __device__ __forceinline__ void get8(const unsigned char* hi, const unsigned cha
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
   }
+}
+
+// fp64 correction of one flagged (row, head), done by one warp: recompute
+// q_i from the layer input and the weights, rescreen the row's keys with the
+// split fp32 Q/K, recompute candidate scores exactly as x_j . (W_k^T q_i) +
+// b_k . q_i, and rewrite the row's probabilities (hi, lo) and their sum.
+template <typename T, int L>
+__device__ __noinline__ void fixup_row(unsigned char* sm, const MegaArgs& a, const MegaLayer& P, int t,
+                                       int rr, int h, bool first, int lane) {
+  constexpr int S = 128 / L;
+  unsigned char* xa = sm + kXA;
+  unsigned char* pbuf = sm + kPB;
+  float* l_s = reinterpret_cast<float*>(sm + kLs);
+  int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
+            const int rs = rr / L, ri = rr % L;
+            int rvl = a.valid_len[t * S + rs];
+            rvl = rvl < 1 ? 1 : (rvl > L ? L : rvl);
+            const int nk = min(ri + 1, rvl);
+            const int kb0 = rs * L;
+            auto xval = [&](int row, int col) -> double {
+              const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
+              const int off = sw128(row, c8) + e8 * 2;
+              double v = (double)to_f32<T>(*reinterpret_cast<const T*>(xa + kh * kTile16 + off));
+              if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
+              return v;
+            };
+            const T* W = reinterpret_cast<const T*>(P.w_qkv);
+            // q_i in fp64: lane c owns dim c
+            double q64 = (double)P.b_qkv[32 * h + lane];
+            for (int tt = 0; tt < kD; ++tt)
+              q64 = fma((double)to_f32<T>(W[(size_t)(32 * h + lane) * kD + tt]), xval(rr, tt), q64);
+            // u = W_k,h^T q_i (lane owns tt = lane + 32 m), u0 = b_k,h . q_i
+            double u[4] = {0, 0, 0, 0};
+            double u0 = 0.0, qq = 0.0;
+            for (int c = 0; c < kDH; ++c) {
+              const double qc = __shfl_sync(0xffffffffu, q64, c);
+              u0 = fma(qc, (double)P.b_qkv[128 + 32 * h + c], u0);
+              qq = fma(qc, qc, qq);
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
+            }
+            auto qk32 = [&](int key) -> float {  // screening score from the split Q, K
+              float acc = 0.f;
+              for (int c = 0; c < kDH; ++c) {
+                const int off = sw64(rr, c * 2), ko = sw64(key, c * 2);
+                const float qf = to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + off)) +
+                                 to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + 8192 + off));
+                const float kf = to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + ko)) +
+                                 to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + 8192 + ko));
+                acc = fmaf(qf, kf, acc);
+              }
+              return acc * rsqrtf((float)kDH);
+            };
+            float best = -INFINITY;
+            for (int j = lane; j < nk; j += 32) best = fmaxf(best, qk32(kb0 + j));
+            best = warp_max(best);
+            const float err = neartie_err((float)sqrt(qq), __int_as_float(kmax_s[h]), kDH);
+            const float thr = best - kTieGap - 2.f * err;
+            double sc_own[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            double Mx = -INFINITY;
+            for (int j0 = 0; j0 < nk; j0 += 32) {
+              const int j = j0 + lane;
+              const float sc = j < nk ? qk32(kb0 + j) : -INFINITY;
+              unsigned need = __ballot_sync(0xffffffffu, j < nk && sc >= thr);
+              double val = (double)sc;
+              while (need) {
+                const int sl = __ffs(need) - 1;
+                need &= need - 1;
+                const int key = kb0 + j0 + sl;
+                double part = 0.0;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) part = fma(xval(key, lane + 32 * m), u[m], part);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == sl) val = (part + u0) * (1.0 / sqrt((double)kDH));
+              }
+              sc_own[j0 / 32] = j < nk ? val : -INFINITY;
+              Mx = fmax(Mx, sc_own[j0 / 32]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+            double wsum = 0.0;
+            float w_own[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const double w = sc_own[m] == -INFINITY ? 0.0 : exp(sc_own[m] - Mx);
+              w_own[m] = (float)w;
+              wsum += w;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int j = lane + 32 * m;
+              if (j >= L) continue;
+              const int key = kb0 + j;
+              const float w = j < nk ? w_own[m] : 0.f;
+              const int kh = key >> 6, c8 = (key & 63) >> 3, e8 = key & 7;
+              const int off = sw128(rr, c8) + e8 * 2;
+              T hv, lv;
+              Split<T>::go(w, hv, lv);
+              *reinterpret_cast<T*>(pbuf + kh * kTile16 + off) = hv;
+              *reinterpret_cast<T*>(pbuf + (2 + kh) * kTile16 + off) = lv;
+            }
+            if (lane == 0) l_s[h * 128 + rr] = (float)wsum;
+            __syncwarp();
+          
 }
 
 template <typename T, int L>
@@ -174,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         case B_SYNC:
           cnt = kCompute;
           break;
+        case B_S_DONE:
+          cnt = 2;  // the S commit + a release arrive of the MMA thread
+          break;
         default: break;
       }
       mbar_init(bar + i, cnt);
@@ -188,7 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   volatile int* abort = abort_flag;
   int* status = a.status;
-
+  // Register split by warpgroup: the control warpgroup (TMA, MMA, two idle
+  // warps) gives registers to the two compute warpgroups.  At launch every
+  // thread holds 168; 128 x 88 + 256 x 208 = 64512 = 384 x 168, and each
+  // SM sub-partition holds one warp of each group: (88 + 208 + 208) x 32 <= 16384.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
   if (warp == 0) {
     // ================================================================ TMA
     if (lane == 0) {
@@ -283,6 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < kH && ok; ++h, ++n_head) {
           ok = wait(B_QKVH_READY, c_qkvh) && wait(B_S_FREE, c_sfree, true);
           if (!ok) break;
+          // Release what the compute threads wrote before QKVH_READY (norms,
+          // the tile's max |k|) to whoever acquires S_DONE.
+          if (lane == 0) mbar_arrive(bar + B_S_DONE);
           if (lane == 0) {
             const uint32_t as[3] = {qb, qb, qb + 8192};
             const uint32_t bs[3] = {kb, kb + 8192, kb};
@@ -343,24 +478,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     commit(B_MMA_DONE);
     mbar_wait_bounded(bar + B_MMA_DONE, 0, status);
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ======================================================== compute warps
-    const int cw = warp - 2;               // 0..7
+    const int cw = warp - 4;               // 0..7
     const int half = cw >> 2;              // column / key half
     const int qd = warp & 3;               // TMEM lane quarter
     const int r = qd * 32 + lane;          // row in the tile
     const int sq = r / L;                  // sequence within the tile
     const int i = r % L;                   // position in the sequence
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    const uint32_t trow = tmem + lane_addr;
     float* qn2_s = reinterpret_cast<float*>(sm + kQn2);
-    float* kn2_s = reinterpret_cast<float*>(sm + kKn2);
     float* xch = reinterpret_cast<float*>(sm + kXch);
     float* xch2 = reinterpret_cast<float*>(sm + kXch2);
     float* xch3 = reinterpret_cast<float*>(sm + kXch3);
     float* l_s = reinterpret_cast<float*>(sm + kLs);
     int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
-    int* flag_cnt = reinterpret_cast<int*>(sm + kFlags);
-    int* flag_rows = flag_cnt + 1;
+    float* vec = reinterpret_cast<float*>(sm + kVec);
     unsigned char* xa = sm + kXA;
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
@@ -388,6 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++c_sync;
       mbar_wait(bar + B_SYNC, par, abort, status);
     };
+    // P row rr (keys [64 kh, 64 kh + 64)) <- 64 values (hi, lo)
+    auto put_p64 = [&](int rr, int kh, const float* p) {
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(rr, c8), p + 8 * c8);
+    };
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const int seq = t * S + sq;
       const bool row_valid = seq < a.B;
@@ -402,253 +544,174 @@ __global__ void __launch_bounds__(kThreads, 1)
         const MegaLayer& P = a.layers[l];
         const bool first = l == 0;
         if (!wait(B_QKV_DONE, c_qkv)) { ok = false; break; }
-        if (threadIdx.x == 64) {
+        // Stage this layer's vectors.  Every reader of the previous layer's
+        // values finished before the QKV product could start.
+        for (int k = threadIdx.x - 128; k < 1152 + a.dff; k += kCompute) {
+          float v;
+          if (k < 384) v = P.b_qkv[k];
+          else if (k < 512) v = P.b_o[k - 384];
+          else if (k < 640) v = P.ln1_g[k - 512];
+          else if (k < 768) v = P.ln1_b[k - 640];
+          else if (k < 896) v = P.b_2[k - 768];
+          else if (k < 1024) v = P.ln2_g[k - 896];
+          else if (k < 1152) v = P.ln2_b[k - 1024];
+          else v = P.b_1[k - 1152];
+          vec[k] = v;
+        }
+        if (threadIdx.x == 128) {
           for (int h = 0; h < kH; ++h) kmax_s[h] = 0;
         }
+        bar_compute();
         for (int h = 0; h < kH && ok; ++h) {
-          // ---- Q_h, K_h, V_h^T into shared memory as (hi, lo); columns [16 half, +16)
+          // ---- head h: half 0 writes Q_h and K_h (all 32 dims), half 1 V_h^T
           if (h > 0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
-          float qv[16], kv[16], vv[16];
-          tmem_ld<16>(tmem + lane_addr + 32 * h + 16 * half, qv);
-          tmem_ld<16>(tmem + lane_addr + 128 + 32 * h + 16 * half, kv);
-          tmem_ld<16>(tmem + lane_addr + 256 + 32 * h + 16 * half, vv);
-          float q2 = 0.f, k2 = 0.f;
+          if (half == 0) {
+            float qv[32], kv[32];
+            tmem_ld32_nw(trow + 32 * h, qv);
+            tmem_ld32_nw(trow + 128 + 32 * h, kv);
+            tmem_wait_ld();
+            float q2 = 0.f, k2 = 0.f;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = 32 * h + 16 * half + c;
-            qv[c] += __ldg(P.b_qkv + col);
-            kv[c] += __ldg(P.b_qkv + 128 + col);
-            vv[c] += __ldg(P.b_qkv + 256 + col);
-            q2 = fmaf(qv[c], qv[c], q2);
-            k2 = fmaf(kv[c], kv[c], k2);
-          }
-          qn2_s[half * 128 + r] = q2;
-          kn2_s[half * 128 + r] = k2;
+            for (int c = 0; c < 32; ++c) {
+              qv[c] += vec[V_BQKV + 32 * h + c];
+              kv[c] += vec[V_BQKV + 128 + 32 * h + c];
+              q2 = fmaf(qv[c], qv[c], q2);
+              k2 = fmaf(kv[c], kv[c], k2);
+            }
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int off = sw64(r, (2 * half + cc) * 16);
-            put8<T>(sm + kQB, sm + kQB + 8192, off, qv + 8 * cc);
-            put8<T>(sm + kKB, sm + kKB + 8192, off, kv + 8 * cc);
-          }
-          {
-            // V^T [dim][key]: this thread's key r, dims [16 half, +16)
+            for (int cc = 0; cc < 4; ++cc) {
+              const int off = sw64(r, cc * 16);
+              put8<T>(sm + kQB, sm + kQB + 8192, off, qv + 8 * cc);
+              put8<T>(sm + kKB, sm + kKB + 8192, off, kv + 8 * cc);
+            }
+            qn2_s[r] = q2;
+            const float kn = warp_max(sqrtf(k2));
+            if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
+          } else {
+            float vv[32];
+            tmem_ld32_nw(trow + 256 + 32 * h, vv);
+            tmem_wait_ld();
+            // V^T [dim][key]: this thread's key r, all 32 dims
             const int kh = r >> 6, kc = r & 63;
             unsigned char* vh = sm + kVB + kh * 4096;
             unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int dim = 16 * half + c;
-              const int off = dim * 128 + ((((kc >> 3) ^ (dim & 7))) << 4) + (kc & 7) * 2;
+            for (int c = 0; c < 32; ++c) {
+              const float v = vv[c] + vec[V_BQKV + 256 + 32 * h + c];
+              const int off = c * 128 + (((kc >> 3) ^ (c & 7)) << 4) + (kc & 7) * 2;
               T hv, lv;
-              Split<T>::go(vv[c], hv, lv);
+              Split<T>::go(v, hv, lv);
               *reinterpret_cast<T*>(vh + off) = hv;
               *reinterpret_cast<T*>(vlo + off) = lv;
             }
           }
           arrive(B_QKVH_READY);
-          // ---- softmax over this row's keys in key half `half`
+          // ---- softmax of S = Q_h K_h^T over the row's visible keys
           if (!wait(B_S_DONE, c_s)) { ok = false; break; }
-          const int k0 = 64 * half;                    // first key of my half
-          const int vis_lo = sq * L, vis_hi = sq * L + limit;
-          const bool any = (k0 < sq * L + L) && (k0 + 64 > sq * L);  // warp-uniform
+          const int k0 = 64 * half;                                 // my key half
+          const bool own = (k0 < sq * L + L) && (k0 + 64 > sq * L); // warp-uniform
           float s[64];
           float m1 = -INFINITY, m2 = -INFINITY;
-          if (any) {
-            tmem_ld<32>(tmem + lane_addr + 384 + k0, s);
-            tmem_ld<32>(tmem + lane_addr + 384 + k0 + 32, s + 32);
+          if (own) {
+            tmem_ld32_nw(trow + 384 + k0, s);
+            tmem_ld32_nw(trow + 384 + k0 + 32, s + 32);
+            tmem_wait_ld();
+          }
+          tc_fence_before();
+          mbar_arrive(bar + B_S_FREE);
+          if (own) {
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
               const int key = k0 + c;
-              float v = (key >= vis_lo && key < vis_hi) ? s[c] * scale_log2 : -INFINITY;
+              const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
               s[c] = v;
               m2 = fmaxf(m2, fminf(m1, v));
               m1 = fmaxf(m1, v);
             }
           }
-          tc_fence_before();
-          mbar_arrive(bar + B_S_FREE);
-          xch[half * 128 + r] = m1;
-          xch2[half * 128 + r] = m2;
-          bar_compute();
-          const float o1 = xch[(1 - half) * 128 + r], o2 = xch2[(1 - half) * 128 + r];
-          const float M = fmaxf(m1, o1);
-          const float M2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-          // per-key |k| of this thread's key r, maxed over the tile
-          {
-            float kn = sqrtf(kn2_s[r] + kn2_s[128 + r]);
-            kn = warp_max(kn);
-            if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
+          float M = m1, M2 = m2, lt = 0.f;
+          if (L == 128) {
+            // a row's keys span both halves: combine max and second max
+            xch[half * 128 + r] = m1;
+            xch2[half * 128 + r] = m2;
+            bar_compute();
+            const float o1 = xch[(1 - half) * 128 + r], o2 = xch2[(1 - half) * 128 + r];
+            M = fmaxf(m1, o1);
+            M2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
           }
-          float lsum = 0.f;
-          {
-            unsigned char* ph = pbuf + half * kTile16;
-            unsigned char* pl = pbuf + (2 + half) * kTile16;
+          if (own) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              s[c] = exp2f(s[c] - M);  // probabilities, in place
+              lt += s[c];
+            }
+            put_p64(r, half, s);
+          } else {
+            // keys of other sequences: probability 0
+            const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
-              float p[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                p[e] = any ? exp2f(s[c8 * 8 + e] - M) : 0.f;
-                lsum += p[e];
-              }
-              put8<T>(ph, pl, sw128(r, c8), p);
+              *reinterpret_cast<uint4*>(pbuf + half * kTile16 + sw128(r, c8)) = z;
+              *reinterpret_cast<uint4*>(pbuf + (2 + half) * kTile16 + sw128(r, c8)) = z;
             }
           }
-          xch3[half * 128 + r] = lsum;
-          bar_compute();
-          const float lt = xch3[r] + xch3[128 + r];
-          if (half == 0) l_s[h * 128 + r] = lt;
-          if (threadIdx.x == 64) *flag_cnt = 0;
-          // near-tie test (natural-log gap); half 0 decides for the row
-          const float qn = sqrtf(qn2_s[r] + qn2_s[128 + r]);
-          const float kmx = __int_as_float(kmax_s[h]);
-          bar_compute();
-          if (half == 0 && row_valid && neartie_flag((M - M2) * 0.69314718055994531f, qn, kmx, kDH)) {
-            int at = atomicAdd(flag_cnt, 1);
-            flag_rows[at] = r;
-          }
-          bar_compute();
-          const int nflag = *flag_cnt;
-          if (nflag > 0) {
-            // fp64 correction of the flagged rows' probabilities (rare).
-            for (int e = cw; e < nflag; e += 8) {
-              const int rr = flag_rows[e];
-              const int rs = rr / L, ri = rr % L;
-              int rvl = a.valid_len[t * S + rs];
-              rvl = rvl < 1 ? 1 : (rvl > L ? L : rvl);
-              const int nk = min(ri + 1, rvl);
-              const int kb0 = rs * L;
-              // x_j = the layer input (hi + lo; the first layer's input is exact in hi)
-              auto xval = [&](int row, int col) -> double {
-                const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
-                const int off = sw128(row, c8) + e8 * 2;
-                double v = (double)to_f32<T>(*reinterpret_cast<const T*>(xa + kh * kTile16 + off));
-                if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
-                return v;
-              };
-              const T* W = reinterpret_cast<const T*>(P.w_qkv);
-              // q_i (fp64), lane c owns dim c
-              double q64 = (double)P.b_qkv[32 * h + lane];
-              for (int tt = 0; tt < kD; ++tt)
-                q64 = fma((double)to_f32<T>(W[(size_t)(32 * h + lane) * kD + tt]), xval(rr, tt), q64);
-              // u = W_k,h^T q_i (lane owns tt = lane + 32 m), u0 = b_k,h . q_i
-              double u[4] = {0, 0, 0, 0};
-              double u0 = 0.0, qn2 = 0.0;
-              for (int c = 0; c < kDH; ++c) {
-                const double qc = __shfl_sync(0xffffffffu, q64, c);
-                u0 = fma(qc, (double)P.b_qkv[128 + 32 * h + c], u0);
-                qn2 = fma(qc, qc, qn2);
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                  u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
-              }
-              // screening scores (fp32 q and k from shared memory), best score
-              auto qk32 = [&](int key) -> float {
-                float acc = 0.f;
-                for (int c = 0; c < kDH; ++c) {
-                  const int off = sw64(rr, c * 2), ko = sw64(key, c * 2);
-                  const float qf = to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + off)) +
-                                   to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + 8192 + off));
-                  const float kf = to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + ko)) +
-                                   to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + 8192 + ko));
-                  acc = fmaf(qf, kf, acc);
-                }
-                return acc * rsqrtf((float)kDH);
-              };
-              float best = -INFINITY;
-              for (int j = lane; j < nk; j += 32) best = fmaxf(best, qk32(kb0 + j));
-              best = warp_max(best);
-              const float err = neartie_err((float)sqrt(qn2), kmx, kDH);
-              const float thr = best - kTieGap - 2.f * err;
-              // Scores of keys kb0 + j (lane j % 32, slot j / 32): exact in fp64
-              // for candidates (x_j . u + u0, all lanes cooperating per key),
-              // the screening fp32 value otherwise.
-              double sc_own[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-              double Mx = -INFINITY;
-              for (int j0 = 0; j0 < nk; j0 += 32) {
-                const int j = j0 + lane;
-                const float sc = j < nk ? qk32(kb0 + j) : -INFINITY;
-                unsigned need = __ballot_sync(0xffffffffu, j < nk && sc >= thr);
-                double val = (double)sc;
-                while (need) {
-                  const int src = __ffs(need) - 1;
-                  need &= need - 1;
-                  const int key = kb0 + j0 + src;
-                  double part = 0.0;
-#pragma unroll
-                  for (int m = 0; m < 4; ++m) part = fma(xval(key, lane + 32 * m), u[m], part);
-#pragma unroll
-                  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                  if (lane == src) val = (part + u0) * (1.0 / sqrt((double)kDH));
-                }
-                sc_own[j0 / 32] = j < nk ? val : -INFINITY;
-                Mx = fmax(Mx, sc_own[j0 / 32]);
-              }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-              double wsum = 0.0;
-              float w_own[4];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const double w = sc_own[m] == -INFINITY ? 0.0 : exp(sc_own[m] - Mx);
-                w_own[m] = (float)w;
-                wsum += w;
-              }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-              // Rewrite this row's probabilities for the keys of its sequence
-              // (keys of other sequences already hold 0).
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const int j = lane + 32 * m;
-                if (j >= L) continue;
-                const int key = kb0 + j;
-                const float w = j < nk ? w_own[m] : 0.f;
-                const int kh = key >> 6, c8 = (key & 63) >> 3, e8 = key & 7;
-                const int off = sw128(rr, c8) + e8 * 2;
-                T hv, lv;
-                Split<T>::go(w, hv, lv);
-                *reinterpret_cast<T*>(pbuf + kh * kTile16 + off) = hv;
-                *reinterpret_cast<T*>(pbuf + (2 + kh) * kTile16 + off) = lv;
-              }
-              if (lane == 0) l_s[h * 128 + rr] = (float)wsum;
-              __syncwarp();
-            }
+          if (L == 128) {
+            xch3[half * 128 + r] = lt;
             bar_compute();
+            lt = xch3[r] + xch3[128 + r];
+          }
+          // The row's deciding thread: its owner (L <= 64) or half 0 (L = 128).
+          const bool decider = (L == 128) ? (half == 0) : own;
+          bool flag = false;
+          if (decider) {
+            l_s[h * 128 + r] = lt;
+            const float qn = sqrtf(qn2_s[r]);
+            const float kmx = __int_as_float(kmax_s[h]);
+            flag = row_valid && neartie_flag((M - M2) * 0.69314718055994531f, qn, kmx, kDH);
+          }
+          unsigned fl = __ballot_sync(0xffffffffu, flag);
+          while (fl) {
+            // fp64 correction of this warp's flagged rows (rare)
+            const int src = __ffs(fl) - 1;
+            fl &= fl - 1;
+            fixup_row<T, L>(sm, a, P, t, qd * 32 + src, h, first, lane);
           }
           arrive(B_P_READY);
         }
         if (!ok) break;
-        // ---- ctx = O / l -> PB (hi, lo); half h takes heads 2 half, 2 half + 1
+        // ---- ctx = O / l -> PB (hi, lo); half h takes heads 2h, 2h + 1
         if (!wait(B_O_DONE, c_o)) { ok = false; break; }
         {
           float o[64];
-          tmem_ld<32>(tmem + lane_addr + 64 * half, o);
-          tmem_ld<32>(tmem + lane_addr + 64 * half + 32, o + 32);
+          tmem_ld32_nw(trow + 64 * half, o);
+          tmem_ld32_nw(trow + 64 * half + 32, o + 32);
+          tmem_wait_ld();
           const float inv0 = 1.f / l_s[(2 * half) * 128 + r];
           const float inv1 = 1.f / l_s[(2 * half + 1) * 128 + r];
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] *= inv0;
 #pragma unroll
           for (int c = 32; c < 64; ++c) o[c] *= inv1;
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), o + 8 * c8);
+          put_p64(r, half, o);
         }
         arrive(B_CTX_READY);
-        // ---- out-projection + b_o + residual, LayerNorm 1 -> y in XA
-        if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
-        auto layernorm = [&](uint32_t tcol, const float* bias, const float* g, const float* be,
-                             bool resid_lo, float* outv) {
-          float v[64];
-          tmem_ld<32>(tmem + lane_addr + tcol + 64 * half, v);
-          tmem_ld<32>(tmem + lane_addr + tcol + 64 * half + 32, v + 32);
+        // LayerNorm of acc (TMEM columns tcol + [64 half, +64)) + bias +
+        // residual (the X buffer); the two halves of a row merge their
+        // (mean, M2) with Chan's formula.
+        auto layernorm = [&](uint32_t tcol, int vb, int vg, int vbe, bool resid_lo, float* v) {
+          tmem_ld32_nw(trow + tcol + 64 * half, v);
+          tmem_ld32_nw(trow + tcol + 64 * half + 32, v + 32);
+          tmem_wait_ld();
+          const float4* b4 = reinterpret_cast<const float4*>(vec + vb + 64 * half);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8) {
             float x8[8];
             get8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), resid_lo, x8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[c8 * 8 + e] += x8[e] + __ldg(bias + 64 * half + c8 * 8 + e);
+            const float4 ba = b4[2 * c8], bb = b4[2 * c8 + 1];
+            v[c8 * 8 + 0] += x8[0] + ba.x; v[c8 * 8 + 1] += x8[1] + ba.y;
+            v[c8 * 8 + 2] += x8[2] + ba.z; v[c8 * 8 + 3] += x8[3] + ba.w;
+            v[c8 * 8 + 4] += x8[4] + bb.x; v[c8 * 8 + 5] += x8[5] + bb.y;
+            v[c8 * 8 + 6] += x8[6] + bb.z; v[c8 * 8 + 7] += x8[7] + bb.w;
           }
           float mean = 0.f;
 #pragma unroll
@@ -662,22 +725,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           bar_compute();
           const float om = xch[(1 - half) * 128 + r], om2 = xch2[(1 - half) * 128 + r];
           bar_compute();
-          // Chan's merge of two 64-column halves (same order on both threads)
           const float ma = half == 0 ? mean : om, mb = half == 0 ? om : mean;
           const float qa = half == 0 ? m2v : om2, qb = half == 0 ? om2 : m2v;
           const float delta = mb - ma;
           const float mu = ma + 0.5f * delta;
           const float var = (qa + qb + delta * delta * 32.f) * (1.f / 128.f);
           const float rstd = rsqrtf(var + 1e-5f);
+          const float4* g4 = reinterpret_cast<const float4*>(vec + vg + 64 * half);
+          const float4* e4 = reinterpret_cast<const float4*>(vec + vbe + 64 * half);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int col = 64 * half + c;
-            outv[c] = (v[c] - mu) * rstd * __ldg(g + col) + __ldg(be + col);
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 g = g4[c4], e = e4[c4];
+            v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * g.x + e.x;
+            v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * g.y + e.y;
+            v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * g.z + e.z;
+            v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * g.w + e.w;
           }
         };
+        // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
+        if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
         {
           float y[64];
-          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, y);
+          layernorm(128, V_BO, V_G1, V_BE1, !first, y);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8)
             put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), y + 8 * c8);
@@ -688,21 +757,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int buf = c & 1;
           if (!(buf == 0 ? wait(B_F1_DONE, c_f1_0) : wait(B_F1_DONE1, c_f1_1))) { ok = false; break; }
           float hv[64];
-          tmem_ld<32>(tmem + lane_addr + 256 + 128 * buf + 64 * half, hv);
-          tmem_ld<32>(tmem + lane_addr + 256 + 128 * buf + 64 * half + 32, hv + 32);
+          tmem_ld32_nw(trow + 256 + 128 * buf + 64 * half, hv);
+          tmem_ld32_nw(trow + 256 + 128 * buf + 64 * half + 32, hv + 32);
+          tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + (buf == 0 ? B_F1_FREE : B_F1_FREE1));
+          const float4* b4 = reinterpret_cast<const float4*>(vec + V_B1 + 128 * c + 64 * half);
 #pragma unroll
-          for (int e = 0; e < 64; ++e) hv[e] = gelu_erf(hv[e] + __ldg(P.b_1 + 128 * c + 64 * half + e));
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 b = b4[c4];
+            hv[4 * c4 + 0] = gelu_erf(hv[4 * c4 + 0] + b.x);
+            hv[4 * c4 + 1] = gelu_erf(hv[4 * c4 + 1] + b.y);
+            hv[4 * c4 + 2] = gelu_erf(hv[4 * c4 + 2] + b.z);
+            hv[4 * c4 + 3] = gelu_erf(hv[4 * c4 + 3] + b.w);
+          }
           if (c > 0) {
             // PB still feeds the previous chunk's second product
             const uint32_t par = (uint32_t)(c_hfree & 1);
             ++c_hfree;
             if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
           }
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), hv + 8 * c8);
+          put_p64(r, half, hv);
           arrive(B_H_READY);
         }
         if (!ok) break;
@@ -714,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++c_hfree;
           if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
           float xo[64];
-          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, xo);
+          layernorm(0, V_B2, V_G2, V_BE2, true, xo);
           if (l + 1 < a.n_layers) {
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
@@ -759,7 +834,8 @@ cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStr
 }  // namespace
 
 bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
-  return d == kD && H == kH && dff % 128 == 0 && dff >= 128 && (L == 32 || L == 64 || L == 128) &&
+  return d == kD && H == kH && dff % 128 == 0 && dff >= 128 && dff <= kMaxDff &&
+         (L == 32 || L == 64 || L == 128) &&
          dt != TL_F32;
 }
 

@@ -207,5 +207,32 @@ template <> struct Split<__nv_bfloat16> {
   }
 };
 
+// Eight fp32 values -> eight (hi, lo) 16-bit pairs packed in two uint4, with
+// paired conversions (cvt to f16x2 / bf16x2 rounds both lanes to nearest).
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo, __half) {
+  uint32_t* hp = reinterpret_cast<uint32_t*>(&hi);
+  uint32_t* lp = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2 h = __float22half2_rn(make_float2(v[2 * e], v[2 * e + 1]));
+    const float2 hf = __half22float2(h);
+    const __half2 l = __float22half2_rn(make_float2(v[2 * e] - hf.x, v[2 * e + 1] - hf.y));
+    hp[e] = *reinterpret_cast<const uint32_t*>(&h);
+    lp[e] = *reinterpret_cast<const uint32_t*>(&l);
+  }
+}
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo, __nv_bfloat16) {
+  uint32_t* hp = reinterpret_cast<uint32_t*>(&hi);
+  uint32_t* lp = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(v[2 * e], v[2 * e + 1]));
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __float22bfloat162_rn(make_float2(v[2 * e] - hf.x, v[2 * e + 1] - hf.y));
+    hp[e] = *reinterpret_cast<const uint32_t*>(&h);
+    lp[e] = *reinterpret_cast<const uint32_t*>(&l);
+  }
+}
+
 }  // namespace tc
 }  // namespace tl
