@@ -181,6 +181,12 @@ tl_status tl_encoder_reset_timing(tl_encoder *h);
 /* Name of kernel class k ("" past the last class). */
 const char *tl_kernel_class_name(int k);
 
+/* Math self-check: for n device floats x, writes the exact-erf GELU
+ * 0.5 x (1 + erff(x / sqrt 2)) to y_erf and the library's branch-free form
+ * (erf from Abramowitz & Stegun 7.1.28, |erf error| <= 3e-7) to y_fast.
+ * Enqueued on stream; no synchronisation. */
+tl_status tl_eval_gelu(const float *x, float *y_erf, float *y_fast, size_t n, void *stream);
+
 /* Static description of a status code. */
 const char *tl_status_string(tl_status s);
 

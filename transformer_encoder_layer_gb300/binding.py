@@ -42,6 +42,7 @@ SIGNATURES = {
     "tl_encoder_read_timing": (_i, [_vp, _i, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i)]),
     "tl_encoder_reset_timing": (_i, [_vp]),
     "tl_kernel_class_name": (ctypes.c_char_p, [_i]),
+    "tl_eval_gelu": (_i, [_vp, _vp, _vp, _sz, _vp]),
 }
 TL_KERNEL_CLASSES = 16
 

@@ -766,10 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const float4 b = b4[c4];
-            hv[4 * c4 + 0] = gelu_erf(hv[4 * c4 + 0] + b.x);
-            hv[4 * c4 + 1] = gelu_erf(hv[4 * c4 + 1] + b.y);
-            hv[4 * c4 + 2] = gelu_erf(hv[4 * c4 + 2] + b.z);
-            hv[4 * c4 + 3] = gelu_erf(hv[4 * c4 + 3] + b.w);
+            hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
+            hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
+            hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
+            hv[4 * c4 + 3] = gelu_as7128(hv[4 * c4 + 3] + b.w);
           }
           if (c > 0) {
             // PB still feeds the previous chunk's second product
