@@ -4,35 +4,39 @@
 // inference", section "Problem decomposition": short sequences fit in
 // shared memory, one CTA owns them across all layers).
 //
-// Shape: d_model = 128, head_dim = 32 (4 heads), d_ff a multiple of 128,
-// sequence length L in {32, 64, 128}: a tile holds 128 / L sequences, which
-// are rows [128 t, 128 t + 128) of the [B*L, d] input.  16-bit I/O (fp16 or
-// bf16); activations are carried as (hi, lo) 16-bit pairs wherever they feed
-// a tensor-core product.
+// Shape: d_model = 128, head_dim = 32 (4 heads), d_ff a multiple of 128 up
+// to 512, sequence length L in {32, 64}: a tile holds 128 / L sequences,
+// which are rows [128 t, 128 t + 128) of the [B*L, d] input.  16-bit I/O
+// (fp16 or bf16); activations are carried as (hi, lo) 16-bit pairs wherever
+// they feed a tensor-core product.
 //
-// One CTA per SM, persistent over tiles.  320 threads:
-//   warp 0      TMA: the input tile (once per tile) and 128 x 64 weight boxes
-//               from L2 into a 2-deep ring, in the order the MMAs use them
-//   warp 1      TMEM (all 512 columns); one thread issues every tcgen05.mma
-//   warps 2-9   two groups of 4 warps ("halves" h = 0, 1); both groups cover
-//               all 128 rows (TMEM lanes), half h takes columns/keys
-//               [64h, 64h + 64) of each row
+// One CTA per SM, persistent over tiles.  384 threads in three warpgroups:
+//   control  warp 0  TMA: the input tile (once per tile) and weight boxes
+//                    from L2 into a 2-deep ring, in the order the MMAs use them
+//            warp 1  TMEM (all 512 columns); one thread issues every MMA
+//            warps 2, 3 idle (they lend their registers: setmaxnreg)
+//   compute  two warpgroups ("halves" 0, 1); both cover all 128 rows (TMEM
+//            lanes); half h takes columns [64h, 64h + 64) of each row, or
+//            [32h, 32h + 32) of a 64-wide FFN chunk
 //
 // Per layer (TMEM columns in brackets):
 //   QKV   acc[0, 384) = X . W_qkv^T      X = (hi, lo) of the layer input
 //   per head h: Q_h, K_h, V_h^T -> shared memory as (hi, lo);
 //         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
-//         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32)
+//         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32).
+//         Head h+1's Q and K are written as soon as S_h is done, so only its
+//         V waits for P_h V_h.
 //   ctx = O / l -> shared memory (hi, lo)
 //   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> X buffer
-//   FFN   per 128-wide chunk c of d_ff: acc1[256 + 128 (c % 2)] = y . W_1c^T,
-//         h_c = gelu(acc1 + b_1c) -> shared memory, acc2[0, 128) += h_c . W_2c^T
-//         (chunk c + 1's first product overlaps chunk c's GELU)
+//   FFN   per 64-wide chunk c of d_ff: acc1[256 + 64 (c % 2)] = y . W_1c^T,
+//         h_c = gelu(acc1 + b_1c) -> one of two shared-memory buffers,
+//         acc2[0, 128) += h_c . W_2c^T; GELU of chunk c overlaps the two
+//         products of chunks c - 1 and c + 1
 //   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
 //
 // Near ties (see neartie.cuh) are corrected in place: a flagged (row, head)
 // has its probabilities recomputed in fp64 from the layer input and the
-// weights before the P . V product.
+// weights, by the warp that owns the row, before the P . V product.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,7 +53,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;  // 3 warpgroups: control (TMA, MMA, 2 idle), compute x 2
+constexpr int kThreads = 384;
 constexpr int kCompute = 256;
 constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kNW = 2;  // weight ring depth
@@ -57,18 +61,19 @@ constexpr int kNW = 2;  // weight ring depth
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16-bit
 constexpr int kXA = 0;                                // [part][khalf] x 16 KB = 64 KB
-constexpr int kPB = kXA + 4 * kTile16;                // [part][khalf] x 16 KB = 64 KB
+constexpr int kPB = kXA + 4 * kTile16;                // P / ctx: [part][khalf]; FFN: 2 x [part]
 constexpr int kQB = kPB + 4 * kTile16;                // [part] 128 x 32, 8 KB each
 constexpr int kKB = kQB + 2 * 8192;                   // [part] 128 x 32
 constexpr int kVB = kKB + 2 * 8192;                   // [part][khalf] 32 x 64, 4 KB each
 constexpr int kWR = kVB + 4 * 4096;                   // [kNW] x 16 KB
 constexpr int kMisc = kWR + kNW * kTile16;
 // misc (floats unless noted)
-constexpr int kQn2 = kMisc;                           // [128] |q_r|^2 of the current head
-constexpr int kXch = kQn2 + 128 * 4;                  // [2][128] exchange 0
-constexpr int kXch2 = kXch + 2 * 128 * 4;             // [2][128] exchange 1
-constexpr int kXch3 = kXch2 + 2 * 128 * 4;            // [2][128] exchange 2
-constexpr int kLs = kXch3 + 2 * 128 * 4;              // [4][128] softmax sums per head
+constexpr int kQn2 = kMisc;                           // [2][128] |q_r|^2, by head parity
+constexpr int kXA1 = kQn2 + 2 * 128 * 4;              // LayerNorm 1 exchange: mean, M2
+constexpr int kXB1 = kXA1 + 2 * 128 * 4;
+constexpr int kXA2 = kXB1 + 2 * 128 * 4;              // LayerNorm 2 exchange
+constexpr int kXB2 = kXA2 + 2 * 128 * 4;
+constexpr int kLs = kXB2 + 2 * 128 * 4;               // [4][128] softmax sums per head
 constexpr int kKmax = kLs + 4 * 128 * 4;              // [4] int (float bits)
 constexpr int kVec = kKmax + 16;                      // the layer's bias / LayerNorm vectors
 constexpr int kMaxDff = 512;
@@ -83,8 +88,8 @@ constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 enum {
   B_X_FULL = 0, B_W_FULL, B_W_FULL1, B_W_EMPTY, B_W_EMPTY1, B_A_READY, B_QKV_DONE, B_QKVH_READY,
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
-  B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_F2_DONE, B_XA_FREE, B_MMA_DONE,
-  B_SYNC, B_COUNT
+  B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
+  B_MMA_DONE, B_SYNC, B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget");
@@ -103,29 +108,7 @@ __device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
   return d;
 }
 
-
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v);
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* v) {
-  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(v));
-}
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 columns without waiting; call tmem_wait_ld() before using any of them.
+// 32 / 16 columns without waiting; call tmem_wait_ld() before using them.
 __device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
@@ -137,6 +120,16 @@ __device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float* v) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -164,113 +157,84 @@ __device__ __forceinline__ void get8(const unsigned char* hi, const unsigned cha
     for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
   }
 }
+// v[0..N) += vec[0..N), N a multiple of 4 (shared-memory float4 reads)
+template <int N>
+__device__ __forceinline__ void add_vec(float* v, const float* vec) {
+  const float4* b4 = reinterpret_cast<const float4*>(vec);
+#pragma unroll
+  for (int c = 0; c < N / 4; ++c) {
+    const float4 b = b4[c];
+    v[4 * c] += b.x; v[4 * c + 1] += b.y; v[4 * c + 2] += b.z; v[4 * c + 3] += b.w;
+  }
+}
 
-// fp64 correction of one flagged (row, head), done by one warp: recompute
-// q_i from the layer input and the weights, rescreen the row's keys with the
-// split fp32 Q/K, recompute candidate scores exactly as x_j . (W_k^T q_i) +
-// b_k . q_i, and rewrite the row's probabilities (hi, lo) and their sum.
+// fp64 correction of one flagged (row, head), done by the warp that owns
+// the row.  Keys kk = k0 + lane + 32 m (m = 0, 1) are this lane's; sc0, sc1
+// are their fp32 screening scores (natural-log units, -inf when masked).
+// Recomputes q_i in fp64 from the layer input and the weights, recomputes
+// the scores of the candidate keys (within 12 + 2E of the best) exactly as
+// x_j . (W_k^T q_i) + b_k . q_i, and returns the row's fp64 softmax weights
+// relative to the exact best score (w0, w1) and their sum (l, every lane).
 template <typename T, int L>
-__device__ __noinline__ void fixup_row(unsigned char* sm, const MegaArgs& a, const MegaLayer& P, int t,
-                                       int rr, int h, bool first, int lane) {
-  constexpr int S = 128 / L;
-  unsigned char* xa = sm + kXA;
-  unsigned char* pbuf = sm + kPB;
-  float* l_s = reinterpret_cast<float*>(sm + kLs);
-  int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
-            const int rs = rr / L, ri = rr % L;
-            int rvl = a.valid_len[t * S + rs];
-            rvl = rvl < 1 ? 1 : (rvl > L ? L : rvl);
-            const int nk = min(ri + 1, rvl);
-            const int kb0 = rs * L;
-            auto xval = [&](int row, int col) -> double {
-              const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
-              const int off = sw128(row, c8) + e8 * 2;
-              double v = (double)to_f32<T>(*reinterpret_cast<const T*>(xa + kh * kTile16 + off));
-              if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
-              return v;
-            };
-            const T* W = reinterpret_cast<const T*>(P.w_qkv);
-            // q_i in fp64: lane c owns dim c
-            double q64 = (double)P.b_qkv[32 * h + lane];
-            for (int tt = 0; tt < kD; ++tt)
-              q64 = fma((double)to_f32<T>(W[(size_t)(32 * h + lane) * kD + tt]), xval(rr, tt), q64);
-            // u = W_k,h^T q_i (lane owns tt = lane + 32 m), u0 = b_k,h . q_i
-            double u[4] = {0, 0, 0, 0};
-            double u0 = 0.0, qq = 0.0;
-            for (int c = 0; c < kDH; ++c) {
-              const double qc = __shfl_sync(0xffffffffu, q64, c);
-              u0 = fma(qc, (double)P.b_qkv[128 + 32 * h + c], u0);
-              qq = fma(qc, qc, qq);
+__device__ __noinline__ void fixup_row(const unsigned char* sm, const MegaLayer& P, int rr, int h,
+                                       bool first, int lane, int k0, float sc0, float sc1,
+                                       float kmx, float& w0, float& w1, float& l) {
+  const unsigned char* xa = sm + kXA;
+  auto xval = [&](int row, int col) -> double {
+    const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
+    const int off = sw128(row, c8) + e8 * 2;
+    double v = (double)to_f32<T>(*reinterpret_cast<const T*>(xa + kh * kTile16 + off));
+    if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
+    return v;
+  };
+  const T* W = reinterpret_cast<const T*>(P.w_qkv);
+  // q_i in fp64: lane c owns dim c
+  double q64 = (double)P.b_qkv[32 * h + lane];
+  for (int tt = 0; tt < kD; ++tt)
+    q64 = fma((double)to_f32<T>(W[(size_t)(32 * h + lane) * kD + tt]), xval(rr, tt), q64);
+  // u = W_k,h^T q_i (lane owns tt = lane + 32 m), u0 = b_k,h . q_i
+  double u[4] = {0, 0, 0, 0};
+  double u0 = 0.0, qq = 0.0;
+  for (int c = 0; c < kDH; ++c) {
+    const double qc = __shfl_sync(0xffffffffu, q64, c);
+    u0 = fma(qc, (double)P.b_qkv[128 + 32 * h + c], u0);
+    qq = fma(qc, qc, qq);
 #pragma unroll
-              for (int m = 0; m < 4; ++m)
-                u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
-            }
-            auto qk32 = [&](int key) -> float {  // screening score from the split Q, K
-              float acc = 0.f;
-              for (int c = 0; c < kDH; ++c) {
-                const int off = sw64(rr, c * 2), ko = sw64(key, c * 2);
-                const float qf = to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + off)) +
-                                 to_f32<T>(*reinterpret_cast<const T*>(sm + kQB + 8192 + off));
-                const float kf = to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + ko)) +
-                                 to_f32<T>(*reinterpret_cast<const T*>(sm + kKB + 8192 + ko));
-                acc = fmaf(qf, kf, acc);
-              }
-              return acc * rsqrtf((float)kDH);
-            };
-            float best = -INFINITY;
-            for (int j = lane; j < nk; j += 32) best = fmaxf(best, qk32(kb0 + j));
-            best = warp_max(best);
-            const float err = neartie_err((float)sqrt(qq), __int_as_float(kmax_s[h]), kDH);
-            const float thr = best - kTieGap - 2.f * err;
-            double sc_own[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            double Mx = -INFINITY;
-            for (int j0 = 0; j0 < nk; j0 += 32) {
-              const int j = j0 + lane;
-              const float sc = j < nk ? qk32(kb0 + j) : -INFINITY;
-              unsigned need = __ballot_sync(0xffffffffu, j < nk && sc >= thr);
-              double val = (double)sc;
-              while (need) {
-                const int sl = __ffs(need) - 1;
-                need &= need - 1;
-                const int key = kb0 + j0 + sl;
-                double part = 0.0;
+    for (int m = 0; m < 4; ++m)
+      u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
+  }
+  const float best = warp_max(fmaxf(sc0, sc1));
+  const float err = neartie_err((float)sqrt(qq), kmx, kDH);
+  const float thr = best - kTieGap - 2.f * err;
+  double sc[2] = {(double)sc0, (double)sc1};
+  double Mx = -INFINITY;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) part = fma(xval(key, lane + 32 * m), u[m], part);
+  for (int m = 0; m < 2; ++m) {
+    const float s32 = m == 0 ? sc0 : sc1;
+    unsigned need = __ballot_sync(0xffffffffu, s32 != -INFINITY && s32 >= thr);
+    while (need) {
+      const int src = __ffs(need) - 1;
+      need &= need - 1;
+      const int key = k0 + src + 32 * m;
+      double part = 0.0;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if (lane == sl) val = (part + u0) * (1.0 / sqrt((double)kDH));
-              }
-              sc_own[j0 / 32] = j < nk ? val : -INFINITY;
-              Mx = fmax(Mx, sc_own[j0 / 32]);
-            }
+      for (int mm = 0; mm < 4; ++mm) part = fma(xval(key, lane + 32 * mm), u[mm], part);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-            double wsum = 0.0;
-            float w_own[4];
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == src) sc[m] = (part + u0) * (1.0 / sqrt((double)kDH));
+    }
+    Mx = fmax(Mx, sc[m]);
+  }
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const double w = sc_own[m] == -INFINITY ? 0.0 : exp(sc_own[m] - Mx);
-              w_own[m] = (float)w;
-              wsum += w;
-            }
+  for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+  const double e0 = sc[0] == -INFINITY ? 0.0 : exp(sc[0] - Mx);
+  const double e1 = sc[1] == -INFINITY ? 0.0 : exp(sc[1] - Mx);
+  double ws = e0 + e1;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int j = lane + 32 * m;
-              if (j >= L) continue;
-              const int key = kb0 + j;
-              const float w = j < nk ? w_own[m] : 0.f;
-              const int kh = key >> 6, c8 = (key & 63) >> 3, e8 = key & 7;
-              const int off = sw128(rr, c8) + e8 * 2;
-              T hv, lv;
-              Split<T>::go(w, hv, lv);
-              *reinterpret_cast<T*>(pbuf + kh * kTile16 + off) = hv;
-              *reinterpret_cast<T*>(pbuf + (2 + kh) * kTile16 + off) = lv;
-            }
-            if (lane == 0) l_s[h * 128 + rr] = (float)wsum;
-            __syncwarp();
-          
+  for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+  w0 = (float)e0;
+  w1 = (float)e1;
+  l = (float)ws;
 }
 
 template <typename T, int L>
@@ -286,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int S = 128 / L;  // sequences per tile
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_tiles = (a.B + S - 1) / S;
-  const int n_chunks = a.dff / 128;
+  const int n_chunks = a.dff / 64;  // 64-wide FFN chunks
   const int T_rows = a.B * L;
 
   if (threadIdx.x == 0) {
@@ -326,11 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       long long w_it = 0, tiles_done = 0;
       bool ok = true;
-      auto wload = [&](const CUtensorMap* m, int x, int y) -> bool {
+      auto wload = [&](const CUtensorMap* m, int x, int y, uint32_t bytes) -> bool {
         const int st = (int)(w_it % kNW);
         const uint32_t ph = (uint32_t)((w_it / kNW) & 1);
         if (!mbar_wait(bar + B_W_EMPTY + st, ph ^ 1, abort, status)) return false;
-        mbar_arrive_expect_tx(bar + B_W_FULL + st, kTile16);
+        mbar_arrive_expect_tx(bar + B_W_FULL + st, bytes);
         tma_load_2d(sm + kWR + st * kTile16, m, bar + B_W_FULL + st, x, y);
         ++w_it;
         return true;
@@ -343,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int l = 0; l < a.n_layers && ok; ++l) {
           const MegaLayer& P = a.layers[l];
           for (int nb = 0; nb < 3 && ok; ++nb)
-            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb);
-          for (int kh = 0; kh < 2 && ok; ++kh) ok = ok && wload(P.map_o, 64 * kh, 0);
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16);
+          for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16);
           for (int c = 0; c <= n_chunks && ok; ++c) {
-            if (c < n_chunks)
-              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 128 * c);
-            if (c >= 1)
-              for (int kh = 0; kh < 2 && ok; ++kh) ok = ok && wload(P.map_2, 128 * (c - 1) + 64 * kh, 0);
+            if (c < n_chunks)  // W_1 rows [64c, 64c + 64): two 64 x 64 boxes
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 64 * c, kTile16 / 2);
+            if (c >= 1 && ok)  // W_2 columns [64(c-1), 64c): one 128 x 64 box
+              ok = wload(P.map_2, 64 * (c - 1), 0, kTile16);
           }
         }
       }
@@ -363,24 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================================================================ MMA
     long long w_it = 0;
-    long long n_a = 0, n_x = 0, n_head = 0, n_layer = 0;
     const uint32_t id128 = idesc_f16(128, 128, kBf);
+    const uint32_t id64 = idesc_f16(128, 64, kBf);
     const uint32_t id32 = idesc_f16(128, 32, kBf);
     bool ok = true;
     const uint32_t xa = smem_u32(sm + kXA), pb = smem_u32(sm + kPB);
     const uint32_t qb = smem_u32(sm + kQB), kb = smem_u32(sm + kKB), vb = smem_u32(sm + kVB);
-    // One 128 x 64 weight box against A (parts x 4 k16 steps) into d.
-    auto wbox = [&](uint32_t d, uint32_t a_base, int parts, bool first) -> bool {
+    // One weight box against A (one or two planes x 4 k16 steps) into d.
+    // A is a 128 x 64 tile at a_base; its lo plane is part_stride further on
+    // (part_stride 0: the hi plane only).
+    auto wbox = [&](uint32_t d, uint32_t a_base, uint32_t part_stride, uint32_t idesc, bool first) -> bool {
       const int st = (int)(w_it % kNW);
       if (!mbar_wait(bar + B_W_FULL + st, (uint32_t)((w_it / kNW) & 1), abort, status)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t w = smem_u32(sm + kWR + st * kTile16);
-        for (int p = 0; p < parts; ++p)
+        const int parts = part_stride == 0 ? 1 : 2;
+        for (int p = 0; p < parts; ++p) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(d, sdesc_sw128(a_base + p * 2 * kTile16 + k * 32), sdesc_sw128(w + k * 32), id128,
+            mma_f16(d, sdesc_sw128(a_base + p * part_stride + k * 32), sdesc_sw128(w + k * 32), idesc,
                     (first && p == 0 && k == 0) ? 0u : 1u);
+        }
         mma_commit(bar + B_W_EMPTY + st);
       }
       __syncwarp();
@@ -398,21 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return true;
     };
-    long long c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0, c_f1free0 = 0, c_f1free1 = 0,
-              c_hr = 0;
+    long long c_x = 0, c_a = 0, c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
+              c_f1free[2] = {0, 0}, c_hr = 0;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      for (int l = 0; l < a.n_layers && ok; ++l, ++n_layer) {
-        // ---- QKV
-        if (l == 0) ok = wait(B_X_FULL, n_x);
-        else ok = wait(B_A_READY, n_a);
-        const int parts = l == 0 ? 1 : 2;
+      for (int l = 0; l < a.n_layers && ok; ++l) {
+        // ---- QKV (the first layer's input is exact in its hi plane)
+        ok = l == 0 ? wait(B_X_FULL, c_x) : wait(B_A_READY, c_a);
+        const uint32_t pstride = l == 0 ? 0u : 2u * kTile16;
         for (int nb = 0; nb < 3 && ok; ++nb)
           for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, parts, kh == 0);
+            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, pstride, id128, kh == 0);
         if (!ok) break;
         commit(B_QKV_DONE);
         // ---- attention, head by head
-        for (int h = 0; h < kH && ok; ++h, ++n_head) {
+        for (int h = 0; h < kH && ok; ++h) {
           ok = wait(B_QKVH_READY, c_qkvh) && wait(B_S_FREE, c_sfree, true);
           if (!ok) break;
           // Release what the compute threads wrote before QKVH_READY (norms,
@@ -450,26 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // ---- out-projection
         ok = wait(B_CTX_READY, c_ctx);
-        for (int kh = 0; kh < 2 && ok; ++kh) ok = wbox(tmem + 128, pb + kh * kTile16, 2, kh == 0);
+        for (int kh = 0; kh < 2 && ok; ++kh)
+          ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0);
         if (!ok) break;
         commit(B_OUT_DONE);
-        // ---- FFN
+        // ---- FFN in 64-wide chunks; h_c alternates between the two halves of PB
         ok = wait(B_Y_READY, c_y);
         for (int c = 0; c <= n_chunks && ok; ++c) {
           if (c < n_chunks) {
             const int buf = c & 1;
-            ok = buf == 0 ? wait(B_F1_FREE, c_f1free0, true) : wait(B_F1_FREE1, c_f1free1, true);
+            ok = wait(B_F1_FREE + buf, c_f1free[buf], true);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox(tmem + 256 + 128 * buf, xa + kh * kTile16, 2, kh == 0);
+              ok = wbox(tmem + 256 + 64 * buf, xa + kh * kTile16, 2u * kTile16, id64, kh == 0);
             if (!ok) break;
             commit(B_F1_DONE + buf);
           }
           if (c >= 1) {
-            ok = wait(B_H_READY, c_hr);
-            for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox(tmem, pb + kh * kTile16, 2, c == 1 && kh == 0);
+            const int hb = (c - 1) & 1;
+            ok = wait(B_H_READY, c_hr) && wbox(tmem, pb + hb * 2 * kTile16, kTile16, id128, c == 1);
             if (!ok) break;
-            commit(B_H_FREE);
+            commit(B_H_FREE + hb);
           }
         }
         if (!ok) break;
@@ -488,20 +455,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = qd * 32 + lane;          // row in the tile
     const int sq = r / L;                  // sequence within the tile
     const int i = r % L;                   // position in the sequence
-    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
-    const uint32_t trow = tmem + lane_addr;
+    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     float* qn2_s = reinterpret_cast<float*>(sm + kQn2);
-    float* xch = reinterpret_cast<float*>(sm + kXch);
-    float* xch2 = reinterpret_cast<float*>(sm + kXch2);
-    float* xch3 = reinterpret_cast<float*>(sm + kXch3);
     float* l_s = reinterpret_cast<float*>(sm + kLs);
     int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
     float* vec = reinterpret_cast<float*>(sm + kVec);
     unsigned char* xa = sm + kXA;
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
-    long long c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1_0 = 0, c_f1_1 = 0, c_hfree = 0,
-              c_f2 = 0;
+    long long c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_hfree[2] = {0, 0},
+              c_f2 = 0, c_sync = 0;
     bool ok = true;
     auto wait = [&](int b, long long& n) -> bool {
       const uint32_t par = (uint32_t)(n & 1);
@@ -517,18 +480,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Barrier of the 256 compute threads on an mbarrier, so that the wait is
     // bounded like every other wait (a bar.sync could not give up).
-    long long c_sync = 0;
     auto bar_compute = [&]() {
       mbar_arrive(bar + B_SYNC);
       const uint32_t par = (uint32_t)(c_sync & 1);
       ++c_sync;
       mbar_wait(bar + B_SYNC, par, abort, status);
     };
-    // P row rr (keys [64 kh, 64 kh + 64)) <- 64 values (hi, lo)
-    auto put_p64 = [&](int rr, int kh, const float* p) {
+    // Half 0 writes Q_h (hi, lo) and |q|^2; half 1 writes K_h and the
+    // tile's max |k|.
+    auto convert_qk = [&](int h) {
+      float v[32];
+      const int col = (half == 0 ? 0 : 128) + 32 * h;
+      tmem_ld32_nw(trow + col, v);
+      tmem_wait_ld();
+      add_vec<32>(v, vec + V_BQKV + col);
+      float n2 = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(rr, c8), p + 8 * c8);
+      for (int c = 0; c < 32; ++c) n2 = fmaf(v[c], v[c], n2);
+      unsigned char* dst = sm + (half == 0 ? kQB : kKB);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) put8<T>(dst, dst + 8192, sw64(r, cc * 16), v + 8 * cc);
+      if (half == 0) {
+        qn2_s[(h & 1) * 128 + r] = n2;
+      } else {
+        const float kn = warp_max(sqrtf(n2));
+        if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
+      }
+    };
+    // V_h^T (hi, lo): this thread's key r, dims [16 half, 16 half + 16).
+    auto convert_v = [&](int h) {
+      float v[16];
+      tmem_ld16_nw(trow + 256 + 32 * h + 16 * half, v);
+      tmem_wait_ld();
+      add_vec<16>(v, vec + V_BQKV + 256 + 32 * h + 16 * half);
+      const int kh = r >> 6, kc = r & 63;
+      unsigned char* vh = sm + kVB + kh * 4096;
+      unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int dim = 16 * half + c;
+        const int off = dim * 128 + (((kc >> 3) ^ (dim & 7)) << 4) + (kc & 7) * 2;
+        T hv, lv;
+        Split<T>::go(v[c], hv, lv);
+        *reinterpret_cast<T*>(vh + off) = hv;
+        *reinterpret_cast<T*>(vlo + off) = lv;
+      }
+    };
+    // LayerNorm of acc (TMEM columns tcol + [64 half, +64)) + bias + residual
+    // (the X buffer); the two halves of a row merge their (mean, M2) with
+    // Chan's formula through an exchange pair used by this LayerNorm only.
+    auto layernorm = [&](uint32_t tcol, int vb, int vg, int vbe, bool resid_lo, float* xm, float* xq,
+                         float* v) {
+      tmem_ld32_nw(trow + tcol + 64 * half, v);
+      tmem_ld32_nw(trow + tcol + 64 * half + 32, v + 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float x8[8];
+        get8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), resid_lo, x8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[c8 * 8 + e] += x8[e];
+      }
+      add_vec<64>(v, vec + vb + 64 * half);
+      float mean = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mean += v[c];
+      mean *= (1.f / 64.f);
+      float m2v = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
+      xm[half * 128 + r] = mean;
+      xq[half * 128 + r] = m2v;
+      bar_compute();
+      const float om = xm[(1 - half) * 128 + r], om2 = xq[(1 - half) * 128 + r];
+      const float ma = half == 0 ? mean : om, mb = half == 0 ? om : mean;
+      const float qa = half == 0 ? m2v : om2, qb = half == 0 ? om2 : m2v;
+      const float delta = mb - ma;
+      const float mu = ma + 0.5f * delta;
+      const float var = (qa + qb + delta * delta * 32.f) * (1.f / 128.f);
+      const float rstd = rsqrtf(var + 1e-5f);
+      const float4* g4 = reinterpret_cast<const float4*>(vec + vg + 64 * half);
+      const float4* e4 = reinterpret_cast<const float4*>(vec + vbe + 64 * half);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 g = g4[c4], e = e4[c4];
+        v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * g.x + e.x;
+        v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * g.y + e.y;
+        v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * g.z + e.z;
+        v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * g.w + e.w;
+      }
     };
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const int seq = t * S + sq;
@@ -540,6 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int limit = min(i + 1, vl);   // visible keys of this row: [sq*L, sq*L + limit)
       const size_t grow = (size_t)t * 128 + r;
+      const int k0 = 64 * half;                                 // my key half
+      const bool own = (k0 <= sq * L) && (sq * L < k0 + 64);    // my half holds my sequence
       for (int l = 0; l < a.n_layers && ok; ++l) {
         const MegaLayer& P = a.layers[l];
         const bool first = l == 0;
@@ -562,56 +604,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < kH; ++h) kmax_s[h] = 0;
         }
         bar_compute();
+        convert_qk(0);
+        convert_v(0);
+        arrive(B_QKVH_READY);
         for (int h = 0; h < kH && ok; ++h) {
-          // ---- head h: half 0 writes Q_h and K_h (all 32 dims), half 1 V_h^T
-          if (h > 0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
-          if (half == 0) {
-            float qv[32], kv[32];
-            tmem_ld32_nw(trow + 32 * h, qv);
-            tmem_ld32_nw(trow + 128 + 32 * h, kv);
-            tmem_wait_ld();
-            float q2 = 0.f, k2 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              qv[c] += vec[V_BQKV + 32 * h + c];
-              kv[c] += vec[V_BQKV + 128 + 32 * h + c];
-              q2 = fmaf(qv[c], qv[c], q2);
-              k2 = fmaf(kv[c], kv[c], k2);
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const int off = sw64(r, cc * 16);
-              put8<T>(sm + kQB, sm + kQB + 8192, off, qv + 8 * cc);
-              put8<T>(sm + kKB, sm + kKB + 8192, off, kv + 8 * cc);
-            }
-            qn2_s[r] = q2;
-            const float kn = warp_max(sqrtf(k2));
-            if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
-          } else {
-            float vv[32];
-            tmem_ld32_nw(trow + 256 + 32 * h, vv);
-            tmem_wait_ld();
-            // V^T [dim][key]: this thread's key r, all 32 dims
-            const int kh = r >> 6, kc = r & 63;
-            unsigned char* vh = sm + kVB + kh * 4096;
-            unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float v = vv[c] + vec[V_BQKV + 256 + 32 * h + c];
-              const int off = c * 128 + (((kc >> 3) ^ (c & 7)) << 4) + (kc & 7) * 2;
-              T hv, lv;
-              Split<T>::go(v, hv, lv);
-              *reinterpret_cast<T*>(vh + off) = hv;
-              *reinterpret_cast<T*>(vlo + off) = lv;
-            }
-          }
-          arrive(B_QKVH_READY);
           // ---- softmax of S = Q_h K_h^T over the row's visible keys
           if (!wait(B_S_DONE, c_s)) { ok = false; break; }
-          const int k0 = 64 * half;                                 // my key half
-          const bool own = (k0 < sq * L + L) && (k0 + 64 > sq * L); // warp-uniform
           float s[64];
-          float m1 = -INFINITY, m2 = -INFINITY;
           if (own) {
             tmem_ld32_nw(trow + 384 + k0, s);
             tmem_ld32_nw(trow + 384 + k0 + 32, s + 32);
@@ -620,32 +619,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(bar + B_S_FREE);
           if (own) {
+            const float qn = sqrtf(qn2_s[(h & 1) * 128 + r]);
+            const float kmx = __int_as_float(kmax_s[h]);
+            // the second-best score matters only where fp32 scores can be off
+            const bool track = __any_sync(0xffffffffu, neartie_err(qn, kmx, kDH) > kTieErrMin);
+            float m1 = -INFINITY, m2 = -INFINITY;
+            if (track) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const int key = k0 + c;
-              const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
-              s[c] = v;
-              m2 = fmaxf(m2, fminf(m1, v));
-              m1 = fmaxf(m1, v);
-            }
-          }
-          float M = m1, M2 = m2, lt = 0.f;
-          if (L == 128) {
-            // a row's keys span both halves: combine max and second max
-            xch[half * 128 + r] = m1;
-            xch2[half * 128 + r] = m2;
-            bar_compute();
-            const float o1 = xch[(1 - half) * 128 + r], o2 = xch2[(1 - half) * 128 + r];
-            M = fmaxf(m1, o1);
-            M2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-          }
-          if (own) {
+              for (int c = 0; c < 64; ++c) {
+                const int key = k0 + c;
+                const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
+                s[c] = v;
+                m2 = fmaxf(m2, fminf(m1, v));
+                m1 = fmaxf(m1, v);
+              }
+            } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              s[c] = exp2f(s[c] - M);  // probabilities, in place
-              lt += s[c];
+              for (int c = 0; c < 64; ++c) {
+                const int key = k0 + c;
+                const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
+                s[c] = v;
+                m1 = fmaxf(m1, v);
+              }
             }
-            put_p64(r, half, s);
+            const bool flag = track && row_valid &&
+                              neartie_flag((m1 - m2) * 0.69314718055994531f, qn, kmx, kDH);
+            unsigned fl = __ballot_sync(0xffffffffu, flag);
+            float lt = 0.f;
+            while (fl) {
+              // fp64 correction of this warp's flagged rows (rare)
+              const int src = __ffs(fl) - 1;
+              fl &= fl - 1;
+              float sc0 = 0.f, sc1 = 0.f;
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const float v = __shfl_sync(0xffffffffu, s[c], src) * 0.69314718055994531f;
+                if (lane == (c & 31)) {
+                  if (c < 32) sc0 = v;
+                  else sc1 = v;
+                }
+              }
+              float w0, w1, lrow;
+              fixup_row<T, L>(sm, P, qd * 32 + src, h, first, lane, k0, sc0, sc1, kmx, w0, w1, lrow);
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const float w = __shfl_sync(0xffffffffu, c < 32 ? w0 : w1, c & 31);
+                if (lane == src) s[c] = w;
+              }
+              if (lane == src) lt = lrow;
+            }
+            if (!flag) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                s[c] = exp2f(s[c] - m1);  // probabilities, in place
+                lt += s[c];
+              }
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), s + 8 * c8);
+            l_s[h * 128 + r] = lt;
           } else {
             // keys of other sequences: probability 0
             const uint4 z = make_uint4(0, 0, 0, 0);
@@ -655,28 +688,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(pbuf + (2 + half) * kTile16 + sw128(r, c8)) = z;
             }
           }
-          if (L == 128) {
-            xch3[half * 128 + r] = lt;
-            bar_compute();
-            lt = xch3[r] + xch3[128 + r];
-          }
-          // The row's deciding thread: its owner (L <= 64) or half 0 (L = 128).
-          const bool decider = (L == 128) ? (half == 0) : own;
-          bool flag = false;
-          if (decider) {
-            l_s[h * 128 + r] = lt;
-            const float qn = sqrtf(qn2_s[r]);
-            const float kmx = __int_as_float(kmax_s[h]);
-            flag = row_valid && neartie_flag((M - M2) * 0.69314718055994531f, qn, kmx, kDH);
-          }
-          unsigned fl = __ballot_sync(0xffffffffu, flag);
-          while (fl) {
-            // fp64 correction of this warp's flagged rows (rare)
-            const int src = __ffs(fl) - 1;
-            fl &= fl - 1;
-            fixup_row<T, L>(sm, a, P, t, qd * 32 + src, h, first, lane);
-          }
           arrive(B_P_READY);
+          if (h + 1 < kH) {
+            // Q_{h+1}, K_{h+1} may overwrite Q_h, K_h now (S_h is done); V
+            // waits until P_h V_h has read V_h.
+            convert_qk(h + 1);
+            if (!wait(B_O_DONE, c_o)) { ok = false; break; }
+            convert_v(h + 1);
+            arrive(B_QKVH_READY);
+          }
         }
         if (!ok) break;
         // ---- ctx = O / l -> PB (hi, lo); half h takes heads 2h, 2h + 1
@@ -692,104 +712,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) o[c] *= inv0;
 #pragma unroll
           for (int c = 32; c < 64; ++c) o[c] *= inv1;
-          put_p64(r, half, o);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), o + 8 * c8);
         }
         arrive(B_CTX_READY);
-        // LayerNorm of acc (TMEM columns tcol + [64 half, +64)) + bias +
-        // residual (the X buffer); the two halves of a row merge their
-        // (mean, M2) with Chan's formula.
-        auto layernorm = [&](uint32_t tcol, int vb, int vg, int vbe, bool resid_lo, float* v) {
-          tmem_ld32_nw(trow + tcol + 64 * half, v);
-          tmem_ld32_nw(trow + tcol + 64 * half + 32, v + 32);
-          tmem_wait_ld();
-          const float4* b4 = reinterpret_cast<const float4*>(vec + vb + 64 * half);
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            float x8[8];
-            get8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), resid_lo, x8);
-            const float4 ba = b4[2 * c8], bb = b4[2 * c8 + 1];
-            v[c8 * 8 + 0] += x8[0] + ba.x; v[c8 * 8 + 1] += x8[1] + ba.y;
-            v[c8 * 8 + 2] += x8[2] + ba.z; v[c8 * 8 + 3] += x8[3] + ba.w;
-            v[c8 * 8 + 4] += x8[4] + bb.x; v[c8 * 8 + 5] += x8[5] + bb.y;
-            v[c8 * 8 + 6] += x8[6] + bb.z; v[c8 * 8 + 7] += x8[7] + bb.w;
-          }
-          float mean = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mean += v[c];
-          mean *= (1.f / 64.f);
-          float m2v = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
-          xch[half * 128 + r] = mean;
-          xch2[half * 128 + r] = m2v;
-          bar_compute();
-          const float om = xch[(1 - half) * 128 + r], om2 = xch2[(1 - half) * 128 + r];
-          bar_compute();
-          const float ma = half == 0 ? mean : om, mb = half == 0 ? om : mean;
-          const float qa = half == 0 ? m2v : om2, qb = half == 0 ? om2 : m2v;
-          const float delta = mb - ma;
-          const float mu = ma + 0.5f * delta;
-          const float var = (qa + qb + delta * delta * 32.f) * (1.f / 128.f);
-          const float rstd = rsqrtf(var + 1e-5f);
-          const float4* g4 = reinterpret_cast<const float4*>(vec + vg + 64 * half);
-          const float4* e4 = reinterpret_cast<const float4*>(vec + vbe + 64 * half);
-#pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 g = g4[c4], e = e4[c4];
-            v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * g.x + e.x;
-            v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * g.y + e.y;
-            v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * g.z + e.z;
-            v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * g.w + e.w;
-          }
-        };
         // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
         if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
         {
           float y[64];
-          layernorm(128, V_BO, V_G1, V_BE1, !first, y);
+          layernorm(128, V_BO, V_G1, V_BE1, !first, reinterpret_cast<float*>(sm + kXA1),
+                    reinterpret_cast<float*>(sm + kXB1), y);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8)
             put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), y + 8 * c8);
         }
         arrive(B_Y_READY);
-        // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB
+        // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB half (c % 2)
         for (int c = 0; c < n_chunks && ok; ++c) {
           const int buf = c & 1;
-          if (!(buf == 0 ? wait(B_F1_DONE, c_f1_0) : wait(B_F1_DONE1, c_f1_1))) { ok = false; break; }
-          float hv[64];
-          tmem_ld32_nw(trow + 256 + 128 * buf + 64 * half, hv);
-          tmem_ld32_nw(trow + 256 + 128 * buf + 64 * half + 32, hv + 32);
+          if (!wait(B_F1_DONE + buf, c_f1[buf])) { ok = false; break; }
+          float hv[32];
+          tmem_ld32_nw(trow + 256 + 64 * buf + 32 * half, hv);
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(bar + (buf == 0 ? B_F1_FREE : B_F1_FREE1));
-          const float4* b4 = reinterpret_cast<const float4*>(vec + V_B1 + 128 * c + 64 * half);
+          mbar_arrive(bar + B_F1_FREE + buf);
+          const float4* b4 = reinterpret_cast<const float4*>(vec + V_B1 + 64 * c + 32 * half);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
+          for (int c4 = 0; c4 < 8; ++c4) {
             const float4 b = b4[c4];
             hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
             hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
             hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
             hv[4 * c4 + 3] = gelu_as7128(hv[4 * c4 + 3] + b.w);
           }
-          if (c > 0) {
-            // PB still feeds the previous chunk's second product
-            const uint32_t par = (uint32_t)(c_hfree & 1);
-            ++c_hfree;
-            if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
+          if (c >= 2) {
+            // this buffer last fed the second product of chunk c - 2
+            if (!wait(B_H_FREE + buf, c_hfree[buf])) { ok = false; break; }
           }
-          put_p64(r, half, hv);
+          unsigned char* hb = pbuf + buf * 2 * kTile16;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) put8<T>(hb, hb + kTile16, sw128(r, 4 * half + c8), hv + 8 * c8);
           arrive(B_H_READY);
         }
         if (!ok) break;
         // ---- FFN2 + b_2 + residual y, LayerNorm 2
         if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
+        // The last two chunks' buffer releases complete with f2_done: keep
+        // the per-buffer counts in step.
+        for (int c = (n_chunks >= 2 ? n_chunks - 2 : 0); c < n_chunks && ok; ++c)
+          ok = wait(B_H_FREE + (c & 1), c_hfree[c & 1]);
+        if (!ok) break;
         {
-          // the last chunk's h_free completes with f2_done: keep the count in step
-          const uint32_t par = (uint32_t)(c_hfree & 1);
-          ++c_hfree;
-          if (!mbar_wait(bar + B_H_FREE, par, abort, status)) { ok = false; break; }
           float xo[64];
-          layernorm(0, V_B2, V_G2, V_BE2, true, xo);
+          layernorm(0, V_B2, V_G2, V_BE2, true, reinterpret_cast<float*>(sm + kXA2),
+                    reinterpret_cast<float*>(sm + kXB2), xo);
           if (l + 1 < a.n_layers) {
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
@@ -835,8 +812,7 @@ cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStr
 
 bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
   return d == kD && H == kH && dff % 128 == 0 && dff >= 128 && dff <= kMaxDff &&
-         (L == 32 || L == 64 || L == 128) &&
-         dt != TL_F32;
+         (L == 32 || L == 64) && dt != TL_F32;
 }
 
 cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int num_sms, cudaStream_t s) {
@@ -847,12 +823,10 @@ cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (bf16) {
     if (L == 32) return launch_l<__nv_bfloat16, 32>(mx, a, grid, s);
-    if (L == 64) return launch_l<__nv_bfloat16, 64>(mx, a, grid, s);
-    return launch_l<__nv_bfloat16, 128>(mx, a, grid, s);
+    return launch_l<__nv_bfloat16, 64>(mx, a, grid, s);
   }
   if (L == 32) return launch_l<__half, 32>(mx, a, grid, s);
-  if (L == 64) return launch_l<__half, 64>(mx, a, grid, s);
-  return launch_l<__half, 128>(mx, a, grid, s);
+  return launch_l<__half, 64>(mx, a, grid, s);
 }
 
 }  // namespace tl
