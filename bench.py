@@ -92,6 +92,7 @@ def kernel_work(cls, shape, counts):
         "tc_gemm_out_ln": ("tensor", pl["out"]), "tc_gemm_ffn1": ("tensor", pl["ffn1"]),
         "tc_gemm_ffn2_ln": ("tensor", pl["ffn2"]),
         "megakernel": ("tensor", counts["flops"]),
+        "dag": ("alu", counts["flops"]),
     }
     return table.get(cls)
 
@@ -351,7 +352,7 @@ def run_ours(args, shape):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if path == "simt" else shape.dtype, "data": "synthetic",
+        "dtype": "f32" if path in ("simt", "dag") else shape.dtype, "data": "synthetic",
         "config": {"workload": shape.name, "n_layers": shape.n_layers, "d_model": shape.d_model,
                    "n_heads": shape.n_heads, "d_ff": shape.d_ff, "batch_per_gpu": shape.batch,
                    "global_batch": ws * shape.batch, "seq_len": shape.seq_len,
@@ -383,7 +384,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--path", default="auto", choices=["auto", "simt", "layered", "mega"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "layered", "mega", "dag"])
     ap.add_argument("--cpu-seqs", type=int, default=1024,
                     help="sequences in the bounded CPU-oracle sample")
     ap.add_argument("--ref-seqs", type=int, default=64,

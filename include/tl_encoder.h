@@ -64,12 +64,18 @@ typedef enum {
  *   LAYERED   tcgen05/TMEM GEMMs fed by TMA with fused epilogues, plus the
  *             flash-attention kernel; one launch per step per layer
  *   MEGA      sequence-resident megakernel: every layer of a 128-row tile of
- *             whole sequences in one CTA, activations kept on chip          */
+ *             whole sequences in one CTA, activations kept on chip
+ *   DAG       persistent task-graph megakernel for fp32 I/O and few tokens:
+ *             one launch per forward; CTAs pop (layer, step, row block, tile)
+ *             tasks from a queue and wait on per-row-block counters
+ *             ("Hyper-optimized megakernel-hybrid transformer inference",
+ *             section "Problem decomposition")                              */
 typedef enum {
   TL_PATH_AUTO = 0,
   TL_PATH_SIMT = 1,
   TL_PATH_LAYERED = 2,
-  TL_PATH_MEGA = 3
+  TL_PATH_MEGA = 3,
+  TL_PATH_DAG = 4
 } tl_path;
 
 typedef struct tl_encoder tl_encoder; /* opaque handle */

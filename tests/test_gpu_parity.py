@@ -33,7 +33,7 @@ def _paths_for(shape):
     enc = binding.Encoder(make_inputs(shape.with_(batch=1, seq_len=1, vl_lo=1, vl_hi=1)).layers,
                           shape.d_model, shape.n_heads, shape.d_ff, shape.dtype)
     out = []
-    for p in ("simt", "layered", "mega"):
+    for p in ("simt", "layered", "mega", "dag"):
         enc.set_path(p)
         try:
             enc.plan(shape.batch, shape.seq_len)
@@ -240,3 +240,66 @@ def test_mega_matches_layered_closely():
     a = _run(inp, "mega")
     b = _run(inp, "layered")
     assert np.max(np.abs(a - b)) < 2e-3
+
+
+# ------------------------------------------------------ task-graph path
+@pytest.mark.parametrize("d,H,dff,n_layers,batch,L,vl_lo", [
+    (256, 8, 1024, 2, 1, 512, 384),   # the batch-1 d256 workload's layer
+    (32, 2, 128, 2, 4, 32, 16),       # the d32 workload: two sequences per row block
+    (64, 1, 256, 3, 3, 100, 1),       # head_dim 64, ragged row blocks
+    (80, 5, 320, 2, 2, 70, 5),        # ragged column tiles and K chunks
+    (1024, 16, 512, 1, 1, 96, 60),    # split-K out-projection (4 chunks)
+    (128, 8, 512, 8, 2, 33, 1),       # eight layers
+])
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_dag_shapes(d, H, dff, n_layers, batch, L, vl_lo, scale):
+    s = tiny_shape(dtype="f32", batch=batch, seq_len=L, vl_lo=vl_lo, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=dff, n_layers=n_layers)
+    assert "dag" in _paths_for(s)
+    _check(make_inputs(s, seed=7, input_scale=scale), "dag")
+
+
+def test_dag_is_auto_for_fp32_small_batches():
+    from transformer_encoder_layer_gb300 import binding
+    for name in ("batch1_d256_L512", "tiny_d32_L32"):
+        s = SHAPES[name]
+        inp = make_inputs(s.with_(batch=1, seq_len=1, vl_lo=1, vl_hi=1))
+        enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+        assert enc.plan(s.batch, s.seq_len) == "dag"
+        assert enc.plan(64, 1024) == "simt"  # 65536 tokens: layer by layer
+        enc.close()
+
+
+def test_dag_deterministic_and_matches_simt():
+    s = SHAPES["batch1_d256_L512"]
+    inp = make_inputs(s, seed=11)
+    a = _run(inp, "dag")
+    b = _run(inp, "dag")
+    assert np.array_equal(a, b)  # no atomics in the arithmetic
+    c = _run(inp, "simt")
+    assert np.max(np.abs(a - c)) < 1e-3
+
+
+def test_dag_stalled_dependency_times_out(monkeypatch):
+    # The first task waits on a counter target no task reaches: the bounded
+    # wait gives up, every CTA drains the queue, and the status word reports
+    # the timeout.  The context stays usable for the next forward.
+    from transformer_encoder_layer_gb300 import binding
+    s = SHAPES["batch1_d256_L512"]
+    inp = make_inputs(s, seed=0)
+    x = torch.from_numpy(to_storage(inp.x, "f32")).cuda()
+    vl = torch.from_numpy(inp.valid_len.astype(np.int32)).cuda()
+    monkeypatch.setenv("TL_DAG_INJECT_STALL", "1")
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    monkeypatch.delenv("TL_DAG_INJECT_STALL")
+    assert enc.plan(1, s.seq_len) == "dag"
+    enc.forward(x, vl, check=False)
+    torch.cuda.synchronize()
+    assert enc.get_status() == 7  # TL_ERR_DEVICE_TIMEOUT
+    enc.close()
+    good = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    out = good.forward(x, vl)
+    ref = oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, s.n_heads)
+    ok, util, where = gate(out.cpu().numpy().astype(np.float64), ref)
+    assert ok, f"after timeout: envelope {util:.3f} at {where}"
+    good.close()

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libtl_encoder.so")
 
 TL_F32, TL_F16, TL_BF16 = 0, 1, 2
 DTYPE_CODES = {"f32": TL_F32, "f16": TL_F16, "bf16": TL_BF16}
-PATHS = {"auto": 0, "simt": 1, "layered": 2, "mega": 3}
+PATHS = {"auto": 0, "simt": 1, "layered": 2, "mega": 3, "dag": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 STATUS = {0: "TL_OK", 1: "TL_ERR_INVALID_ARG", 2: "TL_ERR_UNSUPPORTED_SHAPE", 3: "TL_ERR_CUDA",
           4: "TL_ERR_OUT_OF_MEMORY", 5: "TL_ERR_WORKSPACE_TOO_SMALL", 6: "TL_ERR_BAD_VALID_LEN",

@@ -127,6 +127,10 @@ tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d
   h->dtype = dtype;
   // Debug switch: CUDA-core attention inside the layered path (cross-checks).
   if (const char* e = getenv("TL_SIMT_ATTENTION")) h->simt_attention = e[0] == '1';
+  // Test hook for the bounded waits of the task-graph path: its first task
+  // waits on a counter target no task reaches, so the forward must end with
+  // TL_ERR_DEVICE_TIMEOUT after the wait's deadline.
+  if (const char* e = getenv("TL_DAG_INJECT_STALL")) h->dag_inject_stall = e[0] == '1';
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     delete h;
@@ -202,7 +206,7 @@ tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d
 }
 
 tl_status tl_encoder_set_path(tl_encoder* h, tl_path path) {
-  if (!h || path < TL_PATH_AUTO || path > TL_PATH_MEGA) return TL_ERR_INVALID_ARG;
+  if (!h || path < TL_PATH_AUTO || path > TL_PATH_DAG) return TL_ERR_INVALID_ARG;
   h->path = path;
   return TL_OK;
 }

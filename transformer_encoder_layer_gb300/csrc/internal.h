@@ -28,7 +28,7 @@ struct tl_layer_dev {
 enum tl_kernel_class {
   KC_SIMT_GEMM_QKV = 0, KC_SIMT_ATTENTION, KC_SIMT_GEMM_OUT, KC_SIMT_LAYERNORM,
   KC_SIMT_GEMM_FFN1, KC_SIMT_GEMM_FFN2, KC_TC_GEMM_QKV, KC_TC_ATTENTION,
-  KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX,
+  KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX, KC_DAG,
   KC_COUNT
 };
 
@@ -39,6 +39,7 @@ struct tl_encoder {
   tl_dtype dtype = TL_F32;
   tl_path path = TL_PATH_AUTO;
   bool simt_attention = false;  // layered path: CUDA-core attention instead of tcgen05
+  bool dag_inject_stall = false;  // task-graph path: make the first wait time out (tests)
   int device = 0;
   int num_sms = 0;
   void* wbuf = nullptr;      // one allocation holding every packed parameter

@@ -3,7 +3,9 @@
 #include "internal.h"
 #include "paths.h"
 
+#include <algorithm>
 #include <vector>
+#include "dag.h"
 #include "mega.h"
 #include "tc_attention.h"
 #include "tc_gemm.h"
@@ -258,6 +260,63 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
   return e;
 }
 
+
+// ------------------------------------------------------------------- DAG
+// fp32 workspace of the task-graph kernel; the counters come first so one
+// small memset per forward resets them.
+struct DagWs {
+  int* cnt;
+  float *xs0, *xs1, *q, *k, *v, *ctx, *y, *hb, *part;
+  int RB;
+  size_t cnt_bytes, bytes;
+};
+
+DagWs dag_layout(const tl_encoder* h, int B, int L, void* base) {
+  const size_t T = (size_t)B * L, d = h->d;
+  DagWs w;
+  w.RB = (int)((T + kDagRows - 1) / kDagRows);
+  const int kc_max = (int)((std::max(h->d, h->dff) + kDagKChunk - 1) / kDagKChunk);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align256(off + bytes); return at; };
+  char* b = (char*)base;
+  w.cnt_bytes = (size_t)dag_counter_ints(h->n_layers, w.RB) * 4;
+  size_t oc = take(w.cnt_bytes);
+  size_t o[10];
+  for (int i = 0; i < 8; ++i) o[i] = take(T * d * 4);  // xs0 xs1 q k v ctx y (+1 spare slot)
+  o[8] = take(T * h->dff * 4);
+  o[9] = take((size_t)kc_max * T * d * 4);
+  w.cnt = (int*)(b + oc);
+  w.xs0 = (float*)(b + o[0]); w.xs1 = (float*)(b + o[1]); w.q = (float*)(b + o[2]);
+  w.k = (float*)(b + o[3]); w.v = (float*)(b + o[4]); w.ctx = (float*)(b + o[5]);
+  w.y = (float*)(b + o[6]); w.hb = (float*)(b + o[8]); w.part = (float*)(b + o[9]);
+  w.bytes = off;
+  return w;
+}
+
+bool dag_ok(const tl_encoder* h) { return dag_supported(h->d, h->H, h->dff, h->n_layers, h->dtype); }
+
+cudaError_t run_dag(tl_encoder* h, const void* x, int B, int L, const int32_t* vl, void* out,
+                    void* ws, cudaStream_t s) {
+  DagWs w = dag_layout(h, B, L, ws);
+  DagArgs a{};
+  for (int l = 0; l < h->n_layers; ++l) a.layers[l] = h->layers[l];
+  a.n_layers = h->n_layers;
+  a.x = (const float*)x; a.out = (float*)out; a.vl = vl;
+  a.xs0 = w.xs0; a.xs1 = w.xs1; a.q = w.q; a.k = w.k; a.v = w.v; a.ctx = w.ctx; a.y = w.y;
+  a.hb = w.hb; a.part = w.part;
+  a.cnt = w.cnt;
+  const int nc = dag_counter_ints(h->n_layers, w.RB);
+  a.head = w.cnt + nc - 2;
+  a.abort = w.cnt + nc - 1;
+  a.status = h->status;
+  a.B = B; a.L = L; a.T = B * L; a.RB = w.RB; a.d = h->d; a.H = h->H; a.dh = h->dh; a.dff = h->dff;
+  a.inject_stall = h->dag_inject_stall ? 1 : 0;
+  cudaError_t e = cudaMemsetAsync(w.cnt, 0, w.cnt_bytes, s);
+  if (e != cudaSuccess) return e;
+  KernelTimer t(h, KC_DAG, s);
+  return dag_forward(a, h->num_sms, s);
+}
+
 }  // namespace
 
 // Packed extras: per layer four weight tensor maps (for the megakernel's TMA
@@ -308,12 +367,17 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
       return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_AUTO;
     case TL_PATH_MEGA:
       return mega_ok(h, L) ? TL_PATH_MEGA : TL_PATH_AUTO;
+    case TL_PATH_DAG:
+      return dag_ok(h) ? TL_PATH_DAG : TL_PATH_AUTO;
     case TL_PATH_AUTO:
       // The frozen plan table: short sequences of the d_model = 128 family
       // stay resident in one CTA for the whole stack; other 16-bit shapes
       // run the layered tensor-core path; fp32 I/O keeps fp32 weights, which
-      // the 16-bit MMAs cannot hold exactly, and runs on the CUDA cores.
+      // the 16-bit MMAs cannot hold exactly, and runs on the CUDA cores: in
+      // one task-graph launch while the tokens fill a few waves of 64-row
+      // tiles, else layer by layer.
       if (mega_ok(h, L)) return TL_PATH_MEGA;
+      if (dag_ok(h) && (long long)B * L <= kDagAutoMaxTokens) return TL_PATH_DAG;
       return layered_supported(h) ? TL_PATH_LAYERED : TL_PATH_SIMT;
     default:
       return TL_PATH_AUTO;  // not built for this shape
@@ -323,6 +387,7 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
 size_t path_workspace_bytes(const tl_encoder* h, tl_path p, int B, int L) {
   if (p == TL_PATH_SIMT) return simt_layout(h, B, L, nullptr).bytes;
   if (p == TL_PATH_LAYERED) return layered_layout(h, B, L, nullptr).bytes;
+  if (p == TL_PATH_DAG) return dag_layout(h, B, L, nullptr).bytes;
   return 0;  // the megakernel needs no scratch memory
 }
 
@@ -330,6 +395,7 @@ cudaError_t run_path(tl_encoder* h, tl_path p, const void* x, int B, int L, cons
                      void* out, void* ws, cudaStream_t s) {
   if (p == TL_PATH_SIMT) return run_simt(h, x, B, L, vl, out, ws, s);
   if (p == TL_PATH_LAYERED) return run_layered(h, x, B, L, vl, out, ws, s);
+  if (p == TL_PATH_DAG) return run_dag(h, x, B, L, vl, out, ws, s);
   if (p == TL_PATH_MEGA) {
     MegaArgs a{(const MegaLayer*)h->mega_layers, h->n_layers, B, h->dff, vl, out, h->status};
     KernelTimer t(h, KC_MEGA, s);
