@@ -7,28 +7,34 @@
 // The graph is a pure function of the shape, so nothing is uploaded: task t
 // decodes to (layer, kind, row block, tile).  Per layer, in queue order (a
 // topological order of the graph):
-//   QKV (rb, n)      64 x 64 tile of x W_qkv^T + b_qkv, scattered head-major
-//   ATT (rb, h)      attention of the block's 64 query rows for head h;
-//                    row blocks are queued last-first, the longest first
-//   OUT (rb, n, kc)  64 x 64 tile of ctx W_o^T over one 256-wide K chunk;
-//                    chunk 0 also adds b_o and the residual
-//   LN1 (rb)         y = LayerNorm1(sum of the OUT chunks), rows of rb
-//   F1  (rb, n)      64 x 64 tile of gelu(y W_1^T + b_1)
-//   F2  (rb, n, kc)  64 x 64 tile of h W_2^T over one K chunk; chunk 0 also
-//                    adds b_2 and y
-//   LN2 (rb)         x' = LayerNorm2(sum of the F2 chunks): the next layer's
-//                    input, or the output
+//   QKV (rb, n)         64 x 64 tile of x W_qkv^T + b_qkv, scattered head-major
+//   ATT (rb, half, h)   attention of 32 query rows for head h; row blocks are
+//                       queued last-first, the longest first
+//   OUT (rb, n, kc)     64 x 64 tile of ctx W_o^T over one 256-wide K chunk;
+//                       chunk 0 also adds b_o and the residual
+//   F1  (rb, n)         64 x 64 tile of gelu(y W_1^T + b_1)
+//   F2  (rb, n, kc)     64 x 64 tile of h W_2^T over one K chunk; chunk 0 also
+//                       adds b_2 and y
+// The two LayerNorms are not queued: the OUT (F2) task that completes a row
+// block last sums its K-chunk partials in a fixed order and normalises the
+// block's rows (y, or the next layer's input / the output).
+//
 // A task waits (bounded) on the completion counters of what it reads, then
-// bumps its own.  It only ever waits on tasks earlier in the queue, each of
-// which a running CTA has already taken, so the graph cannot deadlock, with
-// any number of resident CTAs.  A QKV task of layer l also waits for every
-// layer l-1 attention task that reads keys of its rows, so the single Q/K/V,
-// ctx and activation buffers are never overwritten under a reader.
+// bumps its own.  It only ever waits on tasks earlier in the queue, so the
+// lowest unfinished task is always running with its inputs ready: no
+// deadlock, with any number of resident CTAs, also while each CTA holds the
+// index of its next task (popped early to hide the atomic's latency).  A QKV
+// task of layer l also waits for every layer l-1 attention task that reads
+// keys of its rows, so the single Q/K/V, ctx and activation buffers are
+// never overwritten under a reader.
 //
 // The path serves fp32 I/O, whose weights no 16-bit tensor-core operand
 // holds exactly: its arithmetic is fp32 on the CUDA cores, tiles staged in
-// shared memory with cp.async.  The attention keeps the near-tie test and
-// corrects flagged rows in fp64 inside the same task.
+// shared memory with cp.async.  Each CTA runs a handful of tasks of
+// different kinds per forward, so the code is kept compact (instruction
+// fetch of cold, heavily unrolled code dominated the first version).  The
+// attention keeps the near-tie test and corrects flagged rows in fp64 inside
+// the same task.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -41,14 +47,18 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int R = kDagRows;
+constexpr int kAttRows = 32;  // query rows of one attention task
 constexpr long long kWait = 4000000000LL;  // ~2 s of SM cycles per dependency wait
 enum { K_QKV = 0, K_ATT, K_OUT, K_LN1, K_F1, K_F2, K_LN2, K_KINDS };
+// Queue order within a layer: QKV, ATT, OUT, F1, F2 (the LayerNorms are not queued).
+__host__ __device__ constexpr int queued_kind(int q) { return q < 3 ? q : q + 1; }
 
 // Tasks of one layer, per kind.
 struct Plan {
   int nt3, ntd, ntf;  // 64-wide column tiles of 3d, d and d_ff
   int kco, kcf;       // K chunks of the out-projection (K = d) and FFN2 (K = d_ff)
-  int n[K_KINDS];
+  int n[K_KINDS];     // queued tasks per kind (0 for the LayerNorms)
+  int target[K_KINDS];  // completions per row block
   int per_layer;
 };
 
@@ -59,15 +69,18 @@ __host__ __device__ inline Plan make_plan(int RB, int H, int d, int dff) {
   p.ntf = (dff + 63) / 64;
   p.kco = (d + kDagKChunk - 1) / kDagKChunk;
   p.kcf = (dff + kDagKChunk - 1) / kDagKChunk;
-  p.n[K_QKV] = RB * p.nt3;
-  p.n[K_ATT] = RB * H;
-  p.n[K_OUT] = RB * p.ntd * p.kco;
-  p.n[K_LN1] = RB;
-  p.n[K_F1] = RB * p.ntf;
-  p.n[K_F2] = RB * p.ntd * p.kcf;
-  p.n[K_LN2] = RB;
+  p.target[K_QKV] = p.nt3;
+  p.target[K_ATT] = (R / kAttRows) * H;
+  p.target[K_OUT] = p.ntd * p.kco;
+  p.target[K_LN1] = 1;
+  p.target[K_F1] = p.ntf;
+  p.target[K_F2] = p.ntd * p.kcf;
+  p.target[K_LN2] = 1;
   p.per_layer = 0;
-  for (int k = 0; k < K_KINDS; ++k) p.per_layer += p.n[k];
+  for (int k = 0; k < K_KINDS; ++k) {
+    p.n[k] = (k == K_LN1 || k == K_LN2) ? 0 : RB * p.target[k];
+    p.per_layer += p.n[k];
+  }
   return p;
 }
 
@@ -93,15 +106,33 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Wait until at most n of this thread's cp.async groups are pending.
+__device__ __forceinline__ void cp_wait_n(int n) {
+  switch (n) {
+    case 0: cp_wait<0>(); break;
+    case 1: cp_wait<1>(); break;
+    case 2: cp_wait<2>(); break;
+    case 3: cp_wait<3>(); break;
+    case 4: cp_wait<4>(); break;
+    case 5: cp_wait<5>(); break;
+    case 6: cp_wait<6>(); break;
+    default: cp_wait<7>(); break;
+  }
+}
+
 // ------------------------------------------------------------------ GEMM
+// A whole K chunk (<= 256) of both operands is staged at once, one cp.async
+// group per 32-wide slab, so the copies of every slab are in flight together
+// and compute on slab s overlaps the arrival of the later ones.
+constexpr int kGemmLd = kDagKChunk + 4;  // row stride in floats (16-byte multiple, 4-bank skew)
 struct GemmSmem {
-  float a[2][R][36];  // [stage][row][k], 32-wide K slabs, rows padded to 144 B
-  float w[2][64][36];
+  float a[R][kGemmLd];
+  float w[64][kGemmLd];
 };
 
-// acc = A[m0.., k0..k1) . W[n0.., k0..k1)^T for a 64 x 64 tile.  Thread
-// (ty, tx) = (tid / 16, tid % 16) owns rows ty + 16 i and columns tx + 16 j.
-// K (lda, ldw and k1) must be a multiple of 4.
+// acc = A[m0.., k0..k1) . W[n0.., k0..k1)^T for a 64 x 64 tile, in K chunks
+// of 256.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows ty + 16 i and
+// columns tx + 16 j.  K (lda, ldw and k1) must be a multiple of 4.
 __device__ __forceinline__ void gemm_tile(const float* A, int lda, const float* W, int ldw, int M,
                                           int N, int k0, int k1, int m0, int n0,
                                           float (&acc)[4][4], GemmSmem& sm) {
@@ -110,108 +141,145 @@ __device__ __forceinline__ void gemm_tile(const float* A, int lda, const float* 
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  const int nslab = (k1 - k0 + 31) / 32;
-  auto issue = [&](int s) {
-    const int st = s & 1, kb = k0 + s * 32;
+  for (int kb = k0; kb < k1; kb += kDagKChunk) {
+    const int ke = min(k1, kb + kDagKChunk);
+    const int nslab = (ke - kb + 31) / 32;  // <= 8
+    for (int s = 0; s < nslab; ++s) {
 #pragma unroll
-    for (int c = tid; c < R * 8; c += kThreads) {
-      const int row = c / 8, kc = (c % 8) * 4, k = kb + kc;
-      const bool kin = k < k1;
-      const bool pa = kin && m0 + row < M, pw = kin && n0 + row < N;
-      cp16(&sm.a[st][row][kc], pa ? A + (size_t)(m0 + row) * lda + k : A, pa);
-      cp16(&sm.w[st][row][kc], pw ? W + (size_t)(n0 + row) * ldw + k : W, pw);
+      for (int c = tid; c < R * 8; c += kThreads) {
+        const int row = c / 8, kl = s * 32 + (c % 8) * 4, k = kb + kl;
+        const bool kin = k < ke;
+        const bool pa = kin && m0 + row < M, pw = kin && n0 + row < N;
+        cp16(&sm.a[row][kl], pa ? A + (size_t)(m0 + row) * lda + k : A, pa);
+        cp16(&sm.w[row][kl], pw ? W + (size_t)(n0 + row) * ldw + k : W, pw);
+      }
+      cp_commit();
     }
-    cp_commit();
-  };
-  issue(0);
-  for (int s = 0; s < nslab; ++s) {
-    if (s + 1 < nslab) {
-      issue(s + 1);
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
+    for (int s = 0; s < nslab; ++s) {
+      cp_wait_n(nslab - 1 - s);
+      __syncthreads();
+#pragma unroll 2
+      for (int kk = s * 32; kk < s * 32 + 32; kk += 4) {
+        float4 av[4], wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4*>(&sm.a[ty + 16 * i][kk]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j] = *reinterpret_cast<const float4*>(&sm.w[tx + 16 * j][kk]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[i][j] = fmaf(av[i].x, wv[j].x, acc[i][j]);
+            acc[i][j] = fmaf(av[i].y, wv[j].y, acc[i][j]);
+            acc[i][j] = fmaf(av[i].z, wv[j].z, acc[i][j]);
+            acc[i][j] = fmaf(av[i].w, wv[j].w, acc[i][j]);
+          }
+      }
     }
-    __syncthreads();
-    const int st = s & 1;
-#pragma unroll
-    for (int kk = 0; kk < 32; kk += 4) {
-      float4 av[4], wv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4*>(&sm.a[st][ty + 16 * i][kk]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wv[j] = *reinterpret_cast<const float4*>(&sm.w[st][tx + 16 * j][kk]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] = fmaf(av[i].x, wv[j].x, acc[i][j]);
-          acc[i][j] = fmaf(av[i].y, wv[j].y, acc[i][j]);
-          acc[i][j] = fmaf(av[i].z, wv[j].z, acc[i][j]);
-          acc[i][j] = fmaf(av[i].w, wv[j].w, acc[i][j]);
-        }
-    }
-    __syncthreads();
+    __syncthreads();  // the staging buffers are free again
   }
 }
 
 // ------------------------------------------------------------- LayerNorm
-// Rows of block rb: r = sum over the kc partial planes (in order), then
-// (r - mean) / sqrt(var + 1e-5) * g + b, two-pass in fp32, one warp per row.
-__device__ void ln_rows(const float* part, int kc, size_t plane, const float* g, const float* be,
-                        float* out, int rb, int T, int d) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int rr = warp; rr < R; rr += kThreads / 32) {
-    const int row = rb * R + rr;
-    if (row >= T) break;
-    const float* p = part + (size_t)row * d;
-    float v[32];
-    float sum = 0.f;
+// Rows of block rb: r = part[0] + part[1] + ... (K-chunk partials, in that
+// order), then (r - mean) / sqrt(var + 1e-5) * g + b, two-pass in fp32.  The
+// sums are formed with 16 independent 16-byte loads in flight per thread and
+// parked in shared memory (at most 64 KB a pass); one warp then normalises
+// each row from there.
+__device__ __noinline__ void ln_block(const float* part, int kc, size_t plane, const float* g,
+                                      const float* be, float* out, int rb, int T, int d,
+                                      float* sbuf) {
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int rows = min(R, T - rb * R);
+  const int rp = min(R, 16384 / d);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = 0; r0 < rows; r0 += rp) {
+    const int nr = min(rp, rows - r0);
+    const int nch = nr * d / 4;  // <= 4096 chunks: 16 per thread
+    const float4* src = reinterpret_cast<const float4*>(part + (size_t)(rb * R + r0) * d);
+    float4 acc[16];
 #pragma unroll
-    for (int it = 0; it < 32; ++it) {
-      const int c = lane + 32 * it;
-      float s = 0.f;
-      if (c < d) {
-        s = __ldcg(p + c);
-        for (int q = 1; q < kc; ++q) s += __ldcg(p + q * plane + c);
+    for (int u = 0; u < 16; ++u) {
+      const int c = tid + u * kThreads;
+      acc[u] = c < nch ? __ldcg(src + c) : z;
+    }
+    for (int q = 1; q < kc; ++q) {
+      const float4* sq = src + q * (plane / 4);
+      float4 t[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int c = tid + u * kThreads;
+        t[u] = c < nch ? __ldcg(sq + c) : z;
       }
-      v[it] = s;
-      sum += s;
-    }
-    const float mean = warp_sum(sum) / d;
-    float sq = 0.f;
 #pragma unroll
-    for (int it = 0; it < 32; ++it) {
-      const int c = lane + 32 * it;
-      if (c < d) sq = fmaf(v[it] - mean, v[it] - mean, sq);
+      for (int u = 0; u < 16; ++u) {
+        acc[u].x += t[u].x; acc[u].y += t[u].y; acc[u].z += t[u].z; acc[u].w += t[u].w;
+      }
     }
-    const float rstd = rsqrtf(warp_sum(sq) / d + 1e-5f);
 #pragma unroll
-    for (int it = 0; it < 32; ++it) {
-      const int c = lane + 32 * it;
-      if (c < d) out[(size_t)row * d + c] = (v[it] - mean) * rstd * g[c] + be[c];
+    for (int u = 0; u < 16; ++u) {
+      const int c = tid + u * kThreads;
+      if (c < nch) reinterpret_cast<float4*>(sbuf)[c] = acc[u];
     }
+    __syncthreads();
+    for (int rr = warp; rr < nr; rr += kThreads / 32) {
+      const float* x = sbuf + (size_t)rr * d;
+      float sum = 0.f;
+      for (int c = lane; c < d; c += 32) sum += x[c];
+      const float mean = warp_sum(sum) / d;
+      float sq = 0.f;
+      for (int c = lane; c < d; c += 32) sq = fmaf(x[c] - mean, x[c] - mean, sq);
+      const float rstd = rsqrtf(warp_sum(sq) / d + 1e-5f);
+      float* o = out + (size_t)(rb * R + r0 + rr) * d;
+      for (int c = lane; c < d; c += 32) o[c] = (x[c] - mean) * rstd * g[c] + be[c];
+    }
+    __syncthreads();
   }
 }
 
 // ------------------------------------------------------------- attention
+constexpr int kAttStages = 4;  // K/V tiles in flight
 template <int DH>
 struct AttSmem {
-  float k[2][64][DH + 4];
-  float v[2][64][DH + 4];
-  float kn2[2][64];
+  float k[kAttStages][64][DH + 4];
+  float v[kAttStages][64][DH + 4];
+  float kn2[kAttStages][64];
 };
 
-// One (row block, head): 4 threads per query row, each taking every 4th key
-// of a 64-key tile; online softmax in the log2 domain; the four partial
-// states merged at the end.  Rows whose two best scores are close relative
-// to the fp32 score error are corrected in fp64 before the task completes.
+// fp64 correction of the flagged rows, one warp per row (rare: kept out of line).
+__device__ __noinline__ void fix_rows(const DagArgs& a, int l, const float* x_in, const int* list,
+                                      int n, double* dsm) {
+  FixupArgs fa{};
+  fa.x = Plane{x_in, nullptr, 0};
+  fa.w_qkv = a.layers[l].w_qkv;
+  fa.w_kind = 0;
+  fa.b_qkv = a.layers[l].b_qkv;
+  fa.q = Plane{a.q, nullptr, 0};
+  fa.k = Plane{a.k, nullptr, 0};
+  fa.v = Plane{a.v, nullptr, 0};
+  fa.v_transposed = 0;
+  fa.Lp = a.L;
+  fa.ctx_hi = a.ctx;
+  fa.ctx_kind = 0;
+  fa.valid_len = a.vl;
+  fa.B = a.B; fa.H = a.H; fa.L = a.L; fa.dh = a.dh; fa.d = a.d;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  double* q64 = dsm + (size_t)warp * (a.dh + a.d);
+  for (int e = warp; e < n; e += kThreads / 32) ntie::neartie_fix_entry(fa, list[e], q64, q64 + a.dh, lane);
+}
+
+// 32 query rows x one head: 8 threads per row, each taking every 8th key of
+// a 64-key tile, online softmax key by key in the log2 domain; the eight
+// partial states are merged at the end.  Rows whose two best scores are
+// close relative to the fp32 score error are corrected in fp64.
 template <int DH>
-__device__ void attention_task(const DagArgs& a, int l, int rb, int h, const float* x_in,
+__device__ void attention_task(const DagArgs& a, int l, int rb, int half, int h, const float* x_in,
                                unsigned char* smem_raw, int* flag_s, int* nflag_s) {
   AttSmem<DH>& sm = *reinterpret_cast<AttSmem<DH>*>(smem_raw);
-  const int tid = threadIdx.x, row = tid >> 2, sub = tid & 3;
+  const int tid = threadIdx.x, row = tid >> 3, sub = tid & 7;
   const int H = a.H, L = a.L, T = a.T;
-  const int rg = rb * R + row;
+  const int r_first = rb * R + half * kAttRows;
+  const int rg = r_first + row;
   const bool active = rg < T;
   const int b = active ? rg / L : 0, i = active ? rg % L : 0;
   int vl = a.vl[b];
@@ -220,11 +288,11 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int h, const flo
     vl = vl < 1 ? 1 : L;
   }
   const int key_lo = b * L, key_end = active ? b * L + min(i + 1, vl) : 0;  // visible [lo, end)
-  const int g_lo = ((rb * R) / L) * L, g_hi = min(rb * R + R, T);          // block's keys
+  const int g_lo = (r_first / L) * L, g_hi = min(r_first + kAttRows, T);  // the task's keys
   const int ntile = (g_hi - g_lo + 63) / 64;
 
   auto issue = [&](int t) {
-    const int st = t & 1;
+    const int st = t % kAttStages;
     constexpr int CPK = DH / 4;  // 16-byte chunks per key row
     for (int c = tid; c < 64 * CPK; c += kThreads) {
       const int jj = c / CPK, cc = (c % CPK) * 4, g = g_lo + t * 64 + jj;
@@ -235,7 +303,7 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int h, const flo
     }
     cp_commit();
   };
-  issue(0);
+  for (int t = 0; t < kAttStages && t < ntile; ++t) issue(t);
 
   const float scale_log2 = rsqrtf((float)DH) * 1.4426950408889634f;
   float q[DH], o[DH];
@@ -255,14 +323,10 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int h, const flo
   float m = -INFINITY, lsum = 0.f, m1 = -INFINITY, m2 = -INFINITY, kn2max = 0.f;
 
   for (int t = 0; t < ntile; ++t) {
-    if (t + 1 < ntile) {
-      issue(t + 1);
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
+    // issued so far: tiles 0 .. min(ntile - 1, t - 1 + stages); tile t must have landed
+    cp_wait_n(min(ntile - 1 - t, kAttStages - 1));
     __syncthreads();
-    const int st = t & 1;
+    const int st = t % kAttStages;
     {  // squared key norms of the tile, 4 threads per key
       const int key = tid >> 2, part = tid & 3;
       float s = 0.f;
@@ -277,60 +341,47 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int h, const flo
     }
     __syncthreads();
     const int gbase = g_lo + t * 64;
-    if (gbase < key_end && gbase + 64 > key_lo) {
-      float s[16];
-      float mt = -INFINITY;
+    const int u_lo = max(0, (key_lo - gbase - sub + 7) / 8);
+    const int u_hi = min(8, (key_end - gbase - sub + 7) / 8);
+#pragma unroll 1
+    for (int u = u_lo; u < u_hi; ++u) {
+      const int jj = sub + 8 * u;
+      float dot = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int jj = sub + 4 * u, g = gbase + jj;
-        if (g >= key_lo && g < key_end) {
-          float dot = 0.f;
-#pragma unroll
-          for (int c = 0; c < DH; c += 4) {
-            const float4 kv = *reinterpret_cast<const float4*>(&sm.k[st][jj][c]);
-            dot = fmaf(q[c], kv.x, dot);
-            dot = fmaf(q[c + 1], kv.y, dot);
-            dot = fmaf(q[c + 2], kv.z, dot);
-            dot = fmaf(q[c + 3], kv.w, dot);
-          }
-          s[u] = dot;
-          m2 = fmaxf(m2, fminf(m1, dot));
-          m1 = fmaxf(m1, dot);
-          kn2max = fmaxf(kn2max, sm.kn2[st][jj]);
-        } else {
-          s[u] = -INFINITY;
-        }
-        mt = fmaxf(mt, s[u]);
+      for (int c = 0; c < DH; c += 4) {
+        const float4 kv = *reinterpret_cast<const float4*>(&sm.k[st][jj][c]);
+        dot = fmaf(q[c], kv.x, dot);
+        dot = fmaf(q[c + 1], kv.y, dot);
+        dot = fmaf(q[c + 2], kv.z, dot);
+        dot = fmaf(q[c + 3], kv.w, dot);
       }
-      if (mt > m) {
-        const float corr = exp2f(m - mt);  // 0 while m = -inf
+      m2 = fmaxf(m2, fminf(m1, dot));
+      m1 = fmaxf(m1, dot);
+      kn2max = fmaxf(kn2max, sm.kn2[st][jj]);
+      if (dot > m) {  // a new running maximum: rescale (a few times per row)
+        const float corr = exp2f(m - dot);  // 0 while m = -inf
         lsum *= corr;
 #pragma unroll
         for (int c = 0; c < DH; ++c) o[c] *= corr;
-        m = mt;
+        m = dot;
       }
-      if (m != -INFINITY) {
+      const float p = exp2f(dot - m);
+      lsum += p;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float p = exp2f(s[u] - m);  // 0 for masked keys
-          lsum += p;
-          const int jj = sub + 4 * u;
-#pragma unroll
-          for (int c = 0; c < DH; c += 4) {
-            const float4 vv = *reinterpret_cast<const float4*>(&sm.v[st][jj][c]);
-            o[c] = fmaf(p, vv.x, o[c]);
-            o[c + 1] = fmaf(p, vv.y, o[c + 1]);
-            o[c + 2] = fmaf(p, vv.z, o[c + 2]);
-            o[c + 3] = fmaf(p, vv.w, o[c + 3]);
-          }
-        }
+      for (int c = 0; c < DH; c += 4) {
+        const float4 vv = *reinterpret_cast<const float4*>(&sm.v[st][jj][c]);
+        o[c] = fmaf(p, vv.x, o[c]);
+        o[c + 1] = fmaf(p, vv.y, o[c + 1]);
+        o[c + 2] = fmaf(p, vv.z, o[c + 2]);
+        o[c + 3] = fmaf(p, vv.w, o[c + 3]);
       }
     }
     __syncthreads();
+    if (t + kAttStages < ntile) issue(t + kAttStages);
   }
-  // merge the four partial states of the row (adjacent lanes)
+  // merge the eight partial states of the row (adjacent lanes)
 #pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
+  for (int off = 1; off <= 4; off <<= 1) {
     const float mo = __shfl_xor_sync(0xffffffffu, m, off);
     const float lo = __shfl_xor_sync(0xffffffffu, lsum, off);
     const float a1 = __shfl_xor_sync(0xffffffffu, m1, off);
@@ -362,34 +413,15 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int h, const flo
   }
   __syncthreads();
   const int nflag = *nflag_s;
-  if (nflag > 0) {
-    FixupArgs fa{};
-    fa.x = Plane{x_in, nullptr, 0};
-    fa.w_qkv = a.layers[l].w_qkv;
-    fa.w_kind = 0;
-    fa.b_qkv = a.layers[l].b_qkv;
-    fa.q = Plane{a.q, nullptr, 0};
-    fa.k = Plane{a.k, nullptr, 0};
-    fa.v = Plane{a.v, nullptr, 0};
-    fa.v_transposed = 0;
-    fa.Lp = L;
-    fa.ctx_hi = a.ctx;
-    fa.ctx_kind = 0;
-    fa.valid_len = a.vl;
-    fa.B = a.B; fa.H = H; fa.L = L; fa.dh = DH; fa.d = a.d;
-    const int warp = tid / 32, lane = tid % 32;
-    double* q64 = reinterpret_cast<double*>(smem_raw) + (size_t)warp * (DH + a.d);
-    for (int e = warp; e < nflag; e += kThreads / 32)
-      ntie::neartie_fix_entry(fa, flag_s[e], q64, q64 + DH, lane);
-  }
+  if (nflag > 0) fix_rows(a, l, x_in, flag_s, nflag, reinterpret_cast<double*>(smem_raw));
 }
 
 // ---------------------------------------------------------------- kernel
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant__ DagArgs a) {
   extern __shared__ __align__(16) unsigned char dag_smem[];
-  __shared__ int task_s, go_s, nflag_s;
-  __shared__ int flag_s[R];
+  __shared__ int task_s, go_s, last_s, nflag_s;
+  __shared__ int flag_s[kAttRows];
   const int tid = threadIdx.x;
   const Plan pl = make_plan(a.RB, a.H, a.d, a.dff);
   const int total = a.n_layers * pl.per_layer;
@@ -402,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
     const long long t0 = clock64();
     while (ld_acquire(c) < target) {
       if (*(volatile int*)a.abort) return false;
-      __nanosleep(64);
+      __nanosleep(32);
       if (clock64() - t0 > kWait) {
         atomicExch(a.abort, 1);
         set_status(a.status, TL_ERR_DEVICE_TIMEOUT);
@@ -411,13 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
     }
     return true;
   };
-  // Every thread's writes are ordered before the release of the counter.
-  auto signal = [&](int* c) {
+  // Release the block's writes through counter c; true in the whole block
+  // when this was the completion that reached `target`.
+  auto complete = [&](int* c, int target) -> bool {
     __syncthreads();
     if (tid == 0) {
       __threadfence();
-      atomicAdd(c, 1);
+      const int old = atomicAdd(c, 1);
+      if (old == target - 1) __threadfence();  // acquire the other tasks' writes
+      last_s = old == target - 1;
     }
+    __syncthreads();
+    return last_s;
   };
   // The row blocks holding rows of the sequences that meet block rb.
   auto rb_first = [&](int rb) { return ((rb * R) / L) * L / R; };
@@ -426,27 +463,41 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
     return min(((last_row / L + 1) * L - 1) / R, RB - 1);
   };
 
+  int next = 0;
+  if (tid == 0) next = atomicAdd(a.head, 1);
   while (true) {
     __syncthreads();
-    if (tid == 0) task_s = atomicAdd(a.head, 1);
+    if (tid == 0) {
+      task_s = next;
+      next = atomicAdd(a.head, 1);  // consumed on the next iteration
+    }
     __syncthreads();
     const int t = task_s;
     if (t >= total) break;
     const int l = t / pl.per_layer;
     int rem = t % pl.per_layer, kind = 0;
-    while (rem >= pl.n[kind]) rem -= pl.n[kind++];
+    for (int q = 0; q < 5; ++q) {
+      kind = queued_kind(q);
+      if (rem < pl.n[kind]) break;
+      rem -= pl.n[kind];
+    }
     const tl_layer_dev& P = a.layers[l];
     const float* x_in = l == 0 ? a.x : ((l & 1) ? a.xs1 : a.xs0);  // this layer's input
     float* x_next = (l & 1) ? a.xs0 : a.xs1;
     // task coordinates
-    int rb = 0, nt = 0, kc = 0, h = 0;
+    int rb = 0, nt = 0, kc = 0, h = 0, half = 0;
     switch (kind) {
       case K_QKV: rb = rem / pl.nt3; nt = rem % pl.nt3; break;
-      case K_ATT: rb = RB - 1 - rem / H; h = rem % H; break;
+      case K_ATT: {
+        const int per = pl.target[K_ATT], hh = rem % per;
+        rb = RB - 1 - rem / per;
+        half = R / kAttRows - 1 - hh / H;
+        h = hh % H;
+        break;
+      }
       case K_OUT: rb = rem / (pl.ntd * pl.kco); nt = (rem / pl.kco) % pl.ntd; kc = rem % pl.kco; break;
       case K_F1: rb = rem / pl.ntf; nt = rem % pl.ntf; break;
-      case K_F2: rb = rem / (pl.ntd * pl.kcf); nt = (rem / pl.kcf) % pl.ntd; kc = rem % pl.kcf; break;
-      default: rb = rem; break;
+      default: rb = rem / (pl.ntd * pl.kcf); nt = (rem / pl.kcf) % pl.ntd; kc = rem % pl.kcf; break;
     }
     // ------------------------------------------------------ dependencies
     if (tid == 0) {
@@ -456,17 +507,16 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
         case K_QKV:
           if (l > 0) {
             ok = ok && wait_ge(counter(l - 1, K_LN2, rb), 1);
-            for (int r2 = rb; ok && r2 <= rb_last(rb); ++r2) ok = wait_ge(counter(l - 1, K_ATT, r2), H);
+            for (int r2 = rb; ok && r2 <= rb_last(rb); ++r2)
+              ok = wait_ge(counter(l - 1, K_ATT, r2), pl.target[K_ATT]);
           }
           break;
         case K_ATT:
           for (int r2 = rb_first(rb); ok && r2 <= rb; ++r2) ok = wait_ge(counter(l, K_QKV, r2), pl.nt3);
           break;
-        case K_OUT: ok = ok && wait_ge(counter(l, K_ATT, rb), H); break;
-        case K_LN1: ok = ok && wait_ge(counter(l, K_OUT, rb), pl.ntd * pl.kco); break;
+        case K_OUT: ok = ok && wait_ge(counter(l, K_ATT, rb), pl.target[K_ATT]); break;
         case K_F1: ok = ok && wait_ge(counter(l, K_LN1, rb), 1); break;
-        case K_F2: ok = ok && wait_ge(counter(l, K_F1, rb), pl.ntf); break;
-        default: ok = ok && wait_ge(counter(l, K_F2, rb), pl.ntd * pl.kcf); break;
+        default: ok = ok && wait_ge(counter(l, K_F1, rb), pl.ntf); break;
       }
       if (ok) __threadfence();
       go_s = ok;
@@ -475,30 +525,33 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
     if (!go_s) continue;  // aborted: drain the queue without work
     // --------------------------------------------------------------- work
     if (kind == K_ATT) {
-      attention_task<DH>(a, l, rb, h, x_in, dag_smem, flag_s, &nflag_s);
-    } else if (kind == K_LN1) {
-      ln_rows(a.part, pl.kco, plane, P.ln1_g, P.ln1_b, a.y, rb, T, d);
-    } else if (kind == K_LN2) {
-      ln_rows(a.part, pl.kcf, plane, P.ln2_g, P.ln2_b, l + 1 < a.n_layers ? x_next : a.out, rb, T, d);
-    } else {
-      GemmSmem& gs = *reinterpret_cast<GemmSmem*>(dag_smem);
-      float acc[4][4];
-      const int m0 = rb * R, n0 = nt * 64;
-      int N = d;
-      if (kind == K_QKV) {
-        N = 3 * d;
-        gemm_tile(x_in, d, (const float*)P.w_qkv, d, T, N, 0, d, m0, n0, acc, gs);
-      } else if (kind == K_OUT) {
-        gemm_tile(a.ctx, d, (const float*)P.w_o, d, T, N, kc * kDagKChunk,
-                  min(d, (kc + 1) * kDagKChunk), m0, n0, acc, gs);
-      } else if (kind == K_F1) {
-        N = a.dff;
-        gemm_tile(a.y, d, (const float*)P.w_1, d, T, N, 0, d, m0, n0, acc, gs);
-      } else {
-        gemm_tile(a.hb, a.dff, (const float*)P.w_2, a.dff, T, N, kc * kDagKChunk,
-                  min(a.dff, (kc + 1) * kDagKChunk), m0, n0, acc, gs);
+      attention_task<DH>(a, l, rb, half, h, x_in, dag_smem, flag_s, &nflag_s);
+      complete(counter(l, K_ATT, rb), pl.target[K_ATT]);
+      continue;
+    }
+    GemmSmem& gs = *reinterpret_cast<GemmSmem*>(dag_smem);
+    float acc[4][4];
+    const int m0 = rb * R, n0 = nt * 64;
+    const int tx = tid % 16, ty = tid / 16;
+    if (kind == K_QKV) {
+      gemm_tile(x_in, d, (const float*)P.w_qkv, d, T, 3 * d, 0, d, m0, n0, acc, gs);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int mm = m0 + ty + 16 * i;
+        if (mm >= T) continue;
+        const size_t rowbase = (size_t)(mm / L) * H * L + mm % L;  // ((b H) L + t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + tx + 16 * j;
+          if (n >= 3 * d) continue;
+          const int which = n / d, w = n % d, hh = w / DH, c = w % DH;
+          float* dst = which == 0 ? a.q : which == 1 ? a.k : a.v;
+          dst[(rowbase + (size_t)hh * L) * DH + c] = acc[i][j] + P.b_qkv[n];
+        }
       }
-      const int tx = tid % 16, ty = tid / 16;
+      complete(counter(l, K_QKV, rb), pl.nt3);
+    } else if (kind == K_F1) {
+      gemm_tile(a.y, d, (const float*)P.w_1, d, T, a.dff, 0, d, m0, n0, acc, gs);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int mm = m0 + ty + 16 * i;
@@ -506,25 +559,43 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int n = n0 + tx + 16 * j;
-          if (n >= N) continue;
-          const float v = acc[i][j];
-          if (kind == K_QKV) {
-            const int which = n / d, w = n % d, hh = w / DH, c = w % DH;
-            float* dst = which == 0 ? a.q : which == 1 ? a.k : a.v;
-            dst[(((size_t)(mm / L) * H + hh) * L + mm % L) * DH + c] = v + P.b_qkv[n];
-          } else if (kind == K_OUT) {
-            const size_t at = (size_t)mm * d + n;
-            a.part[kc * plane + at] = kc == 0 ? v + P.b_o[n] + __ldcg(x_in + at) : v;
-          } else if (kind == K_F1) {
-            a.hb[(size_t)mm * a.dff + n] = gelu_erf(v + P.b_1[n]);
-          } else {
-            const size_t at = (size_t)mm * d + n;
-            a.part[kc * plane + at] = kc == 0 ? v + P.b_2[n] + __ldcg(a.y + at) : v;
-          }
+          if (n < a.dff) a.hb[(size_t)mm * a.dff + n] = gelu_erf(acc[i][j] + P.b_1[n]);
+        }
+      }
+      complete(counter(l, K_F1, rb), pl.ntf);
+    } else {
+      // OUT or F2: a K-chunk partial; chunk 0 carries the bias and residual.
+      const bool out = kind == K_OUT;
+      const int K = out ? d : a.dff;
+      gemm_tile(out ? a.ctx : a.hb, K, (const float*)(out ? P.w_o : P.w_2), K, T, d, kc * kDagKChunk,
+                min(K, (kc + 1) * kDagKChunk), m0, n0, acc, gs);
+      const float* bias = out ? P.b_o : P.b_2;
+      const float* res = out ? x_in : a.y;
+      float* dst = a.part + kc * plane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int mm = m0 + ty + 16 * i;
+        if (mm >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + tx + 16 * j;
+          if (n >= d) continue;
+          const size_t at = (size_t)mm * d + n;
+          dst[at] = kc == 0 ? acc[i][j] + bias[n] + __ldcg(res + at) : acc[i][j];
+        }
+      }
+      if (complete(counter(l, kind, rb), pl.target[kind])) {
+        // the row block's last chunk: LayerNorm its rows now
+        if (out) {
+          ln_block(a.part, pl.kco, plane, P.ln1_g, P.ln1_b, a.y, rb, T, d, (float*)dag_smem);
+          complete(counter(l, K_LN1, rb), 1);
+        } else {
+          ln_block(a.part, pl.kcf, plane, P.ln2_g, P.ln2_b, l + 1 < a.n_layers ? x_next : a.out, rb,
+                   T, d, (float*)dag_smem);
+          complete(counter(l, K_LN2, rb), 1);
         }
       }
     }
-    signal(counter(l, kind, rb));
   }
 }
 
@@ -543,8 +614,8 @@ cudaError_t launch(const DagArgs& a, int grid, cudaStream_t s) {
 bool dag_supported(int d, int H, int dff, int n_layers, tl_dtype t) {
   if (t != TL_F32 || H < 1 || d % H || n_layers < 1 || n_layers > kDagMaxLayers) return false;
   const int dh = d / H;
-  // 16-byte cp.async rows need d and d_ff multiples of 4; LayerNorm keeps a
-  // row in 32 registers per lane.
+  // 16-byte cp.async rows need d and d_ff multiples of 4; a LayerNorm pass
+  // parks at least 16 rows of d in 64 KB of shared memory.
   return (dh == 16 || dh == 32 || dh == 64) && d <= 1024 && dff % 4 == 0 && dff >= 4;
 }
 
@@ -553,9 +624,11 @@ int dag_counter_ints(int n_layers, int RB) { return n_layers * K_KINDS * RB + 2;
 size_t dag_dyn_smem(int d, int dh) {
   size_t att = dh == 16 ? sizeof(AttSmem<16>) : dh == 32 ? sizeof(AttSmem<32>) : sizeof(AttSmem<64>);
   size_t fix = (size_t)(kThreads / 32) * (dh + d) * sizeof(double);
+  size_t ln = (size_t)(R < 16384 / d ? R : 16384 / d) * d * sizeof(float);
   size_t m = sizeof(GemmSmem);
   if (att > m) m = att;
   if (fix > m) m = fix;
+  if (ln > m) m = ln;
   return m;
 }
 
