@@ -121,17 +121,18 @@ __device__ __forceinline__ void cp_wait_n(int n) {
 }
 
 // ------------------------------------------------------------------ GEMM
-// A whole K chunk (<= 256) of both operands is staged at once, one cp.async
-// group per 32-wide slab, so the copies of every slab are in flight together
-// and compute on slab s overlaps the arrival of the later ones.
-constexpr int kGemmLd = kDagKChunk + 4;  // row stride in floats (16-byte multiple, 4-bank skew)
+// 128 columns of K of both operands are staged at once, one cp.async group
+// per 32-wide slab, so the copies of every slab are in flight together and
+// compute on slab s overlaps the arrival of the later ones.
+constexpr int kStageK = 128;           // K staged in shared memory at once
+constexpr int kGemmLd = kStageK + 4;   // row stride in floats (16-byte multiple, 4-bank skew)
 struct GemmSmem {
   float a[R][kGemmLd];
   float w[64][kGemmLd];
 };
 
-// acc = A[m0.., k0..k1) . W[n0.., k0..k1)^T for a 64 x 64 tile, in K chunks
-// of 256.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows ty + 16 i and
+// acc = A[m0.., k0..k1) . W[n0.., k0..k1)^T for a 64 x 64 tile, staged 128
+// columns of K at a time.  Thread (ty, tx) = (tid / 16, tid % 16) owns rows ty + 16 i and
 // columns tx + 16 j.  K (lda, ldw and k1) must be a multiple of 4.
 __device__ __forceinline__ void gemm_tile(const float* A, int lda, const float* W, int ldw, int M,
                                           int N, int k0, int k1, int m0, int n0,
@@ -141,9 +142,9 @@ __device__ __forceinline__ void gemm_tile(const float* A, int lda, const float* 
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int kb = k0; kb < k1; kb += kDagKChunk) {
-    const int ke = min(k1, kb + kDagKChunk);
-    const int nslab = (ke - kb + 31) / 32;  // <= 8
+  for (int kb = k0; kb < k1; kb += kStageK) {
+    const int ke = min(k1, kb + kStageK);
+    const int nslab = (ke - kb + 31) / 32;  // <= 4
     for (int s = 0; s < nslab; ++s) {
 #pragma unroll
       for (int c = tid; c < R * 8; c += kThreads) {
@@ -417,8 +418,14 @@ __device__ void attention_task(const DagArgs& a, int l, int rb, int half, int h,
 }
 
 // ---------------------------------------------------------------- kernel
+// One CTA per SM: two co-resident CTAs (head_dim <= 32 at 128 registers)
+// measured slower on the batch-1 d_model = 256 workload, each task taking
+// longer while sharing the SM and the attention spilling.
 template <int DH>
-__global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant__ DagArgs a) {
+constexpr int dag_ctas_per_sm() { return 1; }
+
+template <int DH>
+__global__ void __launch_bounds__(kThreads, dag_ctas_per_sm<DH>()) dag_kernel(const __grid_constant__ DagArgs a) {
   extern __shared__ __align__(16) unsigned char dag_smem[];
   __shared__ int task_s, go_s, last_s, nflag_s;
   __shared__ int flag_s[kAttRows];
@@ -600,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1) dag_kernel(const __grid_constant_
 }
 
 template <int DH>
-cudaError_t launch(const DagArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch(const DagArgs& a, int total, int num_sms, cudaStream_t s) {
+  const int per_sm = dag_ctas_per_sm<DH>();
+  const int grid = total < per_sm * num_sms ? total : per_sm * num_sms;  // all resident
   const size_t smem = dag_dyn_smem(a.d, DH);
   auto k = dag_kernel<DH>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -635,11 +644,10 @@ size_t dag_dyn_smem(int d, int dh) {
 cudaError_t dag_forward(const DagArgs& a, int num_sms, cudaStream_t s) {
   const Plan pl = make_plan(a.RB, a.H, a.d, a.dff);
   const int total = a.n_layers * pl.per_layer;
-  const int grid = total < num_sms ? total : num_sms;  // one resident CTA per SM
   const int dh = a.d / a.H;
-  if (dh == 16) return launch<16>(a, grid, s);
-  if (dh == 32) return launch<32>(a, grid, s);
-  return launch<64>(a, grid, s);
+  if (dh == 16) return launch<16>(a, total, num_sms, s);
+  if (dh == 32) return launch<32>(a, total, num_sms, s);
+  return launch<64>(a, total, num_sms, s);
 }
 
 }  // namespace tl
