@@ -10,14 +10,16 @@
 // (fp16 or bf16); activations are carried as (hi, lo) 16-bit pairs wherever
 // they feed a tensor-core product.
 //
-// One CTA per SM, persistent over tiles.  384 threads in three warpgroups:
+// One CTA per SM, persistent over tiles.  576 threads:
 //   control  warp 0  TMA: the input tile (once per tile) and weight boxes
 //                    from L2 into a 2-deep ring, in the order the MMAs use them
 //            warp 1  TMEM (all 512 columns); one thread issues every MMA
-//            warps 2, 3 idle (they lend their registers: setmaxnreg)
-//   compute  two warpgroups ("halves" 0, 1); both cover all 128 rows (TMEM
-//            lanes); half h takes columns [64h, 64h + 64) of each row, or
-//            [32h, 32h + 32) of a 64-wide FFN chunk
+//   compute  16 warps in four column groups g = 0..3 of four warps; the four
+//            warps of a group cover the 128 rows (TMEM lane quarters), and
+//            group g takes columns [32g, 32g + 32) of a 128-wide row, head
+//            g for the context, 16 of a 64-wide FFN chunk, and every 4th
+//            8-key chunk of the attention scores.  Four warps per SM
+//            sub-partition hide the latency of the CUDA-core phases.
 //
 // Per layer (TMEM columns in brackets):
 //   QKV   acc[0, 384) = X . W_qkv^T      X = (hi, lo) of the layer input
@@ -25,7 +27,8 @@
 //         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
 //         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32).
 //         Head h+1's Q and K are written as soon as S_h is done, so only its
-//         V waits for P_h V_h.
+//         V waits for P_h V_h.  The row maximum (and the second best score)
+//         is merged across the four groups through shared memory.
 //   ctx = O / l -> shared memory (hi, lo)
 //   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> X buffer
 //   FFN   per 64-wide chunk c of d_ff: acc1[256 + 64 (c % 2)] = y . W_1c^T,
@@ -33,10 +36,12 @@
 //         acc2[0, 128) += h_c . W_2c^T; GELU of chunk c overlaps the two
 //         products of chunks c - 1 and c + 1
 //   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
+// The LayerNorm statistics of a row merge the four groups' (mean, M2) with
+// Chan's pairwise formula in a fixed order.
 //
 // Near ties (see neartie.cuh) are corrected in place: a flagged (row, head)
 // has its probabilities recomputed in fp64 from the layer input and the
-// weights, by the warp that owns the row, before the P . V product.
+// weights, by the group-0 warp that owns the row, before the P . V product.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,8 +58,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;
-constexpr int kCompute = 256;
+constexpr int kCtrlWarps = 2;
+constexpr int kCompute = 512;
+constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kNW = 2;  // weight ring depth
 
@@ -68,21 +74,14 @@ constexpr int kVB = kKB + 2 * 8192;                   // [part][khalf] 32 x 64, 
 constexpr int kWR = kVB + 4 * 4096;                   // [kNW] x 16 KB
 constexpr int kMisc = kWR + kNW * kTile16;
 // misc (floats unless noted)
-constexpr int kQn2 = kMisc;                           // [2][128] |q_r|^2, by head parity
-constexpr int kXA1 = kQn2 + 2 * 128 * 4;              // LayerNorm 1 exchange: mean, M2
-constexpr int kXB1 = kXA1 + 2 * 128 * 4;
-constexpr int kXA2 = kXB1 + 2 * 128 * 4;              // LayerNorm 2 exchange
-constexpr int kXB2 = kXA2 + 2 * 128 * 4;
-constexpr int kLs = kXB2 + 2 * 128 * 4;               // [4][128] softmax sums per head
-constexpr int kKmax = kLs + 4 * 128 * 4;              // [4] int (float bits)
-constexpr int kVec = kKmax + 16;                      // the layer's bias / LayerNorm vectors
-constexpr int kMaxDff = 512;
-// offsets (floats) inside the vector block
-constexpr int V_BQKV = 0, V_BO = 384, V_G1 = 512, V_BE1 = 640, V_B2 = 768, V_G2 = 896,
-              V_BE2 = 1024, V_B1 = 1152, V_COUNT = 1152 + kMaxDff;
-constexpr int kBars = ((kVec + V_COUNT * 4 + 7) / 8) * 8;
+constexpr int kQn2 = kMisc;                           // [2 head parity][2 group][128] partial |q_r|^2
+constexpr int kEx = kQn2 + 2 * 2 * 128 * 4;           // [2][4 group][128] exchange: (m1, m2) or (mean, M2)
+constexpr int kLs = kEx + 2 * 4 * 128 * 4;            // [4 head][4 group][128] partial softmax sums
+constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max partial |k|^2 (float bits)
+constexpr int kBars = kKmax + 64;
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
+constexpr int kMaxDff = 512;
 
 // mbarrier indices
 enum {
@@ -132,6 +131,13 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float* v) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
@@ -157,28 +163,38 @@ __device__ __forceinline__ void get8(const unsigned char* hi, const unsigned cha
     for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
   }
 }
-// v[0..N) += vec[0..N), N a multiple of 4 (shared-memory float4 reads)
+// v[0..N) += vec[0..N): a layer vector in global memory (read through L1),
+// N a multiple of 4, vec 16-byte aligned.
 template <int N>
 __device__ __forceinline__ void add_vec(float* v, const float* vec) {
   const float4* b4 = reinterpret_cast<const float4*>(vec);
 #pragma unroll
   for (int c = 0; c < N / 4; ++c) {
-    const float4 b = b4[c];
+    const float4 b = __ldg(b4 + c);
     v[4 * c] += b.x; v[4 * c + 1] += b.y; v[4 * c + 2] += b.z; v[4 * c + 3] += b.w;
   }
 }
 
-// fp64 correction of one flagged (row, head), done by the warp that owns
-// the row.  Keys kk = k0 + lane + 32 m (m = 0, 1) are this lane's; sc0, sc1
-// are their fp32 screening scores (natural-log units, -inf when masked).
-// Recomputes q_i in fp64 from the layer input and the weights, recomputes
-// the scores of the candidate keys (within 12 + 2E of the best) exactly as
-// x_j . (W_k^T q_i) + b_k . q_i, and returns the row's fp64 softmax weights
-// relative to the exact best score (w0, w1) and their sum (l, every lane).
+// The (hi, lo) slots of element (row rr, key column kc) of the P buffer.
+__device__ __forceinline__ void p_slot(int rr, int kc, int& hi_off, int& lo_off) {
+  const int kh = kc >> 6;
+  const int off = sw128(rr, (kc & 63) >> 3) + (kc & 7) * 2;
+  hi_off = kPB + kh * kTile16 + off;
+  lo_off = kPB + (2 + kh) * kTile16 + off;
+}
+
+// fp64 correction of one flagged (row rr, head h), done by a whole warp.
+// The row's fp32 scores (log2 units, scaled, -inf where masked) were parked
+// in its own P slots as bit patterns (high half in the hi plane, low half in
+// the lo plane); lane owns keys kk = lane + 32 m of sequence sq.  Recomputes
+// q_i in fp64 from the layer input and the weights, recomputes the scores of
+// the candidate keys (within 12 + 2E of the best) exactly as
+// x_j . (W_k^T q_i) + b_k . q_i, writes the row's softmax weights relative
+// to the exact best score into the P slots and returns their sum.
 template <typename T, int L>
-__device__ __noinline__ void fixup_row(const unsigned char* sm, const MegaLayer& P, int rr, int h,
-                                       bool first, int lane, int k0, float sc0, float sc1,
-                                       float kmx, float& w0, float& w1, float& l) {
+__device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, int rr, int sq, int h,
+                                        bool first, int lane, float kmx) {
+  constexpr int NK = L / 32;  // keys per lane
   const unsigned char* xa = sm + kXA;
   auto xval = [&](int row, int col) -> double {
     const int kh = col >> 6, c8 = (col & 63) >> 3, e8 = col & 7;
@@ -187,6 +203,15 @@ __device__ __noinline__ void fixup_row(const unsigned char* sm, const MegaLayer&
     if (!first) v += (double)to_f32<T>(*reinterpret_cast<const T*>(xa + (2 + kh) * kTile16 + off));
     return v;
   };
+  float sc[NK];  // screening scores, natural-log units
+#pragma unroll
+  for (int m = 0; m < NK; ++m) {
+    int ho, lo;
+    p_slot(rr, sq * L + lane + 32 * m, ho, lo);
+    const uint32_t bits = ((uint32_t)*reinterpret_cast<const uint16_t*>(sm + ho) << 16) |
+                          (uint32_t)*reinterpret_cast<const uint16_t*>(sm + lo);
+    sc[m] = __uint_as_float(bits) * 0.69314718055994531f;
+  }
   const T* W = reinterpret_cast<const T*>(P.w_qkv);
   // q_i in fp64: lane c owns dim c
   double q64 = (double)P.b_qkv[32 * h + lane];
@@ -203,40 +228,52 @@ __device__ __noinline__ void fixup_row(const unsigned char* sm, const MegaLayer&
     for (int m = 0; m < 4; ++m)
       u[m] = fma(qc, (double)to_f32<T>(W[(size_t)(128 + 32 * h + c) * kD + lane + 32 * m]), u[m]);
   }
-  const float best = warp_max(fmaxf(sc0, sc1));
+  float best = -INFINITY;
+#pragma unroll
+  for (int m = 0; m < NK; ++m) best = fmaxf(best, sc[m]);
+  best = warp_max(best);
   const float err = neartie_err((float)sqrt(qq), kmx, kDH);
   const float thr = best - kTieGap - 2.f * err;
-  double sc[2] = {(double)sc0, (double)sc1};
+  double s64[NK];
   double Mx = -INFINITY;
 #pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const float s32 = m == 0 ? sc0 : sc1;
-    unsigned need = __ballot_sync(0xffffffffu, s32 != -INFINITY && s32 >= thr);
+  for (int m = 0; m < NK; ++m) {
+    s64[m] = (double)sc[m];
+    unsigned need = __ballot_sync(0xffffffffu, sc[m] != -INFINITY && sc[m] >= thr);
     while (need) {
       const int src = __ffs(need) - 1;
       need &= need - 1;
-      const int key = k0 + src + 32 * m;
+      const int key = sq * L + src + 32 * m;  // the key's row in the tile
       double part = 0.0;
 #pragma unroll
       for (int mm = 0; mm < 4; ++mm) part = fma(xval(key, lane + 32 * mm), u[mm], part);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (lane == src) sc[m] = (part + u0) * (1.0 / sqrt((double)kDH));
+      if (lane == src) s64[m] = (part + u0) * (1.0 / sqrt((double)kDH));
     }
-    Mx = fmax(Mx, sc[m]);
+    Mx = fmax(Mx, s64[m]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Mx = fmax(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-  const double e0 = sc[0] == -INFINITY ? 0.0 : exp(sc[0] - Mx);
-  const double e1 = sc[1] == -INFINITY ? 0.0 : exp(sc[1] - Mx);
-  double ws = e0 + e1;
+  double ws = 0.0;
+#pragma unroll
+  for (int m = 0; m < NK; ++m) {
+    const double e = s64[m] == -INFINITY ? 0.0 : exp(s64[m] - Mx);
+    ws += e;
+    T hv, lv;
+    Split<T>::go((float)e, hv, lv);
+    int ho, lo;
+    p_slot(rr, sq * L + lane + 32 * m, ho, lo);
+    *reinterpret_cast<T*>(sm + ho) = hv;
+    *reinterpret_cast<T*>(sm + lo) = lv;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-  w0 = (float)e0;
-  w1 = (float)e1;
-  l = (float)ws;
+  return (float)ws;
 }
 
+// 576 threads: registers are granted to warps in groups of four, so the 18
+// warps hold 20 warps' worth, 96 registers per thread.
 template <typename T, int L>
 __global__ void __launch_bounds__(kThreads, 1)
     mega_kernel(const __grid_constant__ CUtensorMap map_x, const MegaArgs a) {
@@ -279,12 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   volatile int* abort = abort_flag;
   int* status = a.status;
-  // Register split by warpgroup: the control warpgroup (TMA, MMA, two idle
-  // warps) gives registers to the two compute warpgroups.  At launch every
-  // thread holds 168; 128 x 88 + 256 x 208 = 64512 = 384 x 168, and each
-  // SM sub-partition holds one warp of each group: (88 + 208 + 208) x 32 <= 16384.
-  if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+  // Every thread keeps the launch's 96 registers.
+  if (warp < kCtrlWarps) {
   if (warp == 0) {
     // ================================================================ TMA
     if (lane == 0) {
@@ -447,26 +480,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(bar + B_MMA_DONE, 0, status);
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ======================================================== compute warps
-    const int cw = warp - 4;               // 0..7
-    const int half = cw >> 2;              // column / key half
-    const int qd = warp & 3;               // TMEM lane quarter
+    const int cw = warp - kCtrlWarps;      // 0..15
+    const int g = cw >> 2;                 // column group
+    const int qd = warp & 3;               // TMEM lane quarter (fixed by the warp index)
     const int r = qd * 32 + lane;          // row in the tile
     const int sq = r / L;                  // sequence within the tile
     const int i = r % L;                   // position in the sequence
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     float* qn2_s = reinterpret_cast<float*>(sm + kQn2);
+    float* ex = reinterpret_cast<float*>(sm + kEx);
     float* l_s = reinterpret_cast<float*>(sm + kLs);
     int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
-    float* vec = reinterpret_cast<float*>(sm + kVec);
     unsigned char* xa = sm + kXA;
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
-    long long c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_hfree[2] = {0, 0},
-              c_f2 = 0, c_sync = 0;
+    constexpr int NM = L / 32;  // own 8-key chunks of a row per group
+    int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_hfree[2] = {0, 0}, c_f2 = 0,
+        c_sync = 0;  // completed phases per barrier (parity = count & 1)
     bool ok = true;
-    auto wait = [&](int b, long long& n) -> bool {
+    auto wait = [&](int b, int& n) -> bool {
       const uint32_t par = (uint32_t)(n & 1);
       ++n;
       if (!mbar_wait(bar + b, par, abort, status)) return false;
@@ -478,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar + b);
     };
-    // Barrier of the 256 compute threads on an mbarrier, so that the wait is
+    // Barrier of the 512 compute threads on an mbarrier, so that the wait is
     // bounded like every other wait (a bar.sync could not give up).
     auto bar_compute = [&]() {
       mbar_arrive(bar + B_SYNC);
@@ -486,39 +519,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++c_sync;
       mbar_wait(bar + B_SYNC, par, abort, status);
     };
-    // Half 0 writes Q_h (hi, lo) and |q|^2; half 1 writes K_h and the
-    // tile's max |k|.
-    auto convert_qk = [&](int h) {
-      float v[32];
-      const int col = (half == 0 ? 0 : 128) + 32 * h;
-      tmem_ld32_nw(trow + col, v);
+    // Groups 0, 1 write 16 columns each of Q_h (hi, lo) and a partial |q|^2;
+    // groups 2, 3 write K_h and the tile's largest partial |k|^2.
+    auto convert_qk = [&](int h, const MegaLayer& P) {
+      float v[16];
+      const bool isq = g < 2;
+      const int c0 = 16 * (g & 1);
+      const int col = (isq ? 0 : 128) + 32 * h + c0;
+      tmem_ld16_nw(trow + col, v);
       tmem_wait_ld();
-      add_vec<32>(v, vec + V_BQKV + col);
+      add_vec<16>(v, P.b_qkv + col);
       float n2 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) n2 = fmaf(v[c], v[c], n2);
-      unsigned char* dst = sm + (half == 0 ? kQB : kKB);
+      for (int c = 0; c < 16; ++c) n2 = fmaf(v[c], v[c], n2);
+      unsigned char* dst = sm + (isq ? kQB : kKB);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) put8<T>(dst, dst + 8192, sw64(r, cc * 16), v + 8 * cc);
-      if (half == 0) {
-        qn2_s[(h & 1) * 128 + r] = n2;
+      for (int cc = 0; cc < 2; ++cc) put8<T>(dst, dst + 8192, sw64(r, (2 * (g & 1) + cc) * 16), v + 8 * cc);
+      if (isq) {
+        qn2_s[((h & 1) * 2 + (g & 1)) * 128 + r] = n2;
       } else {
-        const float kn = warp_max(sqrtf(n2));
-        if (lane == 0) atomicMax(kmax_s + h, __float_as_int(kn));
+        const float kn = warp_max(n2);
+        if (lane == 0) atomicMax(kmax_s + 2 * h + (g & 1), __float_as_int(kn));
       }
     };
-    // V_h^T (hi, lo): this thread's key r, dims [16 half, 16 half + 16).
-    auto convert_v = [&](int h) {
-      float v[16];
-      tmem_ld16_nw(trow + 256 + 32 * h + 16 * half, v);
+    // V_h^T (hi, lo): this thread's key r, dims [8g, 8g + 8).
+    auto convert_v = [&](int h, const MegaLayer& P) {
+      float v[8];
+      tmem_ld8_nw(trow + 256 + 32 * h + 8 * g, v);
       tmem_wait_ld();
-      add_vec<16>(v, vec + V_BQKV + 256 + 32 * h + 16 * half);
+      add_vec<8>(v, P.b_qkv + 256 + 32 * h + 8 * g);
       const int kh = r >> 6, kc = r & 63;
       unsigned char* vh = sm + kVB + kh * 4096;
       unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int dim = 16 * half + c;
+      for (int c = 0; c < 8; ++c) {
+        const int dim = 8 * g + c;
         const int off = dim * 128 + (((kc >> 3) ^ (dim & 7)) << 4) + (kc & 7) * 2;
         T hv, lv;
         Split<T>::go(v[c], hv, lv);
@@ -526,48 +561,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<T*>(vlo + off) = lv;
       }
     };
-    // LayerNorm of acc (TMEM columns tcol + [64 half, +64)) + bias + residual
-    // (the X buffer); the two halves of a row merge their (mean, M2) with
-    // Chan's formula through an exchange pair used by this LayerNorm only.
-    auto layernorm = [&](uint32_t tcol, int vb, int vg, int vbe, bool resid_lo, float* xm, float* xq,
-                         float* v) {
-      tmem_ld32_nw(trow + tcol + 64 * half, v);
-      tmem_ld32_nw(trow + tcol + 64 * half + 32, v + 32);
+    // LayerNorm of acc (TMEM columns tcol + [32g, +32)) + bias + residual
+    // (the X buffer): per-group (mean, M2) over 32 columns, merged through
+    // the exchange with Chan's formula, (01)(23) then the two pairs.
+    auto layernorm = [&](uint32_t tcol, const float* bias, const float* gam, const float* bet,
+                         bool resid_lo, float* v) {
+      tmem_ld32_nw(trow + tcol + 32 * g, v);
       tmem_wait_ld();
+      const int kh = g >> 1;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int cc = 0; cc < 4; ++cc) {
         float x8[8];
-        get8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), resid_lo, x8);
+        get8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), resid_lo, x8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[c8 * 8 + e] += x8[e];
+        for (int e = 0; e < 8; ++e) v[cc * 8 + e] += x8[e];
       }
-      add_vec<64>(v, vec + vb + 64 * half);
+      add_vec<32>(v, bias + 32 * g);
       float mean = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mean += v[c];
-      mean *= (1.f / 64.f);
+      for (int c = 0; c < 32; ++c) mean += v[c];
+      mean *= (1.f / 32.f);
       float m2v = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
-      xm[half * 128 + r] = mean;
-      xq[half * 128 + r] = m2v;
+      for (int c = 0; c < 32; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
+      ex[g * 128 + r] = mean;
+      ex[(4 + g) * 128 + r] = m2v;
       bar_compute();
-      const float om = xm[(1 - half) * 128 + r], om2 = xq[(1 - half) * 128 + r];
-      const float ma = half == 0 ? mean : om, mb = half == 0 ? om : mean;
-      const float qa = half == 0 ? m2v : om2, qb = half == 0 ? om2 : m2v;
-      const float delta = mb - ma;
-      const float mu = ma + 0.5f * delta;
-      const float var = (qa + qb + delta * delta * 32.f) * (1.f / 128.f);
-      const float rstd = rsqrtf(var + 1e-5f);
-      const float4* g4 = reinterpret_cast<const float4*>(vec + vg + 64 * half);
-      const float4* e4 = reinterpret_cast<const float4*>(vec + vbe + 64 * half);
+      float mg[4], qg[4];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 g = g4[c4], e = e4[c4];
-        v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * g.x + e.x;
-        v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * g.y + e.y;
-        v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * g.z + e.z;
-        v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * g.w + e.w;
+      for (int k = 0; k < 4; ++k) {
+        mg[k] = ex[k * 128 + r];
+        qg[k] = ex[(4 + k) * 128 + r];
+      }
+      const float d01 = mg[1] - mg[0], d23 = mg[3] - mg[2];
+      const float m01 = mg[0] + 0.5f * d01, m23 = mg[2] + 0.5f * d23;
+      const float q01 = qg[0] + qg[1] + d01 * d01 * 16.f, q23 = qg[2] + qg[3] + d23 * d23 * 16.f;
+      const float dd = m23 - m01;
+      const float mu = m01 + 0.5f * dd;
+      const float var = (q01 + q23 + dd * dd * 32.f) * (1.f / 128.f);
+      const float rstd = rsqrtf(var + 1e-5f);
+      const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * g);
+      const float4* e4 = reinterpret_cast<const float4*>(bet + 32 * g);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 gg = __ldg(g4 + c4), e = __ldg(e4 + c4);
+        v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * gg.x + e.x;
+        v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * gg.y + e.y;
+        v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * gg.z + e.z;
+        v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * gg.w + e.w;
       }
     };
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -580,167 +621,168 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int limit = min(i + 1, vl);   // visible keys of this row: [sq*L, sq*L + limit)
       const size_t grow = (size_t)t * 128 + r;
-      const int k0 = 64 * half;                                 // my key half
-      const bool own = (k0 <= sq * L) && (sq * L < k0 + 64);    // my half holds my sequence
       for (int l = 0; l < a.n_layers && ok; ++l) {
         const MegaLayer& P = a.layers[l];
         const bool first = l == 0;
         if (!wait(B_QKV_DONE, c_qkv)) { ok = false; break; }
-        // Stage this layer's vectors.  Every reader of the previous layer's
-        // values finished before the QKV product could start.
-        for (int k = threadIdx.x - 128; k < 1152 + a.dff; k += kCompute) {
-          float v;
-          if (k < 384) v = P.b_qkv[k];
-          else if (k < 512) v = P.b_o[k - 384];
-          else if (k < 640) v = P.ln1_g[k - 512];
-          else if (k < 768) v = P.ln1_b[k - 640];
-          else if (k < 896) v = P.b_2[k - 768];
-          else if (k < 1024) v = P.ln2_g[k - 896];
-          else if (k < 1152) v = P.ln2_b[k - 1024];
-          else v = P.b_1[k - 1152];
-          vec[k] = v;
-        }
-        if (threadIdx.x == 128) {
-          for (int h = 0; h < kH; ++h) kmax_s[h] = 0;
+        // Every reader of the previous layer's maxima finished before the
+        // QKV product could start.
+        if (threadIdx.x == kCtrlWarps * 32) {
+          for (int k = 0; k < 2 * kH; ++k) kmax_s[k] = 0;
         }
         bar_compute();
-        convert_qk(0);
-        convert_v(0);
+        convert_qk(0, P);
+        convert_v(0, P);
         arrive(B_QKVH_READY);
         for (int h = 0; h < kH && ok; ++h) {
-          // ---- softmax of S = Q_h K_h^T over the row's visible keys
+          // ---- softmax of S = Q_h K_h^T over the row's visible keys; this
+          // group holds own chunks g + 4m (keys 8 (g + 4m) .. + 8)
           if (!wait(B_S_DONE, c_s)) { ok = false; break; }
-          float s[64];
-          if (own) {
-            tmem_ld32_nw(trow + 384 + k0, s);
-            tmem_ld32_nw(trow + 384 + k0 + 32, s + 32);
-            tmem_wait_ld();
-          }
+          float s[8 * NM];
+#pragma unroll
+          for (int m = 0; m < NM; ++m) tmem_ld8_nw(trow + 384 + sq * L + 8 * (g + 4 * m), s + 8 * m);
+          tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + B_S_FREE);
-          if (own) {
-            const float qn = sqrtf(qn2_s[(h & 1) * 128 + r]);
-            const float kmx = __int_as_float(kmax_s[h]);
-            // the second-best score matters only where fp32 scores can be off
-            const bool track = __any_sync(0xffffffffu, neartie_err(qn, kmx, kDH) > kTieErrMin);
-            float m1 = -INFINITY, m2 = -INFINITY;
-            if (track) {
+          const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
+          const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
+          // the second-best score matters only where fp32 scores can be off
+          const bool track = neartie_err(qn, kmx, kDH) > kTieErrMin;
+          float m1 = -INFINITY, m2 = -INFINITY;
 #pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const int key = k0 + c;
-                const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
-                s[c] = v;
-                m2 = fmaxf(m2, fminf(m1, v));
-                m1 = fmaxf(m1, v);
-              }
-            } else {
+          for (int m = 0; m < NM; ++m)
 #pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const int key = k0 + c;
-                const float v = (key >= sq * L && key < sq * L + limit) ? s[c] * scale_log2 : -INFINITY;
-                s[c] = v;
-                m1 = fmaxf(m1, v);
-              }
+            for (int e = 0; e < 8; ++e) {
+              const int kk = 8 * (g + 4 * m) + e;
+              const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
+              s[8 * m + e] = v;
+              m2 = fmaxf(m2, fminf(m1, v));
+              m1 = fmaxf(m1, v);
             }
-            const bool flag = track && row_valid &&
-                              neartie_flag((m1 - m2) * 0.69314718055994531f, qn, kmx, kDH);
-            unsigned fl = __ballot_sync(0xffffffffu, flag);
-            float lt = 0.f;
-            while (fl) {
-              // fp64 correction of this warp's flagged rows (rare)
-              const int src = __ffs(fl) - 1;
-              fl &= fl - 1;
-              float sc0 = 0.f, sc1 = 0.f;
+          ex[g * 128 + r] = m1;
+          ex[(4 + g) * 128 + r] = m2;
+          if (track) {
+            // park the raw scores in this row's P slots for a possible fp64 fix-up
 #pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const float v = __shfl_sync(0xffffffffu, s[c], src) * 0.69314718055994531f;
-                if (lane == (c & 31)) {
-                  if (c < 32) sc0 = v;
-                  else sc1 = v;
-                }
+            for (int m = 0; m < NM; ++m) {
+              uint4 hv, lv;
+              uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
+              uint32_t* lw = reinterpret_cast<uint32_t*>(&lv);
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint32_t b0 = __float_as_uint(s[8 * m + 2 * w]), b1 = __float_as_uint(s[8 * m + 2 * w + 1]);
+                hw[w] = (b0 >> 16) | (b1 & 0xFFFF0000u);
+                lw[w] = (b0 & 0xFFFFu) | (b1 << 16);
               }
-              float w0, w1, lrow;
-              fixup_row<T, L>(sm, P, qd * 32 + src, h, first, lane, k0, sc0, sc1, kmx, w0, w1, lrow);
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const float w = __shfl_sync(0xffffffffu, c < 32 ? w0 : w1, c & 31);
-                if (lane == src) s[c] = w;
-              }
-              if (lane == src) lt = lrow;
-            }
-            if (!flag) {
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                s[c] = exp2f(s[c] - m1);  // probabilities, in place
-                lt += s[c];
-              }
-            }
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), s + 8 * c8);
-            l_s[h * 128 + r] = lt;
-          } else {
-            // keys of other sequences: probability 0
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              *reinterpret_cast<uint4*>(pbuf + half * kTile16 + sw128(r, c8)) = z;
-              *reinterpret_cast<uint4*>(pbuf + (2 + half) * kTile16 + sw128(r, c8)) = z;
+              const int kc = sq * L + 8 * (g + 4 * m);
+              int ho, lo;
+              p_slot(r, kc, ho, lo);
+              *reinterpret_cast<uint4*>(sm + ho) = hv;
+              *reinterpret_cast<uint4*>(sm + lo) = lv;
             }
           }
+          bar_compute();
+          float M1 = -INFINITY, M2 = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float a1 = ex[k * 128 + r], a2 = ex[(4 + k) * 128 + r];
+            M2 = fmaxf(fmaxf(M2, a2), fminf(M1, a1));
+            M1 = fmaxf(M1, a1);
+          }
+          const bool flag = track && row_valid &&
+                            neartie_flag((M1 - M2) * 0.69314718055994531f, qn, kmx, kDH);
+          float lt = 0.f;
+          if (!flag) {
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                s[8 * m + e] = exp2f(s[8 * m + e] - M1);  // probabilities, in place
+                lt += s[8 * m + e];
+              }
+              int ho, lo;
+              p_slot(r, sq * L + 8 * (g + 4 * m), ho, lo);
+              put8<T>(sm + ho, sm + lo, 0, s + 8 * m);
+            }
+          }
+          if (h == 0) {
+            // keys of the other sequences: probability 0 (these chunks keep it for the layer)
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int kc = 8 * (g + 4 * m);
+              if (kc >= sq * L && kc < sq * L + L) continue;
+              int ho, lo;
+              p_slot(r, kc, ho, lo);
+              *reinterpret_cast<uint4*>(sm + ho) = z;
+              *reinterpret_cast<uint4*>(sm + lo) = z;
+            }
+          }
+          if (g == 0) {
+            // fp64 correction of this warp's flagged rows (rare)
+            unsigned fl = __ballot_sync(0xffffffffu, flag);
+            while (fl) {
+              const int src = __ffs(fl) - 1;
+              fl &= fl - 1;
+              const int rr = qd * 32 + src;
+              const float kmx_src = __shfl_sync(0xffffffffu, kmx, src);
+              const float lrow = fixup_row<T, L>(sm, P, rr, rr / L, h, first, lane, kmx_src);
+              if (lane == src) lt = lrow;
+            }
+          }
+          l_s[(h * 4 + g) * 128 + r] = lt;
           arrive(B_P_READY);
           if (h + 1 < kH) {
             // Q_{h+1}, K_{h+1} may overwrite Q_h, K_h now (S_h is done); V
             // waits until P_h V_h has read V_h.
-            convert_qk(h + 1);
+            convert_qk(h + 1, P);
             if (!wait(B_O_DONE, c_o)) { ok = false; break; }
-            convert_v(h + 1);
+            convert_v(h + 1, P);
             arrive(B_QKVH_READY);
           }
         }
         if (!ok) break;
-        // ---- ctx = O / l -> PB (hi, lo); half h takes heads 2h, 2h + 1
+        // ---- ctx = O / l -> PB (hi, lo); group g takes head g
         if (!wait(B_O_DONE, c_o)) { ok = false; break; }
         {
-          float o[64];
-          tmem_ld32_nw(trow + 64 * half, o);
-          tmem_ld32_nw(trow + 64 * half + 32, o + 32);
+          float o[32];
+          tmem_ld32_nw(trow + 32 * g, o);
           tmem_wait_ld();
-          const float inv0 = 1.f / l_s[(2 * half) * 128 + r];
-          const float inv1 = 1.f / l_s[(2 * half + 1) * 128 + r];
+          const float lsum = l_s[(g * 4) * 128 + r] + l_s[(g * 4 + 1) * 128 + r] +
+                             l_s[(g * 4 + 2) * 128 + r] + l_s[(g * 4 + 3) * 128 + r];
+          const float inv = 1.f / lsum;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] *= inv0;
+          for (int c = 0; c < 32; ++c) o[c] *= inv;
+          const int kh = g >> 1;
 #pragma unroll
-          for (int c = 32; c < 64; ++c) o[c] *= inv1;
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            put8<T>(pbuf + half * kTile16, pbuf + (2 + half) * kTile16, sw128(r, c8), o + 8 * c8);
+          for (int cc = 0; cc < 4; ++cc)
+            put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), o + 8 * cc);
         }
         arrive(B_CTX_READY);
         // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
         if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
         {
-          float y[64];
-          layernorm(128, V_BO, V_G1, V_BE1, !first, reinterpret_cast<float*>(sm + kXA1),
-                    reinterpret_cast<float*>(sm + kXB1), y);
+          float y[32];
+          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, y);
+          const int kh = g >> 1;
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), y + 8 * c8);
+          for (int cc = 0; cc < 4; ++cc)
+            put8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), y + 8 * cc);
         }
         arrive(B_Y_READY);
         // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB half (c % 2)
         for (int c = 0; c < n_chunks && ok; ++c) {
           const int buf = c & 1;
           if (!wait(B_F1_DONE + buf, c_f1[buf])) { ok = false; break; }
-          float hv[32];
-          tmem_ld32_nw(trow + 256 + 64 * buf + 32 * half, hv);
+          float hv[16];
+          tmem_ld16_nw(trow + 256 + 64 * buf + 16 * g, hv);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + B_F1_FREE + buf);
-          const float4* b4 = reinterpret_cast<const float4*>(vec + V_B1 + 64 * c + 32 * half);
+          const float4* b4 = reinterpret_cast<const float4*>(P.b_1 + 64 * c + 16 * g);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 b = b4[c4];
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 b = __ldg(b4 + c4);
             hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
             hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
             hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
@@ -752,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           unsigned char* hb = pbuf + buf * 2 * kTile16;
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) put8<T>(hb, hb + kTile16, sw128(r, 4 * half + c8), hv + 8 * c8);
+          for (int cc = 0; cc < 2; ++cc) put8<T>(hb, hb + kTile16, sw128(r, 2 * g + cc), hv + 8 * cc);
           arrive(B_H_READY);
         }
         if (!ok) break;
@@ -764,18 +806,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait(B_H_FREE + (c & 1), c_hfree[c & 1]);
         if (!ok) break;
         {
-          float xo[64];
-          layernorm(0, V_B2, V_G2, V_BE2, true, reinterpret_cast<float*>(sm + kXA2),
-                    reinterpret_cast<float*>(sm + kXB2), xo);
+          float xo[32];
+          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, xo);
+          const int kh = g >> 1;
           if (l + 1 < a.n_layers) {
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              put8<T>(xa + half * kTile16, xa + (2 + half) * kTile16, sw128(r, c8), xo + 8 * c8);
+            for (int cc = 0; cc < 4; ++cc)
+              put8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), xo + 8 * cc);
             arrive(B_A_READY);
           } else if (row_valid && grow < (size_t)T_rows) {
-            T* dst = reinterpret_cast<T*>(a.out) + grow * kD + 64 * half;
+            T* dst = reinterpret_cast<T*>(a.out) + grow * kD + 32 * g;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c8 = 0; c8 < 4; ++c8) {
               uint4 u;
               T* up = reinterpret_cast<T*>(&u);
 #pragma unroll
