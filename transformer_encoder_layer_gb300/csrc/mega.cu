@@ -62,7 +62,8 @@ constexpr int kCtrlWarps = 2;
 constexpr int kCompute = 512;
 constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
-constexpr int kNW = 2;  // weight ring depth
+constexpr int kNW = 2;     // regular weight ring slots
+constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/V buffers
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16-bit
@@ -85,13 +86,20 @@ constexpr int kMaxDff = 512;
 
 // mbarrier indices
 enum {
-  B_X_FULL = 0, B_W_FULL, B_W_FULL1, B_W_EMPTY, B_W_EMPTY1, B_A_READY, B_QKV_DONE, B_QKVH_READY,
+  B_X_FULL = 0, B_W_FULL, B_W_EMPTY = B_W_FULL + kNSlot, B_A_READY = B_W_EMPTY + kNSlot,
+  B_QKV_DONE, B_QKVH_READY,
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC, B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget");
+
+// Weight slot st: the two regular ring slots, then (FFN boxes only) the
+// Q/K/V buffers, which are free from the end of the layer's out-projection
+// until its next QKV product.  FFN boxes of a layer take slots 0, 1, 2, 3,
+// 4, 0, ... in turn from slot 0; the other boxes alternate between 0 and 1.
+__device__ __forceinline__ int wslot_off(int st) { return st < kNW ? kWR + st * kTile16 : kQB + (st - kNW) * kTile16; }
 
 __device__ __forceinline__ int sw128(int r, int c8) { return r * 128 + ((c8 ^ (r & 7)) << 4); }
 __device__ __forceinline__ int sw64(int r, int c_bytes) {
@@ -321,15 +329,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ================================================================ TMA
     if (lane == 0) {
-      long long w_it = 0, tiles_done = 0;
+      long long tiles_done = 0;
+      int reg_it = 0, ffn_it = 0;
+      uint32_t par = 0, used = 0, out_par = 0;  // per-slot phase parity, slots ever loaded
       bool ok = true;
-      auto wload = [&](const CUtensorMap* m, int x, int y, uint32_t bytes) -> bool {
-        const int st = (int)(w_it % kNW);
-        const uint32_t ph = (uint32_t)((w_it / kNW) & 1);
-        if (!mbar_wait(bar + B_W_EMPTY + st, ph ^ 1, abort, status)) return false;
+      auto wload = [&](const CUtensorMap* m, int x, int y, uint32_t bytes, bool ffn) -> bool {
+        const int idx = ffn ? ffn_it++ : reg_it++;
+        const int st = ffn ? idx % kNSlot : idx % kNW;
+        if (ffn && idx == kNW) {
+          // the layer's first borrowed slot: its attention must be over
+          if (!mbar_wait(bar + B_OUT_DONE, out_par, abort, status)) return false;
+          out_par ^= 1;
+        }
+        if (!mbar_wait(bar + B_W_EMPTY + st, ((par >> st) & 1) ^ 1, abort, status)) return false;
         mbar_arrive_expect_tx(bar + B_W_FULL + st, bytes);
-        tma_load_2d(sm + kWR + st * kTile16, m, bar + B_W_FULL + st, x, y);
-        ++w_it;
+        tma_load_2d(sm + wslot_off(st), m, bar + B_W_FULL + st, x, y);
+        par ^= 1u << st;
+        used |= 1u << st;
         return true;
       };
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles_done) {
@@ -340,26 +356,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int l = 0; l < a.n_layers && ok; ++l) {
           const MegaLayer& P = a.layers[l];
           for (int nb = 0; nb < 3 && ok; ++nb)
-            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16);
-          for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16);
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16, false);
+          for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
+          ffn_it = 0;  // at least three FFN boxes per layer: slot 2 is used, OUT_DONE waited once
           for (int c = 0; c <= n_chunks && ok; ++c) {
             if (c < n_chunks)  // W_1 rows [64c, 64c + 64): two 64 x 64 boxes
-              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 64 * c, kTile16 / 2);
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 64 * c, kTile16 / 2, true);
             if (c >= 1 && ok)  // W_2 columns [64(c-1), 64c): one 128 x 64 box
-              ok = wload(P.map_2, 64 * (c - 1), 0, kTile16);
+              ok = wload(P.map_2, 64 * (c - 1), 0, kTile16, true);
           }
         }
       }
-      // Drain the loads in flight.
-      for (long long r = 1; r <= w_it && r <= kNW; ++r) {
-        const long long it = w_it - r;
-        mbar_wait_bounded(bar + B_W_FULL + (int)(it % kNW), (uint32_t)((it / kNW) & 1), status);
-      }
+      // Drain the loads in flight: each slot's last load.
+      for (int st = 0; st < kNSlot; ++st)
+        if ((used >> st) & 1) mbar_wait_bounded(bar + B_W_FULL + st, ((par >> st) & 1) ^ 1, status);
       if (tiles_done > 0) mbar_wait_bounded(bar + B_X_FULL, (uint32_t)((tiles_done - 1) & 1), status);
     }
   } else if (warp == 1) {
     // ================================================================ MMA
-    long long w_it = 0;
+    int reg_it = 0, ffn_it = 0;  // the same slot sequence as the TMA thread
+    uint32_t par = 0;            // per-slot phase parity
     const uint32_t id128 = idesc_f16(128, 128, kBf);
     const uint32_t id64 = idesc_f16(128, 64, kBf);
     const uint32_t id32 = idesc_f16(128, 32, kBf);
@@ -369,12 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One weight box against A (one or two planes x 4 k16 steps) into d.
     // A is a 128 x 64 tile at a_base; its lo plane is part_stride further on
     // (part_stride 0: the hi plane only).
-    auto wbox = [&](uint32_t d, uint32_t a_base, uint32_t part_stride, uint32_t idesc, bool first) -> bool {
-      const int st = (int)(w_it % kNW);
-      if (!mbar_wait(bar + B_W_FULL + st, (uint32_t)((w_it / kNW) & 1), abort, status)) return false;
+    auto wbox = [&](uint32_t d, uint32_t a_base, uint32_t part_stride, uint32_t idesc, bool first,
+                    bool ffn) -> bool {
+      const int st = ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
+      if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
+      par ^= 1u << st;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t w = smem_u32(sm + kWR + st * kTile16);
+        const uint32_t w = smem_u32(sm + wslot_off(st));
         const int parts = part_stride == 0 ? 1 : 2;
         for (int p = 0; p < parts; ++p) {
 #pragma unroll
@@ -385,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar + B_W_EMPTY + st);
       }
       __syncwarp();
-      ++w_it;
       return true;
     };
     auto commit = [&](int b) {
@@ -408,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pstride = l == 0 ? 0u : 2u * kTile16;
         for (int nb = 0; nb < 3 && ok; ++nb)
           for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, pstride, id128, kh == 0);
+            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, pstride, id128, kh == 0, false);
         if (!ok) break;
         commit(B_QKV_DONE);
         // ---- attention, head by head
@@ -451,23 +468,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- out-projection
         ok = wait(B_CTX_READY, c_ctx);
         for (int kh = 0; kh < 2 && ok; ++kh)
-          ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0);
+          ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
         if (!ok) break;
         commit(B_OUT_DONE);
         // ---- FFN in 64-wide chunks; h_c alternates between the two halves of PB
         ok = wait(B_Y_READY, c_y);
+        ffn_it = 0;
         for (int c = 0; c <= n_chunks && ok; ++c) {
           if (c < n_chunks) {
             const int buf = c & 1;
             ok = wait(B_F1_FREE + buf, c_f1free[buf], true);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox(tmem + 256 + 64 * buf, xa + kh * kTile16, 2u * kTile16, id64, kh == 0);
+              ok = wbox(tmem + 256 + 64 * buf, xa + kh * kTile16, 2u * kTile16, id64, kh == 0, true);
             if (!ok) break;
             commit(B_F1_DONE + buf);
           }
           if (c >= 1) {
             const int hb = (c - 1) & 1;
-            ok = wait(B_H_READY, c_hr) && wbox(tmem, pb + hb * 2 * kTile16, kTile16, id128, c == 1);
+            ok = wait(B_H_READY, c_hr) && wbox(tmem, pb + hb * 2 * kTile16, kTile16, id128, c == 1, true);
             if (!ok) break;
             commit(B_H_FREE + hb);
           }
