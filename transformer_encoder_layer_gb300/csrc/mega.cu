@@ -10,10 +10,11 @@
 // (fp16 or bf16); activations are carried as (hi, lo) 16-bit pairs wherever
 // they feed a tensor-core product.
 //
-// One CTA per SM, persistent over tiles.  576 threads:
+// One CTA per SM, persistent over tiles.  640 threads in five warpgroups:
 //   control  warp 0  TMA: the input tile (once per tile) and weight boxes
 //                    from L2 into a 2-deep ring, in the order the MMAs use them
 //            warp 1  TMEM (all 512 columns); one thread issues every MMA
+//            warps 2, 3 idle (they lend their registers: setmaxnreg)
 //   compute  16 warps in four column groups g = 0..3 of four warps; the four
 //            warps of a group cover the 128 rows (TMEM lane quarters), and
 //            group g takes columns [32g, 32g + 32) of a 128-wide row, head
@@ -58,7 +59,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kCtrlWarps = 2;
+constexpr int kCtrlWarps = 4;  // one warpgroup: TMA, MMA, two idle warps
 constexpr int kCompute = 512;
 constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
@@ -280,8 +281,10 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
   return (float)ws;
 }
 
-// 576 threads: registers are granted to warps in groups of four, so the 18
-// warps hold 20 warps' worth, 96 registers per thread.
+// Registers: 96 per thread at launch (an SM sub-partition holds five warps
+// of 16384 / 5 / 32 registers); setmaxnreg then moves them from the control
+// warpgroup (64 each) to the compute warps (104 each): 128 x 64 + 512 x 104
+// = 61440 = 640 x 96, and per sub-partition 32 x (64 + 4 x 104) <= 16384.
 template <typename T, int L>
 __global__ void __launch_bounds__(kThreads, 1)
     mega_kernel(const __grid_constant__ CUtensorMap map_x, const MegaArgs a) {
@@ -324,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   volatile int* abort = abort_flag;
   int* status = a.status;
-  // Every thread keeps the launch's 96 registers.
   if (warp < kCtrlWarps) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
   if (warp == 0) {
     // ================================================================ TMA
     if (lane == 0) {
@@ -498,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(bar + B_MMA_DONE, 0, status);
   }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
     // ======================================================== compute warps
     const int cw = warp - kCtrlWarps;      // 0..15
     const int g = cw >> 2;                 // column group
