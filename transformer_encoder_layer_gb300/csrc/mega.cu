@@ -80,10 +80,11 @@ constexpr int kQn2 = kMisc;                           // [2 head parity][2 group
 constexpr int kEx = kQn2 + 2 * 2 * 128 * 4;           // [2][4 group][128] exchange: (m1, m2) or (mean, M2)
 constexpr int kLs = kEx + 2 * 4 * 128 * 4;            // [4 head][4 group][128] partial softmax sums
 constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max partial |k|^2 (float bits)
-constexpr int kBars = kKmax + 64;
+constexpr int kMaxDff = 512;
+constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
+constexpr int kBars = kVec + (384 + kMaxDff) * 4;
 constexpr int kNumBars = 32;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
-constexpr int kMaxDff = 512;
 
 // mbarrier indices
 enum {
@@ -172,14 +173,14 @@ __device__ __forceinline__ void get8(const unsigned char* hi, const unsigned cha
     for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
   }
 }
-// v[0..N) += vec[0..N): a layer vector in global memory (read through L1),
-// N a multiple of 4, vec 16-byte aligned.
+// v[0..N) += vec[0..N), N a multiple of 4, vec 16-byte aligned (shared or
+// global memory).
 template <int N>
 __device__ __forceinline__ void add_vec(float* v, const float* vec) {
   const float4* b4 = reinterpret_cast<const float4*>(vec);
 #pragma unroll
   for (int c = 0; c < N / 4; ++c) {
-    const float4 b = __ldg(b4 + c);
+    const float4 b = b4[c];
     v[4 * c] += b.x; v[4 * c + 1] += b.y; v[4 * c + 2] += b.z; v[4 * c + 3] += b.w;
   }
 }
@@ -514,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* ex = reinterpret_cast<float*>(sm + kEx);
     float* l_s = reinterpret_cast<float*>(sm + kLs);
     int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
+    const float* vec_s = reinterpret_cast<const float*>(sm + kVec);  // b_qkv, then b_1 at 384
     unsigned char* xa = sm + kXA;
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col = (isq ? 0 : 128) + 32 * h + c0;
       tmem_ld16_nw(trow + col, v);
       tmem_wait_ld();
-      add_vec<16>(v, P.b_qkv + col);
+      add_vec<16>(v, vec_s + col);
       float n2 = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) n2 = fmaf(v[c], v[c], n2);
@@ -569,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[8];
       tmem_ld8_nw(trow + 256 + 32 * h + 8 * g, v);
       tmem_wait_ld();
-      add_vec<8>(v, P.b_qkv + 256 + 32 * h + 8 * g);
+      add_vec<8>(v, vec_s + 256 + 32 * h + 8 * g);
       const int kh = r >> 6, kc = r & 63;
       unsigned char* vh = sm + kVB + kh * 4096;
       unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
@@ -652,6 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == kCtrlWarps * 32) {
           for (int k = 0; k < 2 * kH; ++k) kmax_s[k] = 0;
         }
+        // Stage this layer's b_qkv and b_1 (the previous layer's readers are done).
+        for (int k = threadIdx.x - kCtrlWarps * 32; k < 384 + a.dff; k += kCompute)
+          reinterpret_cast<float*>(sm + kVec)[k] = k < 384 ? P.b_qkv[k] : P.b_1[k - 384];
         bar_compute();
         convert_qk(0, P);
         convert_v(0, P);
@@ -801,10 +806,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + B_F1_FREE + buf);
-          const float4* b4 = reinterpret_cast<const float4*>(P.b_1 + 64 * c + 16 * g);
+          const float4* b4 = reinterpret_cast<const float4*>(vec_s + 384 + 64 * c + 16 * g);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 b = __ldg(b4 + c4);
+            const float4 b = b4[c4];
             hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
             hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
             hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
