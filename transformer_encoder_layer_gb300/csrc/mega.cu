@@ -31,12 +31,16 @@
 //         V waits for P_h V_h.  The row maximum (and the second best score)
 //         is merged across the four groups through shared memory.
 //   ctx = O / l -> shared memory (hi, lo)
-//   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> X buffer
+//   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> TMEM
+//         [128, 256) as (hi, lo) 16-bit pairs, the A operand of FFN1 read
+//         straight from tensor memory
 //   FFN   per 64-wide chunk c of d_ff: acc1[256 + 64 (c % 2)] = y . W_1c^T,
-//         h_c = gelu(acc1 + b_1c) -> one of two shared-memory buffers,
-//         acc2[0, 128) += h_c . W_2c^T; GELU of chunk c overlaps the two
-//         products of chunks c - 1 and c + 1
+//         h_c = gelu(acc1 + b_1c) -> TMEM [384 + 64 (c % 2), +64) as (hi, lo),
+//         acc2[0, 128) += h_c . W_2c^T (A from tensor memory again); GELU of
+//         chunk c overlaps the two products of chunks c - 1 and c + 1.  Only
+//         the weights are read from shared memory by these products.
 //   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
+//         (y read back from tensor memory)
 // The LayerNorm statistics of a row merge the four groups' (mean, M2) with
 // Chan's pairwise formula in a fixed order.
 //
@@ -63,6 +67,8 @@ constexpr int kCtrlWarps = 4;  // one warpgroup: TMA, MMA, two idle warps
 constexpr int kCompute = 512;
 constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
+constexpr int kTY = 128;   // TMEM columns of y (hi [128, 192), lo [192, 256))
+constexpr int kTH = 384;   // TMEM columns of the GELU chunks: buffer b hi at 384 + 64 b, lo + 32
 constexpr int kNW = 2;     // regular weight ring slots
 constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/V buffers
 
@@ -149,6 +155,32 @@ __device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, float* v) {
                : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 8 / 16 32-bit columns of this thread's TMEM lane; call tmem_wait_st()
+// before signalling that they are written.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* w) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// D (+)= A . B^T with A read from tensor memory (128 lanes = rows, K packed
+// two 16-bit elements per 32-bit column) and B from a shared-memory descriptor.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
 template <typename T>
@@ -172,6 +204,14 @@ __device__ __forceinline__ void get8(const unsigned char* hi, const unsigned cha
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
   }
+}
+// The two 16-bit values packed in a 32-bit word (element 2e in the low half).
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
 }
 // v[0..N) += vec[0..N), N a multiple of 4, vec 16-byte aligned (shared or
 // global memory).
@@ -409,6 +449,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
+    // The same with A in tensor memory: columns a_col + 8 k (k16 step k) of
+    // the hi part, part_cols further on for the lo part.
+    auto wbox_ta = [&](uint32_t d, uint32_t a_col, uint32_t part_cols, uint32_t idesc, bool first,
+                       bool ffn) -> bool {
+      const int st = ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
+      if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
+      par ^= 1u << st;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t w = smem_u32(sm + wslot_off(st));
+        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16_ta(d, tmem + a_col + p * part_cols + 8 * k, sdesc_sw128(w + k * 32), idesc,
+                       (first && p == 0 && k == 0) ? 0u : 1u);
+        }
+        mma_commit(bar + B_W_EMPTY + st);
+      }
+      __syncwarp();
+      return true;
+    };
     auto commit = [&](int b) {
       if (lane == 0) mma_commit(bar + b);
       __syncwarp();
@@ -483,13 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = c & 1;
             ok = wait(B_F1_FREE + buf, c_f1free[buf], true);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox(tmem + 256 + 64 * buf, xa + kh * kTile16, 2u * kTile16, id64, kh == 0, true);
+              ok = wbox_ta(tmem + 256 + 64 * buf, kTY + 32 * kh, 64, id64, kh == 0, true);
             if (!ok) break;
             commit(B_F1_DONE + buf);
           }
           if (c >= 1) {
             const int hb = (c - 1) & 1;
-            ok = wait(B_H_READY, c_hr) && wbox(tmem, pb + hb * 2 * kTile16, kTile16, id128, c == 1, true);
+            ok = wait(B_H_READY, c_hr) && wbox_ta(tmem, kTH + 64 * hb, 32, id128, c == 1, true);
             if (!ok) break;
             commit(B_H_FREE + hb);
           }
@@ -589,16 +650,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (the X buffer): per-group (mean, M2) over 32 columns, merged through
     // the exchange with Chan's formula, (01)(23) then the two pairs.
     auto layernorm = [&](uint32_t tcol, const float* bias, const float* gam, const float* bet,
-                         bool resid_lo, float* v) {
+                         bool resid_lo, bool resid_tmem, float* v) {
       tmem_ld32_nw(trow + tcol + 32 * g, v);
-      tmem_wait_ld();
-      const int kh = g >> 1;
+      if (resid_tmem) {
+        // the residual y: (hi, lo) words [16g, 16g + 16) of TMEM columns kTY, kTY + 64
+        uint32_t hw[16], lw[16];
+        tmem_ld16_nw(trow + kTY + 16 * g, reinterpret_cast<float*>(hw));
+        tmem_ld16_nw(trow + kTY + 64 + 16 * g, reinterpret_cast<float*>(lw));
+        tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float x8[8];
-        get8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), resid_lo, x8);
+        for (int e = 0; e < 16; ++e) {
+          const float2 a2 = unpack2<T>(hw[e]), b2 = unpack2<T>(lw[e]);
+          v[2 * e] += a2.x + b2.x;
+          v[2 * e + 1] += a2.y + b2.y;
+        }
+      } else {
+        tmem_wait_ld();
+        const int kh = g >> 1;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[cc * 8 + e] += x8[e];
+        for (int cc = 0; cc < 4; ++cc) {
+          float x8[8];
+          get8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), resid_lo, x8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[cc * 8 + e] += x8[e];
+        }
       }
       add_vec<32>(v, bias + 32 * g);
       float mean = 0.f;
@@ -790,11 +865,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
         {
           float y[32];
-          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, y);
-          const int kh = g >> 1;
+          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, false, y);
+          // y -> TMEM [128, 256) as (hi, lo) words: group g holds K columns
+          // [32g, 32g + 32).  Every group read its out-projection accumulator
+          // (the same columns) before the LayerNorm's exchange barrier.
+          uint32_t hw[16], lw[16];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
-            put8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), y + 8 * cc);
+            split8(y + 8 * cc, *reinterpret_cast<uint4*>(hw + 4 * cc), *reinterpret_cast<uint4*>(lw + 4 * cc), T());
+          tmem_st16(trow + kTY + 16 * g, hw);
+          tmem_st16(trow + kTY + 64 + 16 * g, lw);
+          tmem_wait_st();
         }
         arrive(B_Y_READY);
         // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB half (c % 2)
@@ -819,9 +900,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this buffer last fed the second product of chunk c - 2
             if (!wait(B_H_FREE + buf, c_hfree[buf])) { ok = false; break; }
           }
-          unsigned char* hb = pbuf + buf * 2 * kTile16;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) put8<T>(hb, hb + kTile16, sw128(r, 2 * g + cc), hv + 8 * cc);
+          // h_c -> TMEM as (hi, lo) words: group g holds the chunk's K columns [16g, 16g + 16)
+          uint32_t hw[8], lw[8];
+          split8(hv, *reinterpret_cast<uint4*>(hw), *reinterpret_cast<uint4*>(lw), T());
+          split8(hv + 8, *reinterpret_cast<uint4*>(hw + 4), *reinterpret_cast<uint4*>(lw + 4), T());
+          tmem_st8(trow + kTH + 64 * buf + 8 * g, hw);
+          tmem_st8(trow + kTH + 64 * buf + 32 + 8 * g, lw);
+          tmem_wait_st();
           arrive(B_H_READY);
         }
         if (!ok) break;
@@ -834,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         {
           float xo[32];
-          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, xo);
+          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo);
           const int kh = g >> 1;
           if (l + 1 < a.n_layers) {
 #pragma unroll
