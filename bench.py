@@ -97,16 +97,17 @@ def kernel_work(cls, shape, counts):
     return table.get(cls)
 
 
-def traffic_from_profiles(cls):
-    """DRAM bytes per launch of kernel class `cls` from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+def traffic_from_profiles(cls, workload):
+    """DRAM bytes per launch of kernel class `cls` on `workload` from the
+    committed ncu summary (an entry "cls@workload", else "cls"), if it was
+    taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         t = json.load(f)
-    e = t.get(cls)
-    if not e:
+    e = t.get(f"{cls}@{workload}") or t.get(cls)
+    if not e or e.get("workload", workload) != workload:
         return None
     src = os.path.join(ROOT, "transformer_encoder_layer_gb300", "csrc", e["source"])
     if not os.path.exists(src):
@@ -343,7 +344,7 @@ def run_ours(args, shape):
             achieved, peak, unit = (n_launch_work / avg_s / 1e12,
                                     peaks["bf16_tflops_sustained"], "TFLOP/s")
         roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic_from_profiles(dom),
+                "frac": achieved / peak, "traffic": traffic_from_profiles(dom, shape.name),
                 "peak_source": peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max clock)"
                                                   if bound == "alu" else ""),
                 "share_of_step": ms / total_ms if total_ms else None,
