@@ -40,6 +40,12 @@ using namespace tc;
 constexpr int kThreads = 192;
 constexpr int kBQ = 128, kBKV = 64, kStages = 3;
 
+// CTAs per SM: head_dim 16 fits two (about 97 KB of shared memory and 256
+// TMEM columns each), which doubles the softmax warps per SM sub-partition,
+// the bound at that head size; larger heads keep one.
+template <int DH>
+constexpr int ctas_per_sm() { return DH == 16 ? 2 : 1; }
+
 // Shared-memory descriptor for a K-major operand whose rows are `row_bytes`
 // (32, 64 or 128) long, swizzled at the same width: 8-row atoms of
 // 8*row_bytes bytes.
@@ -79,7 +85,7 @@ struct Layout {
 };
 
 template <typename T, int DH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     tc_attention_kernel(const __grid_constant__ CUtensorMap mqh, const __grid_constant__ CUtensorMap mql,
                         const __grid_constant__ CUtensorMap mkh, const __grid_constant__ CUtensorMap mkl,
                         const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
@@ -418,7 +424,8 @@ cudaError_t launch_dh(const TcAttnArgs& a, const CUtensorMap* maps, int grid, cu
   const size_t smem = Lay::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  static_assert(ctas_per_sm<DH>() * (Lay::kBytes + 1024) <= 232448, "shared memory per SM");
+  k<<<grid * ctas_per_sm<DH>(), kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
   return cudaGetLastError();
 }
 
@@ -439,7 +446,7 @@ cudaError_t tc_attention(const TcAttnArgs& a, bool bf16, int num_sms, cudaStream
             make_tmap_2d(&maps[5], a.vt_lo, bf16, (uint64_t)a.B * a.H * dh, a.Lp, a.Lp, kBKV, dh, 128);
   if (!ok) return cudaErrorInvalidValue;
   const int items = a.B * a.H * ((a.L + kBQ - 1) / kBQ);
-  const int grid = items < num_sms ? items : num_sms;
+  const int grid = items < num_sms ? items : num_sms;  // per resident CTA slot (launch_dh scales)
   if (bf16) {
     if (dh == 16) return launch_dh<__nv_bfloat16, 16>(a, maps, grid, s);
     if (dh == 32) return launch_dh<__nv_bfloat16, 32>(a, maps, grid, s);
