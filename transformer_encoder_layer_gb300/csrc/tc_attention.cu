@@ -307,6 +307,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         ok = false;
         break;
       }
+      // The second-best score matters only where fp32 scores can be off.
+      const float kmax_plane = __int_as_float(a.kmax[plane]);
+      const bool track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
       // Fold O_{jo} (computed against the running max after tile jo) into acc.
       auto fold_o = [&](int jo) -> bool {
         const int ob = (int)(o_it & 1);
@@ -349,13 +352,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const int k0 = j * kBKV;
         const bool needs_mask = k0 + kBKV > full_keys;
         float tmax = -INFINITY;
+        if (track) {
 #pragma unroll
-        for (int c = 0; c < kBKV; ++c) {
-          float v = s[c] * scale_log2;
-          if (needs_mask && k0 + c >= limit) v = -INFINITY;
-          s[c] = v;
-          m2 = fmaxf(m2, fminf(fmaxf(m, tmax), v));
-          tmax = fmaxf(tmax, v);
+          for (int c = 0; c < kBKV; ++c) {
+            float v = s[c] * scale_log2;
+            if (needs_mask && k0 + c >= limit) v = -INFINITY;
+            s[c] = v;
+            m2 = fmaxf(m2, fminf(fmaxf(m, tmax), v));
+            tmax = fmaxf(tmax, v);
+          }
+        } else {
+          // no near tie possible for this row: the second-best score is not needed
+#pragma unroll
+          for (int c = 0; c < kBKV; ++c) {
+            float v = s[c] * scale_log2;
+            if (needs_mask && k0 + c >= limit) v = -INFINITY;
+            s[c] = v;
+            tmax = fmaxf(tmax, v);
+          }
         }
         const float mn = fmaxf(m, tmax);
         // A row with no visible key in this tile keeps its max; its
@@ -371,15 +385,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         unsigned char* pl = ph + Lay::kPBytes;
 #pragma unroll
         for (int c8 = 0; c8 < kBKV / 8; ++c8) {
-          uint4 hv, lv;
-          T* hp = reinterpret_cast<T*>(&hv);
-          T* lp = reinterpret_cast<T*>(&lv);
+          float p8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float p = exp2f(s[c8 * 8 + e] - mref);
-            l += p;
-            Split<T>::go(p, hp[e], lp[e]);
+            p8[e] = exp2f(s[c8 * 8 + e] - mref);
+            l += p8[e];
           }
+          uint4 hv, lv;
+          split8(p8, hv, lv, T());
           const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(ph + off) = hv;
           *reinterpret_cast<uint4*>(pl + off) = lv;
@@ -403,8 +416,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           *reinterpret_cast<uint4*>(ctx_hi + at + c8 * 8) = hv;
           *reinterpret_cast<uint4*>(ctx_lo + at + c8 * 8) = lv;
         }
-        const float kmax = __int_as_float(a.kmax[plane]);
-        if (neartie_flag((m - m2) * 0.69314718055994531f, sqrtf(qn2), kmax, DH))
+        if (track && neartie_flag((m - m2) * 0.69314718055994531f, sqrtf(qn2), kmax_plane, DH))
           neartie_push(a.ties, plane * a.L + i);
       }
     }
