@@ -93,6 +93,7 @@ def kernel_work(cls, shape, counts):
         "tc_gemm_ffn2_ln": ("tensor", pl["ffn2"]),
         "megakernel": ("tensor", counts["flops"]),
         "dag": ("alu", counts["flops"]),
+        "megakernel_simt": ("alu", counts["flops"]),
     }
     return table.get(cls)
 
@@ -353,7 +354,7 @@ def run_ours(args, shape):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if path in ("simt", "dag") else shape.dtype, "data": "synthetic",
+        "dtype": "f32" if shape.dtype == "f32" else shape.dtype, "data": "synthetic",
         "config": {"workload": shape.name, "n_layers": shape.n_layers, "d_model": shape.d_model,
                    "n_heads": shape.n_heads, "d_ff": shape.d_ff, "batch_per_gpu": shape.batch,
                    "global_batch": ws * shape.batch, "seq_len": shape.seq_len,

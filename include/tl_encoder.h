@@ -64,7 +64,10 @@ typedef enum {
  *   LAYERED   tcgen05/TMEM GEMMs fed by TMA with fused epilogues, plus the
  *             flash-attention kernel; one launch per step per layer
  *   MEGA      sequence-resident megakernel: every layer of a 128-row tile of
- *             whole sequences in one CTA, activations kept on chip
+ *             whole sequences in one CTA, activations kept on chip (16-bit
+ *             I/O, d_model 128, tensor cores); for fp32 I/O with d_model <= 64,
+ *             head_dim <= 32, L <= 64 and d_ff <= 256, one sequence per CTA
+ *             on CUDA cores
  *   DAG       persistent task-graph megakernel for fp32 I/O and few tokens:
  *             one launch per forward; CTAs pop (layer, step, row block, tile)
  *             tasks from a queue and wait on per-row-block counters

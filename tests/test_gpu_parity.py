@@ -259,15 +259,40 @@ def test_dag_shapes(d, H, dff, n_layers, batch, L, vl_lo, scale):
     _check(make_inputs(s, seed=7, input_scale=scale), "dag")
 
 
-def test_dag_is_auto_for_fp32_small_batches():
+def test_auto_dispatch_for_fp32():
     from transformer_encoder_layer_gb300 import binding
-    for name in ("batch1_d256_L512", "tiny_d32_L32"):
+    for name, want in (("batch1_d256_L512", "dag"), ("tiny_d32_L32", "mega")):
         s = SHAPES[name]
         inp = make_inputs(s.with_(batch=1, seq_len=1, vl_lo=1, vl_hi=1))
         enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
-        assert enc.plan(s.batch, s.seq_len) == "dag"
-        assert enc.plan(64, 1024) == "simt"  # 65536 tokens: layer by layer
+        assert enc.plan(s.batch, s.seq_len) == want
+        assert enc.plan(64, 1024) == "simt"  # 65536 tokens of long sequences: layer by layer
         enc.close()
+
+
+# ------------------------------------- sequence-resident path, CUDA cores
+@pytest.mark.parametrize("d,H,dff,n_layers,batch,L", [
+    (32, 2, 128, 2, 4, 32),     # the d32 workload's layer
+    (64, 2, 256, 2, 3, 64),     # head_dim 32, the largest supported sizes
+    (64, 4, 256, 3, 5, 17),     # head_dim 16, ragged length
+    (32, 1, 64, 1, 2, 1),       # one token
+    (48, 3, 192, 2, 3, 40),     # head_dim 16, d not a power of two
+])
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_mega_simt_shapes(d, H, dff, n_layers, batch, L, scale):
+    s = tiny_shape(dtype="f32", batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=dff, n_layers=n_layers)
+    assert "mega" in _paths_for(s)
+    _check(make_inputs(s, seed=8, input_scale=scale), "mega")
+
+
+def test_mega_simt_matches_dag_and_simt():
+    s = SHAPES["tiny_d32_L32"]
+    inp = make_inputs(s, seed=12)
+    a = _run(inp, "mega")
+    assert np.array_equal(a, _run(inp, "mega"))  # deterministic
+    for other in ("dag", "simt"):
+        assert np.max(np.abs(a - _run(inp, other))) < 1e-4
 
 
 def test_dag_deterministic_and_matches_simt():

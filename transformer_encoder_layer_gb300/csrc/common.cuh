@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/tl_encoder.h"
 
 namespace tl {
@@ -43,6 +45,38 @@ __device__ __forceinline__ int load_valid_len(const int32_t* vl, int b, int L, i
     v = v < 1 ? 1 : L;
   }
   return v;
+}
+
+// ------------------------------------------- launch configuration cache
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) is a driver call of some
+// microseconds; launchers call this instead, which sets the attribute once
+// per (kernel, device) and again only when a larger size is asked for.
+inline cudaError_t set_max_dyn_smem(const void* func, size_t bytes) {
+  struct Entry { const void* f; int dev; size_t bytes; };
+  static Entry table[128];
+  static int n = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (table[i].f == func && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (table[i].f == func && table[i].dev == dev) { table[i].bytes = bytes; return cudaSuccess; }
+  if (n < 128) table[n++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
+// ------------------------------------------------------ L2 prefetch
+// Thread idx of `stride` cooperating threads prefetches its share of the
+// 128-byte lines of [p, p + bytes) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, int idx, int stride) {
+  const char* c = reinterpret_cast<const char*>(p);
+  for (size_t off = (size_t)idx * 128; off < bytes; off += (size_t)stride * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
 }
 
 // ------------------------------------------------------ warp reductions

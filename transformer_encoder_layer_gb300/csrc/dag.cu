@@ -470,6 +470,9 @@ __global__ void __launch_bounds__(kThreads, dag_ctas_per_sm<DH>()) dag_kernel(co
     return min(((last_row / L + 1) * L - 1) / R, RB - 1);
   };
 
+  // Every layer's parameters into L2, spread over all threads of the grid.
+  for (int l = 0; l < a.n_layers; ++l)
+    prefetch_layer_l2(a.layers[l], d, a.dff, 4, blockIdx.x * kThreads + tid, gridDim.x * kThreads);
   int next = 0;
   if (tid == 0) next = atomicAdd(a.head, 1);
   while (true) {
@@ -612,7 +615,7 @@ cudaError_t launch(const DagArgs& a, int total, int num_sms, cudaStream_t s) {
   const int grid = total < per_sm * num_sms ? total : per_sm * num_sms;  // all resident
   const size_t smem = dag_dyn_smem(a.d, DH);
   auto k = dag_kernel<DH>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();

@@ -24,11 +24,29 @@ struct tl_layer_dev {
   const float* ln2_g; const float* ln2_b;
 };
 
+// Prefetch every parameter array of layer P (dtype element size es) into L2,
+// as thread idx of `stride` cooperating threads.
+__device__ __forceinline__ void prefetch_layer_l2(const tl_layer_dev& P, int d, int dff, int es, int idx,
+                                                  int stride) {
+  tl::prefetch_l2(P.w_qkv, (size_t)3 * d * d * es, idx, stride);
+  tl::prefetch_l2(P.w_o, (size_t)d * d * es, idx, stride);
+  tl::prefetch_l2(P.w_1, (size_t)dff * d * es, idx, stride);
+  tl::prefetch_l2(P.w_2, (size_t)d * dff * es, idx, stride);
+  tl::prefetch_l2(P.b_qkv, (size_t)3 * d * 4, idx, stride);
+  tl::prefetch_l2(P.b_o, (size_t)d * 4, idx, stride);
+  tl::prefetch_l2(P.ln1_g, (size_t)d * 4, idx, stride);
+  tl::prefetch_l2(P.ln1_b, (size_t)d * 4, idx, stride);
+  tl::prefetch_l2(P.b_1, (size_t)dff * 4, idx, stride);
+  tl::prefetch_l2(P.b_2, (size_t)d * 4, idx, stride);
+  tl::prefetch_l2(P.ln2_g, (size_t)d * 4, idx, stride);
+  tl::prefetch_l2(P.ln2_b, (size_t)d * 4, idx, stride);
+}
+
 // Kernel classes for per-kernel timing (names in timing.cu).
 enum tl_kernel_class {
   KC_SIMT_GEMM_QKV = 0, KC_SIMT_ATTENTION, KC_SIMT_GEMM_OUT, KC_SIMT_LAYERNORM,
   KC_SIMT_GEMM_FFN1, KC_SIMT_GEMM_FFN2, KC_TC_GEMM_QKV, KC_TC_ATTENTION,
-  KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX, KC_DAG,
+  KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX, KC_DAG, KC_MEGA_SIMT,
   KC_COUNT
 };
 

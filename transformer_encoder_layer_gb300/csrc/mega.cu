@@ -956,7 +956,7 @@ template <typename T, int L>
 cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStream_t s) {
   auto k = mega_kernel<T, L>;
   const size_t smem = kSmemBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, smem, s>>>(mx, a);
   return cudaGetLastError();

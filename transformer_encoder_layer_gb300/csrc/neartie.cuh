@@ -56,7 +56,8 @@ __device__ __forceinline__ void neartie_push(NearTieList t, int entry) {
 }
 
 // How the fix-up reads tensors.  kind: 0 fp32, 1 fp16, 2 bf16, 3 fp16 hi/lo
-// pair (value = hi + lo), 4 bf16 hi/lo pair.
+// pair (value = hi + lo), 4 bf16 hi/lo pair: global memory, read through L2
+// only; 5 fp32 through a generic pointer (a CTA's own shared memory).
 struct Plane {
   const void* hi;
   const void* lo;

@@ -18,6 +18,7 @@ __device__ __forceinline__ double ld64(const Plane& p, size_t i) {
     case 0: return (double)__ldcg(reinterpret_cast<const float*>(p.hi) + i);
     case 1: return (double)__half2float(__ushort_as_half(h16(p.hi, i)));
     case 2: return (double)__bfloat162float(__ushort_as_bfloat16(h16(p.hi, i)));
+    case 5: return (double)reinterpret_cast<const float*>(p.hi)[i];  // fp32, generic (shared) memory
     case 3:
       return (double)__half2float(__ushort_as_half(h16(p.hi, i))) +
              (double)__half2float(__ushort_as_half(h16(p.lo, i)));

@@ -7,6 +7,7 @@
 #include <vector>
 #include "dag.h"
 #include "mega.h"
+#include "mega_simt.h"
 #include "tc_attention.h"
 #include "tc_gemm.h"
 
@@ -355,6 +356,7 @@ cudaError_t pack_extra(tl_encoder* h, void* dst, size_t bytes) {
 }
 
 bool mega_ok(const tl_encoder* h, int L) {
+  if (h->dtype == TL_F32) return mega_simt_supported(h->d, h->H, h->dff, L, h->n_layers, h->dtype);
   return h->mega_layers != nullptr && mega_supported(h->d, h->H, h->dff, L, h->dtype);
 }
 
@@ -371,7 +373,8 @@ tl_path choose_path(const tl_encoder* h, int B, int L) {
       return dag_ok(h) ? TL_PATH_DAG : TL_PATH_AUTO;
     case TL_PATH_AUTO:
       // The frozen plan table: short sequences of the d_model = 128 family
-      // stay resident in one CTA for the whole stack; other 16-bit shapes
+      // (16-bit, tensor cores) and of small fp32 models (d_model <= 64, CUDA
+      // cores) stay resident in one CTA for the whole stack; other 16-bit shapes
       // run the layered tensor-core path; fp32 I/O keeps fp32 weights, which
       // the 16-bit MMAs cannot hold exactly, and runs on the CUDA cores: in
       // one task-graph launch while the tokens fill a few waves of 64-row
@@ -396,6 +399,15 @@ cudaError_t run_path(tl_encoder* h, tl_path p, const void* x, int B, int L, cons
   if (p == TL_PATH_SIMT) return run_simt(h, x, B, L, vl, out, ws, s);
   if (p == TL_PATH_LAYERED) return run_layered(h, x, B, L, vl, out, ws, s);
   if (p == TL_PATH_DAG) return run_dag(h, x, B, L, vl, out, ws, s);
+  if (p == TL_PATH_MEGA && h->dtype == TL_F32) {
+    MegaSimtArgs a{};
+    for (int l = 0; l < h->n_layers; ++l) a.layers[l] = h->layers[l];
+    a.n_layers = h->n_layers;
+    a.x = (const float*)x; a.out = (float*)out; a.vl = vl; a.status = h->status;
+    a.B = B; a.L = L; a.d = h->d; a.H = h->H; a.dh = h->dh; a.dff = h->dff;
+    KernelTimer t(h, KC_MEGA_SIMT, s);
+    return mega_simt_forward(a, s);
+  }
   if (p == TL_PATH_MEGA) {
     MegaArgs a{(const MegaLayer*)h->mega_layers, h->n_layers, B, h->dff, vl, out, h->status};
     KernelTimer t(h, KC_MEGA, s);

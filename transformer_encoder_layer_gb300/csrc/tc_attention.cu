@@ -434,7 +434,7 @@ cudaError_t launch_dh(const TcAttnArgs& a, const CUtensorMap* maps, int grid, cu
   using Lay = Layout<T, DH>;
   auto k = tc_attention_kernel<T, DH>;
   const size_t smem = Lay::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   static_assert(ctas_per_sm<DH>() * (Lay::kBytes + 1024) <= 232448, "shared memory per SM");
   k<<<grid * ctas_per_sm<DH>(), kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);

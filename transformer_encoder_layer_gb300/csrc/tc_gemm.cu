@@ -397,7 +397,7 @@ template <typename T, int EPI>
 cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& mw,
                    const TcGemmArgs& a, int grid, size_t smem, cudaStream_t s) {
   auto k = tc_gemm_kernel<T, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, smem, s>>>(m0, m1, mw, a);
   return cudaGetLastError();

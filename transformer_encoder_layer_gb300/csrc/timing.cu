@@ -17,7 +17,7 @@ namespace {
 const char* kNames[KC_COUNT] = {
     "simt_gemm_qkv", "simt_attention", "simt_gemm_out", "simt_layernorm",
     "simt_gemm_ffn1", "simt_gemm_ffn2", "tc_gemm_qkv", "tc_attention",
-    "tc_gemm_out_ln", "tc_gemm_ffn1", "tc_gemm_ffn2_ln", "megakernel", "aux", "dag"};
+    "tc_gemm_out_ln", "tc_gemm_ffn1", "tc_gemm_ffn2_ln", "megakernel", "aux", "dag", "megakernel_simt"};
 }
 
 namespace tl {
