@@ -217,10 +217,10 @@ def test_forward_host_matches_device_forward():
 @pytest.mark.parametrize("dtype,L,dff,n_layers,batch", [
     ("f16", 64, 512, 4, 37),     # the d128 workload's layer, ragged last tile
     ("bf16", 64, 512, 2, 6),
-    ("f16", 32, 256, 2, 9),      # four sequences per tile
-    ("f16", 32, 128, 1, 3),      # d_ff = d
+    ("f16", 64, 256, 2, 9),
+    ("f16", 64, 128, 1, 3),      # d_ff = d
     ("bf16", 64, 384, 3, 2),
-    ("bf16", 32, 512, 2, 5),
+    ("bf16", 64, 512, 2, 5),
 ])
 @pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
 def test_mega_shapes(dtype, L, dff, n_layers, batch, scale):

@@ -75,10 +75,12 @@ constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16-bit
 constexpr int kXA = 0;                                // [part][khalf] x 16 KB = 64 KB
-constexpr int kPB = kXA + 4 * kTile16;                // P / ctx: [part][khalf]; FFN: 2 x [part]
+constexpr int kPB = kXA + 4 * kTile16;                // attention: P [part] 128 x 64 (own keys), then
+                                                      // V^T [buffer][part] 64 x 64; afterwards ctx [part][khalf]
+constexpr int kPV = kPB + 2 * kTile16;                // the two V^T buffers, 16 KB each (hi, lo 8 KB)
 constexpr int kQB = kPB + 4 * kTile16;                // [part] 128 x 32, 8 KB each
 constexpr int kKB = kQB + 2 * 8192;                   // [part] 128 x 32
-constexpr int kVB = kKB + 2 * 8192;                   // [part][khalf] 32 x 64, 4 KB each
+constexpr int kVB = kKB + 2 * 8192;                   // spare during attention; a weight slot in the FFN
 constexpr int kWR = kVB + 4 * 4096;                   // [kNW] x 16 KB
 constexpr int kMisc = kWR + kNW * kTile16;
 // misc (floats unless noted)
@@ -225,12 +227,11 @@ __device__ __forceinline__ void add_vec(float* v, const float* vec) {
   }
 }
 
-// The (hi, lo) slots of element (row rr, key column kc) of the P buffer.
-__device__ __forceinline__ void p_slot(int rr, int kc, int& hi_off, int& lo_off) {
-  const int kh = kc >> 6;
-  const int off = sw128(rr, (kc & 63) >> 3) + (kc & 7) * 2;
-  hi_off = kPB + kh * kTile16 + off;
-  lo_off = kPB + (2 + kh) * kTile16 + off;
+// The (hi, lo) slots of P for row rr and key kk of the row's own sequence.
+__device__ __forceinline__ void p_slot(int rr, int kk, int& hi_off, int& lo_off) {
+  const int off = sw128(rr, kk >> 3) + (kk & 7) * 2;
+  hi_off = kPB + off;
+  lo_off = kPB + kTile16 + off;
 }
 
 // fp64 correction of one flagged (row rr, head h), done by a whole warp.
@@ -257,7 +258,7 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
 #pragma unroll
   for (int m = 0; m < NK; ++m) {
     int ho, lo;
-    p_slot(rr, sq * L + lane + 32 * m, ho, lo);
+    p_slot(rr, lane + 32 * m, ho, lo);
     const uint32_t bits = ((uint32_t)*reinterpret_cast<const uint16_t*>(sm + ho) << 16) |
                           (uint32_t)*reinterpret_cast<const uint16_t*>(sm + lo);
     sc[m] = __uint_as_float(bits) * 0.69314718055994531f;
@@ -313,7 +314,7 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
     T hv, lv;
     Split<T>::go((float)e, hv, lv);
     int ho, lo;
-    p_slot(rr, sq * L + lane + 32 * m, ho, lo);
+    p_slot(rr, lane + 32 * m, ho, lo);
     *reinterpret_cast<T*>(sm + ho) = hv;
     *reinterpret_cast<T*>(sm + lo) = lv;
   }
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id32 = idesc_f16(128, 32, kBf);
     bool ok = true;
     const uint32_t xa = smem_u32(sm + kXA), pb = smem_u32(sm + kPB);
-    const uint32_t qb = smem_u32(sm + kQB), kb = smem_u32(sm + kKB), vb = smem_u32(sm + kVB);
+    const uint32_t qb = smem_u32(sm + kQB), kb = smem_u32(sm + kKB), pv = smem_u32(sm + kPV);
     // One weight box against A (one or two planes x 4 k16 steps) into d.
     // A is a 128 x 64 tile at a_base; its lo plane is part_stride further on
     // (part_stride 0: the hi plane only).
@@ -514,18 +515,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait(B_P_READY, c_p);
           if (!ok) break;
           if (lane == 0) {
-            // O_h = Ph.Vh + Ph.Vl + Pl.Vh over 128 keys (2 halves x 4 steps)
-            const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+            // O_h = Ph.Vh + Ph.Vl + Pl.Vh over the row's own 64 keys (4 steps):
+            // B holds both sequences' V side by side (N = 64), so row r's
+            // result is in columns [96h + 32 s, +32) of its sequence s.
+            const uint32_t vbuf = pv + (uint32_t)((h & 1) * kTile16);
+            const uint32_t as[3] = {pb, pb, pb + kTile16};
+            const uint32_t bs[3] = {vbuf, vbuf + kTile16 / 2, vbuf};
 #pragma unroll
             for (int c = 0; c < 3; ++c)
 #pragma unroll
-              for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_f16(tmem + 32 * h,
-                          sdesc_sw128(pb + (ap[c] * 2 + kh) * kTile16 + k * 32),
-                          sdesc_sw128(vb + (bp[c] * 2 + kh) * 4096 + k * 32), id32,
-                          (c | kh | k) != 0);
+              for (int k = 0; k < 4; ++k)
+                mma_f16(tmem + 96 * h, sdesc_sw128(as[c] + k * 32), sdesc_sw128(bs[c] + k * 32), id64,
+                        (c | k) != 0);
           }
           commit(B_O_DONE);
         }
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[16];
       const bool isq = g < 2;
       const int c0 = 16 * (g & 1);
-      const int col = (isq ? 0 : 128) + 32 * h + c0;
+      const int col = 96 * h + (isq ? 0 : 32) + c0;  // head h's q | k | v columns
       tmem_ld16_nw(trow + col, v);
       tmem_wait_ld();
       add_vec<16>(v, vec_s + col);
@@ -627,18 +628,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) atomicMax(kmax_s + 2 * h + (g & 1), __float_as_int(kn));
       }
     };
-    // V_h^T (hi, lo): this thread's key r, dims [8g, 8g + 8).
+    // V_h^T (hi, lo) into buffer h % 2: the two sequences side by side, row
+    // n = 32 s + dim, column = key position in sequence s.  This thread: key
+    // r (sequence r / 64, position r % 64), dims [8g, 8g + 8).
     auto convert_v = [&](int h, const MegaLayer& P) {
       float v[8];
-      tmem_ld8_nw(trow + 256 + 32 * h + 8 * g, v);
+      tmem_ld8_nw(trow + 96 * h + 64 + 8 * g, v);
       tmem_wait_ld();
-      add_vec<8>(v, vec_s + 256 + 32 * h + 8 * g);
-      const int kh = r >> 6, kc = r & 63;
-      unsigned char* vh = sm + kVB + kh * 4096;
-      unsigned char* vlo = sm + kVB + (2 + kh) * 4096;
+      add_vec<8>(v, vec_s + 96 * h + 64 + 8 * g);
+      const int sv = r >> 6, kc = r & 63;
+      unsigned char* vh = sm + kPV + (h & 1) * kTile16;
+      unsigned char* vlo = vh + kTile16 / 2;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const int dim = 8 * g + c;
+        const int dim = 32 * sv + 8 * g + c;
         const int off = dim * 128 + (((kc >> 3) ^ (dim & 7)) << 4) + (kc & 7) * 2;
         T hv, lv;
         Split<T>::go(v[c], hv, lv);
@@ -731,7 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Stage this layer's b_qkv and b_1 (the previous layer's readers are done).
         for (int k = threadIdx.x - kCtrlWarps * 32; k < 384 + a.dff; k += kCompute)
-          reinterpret_cast<float*>(sm + kVec)[k] = k < 384 ? P.b_qkv[k] : P.b_1[k - 384];
+          reinterpret_cast<float*>(sm + kVec)[k] =
+              k < 384 ? P.b_qkv[((k % 96) >> 5) * 128 + (k / 96) * 32 + (k & 31)]  // head-grouped order
+                      : P.b_1[k - 384];
         bar_compute();
         convert_qk(0, P);
         convert_v(0, P);
@@ -746,6 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + B_S_FREE);
+          // P is single-buffered: P_{h-1} V_{h-1} must be done before this head
+          // writes P (it is, since S_h completed after it; this also keeps the
+          // O_DONE barrier at most one phase ahead of this thread's waits)
+          if (h >= 1 && !wait(B_O_DONE, c_o)) { ok = false; break; }
           const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
           const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
           // the second-best score matters only where fp32 scores can be off
@@ -776,9 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hw[w] = (b0 >> 16) | (b1 & 0xFFFF0000u);
                 lw[w] = (b0 & 0xFFFFu) | (b1 << 16);
               }
-              const int kc = sq * L + 8 * (g + 4 * m);
               int ho, lo;
-              p_slot(r, kc, ho, lo);
+              p_slot(r, 8 * (g + 4 * m), ho, lo);
               *reinterpret_cast<uint4*>(sm + ho) = hv;
               *reinterpret_cast<uint4*>(sm + lo) = lv;
             }
@@ -803,21 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lt += s[8 * m + e];
               }
               int ho, lo;
-              p_slot(r, sq * L + 8 * (g + 4 * m), ho, lo);
+              p_slot(r, 8 * (g + 4 * m), ho, lo);
               put8<T>(sm + ho, sm + lo, 0, s + 8 * m);
-            }
-          }
-          if (h == 0) {
-            // keys of the other sequences: probability 0 (these chunks keep it for the layer)
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int kc = 8 * (g + 4 * m);
-              if (kc >= sq * L && kc < sq * L + L) continue;
-              int ho, lo;
-              p_slot(r, kc, ho, lo);
-              *reinterpret_cast<uint4*>(sm + ho) = z;
-              *reinterpret_cast<uint4*>(sm + lo) = z;
             }
           }
           if (g == 0) {
@@ -835,20 +830,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_s[(h * 4 + g) * 128 + r] = lt;
           arrive(B_P_READY);
           if (h + 1 < kH) {
-            // Q_{h+1}, K_{h+1} may overwrite Q_h, K_h now (S_h is done); V
-            // waits until P_h V_h has read V_h.
+            // Q_{h+1}, K_{h+1} may overwrite Q_h, K_h now (S_h is done); V goes
+            // to the other buffer, whose reader P_{h-1} V_{h-1} was waited for.
             convert_qk(h + 1, P);
-            if (!wait(B_O_DONE, c_o)) { ok = false; break; }
             convert_v(h + 1, P);
             arrive(B_QKVH_READY);
           }
         }
         if (!ok) break;
-        // ---- ctx = O / l -> PB (hi, lo); group g takes head g
+        // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
+        // sequence s are in TMEM columns 96g + 32s
         if (!wait(B_O_DONE, c_o)) { ok = false; break; }
         {
           float o[32];
-          tmem_ld32_nw(trow + 32 * g, o);
+          tmem_ld32_nw(trow + 96 * g + 32 * sq, o);
           tmem_wait_ld();
           const float lsum = l_s[(g * 4) * 128 + r] + l_s[(g * 4 + 1) * 128 + r] +
                              l_s[(g * 4 + 2) * 128 + r] + l_s[(g * 4 + 3) * 128 + r];
@@ -966,7 +961,7 @@ cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStr
 
 bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
   return d == kD && H == kH && dff % 128 == 0 && dff >= 128 && dff <= kMaxDff &&
-         (L == 32 || L == 64) && dt != TL_F32;
+         L == 64 && dt != TL_F32;
 }
 
 cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int num_sms, cudaStream_t s) {
@@ -976,10 +971,8 @@ cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int
   const int tiles = (a.B + S - 1) / S;
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (bf16) {
-    if (L == 32) return launch_l<__nv_bfloat16, 32>(mx, a, grid, s);
     return launch_l<__nv_bfloat16, 64>(mx, a, grid, s);
   }
-  if (L == 32) return launch_l<__half, 32>(mx, a, grid, s);
   return launch_l<__half, 64>(mx, a, grid, s);
 }
 

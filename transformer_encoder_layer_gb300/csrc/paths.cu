@@ -322,9 +322,13 @@ cudaError_t run_dag(tl_encoder* h, const void* x, int B, int L, const int32_t* v
 
 // Packed extras: per layer four weight tensor maps (for the megakernel's TMA
 // loads, which need them in device memory) followed by the MegaLayer array.
+// For the megakernel: per layer four weight tensor maps and a MegaLayer,
+// then a copy of W_qkv with its rows regrouped head by head (q_h, k_h, v_h
+// of head h are rows [96h, 96h + 96)), so that each head's projections land
+// in adjacent TMEM columns.
 size_t packed_extra_bytes(const tl_encoder* h) {
   if (h->dtype == TL_F32 || h->d != 128) return 0;
-  return (size_t)h->n_layers * (4 * sizeof(CUtensorMap) + sizeof(MegaLayer)) + 128;
+  return (size_t)h->n_layers * (4 * sizeof(CUtensorMap) + sizeof(MegaLayer) + 3 * 128 * 128 * 2) + 2048;
 }
 
 cudaError_t pack_extra(tl_encoder* h, void* dst, size_t bytes) {
@@ -334,11 +338,23 @@ cudaError_t pack_extra(tl_encoder* h, void* dst, size_t bytes) {
   char* base = (char*)(((uintptr_t)dst + 63) & ~(uintptr_t)63);
   CUtensorMap* maps_dev = (CUtensorMap*)base;
   MegaLayer* layers_dev = (MegaLayer*)(base + (size_t)nl * 4 * sizeof(CUtensorMap));
+  char* wperm = (char*)(((uintptr_t)(layers_dev + nl) + 1023) & ~(uintptr_t)1023);
+  const size_t wq_bytes = (size_t)3 * d * d * 2;
   std::vector<CUtensorMap> maps(4 * (size_t)nl);
   std::vector<MegaLayer> ml(nl);
+  const int H = h->H, dh = h->dh;
   for (int l = 0; l < nl; ++l) {
     const tl_layer_dev& P = h->layers[l];
-    bool ok = make_tmap_2d(&maps[4 * l + 0], P.w_qkv, bf, 3 * d, d, d, 64, 128, 128) &&
+    char* wq = wperm + (size_t)l * wq_bytes;
+    for (int hh = 0; hh < H; ++hh)
+      for (int part = 0; part < 3; ++part) {
+        const size_t rows = dh, row_bytes = (size_t)d * 2;
+        cudaError_t e = cudaMemcpy(wq + (size_t)(3 * dh * hh + dh * part) * row_bytes,
+                                   (const char*)P.w_qkv + (size_t)(part * d + dh * hh) * row_bytes,
+                                   rows * row_bytes, cudaMemcpyDeviceToDevice);
+        if (e != cudaSuccess) return e;
+      }
+    bool ok = make_tmap_2d(&maps[4 * l + 0], wq, bf, 3 * d, d, d, 64, 128, 128) &&
               make_tmap_2d(&maps[4 * l + 1], P.w_o, bf, d, d, d, 64, 128, 128) &&
               make_tmap_2d(&maps[4 * l + 2], P.w_1, bf, dff, d, d, 64, 64, 128) &&
               make_tmap_2d(&maps[4 * l + 3], P.w_2, bf, d, dff, dff, 64, 128, 128);
