@@ -40,7 +40,8 @@
 //         chunk c overlaps the two products of chunks c - 1 and c + 1.  Only
 //         the weights are read from shared memory by these products.
 //   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
-//         (y read back from tensor memory)
+//         (y read back from tensor memory); x' also goes to TMEM [384, 512)
+//         as (hi, lo) pairs, the next layer's QKV A operand
 // The LayerNorm statistics of a row merge the four groups' (mean, M2) with
 // Chan's pairwise formula in a fixed order.
 //
@@ -69,6 +70,7 @@ constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kTY = 128;   // TMEM columns of y (hi [128, 192), lo [192, 256))
 constexpr int kTH = 384;   // TMEM columns of the GELU chunks: buffer b hi at 384 + 64 b, lo + 32
+constexpr int kTX = 384;   // TMEM columns of the next layer's input (hi [384, 448), lo [448, 512))
 constexpr int kNW = 2;     // regular weight ring slots
 constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/V buffers
 
@@ -488,10 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int l = 0; l < a.n_layers && ok; ++l) {
         // ---- QKV (the first layer's input is exact in its hi plane)
         ok = l == 0 ? wait(B_X_FULL, c_x) : wait(B_A_READY, c_a);
-        const uint32_t pstride = l == 0 ? 0u : 2u * kTile16;
+        // layer 0: x from shared memory (exact in its hi plane); later layers:
+        // the (hi, lo) input LayerNorm 2 also left in TMEM [384, 512)
         for (int nb = 0; nb < 3 && ok; ++nb)
           for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = wbox(tmem + 128 * nb, xa + kh * kTile16, pstride, id128, kh == 0, false);
+            ok = l == 0 ? wbox(tmem + 128 * nb, xa + kh * kTile16, 0u, id128, kh == 0, false)
+                        : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
         if (!ok) break;
         commit(B_QKV_DONE);
         // ---- attention, head by head
@@ -917,9 +921,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo);
           const int kh = g >> 1;
           if (l + 1 < a.n_layers) {
+            // the next layer's input: X buffer (residual, fix-up) and TMEM
+            // [384, 512) as (hi, lo) words, the A operand of its QKV product
+            uint32_t hw[16], lw[16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < 4; ++cc) {
               put8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), xo + 8 * cc);
+              split8(xo + 8 * cc, *reinterpret_cast<uint4*>(hw + 4 * cc), *reinterpret_cast<uint4*>(lw + 4 * cc), T());
+            }
+            tmem_st16(trow + kTX + 16 * g, hw);
+            tmem_st16(trow + kTX + 64 + 16 * g, lw);
+            tmem_wait_st();
             arrive(B_A_READY);
           } else if (row_valid && grow < (size_t)T_rows) {
             T* dst = reinterpret_cast<T*>(a.out) + grow * kD + 32 * g;
