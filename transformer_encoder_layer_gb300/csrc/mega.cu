@@ -18,7 +18,7 @@
 //   compute  16 warps in four column groups g = 0..3 of four warps; the four
 //            warps of a group cover the 128 rows (TMEM lane quarters), and
 //            group g takes columns [32g, 32g + 32) of a 128-wide row, head
-//            g for the context, 16 of a 64-wide FFN chunk, and every 4th
+//            g for the context, 32 of a 128-wide FFN chunk, and every 4th
 //            8-key chunk of the attention scores.  Four warps per SM
 //            sub-partition hide the latency of the CUDA-core phases.
 //
@@ -34,11 +34,11 @@
 //   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> TMEM
 //         [128, 256) as (hi, lo) 16-bit pairs, the A operand of FFN1 read
 //         straight from tensor memory
-//   FFN   per 64-wide chunk c of d_ff: acc1[256 + 64 (c % 2)] = y . W_1c^T,
-//         h_c = gelu(acc1 + b_1c) -> TMEM [384 + 64 (c % 2), +64) as (hi, lo),
-//         acc2[0, 128) += h_c . W_2c^T (A from tensor memory again); GELU of
-//         chunk c overlaps the two products of chunks c - 1 and c + 1.  Only
-//         the weights are read from shared memory by these products.
+//   FFN   per 128-wide chunk c of d_ff: acc1[256 + 128 (c % 2), +128) =
+//         y . W_1c^T; h_c = gelu(acc1 + b_1c) replaces acc1 in the same TMEM
+//         columns as (hi, lo) words; acc2[0, 128) += h_c . W_2c^T (A from
+//         tensor memory again).  GELU of chunk c overlaps the products of
+//         chunks c - 1 and c + 1.  Only the weights come from shared memory.
 //   x' = LN2(acc2 + b_2 + y) -> X buffer, or the output rows on the last layer
 //         (y read back from tensor memory); x' also goes to TMEM [384, 512)
 //         as (hi, lo) pairs, the next layer's QKV A operand
@@ -69,7 +69,7 @@ constexpr int kCompute = 512;
 constexpr int kThreads = kCtrlWarps * 32 + kCompute;
 constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kTY = 128;   // TMEM columns of y (hi [128, 192), lo [192, 256))
-constexpr int kTH = 384;   // TMEM columns of the GELU chunks: buffer b hi at 384 + 64 b, lo + 32
+constexpr int kTF = 256;   // TMEM FFN buffers b = 0, 1 at 256 + 128 b: FFN1 accumulator, then h (hi, lo)
 constexpr int kTX = 384;   // TMEM columns of the next layer's input (hi [384, 448), lo [448, 512))
 constexpr int kNW = 2;     // regular weight ring slots
 constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/V buffers
@@ -159,13 +159,8 @@ __device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, float* v) {
                : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// 8 / 16 32-bit columns of this thread's TMEM lane; call tmem_wait_st()
+// 16 32-bit columns of this thread's TMEM lane; call tmem_wait_st()
 // before signalling that they are written.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* w) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -342,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int S = 128 / L;  // sequences per tile
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_tiles = (a.B + S - 1) / S;
-  const int n_chunks = a.dff / 64;  // 64-wide FFN chunks
+  const int n_chunks = a.dff / 128;  // 128-wide FFN chunks
   const int T_rows = a.B * L;
 
   if (threadIdx.x == 0) {
@@ -407,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
           ffn_it = 0;  // at least three FFN boxes per layer: slot 2 is used, OUT_DONE waited once
           for (int c = 0; c <= n_chunks && ok; ++c) {
-            if (c < n_chunks)  // W_1 rows [64c, 64c + 64): two 64 x 64 boxes
-              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 64 * c, kTile16 / 2, true);
-            if (c >= 1 && ok)  // W_2 columns [64(c-1), 64c): one 128 x 64 box
-              ok = wload(P.map_2, 64 * (c - 1), 0, kTile16, true);
+            if (c < n_chunks)  // W_1 rows [128c, 128c + 128): two 128 x 64 boxes
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 128 * c, kTile16, true);
+            if (c >= 1)  // W_2 columns [128(c-1), 128c): two 128 x 64 boxes
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_2, 128 * (c - 1) + 64 * kh, 0, kTile16, true);
           }
         }
       }
@@ -485,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     long long c_x = 0, c_a = 0, c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
-              c_f1free[2] = {0, 0}, c_hr = 0;
+              c_hfree[2] = {0, 0}, c_hr = 0;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       for (int l = 0; l < a.n_layers && ok; ++l) {
         // ---- QKV (the first layer's input is exact in its hi plane)
@@ -541,27 +536,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
         if (!ok) break;
         commit(B_OUT_DONE);
-        // ---- FFN in 64-wide chunks; h_c alternates between the two halves of PB
+        // ---- FFN in 128-wide chunks; chunk c uses TMEM buffer c % 2 for its
+        // FFN1 accumulator and then, rewritten by GELU, as FFN2's A operand
         ok = wait(B_Y_READY, c_y);
         ffn_it = 0;
         for (int c = 0; c <= n_chunks && ok; ++c) {
           if (c < n_chunks) {
             const int buf = c & 1;
-            ok = wait(B_F1_FREE + buf, c_f1free[buf], true);
+            // the buffer's last reader, FFN2 of chunk c - 2, must be done
+            if (c >= 2) ok = wait(B_H_FREE + buf, c_hfree[buf]);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox_ta(tmem + 256 + 64 * buf, kTY + 32 * kh, 64, id64, kh == 0, true);
+              ok = wbox_ta(tmem + kTF + 128 * buf, kTY + 32 * kh, 64, id128, kh == 0, true);
             if (!ok) break;
             commit(B_F1_DONE + buf);
           }
           if (c >= 1) {
             const int hb = (c - 1) & 1;
-            ok = wait(B_H_READY, c_hr) && wbox_ta(tmem, kTH + 64 * hb, 32, id128, c == 1, true);
+            ok = wait(B_H_READY, c_hr);
+            for (int kh = 0; kh < 2 && ok; ++kh)
+              ok = wbox_ta(tmem, kTF + 128 * hb + 32 * kh, 64, id128, c == 1 && kh == 0, true);
             if (!ok) break;
             commit(B_H_FREE + hb);
           }
         }
         if (!ok) break;
         commit(B_F2_DONE);
+        // keep the per-buffer release counts in step: the last two chunks'
+        // releases were not waited for in the loop
+        for (int c = (n_chunks >= 2 ? n_chunks - 2 : 0); c < n_chunks && ok; ++c)
+          ok = wait(B_H_FREE + (c & 1), c_hfree[c & 1]);
+        if (!ok) break;
       }
     }
     commit(B_MMA_DONE);
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
     constexpr int NM = L / 32;  // own 8-key chunks of a row per group
-    int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_hfree[2] = {0, 0}, c_f2 = 0,
+    int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_f2 = 0,
         c_sync = 0;  // completed phases per barrier (parity = count & 1)
     bool ok = true;
     auto wait = [&](int b, int& n) -> bool {
@@ -877,45 +881,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         arrive(B_Y_READY);
-        // ---- FFN chunks: h_c = gelu(acc1 + b_1) -> PB half (c % 2)
+        // ---- FFN chunks (128 wide): h_c = gelu(acc1 + b_1) replaces acc1 in
+        // its TMEM buffer as (hi, lo) words, the A operand of FFN2
         for (int c = 0; c < n_chunks && ok; ++c) {
           const int buf = c & 1;
+          const uint32_t tb = kTF + 128 * buf;
           if (!wait(B_F1_DONE + buf, c_f1[buf])) { ok = false; break; }
-          float hv[16];
-          tmem_ld16_nw(trow + 256 + 64 * buf + 16 * g, hv);
+          float hv[32];
+          tmem_ld32_nw(trow + tb + 32 * g, hv);
           tmem_wait_ld();
+          // every group has read its accumulator columns before any h words
+          // (which span other groups' columns) are written
           tc_fence_before();
-          mbar_arrive(bar + B_F1_FREE + buf);
-          const float4* b4 = reinterpret_cast<const float4*>(vec_s + 384 + 64 * c + 16 * g);
+          bar_compute();
+          tc_fence_after();
+          const float4* b4 = reinterpret_cast<const float4*>(vec_s + 384 + 128 * c + 32 * g);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < 8; ++c4) {
             const float4 b = b4[c4];
             hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
             hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
             hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
             hv[4 * c4 + 3] = gelu_as7128(hv[4 * c4 + 3] + b.w);
           }
-          if (c >= 2) {
-            // this buffer last fed the second product of chunk c - 2
-            if (!wait(B_H_FREE + buf, c_hfree[buf])) { ok = false; break; }
-          }
-          // h_c -> TMEM as (hi, lo) words: group g holds the chunk's K columns [16g, 16g + 16)
-          uint32_t hw[8], lw[8];
-          split8(hv, *reinterpret_cast<uint4*>(hw), *reinterpret_cast<uint4*>(lw), T());
-          split8(hv + 8, *reinterpret_cast<uint4*>(hw + 4), *reinterpret_cast<uint4*>(lw + 4), T());
-          tmem_st8(trow + kTH + 64 * buf + 8 * g, hw);
-          tmem_st8(trow + kTH + 64 * buf + 32 + 8 * g, lw);
+          // group g holds the chunk's K columns [32g, 32g + 32): words [16g, +16)
+          uint32_t hw[16], lw[16];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            split8(hv + 8 * cc, *reinterpret_cast<uint4*>(hw + 4 * cc), *reinterpret_cast<uint4*>(lw + 4 * cc), T());
+          tmem_st16(trow + tb + 16 * g, hw);
+          tmem_st16(trow + tb + 64 + 16 * g, lw);
           tmem_wait_st();
           arrive(B_H_READY);
         }
         if (!ok) break;
         // ---- FFN2 + b_2 + residual y, LayerNorm 2
         if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
-        // The last two chunks' buffer releases complete with f2_done: keep
-        // the per-buffer counts in step.
-        for (int c = (n_chunks >= 2 ? n_chunks - 2 : 0); c < n_chunks && ok; ++c)
-          ok = wait(B_H_FREE + (c & 1), c_hfree[c & 1]);
-        if (!ok) break;
         {
           float xo[32];
           layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo);

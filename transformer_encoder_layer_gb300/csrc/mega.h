@@ -13,7 +13,7 @@ namespace tl {
 struct MegaLayer {
   const CUtensorMap* map_qkv;  // W_qkv [384, 128], box 64 x 128, 128-byte swizzle
   const CUtensorMap* map_o;    // W_o [128, 128]
-  const CUtensorMap* map_1;    // W_1 [d_ff, 128], box 64 x 64
+  const CUtensorMap* map_1;    // W_1 [d_ff, 128], box 64 x 128
   const CUtensorMap* map_2;    // W_2 [128, d_ff]
   const void* w_qkv;           // raw W_qkv (near-tie correction)
   const float *b_qkv, *b_o, *ln1_g, *ln1_b, *b_1, *b_2, *ln2_g, *ln2_b;

@@ -356,7 +356,7 @@ cudaError_t pack_extra(tl_encoder* h, void* dst, size_t bytes) {
       }
     bool ok = make_tmap_2d(&maps[4 * l + 0], wq, bf, 3 * d, d, d, 64, 128, 128) &&
               make_tmap_2d(&maps[4 * l + 1], P.w_o, bf, d, d, d, 64, 128, 128) &&
-              make_tmap_2d(&maps[4 * l + 2], P.w_1, bf, dff, d, d, 64, 64, 128) &&
+              make_tmap_2d(&maps[4 * l + 2], P.w_1, bf, dff, d, d, 64, 128, 128) &&
               make_tmap_2d(&maps[4 * l + 3], P.w_2, bf, d, dff, dff, 64, 128, 128);
     if (!ok) return cudaSuccess;  // the megakernel path stays unavailable
     MegaLayer& m = ml[l];
