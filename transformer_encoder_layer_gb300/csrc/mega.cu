@@ -27,9 +27,10 @@
 //   per head h: Q_h, K_h, V_h^T -> shared memory as (hi, lo);
 //         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
 //         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32).
-//         Head h+1's Q and K are written as soon as S_h is done, so only its
-//         V waits for P_h V_h.  The row maximum (and the second best score)
-//         is merged across the four groups through shared memory.
+//         Head h+1's Q, K, V are written as soon as S_h has been read, so
+//         S_{h+1} runs during the softmax of head h (P V issued after it).
+//         The row maximum (and the second best score) is merged across the
+//         four groups through shared memory.
 //   ctx = O / l -> shared memory (hi, lo)
 //   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> TMEM
 //         [128, 256) as (hi, lo) 16-bit pairs, the A operand of FFN1 read
@@ -493,10 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
         if (!ok) break;
         commit(B_QKV_DONE);
-        // ---- attention, head by head
-        for (int h = 0; h < kH && ok; ++h) {
-          ok = wait(B_QKVH_READY, c_qkvh) && wait(B_S_FREE, c_sfree, true);
-          if (!ok) break;
+        // ---- attention: S_0, then per head h: S_{h+1} as soon as head h+1's
+        // Q, K, V are in shared memory, then P_h V_h, so the next scores are
+        // computed while the compute warps run the softmax of head h.
+        auto issue_s = [&](int h) -> bool {
+          if (!(wait(B_QKVH_READY, c_qkvh) && wait(B_S_FREE, c_sfree, true))) return false;
           // Release what the compute threads wrote before QKVH_READY (norms,
           // the tile's max |k|) to whoever acquires S_DONE.
           if (lane == 0) mbar_arrive(bar + B_S_DONE);
@@ -511,6 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (c | k) != 0);
           }
           commit(B_S_DONE);
+          return true;
+        };
+        ok = issue_s(0);
+        for (int h = 0; h < kH && ok; ++h) {
+          if (h + 1 < kH && !(ok = issue_s(h + 1))) break;
           ok = wait(B_P_READY, c_p);
           if (!ok) break;
           if (lane == 0) {
@@ -763,6 +770,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // writes P (it is, since S_h completed after it; this also keeps the
           // O_DONE barrier at most one phase ahead of this thread's waits)
           if (h >= 1 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+          if (h + 1 < kH) {
+            // head h+1's Q, K (their buffers' reader S_h is done) and V (its
+            // buffer's reader P_{h-1} V_{h-1} was just waited for), so that
+            // S_{h+1} runs during this softmax
+            convert_qk(h + 1, P);
+            convert_v(h + 1, P);
+            arrive(B_QKVH_READY);
+          }
           const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
           const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
           // the second-best score matters only where fp32 scores can be off
@@ -837,13 +852,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           l_s[(h * 4 + g) * 128 + r] = lt;
           arrive(B_P_READY);
-          if (h + 1 < kH) {
-            // Q_{h+1}, K_{h+1} may overwrite Q_h, K_h now (S_h is done); V goes
-            // to the other buffer, whose reader P_{h-1} V_{h-1} was waited for.
-            convert_qk(h + 1, P);
-            convert_v(h + 1, P);
-            arrive(B_QKVH_READY);
-          }
         }
         if (!ok) break;
         // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
