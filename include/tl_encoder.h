@@ -129,17 +129,32 @@ tl_status tl_encoder_forward(tl_encoder *h, const void *x, int B, int L,
                              const int32_t *valid_len, void *out, void *workspace,
                              size_t workspace_bytes, void *stream);
 
-/* Bytes of device workspace tl_encoder_forward_host() needs: the forward's
- * own scratch plus device copies of x, valid_len and out. */
+/* Bytes of device workspace tl_encoder_forward_host() needs: device copies of
+ * x, valid_len and out, plus the forward's own scratch for one batch slice
+ * (two slices' worth when the call pipelines more than one slice).  Depends
+ * on the handle's slice setting (tl_encoder_set_host_chunks). */
 tl_status tl_encoder_host_workspace_size(const tl_encoder *h, int B, int L, size_t *bytes);
 
 /* The forward pass on HOST buffers: copies x [B, L, d] and valid_len [B] from
- * host memory to the workspace, runs tl_encoder_forward on stream, copies the
- * result to out (host), and synchronises stream before returning.  Pinned
- * host memory makes the copies asynchronous DMA; pageable memory also works. */
+ * host memory to the workspace, runs the forward, copies the result to out
+ * (host), and synchronises before returning.  The batch is cut into slices of
+ * whole sequences that alternate between two internal streams (forked from
+ * and joined back to stream), so that one slice's upload, another's kernels
+ * and a third's download overlap; each sequence is computed from its own
+ * tokens only, so the result is bit-identical to tl_encoder_forward on the
+ * whole batch, and every slice runs the path chosen for the whole batch.
+ * Pinned host memory makes the copies asynchronous DMA; pageable memory also
+ * works, with less overlap.  On error, no copy is still in flight on return. */
 tl_status tl_encoder_forward_host(tl_encoder *h, const void *x_host, int B, int L,
                                   const int32_t *valid_len_host, void *out_host,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Batch slices tl_encoder_forward_host pipelines: 0 (the default) picks them
+ * from the batch's size and path (slices of at least 8 MiB, at most 8; at
+ * most 2 on the layered path; 1 on the task-graph path), 1 turns the pipeline
+ * off, 2..64 asks for that many (capped at B).  TL_ERR_INVALID_ARG outside
+ * 0..64. */
+tl_status tl_encoder_set_host_chunks(tl_encoder *h, int chunks);
 
 /* Synchronise stream, then read and clear the handle's device status word:
  * TL_OK, TL_ERR_BAD_VALID_LEN or TL_ERR_DEVICE_TIMEOUT (the first error seen

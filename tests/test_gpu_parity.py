@@ -213,6 +213,54 @@ def test_forward_host_matches_device_forward():
     enc.close()
 
 
+@pytest.mark.parametrize("path,dtype,d,H,dff,L,batch", [
+    ("mega", "f16", 128, 4, 512, 64, 37),
+    ("mega", "f32", 32, 2, 128, 32, 9),
+    ("layered", "bf16", 128, 2, 256, 96, 7),
+    ("dag", "f32", 64, 2, 256, 40, 5),
+    ("simt", "f32", 64, 4, 128, 33, 6),
+])
+@pytest.mark.parametrize("chunks", [0, 1, 2, 3, 64])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_slices_are_bit_identical(path, dtype, d, H, dff, L, batch, chunks, pinned):
+    """The host-buffer forward cut into batch slices on two streams gives the
+    device forward's bits, pinned or pageable, with a ragged last slice."""
+    from transformer_encoder_layer_gb300 import binding
+    s = tiny_shape(dtype=dtype, batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=dff, n_layers=2)
+    inp = make_inputs(s, seed=11)
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    enc.set_path(path)
+    assert enc.plan(batch, L) == path
+    enc.set_host_chunks(chunks)
+    xh = torch.from_numpy(to_storage(inp.x, dtype))
+    vh = torch.from_numpy(inp.valid_len.astype(np.int32))
+    oh = torch.empty_like(xh)
+    oh.view(torch.uint8).fill_(0xFF)  # NaN in every dtype: each element must be written
+    if pinned:
+        xh, vh, oh = xh.pin_memory(), vh.pin_memory(), oh.pin_memory()
+    enc.forward_host(xh, vh, oh)
+    od = enc.forward(xh.cuda(), vh.cuda()).cpu()
+    assert torch.equal(oh.view(torch.uint8), od.view(torch.uint8))
+    assert enc.get_status() == 0
+    enc.close()
+
+
+def test_host_chunks_setting_is_checked():
+    from transformer_encoder_layer_gb300 import binding
+    s = SHAPES["short_d128_L64_B4096"].with_(batch=4)
+    inp = make_inputs(s, seed=2)
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    for bad in (-1, 65):
+        with pytest.raises(RuntimeError):
+            enc.set_host_chunks(bad)
+    enc.set_host_chunks(1)
+    one = enc.host_workspace_size(4, 64)
+    enc.set_host_chunks(4)
+    assert enc.host_workspace_size(4, 64) >= one
+    enc.close()
+
+
 # ------------------------------------------------- sequence-resident path
 @pytest.mark.parametrize("dtype,L,dff,n_layers,batch", [
     ("f16", 64, 512, 4, 37),     # the d128 workload's layer, ragged last tile

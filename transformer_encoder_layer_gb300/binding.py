@@ -29,6 +29,7 @@ _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "tl_encoder_create": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_vp)]),
     "tl_encoder_set_path": (_i, [_vp, _i]),
+    "tl_encoder_set_host_chunks": (_i, [_vp, _i]),
     "tl_encoder_plan": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_workspace_size": (_i, [_vp, _i, _i, ctypes.POINTER(_sz)]),
     "tl_encoder_forward": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
@@ -155,6 +156,10 @@ class Encoder:
         _check(self.lib.tl_encoder_workspace_size(self.handle, B, L, ctypes.byref(n)),
                "tl_encoder_workspace_size")
         return n.value
+
+    def set_host_chunks(self, chunks: int):
+        """Batch slices forward_host pipelines (0 = automatic, 1 = off)."""
+        _check(self.lib.tl_encoder_set_host_chunks(self.handle, chunks), "tl_encoder_set_host_chunks")
 
     def host_workspace_size(self, B: int, L: int) -> int:
         n = ctypes.c_size_t()

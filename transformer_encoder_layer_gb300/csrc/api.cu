@@ -6,6 +6,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -83,6 +84,63 @@ bool fetch(const void* src, size_t bytes, std::vector<unsigned char>& dst) {
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+constexpr int kMaxHostChunks = 64;
+
+// How the host-buffer forward splits the batch.  Every path computes each
+// sequence from its own tokens only, so a slice of sequences yields the same
+// bits as the whole batch; slices alternate between two streams so that one
+// slice's upload, another's kernels and a third's download overlap.  The
+// path is the one chosen for the whole batch and every slice runs it.
+struct HostPlan {
+  tl_path p;
+  int chunks, bc;  // slices and sequences per slice (the last may be shorter)
+  size_t row;      // bytes of one sequence of x or out
+  size_t io;       // bytes of the device copy of x (and of out), padded
+  size_t fw;       // forward workspace of one slice, padded
+  size_t total;    // device workspace of the whole call
+};
+
+tl_status host_plan(const tl_encoder* h, int B, int L, HostPlan* hp) {
+  const tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  const size_t row = (size_t)L * h->d * dtype_size(h->dtype);
+  int n = h->host_chunks;
+  if (n == 0) {
+    // Automatic: slices of 8 MiB or more, at most 8; the layered path keeps
+    // at least half the batch per slice so that its per-kernel grids stay
+    // full; the task-graph path is sized for one launch over the batch.
+    n = (int)std::min<size_t>(8, (size_t)B * row / ((size_t)8 << 20));
+    if (p == TL_PATH_LAYERED) n = std::min(n, 2);
+    if (p == TL_PATH_DAG) n = 1;
+  }
+  if (row % 16) n = 1;  // every slice of x and out must stay 16-byte aligned
+  n = std::max(1, std::min(n, B));
+  const int bc = (B + n - 1) / n;
+  hp->p = p;
+  hp->chunks = (B + bc - 1) / bc;  // no empty slice
+  hp->bc = bc;
+  hp->row = row;
+  hp->io = align_up((size_t)B * row, 256);
+  hp->fw = align_up(path_workspace_bytes(h, p, bc, L), 256);
+  hp->total = 2 * hp->io + align_up((size_t)B * 4, 256) + (hp->chunks > 1 ? 2 : 1) * hp->fw;
+  return TL_OK;
+}
+
+// The pipeline's streams and events, made on first use on the current device.
+bool host_streams(tl_encoder* h) {
+  for (cudaStream_t& x : h->host_stream)
+    if (!x && cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) {
+      x = nullptr;
+      return false;
+    }
+  for (cudaEvent_t& x : h->host_event)
+    if (!x && cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) {
+      x = nullptr;
+      return false;
+    }
+  return true;
+}
 
 }  // namespace
 
@@ -243,12 +301,18 @@ tl_status tl_encoder_forward(tl_encoder* h, const void* x, int B, int L, const i
   return e == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }
 
+tl_status tl_encoder_set_host_chunks(tl_encoder* h, int chunks) {
+  if (!h || chunks < 0 || chunks > kMaxHostChunks) return TL_ERR_INVALID_ARG;
+  h->host_chunks = chunks;
+  return TL_OK;
+}
+
 tl_status tl_encoder_host_workspace_size(const tl_encoder* h, int B, int L, size_t* bytes) {
-  size_t fw = 0;
-  tl_status s = tl_encoder_workspace_size(h, B, L, &fw);
+  if (!h || !bytes || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  HostPlan hp;
+  tl_status s = host_plan(h, B, L, &hp);
   if (s != TL_OK) return s;
-  const size_t io = align_up((size_t)B * L * h->d * dtype_size(h->dtype), 256);
-  *bytes = 2 * io + align_up((size_t)B * 4, 256) + fw;
+  *bytes = hp.total;
   return TL_OK;
 }
 
@@ -257,28 +321,65 @@ tl_status tl_encoder_forward_host(tl_encoder* h, const void* x_host, int B, int 
                                   size_t workspace_bytes, void* stream) {
   if (!h || !x_host || !valid_len_host || !out_host || !workspace || B < 1 || L < 1)
     return TL_ERR_INVALID_ARG;
-  size_t need = 0;
-  tl_status s = tl_encoder_host_workspace_size(h, B, L, &need);
+  HostPlan hp;
+  tl_status s = host_plan(h, B, L, &hp);
   if (s != TL_OK) return s;
-  if (workspace_bytes < need) return TL_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < hp.total) return TL_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 256)) return TL_ERR_INVALID_ARG;
-  const size_t raw = (size_t)B * L * h->d * dtype_size(h->dtype);
-  const size_t io = align_up(raw, 256);
   char* w = (char*)workspace;
-  void* xd = w;
-  void* od = w + io;
-  int32_t* vld = (int32_t*)(w + 2 * io);
-  char* fw = w + 2 * io + align_up((size_t)B * 4, 256);
+  char* xd = w;
+  char* od = w + hp.io;
+  int32_t* vld = (int32_t*)(w + 2 * hp.io);
+  char* fw[2] = {w + 2 * hp.io + align_up((size_t)B * 4, 256), nullptr};
+  fw[1] = fw[0] + hp.fw;
+  const char* xh = (const char*)x_host;
+  char* oh = (char*)out_host;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(xd, x_host, raw, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(vld, valid_len_host, (size_t)B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return TL_ERR_CUDA;
-  s = tl_encoder_forward(h, xd, B, L, vld, od, fw, workspace_bytes - (fw - w), stream);
-  if (s != TL_OK) return s;
-  if (cudaMemcpyAsync(out_host, od, raw, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaStreamSynchronize(st) != cudaSuccess)
-    return TL_ERR_CUDA;
-  return TL_OK;
+  cudaStream_t ss[2] = {st, st};
+  cudaError_t e = cudaSuccess;
+  if (hp.chunks > 1) {
+    if (!host_streams(h)) return TL_ERR_CUDA;
+    ss[0] = h->host_stream[0];
+    ss[1] = h->host_stream[1];
+    // Fork: both pipeline streams start after the caller's earlier work.
+    if ((e = cudaEventRecord(h->host_event[0], st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ss[0], h->host_event[0], 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ss[1], h->host_event[0], 0)) != cudaSuccess)
+      return TL_ERR_CUDA;
+  }
+  // Slice c: upload, forward and download on stream c % 2.  The download of
+  // slice c - 1 is enqueued after slice c's forward, so that with pageable
+  // buffers (whose downloads return only when done) slice c still computes
+  // while slice c - 1 is copied back.
+  auto down = [&](int c) {
+    const size_t off = (size_t)c * hp.bc * hp.row;
+    const size_t bytes = (size_t)std::min(hp.bc, B - c * hp.bc) * hp.row;
+    return cudaMemcpyAsync(oh + off, od + off, bytes, cudaMemcpyDeviceToHost, ss[c & 1]);
+  };
+  for (int c = 0; c < hp.chunks && e == cudaSuccess; ++c) {
+    const int b0 = c * hp.bc, bn = std::min(hp.bc, B - b0);
+    const size_t off = (size_t)b0 * hp.row, bytes = (size_t)bn * hp.row;
+    cudaStream_t sc = ss[c & 1];
+    if ((e = cudaMemcpyAsync(xd + off, xh + off, bytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(vld + b0, valid_len_host + b0, (size_t)bn * 4, cudaMemcpyHostToDevice,
+                             sc)) != cudaSuccess ||
+        (e = run_path(h, hp.p, xd + off, bn, L, vld + b0, od + off, fw[c & 1], sc)) != cudaSuccess)
+      break;
+    if (c > 0) e = down(c - 1);
+  }
+  if (e == cudaSuccess) e = down(hp.chunks - 1);
+  if (hp.chunks > 1) {
+    // Join: the caller's stream waits for both pipeline streams; both are also
+    // drained below, so no copy touches the caller's buffers after return.
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventRecord(h->host_event[1 + i], ss[i]) == cudaSuccess)
+        cudaStreamWaitEvent(st, h->host_event[1 + i], 0);
+    cudaError_t e0 = cudaStreamSynchronize(ss[0]), e1 = cudaStreamSynchronize(ss[1]);
+    if (e == cudaSuccess) e = e0 != cudaSuccess ? e0 : e1;
+  }
+  const cudaError_t es = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = es;
+  return e == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }
 
 tl_status tl_encoder_get_status(tl_encoder* h, void* stream) {
@@ -295,6 +396,10 @@ tl_status tl_encoder_destroy(tl_encoder* h) {
   if (!h) return TL_OK;
   cudaDeviceSynchronize();
   timing_destroy(h);
+  for (cudaStream_t& x : h->host_stream)
+    if (x) cudaStreamDestroy(x);
+  for (cudaEvent_t& x : h->host_event)
+    if (x) cudaEventDestroy(x);
   if (h->wbuf) cudaFree(h->wbuf);
   if (h->status) cudaFree(h->status);
   delete[] h->layers;

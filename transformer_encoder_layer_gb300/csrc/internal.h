@@ -66,6 +66,12 @@ struct tl_encoder {
   tl_layer_dev* layers = nullptr;  // host array of n_layers
   tl_timing* timing = nullptr;     // non-null while per-kernel timing is on
   const void* mega_layers = nullptr;  // device array of MegaLayer (megakernel path)
+  // Host-buffer forward: batch slices per call (0 = automatic) and the two
+  // non-blocking streams plus fork/join events its copy/compute pipeline uses
+  // (created on first use).
+  int host_chunks = 0;
+  cudaStream_t host_stream[2] = {nullptr, nullptr};
+  cudaEvent_t host_event[3] = {nullptr, nullptr, nullptr};
 };
 
 namespace tl {
