@@ -92,6 +92,20 @@ def test_wide_d1024_subsample(scale):
         _check(make_inputs(s, seed=0, input_scale=scale, batch=2), p)
 
 
+@pytest.mark.parametrize("dtype,d,H,dff,L,batch", [
+    ("bf16", 512, 8, 1024, 37, 3),    # 111 rows: one ragged 128-row block
+    ("f16", 384, 6, 768, 50, 5),      # 192-wide N tiles, two per row
+    ("bf16", 768, 12, 1536, 130, 2),  # three 256-wide N tiles per row
+])
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_layered_rows_over_several_n_tiles(dtype, d, H, dff, L, batch, scale):
+    """LayerNorm GEMMs whose rows span several N tiles (the scratch-row
+    epilogue), with ragged row blocks."""
+    s = tiny_shape(dtype=dtype, batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=dff, n_layers=2)
+    _check(make_inputs(s, seed=4, input_scale=scale), "layered")
+
+
 @pytest.mark.parametrize("scale", INPUT_SCALES)
 def test_long_d64_reduced_length(scale):
     # Same layer as the 100k-token workload, 3000 tokens (ragged tail) so the

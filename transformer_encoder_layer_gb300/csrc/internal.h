@@ -47,7 +47,7 @@ enum tl_kernel_class {
   KC_SIMT_GEMM_QKV = 0, KC_SIMT_ATTENTION, KC_SIMT_GEMM_OUT, KC_SIMT_LAYERNORM,
   KC_SIMT_GEMM_FFN1, KC_SIMT_GEMM_FFN2, KC_TC_GEMM_QKV, KC_TC_ATTENTION,
   KC_TC_GEMM_OUT_LN, KC_TC_GEMM_FFN1, KC_TC_GEMM_FFN2_LN, KC_MEGA, KC_AUX, KC_DAG, KC_MEGA_SIMT,
-  KC_COUNT
+  KC_LN_APPLY, KC_COUNT
 };
 
 struct tl_timing;  // event pool, defined in timing.cu

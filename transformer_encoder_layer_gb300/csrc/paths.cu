@@ -9,6 +9,7 @@
 #include "mega.h"
 #include "mega_simt.h"
 #include "tc_attention.h"
+#include "ln_apply.h"
 #include "tc_gemm.h"
 
 namespace tl {
@@ -126,6 +127,7 @@ bool layered_supported(const tl_encoder* h) {
 struct LayeredWs {
   void *xh, *xl, *qh, *ql, *kh, *kl, *vth, *vtl, *ch, *cl, *yh, *yl, *hh, *hl;
   float *x32, *y32, *rs;
+  float2* stats;  // per-row (mean, rstd) of the LN GEMMs when d spans several N tiles
   int* ties;
   int* kmax;
   int Lp;
@@ -151,12 +153,14 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   o[12] = take(T * h->dff * e); o[13] = take(T * h->dff * e);              // ffn hidden
   o[14] = take(T * d * 4); o[15] = take(T * d * 4);                        // x32, y32
   o[16] = take(d > 256 ? T * d * 4 : 4);                                   // LN scratch
+  const size_t ost = take(d > 256 ? T * 8 : 8);                            // LN row stats
   size_t ot = take((1 + T * h->H) * 4);
   size_t ok_ = take((size_t)B * h->H * 4);
   void** p[14] = {&w.xh, &w.xl, &w.qh, &w.ql, &w.kh, &w.kl, &w.vth, &w.vtl, &w.ch, &w.cl,
                   &w.yh, &w.yl, &w.hh, &w.hl};
   for (int i = 0; i < 14; ++i) *p[i] = b + o[i];
   w.x32 = (float*)(b + o[14]); w.y32 = (float*)(b + o[15]); w.rs = (float*)(b + o[16]);
+  w.stats = (float2*)(b + ost);
   w.ties = (int*)(b + ot);
   w.kmax = (int*)(b + ok_);
   w.bytes = off;
@@ -175,6 +179,14 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
     bool ok = make_tmap_2d(&ma0, p0, bf, rows, K, K, 64, 128, 128);
     ok = ok && make_tmap_2d(&ma1, p1 ? p1 : p0, bf, rows, K, K, 64, 128, 128);
     return ok;
+  };
+  // Rows wider than one N tile: the LN GEMM left pre-normalised rows and
+  // their statistics; normalise them into the GEMM's output buffers.
+  auto apply_ln = [&](const TcGemmArgs& g) -> cudaError_t {
+    if (!g.row_stats) return cudaSuccess;
+    LnApplyArgs la{w.rs, w.stats, g.gamma, g.beta, M, d, g.o32, g.o_hi, g.o_lo, g.o_final};
+    KernelTimer t(h, KC_LN_APPLY, s);
+    return ln_apply(la, bf, h->num_sms, s);
   };
   for (int l = 0; l < h->n_layers; ++l) {
     const tl_layer_dev& P = h->layers[l];
@@ -226,10 +238,14 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
       g.resid = first ? x : (const void*)w.x32; g.resid_kind = first ? 1 : 0;
       g.gamma = P.ln1_g; g.beta = P.ln1_b; g.o32 = w.y32; g.o_hi = w.yh; g.o_lo = w.yl;
       g.rscratch = w.rs; g.status = h->status;
+      if (d > g.BN) g.row_stats = w.stats;
       if (!amaps(w.ch, w.cl, M, d) || !make_tmap_2d(&mw, P.w_o, bf, d, d, d, 64, g.BN, 128))
         return cudaErrorInvalidValue;
-      KernelTimer t(h, KC_TC_GEMM_OUT_LN, s);
-      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+      {
+        KernelTimer t(h, KC_TC_GEMM_OUT_LN, s);
+        if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+      }
+      if ((e = apply_ln(g)) != cudaSuccess) return e;
     }
     // a4: FFN1 + bias + exact GELU.
     {
@@ -252,10 +268,14 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
         g.o32 = w.x32; g.o_hi = w.xh; g.o_lo = w.xl;
       }
       g.rscratch = w.rs; g.status = h->status;
+      if (d > g.BN) g.row_stats = w.stats;
       if (!amaps(w.hh, w.hl, M, dff) || !make_tmap_2d(&mw, P.w_2, bf, d, dff, dff, 64, g.BN, 128))
         return cudaErrorInvalidValue;
-      KernelTimer t(h, KC_TC_GEMM_FFN2_LN, s);
-      if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+      {
+        KernelTimer t(h, KC_TC_GEMM_FFN2_LN, s);
+        if ((e = tc_gemm(ma0, ma1, mw, g, bf, TC_EPI_LN, h->num_sms, s)) != cudaSuccess) return e;
+      }
+      if ((e = apply_ln(g)) != cudaSuccess) return e;
     }
   }
   return e;

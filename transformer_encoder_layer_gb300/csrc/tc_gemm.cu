@@ -23,7 +23,10 @@
 //   LN    + bias + residual, LayerNorm over the full row (the CTA owns all
 //         N columns of its rows; per-32-column (mean, M2) merged with Chan's
 //         formula), written as fp32 and/or (hi, lo) planes, or as the final
-//         output in the I/O dtype.
+//         output in the I/O dtype.  A row wider than one N tile goes to a
+//         scratch row with its (mean, rstd); ln_apply.cu normalises those
+//         rows in a streaming pass while this kernel's tensor cores are free
+//         for the next launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -346,10 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (EPI == TC_EPI_LN && t == tiles_per_unit - 1) {
-          // LN pass 2: normalise and write.
+          // LN pass 2: normalise and write (or hand the row statistics to
+          // the streaming apply pass when the rows went to scratch).
           const float mean = ln_mean;
           const float rstd = rsqrtf(ln_m2 / ln_n + 1e-5f);
-          for (int tt = 0; tt < a.n_tiles; ++tt) {
+          if (a.n_tiles > 1 && a.row_stats) {
+            if (row_ok) a.row_stats[row] = make_float2(mean, rstd);
+          } else for (int tt = 0; tt < a.n_tiles; ++tt) {
             for (int c = 0; c < n_chunks; ++c) {
               float v[32];
               const int n0 = tt * BN + c * 32;

@@ -14,10 +14,12 @@ struct tl_timing {
 };
 
 namespace {
+static_assert(KC_COUNT <= TL_KERNEL_CLASSES, "kernel classes exceed the ABI table");
 const char* kNames[KC_COUNT] = {
     "simt_gemm_qkv", "simt_attention", "simt_gemm_out", "simt_layernorm",
     "simt_gemm_ffn1", "simt_gemm_ffn2", "tc_gemm_qkv", "tc_attention",
-    "tc_gemm_out_ln", "tc_gemm_ffn1", "tc_gemm_ffn2_ln", "megakernel", "aux", "dag", "megakernel_simt"};
+    "tc_gemm_out_ln", "tc_gemm_ffn1", "tc_gemm_ffn2_ln", "megakernel", "aux", "dag", "megakernel_simt",
+    "ln_apply"};
 }
 
 namespace tl {
