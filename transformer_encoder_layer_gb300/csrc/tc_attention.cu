@@ -46,6 +46,15 @@ constexpr int kBQ = 128, kBKV = 64, kStages = 3;
 template <int DH>
 constexpr int ctas_per_sm() { return DH == 16 ? 2 : 1; }
 
+// 2^x by the SFU's approximate base-2 exponential with subnormal results
+// flushed to zero (a probability below 2^-126 of the row maximum's weight is
+// below fp32 resolution of the row sum anyway); 2^-inf = 0.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Shared-memory descriptor for a K-major operand whose rows are `row_bytes`
 // (32, 64 or 128) long, swizzled at the same width: 8-row atoms of
 // 8*row_bytes bytes.
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
 #pragma unroll
       for (int c = 0; c < DH; ++c) acc[c] = 0.f;
       float m = -INFINITY, m2 = -INFINITY, l = 0.f, m_prev_o = -INFINITY;
-      float m_hist[2] = {-INFINITY, -INFINITY};     // running max after tile j (by parity)
+      float m_hist0 = -INFINITY, m_hist1 = -INFINITY;  // running max after tile j (by parity)
       // |q_i| for the near-tie test, from the (hi, lo) Q tile in shared memory.
       float qn2 = 0.f;
       if (mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) {
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const uint32_t ph = (uint32_t)((o_it >> 1) & 1);
         if (!mbar_wait(&o_full[ob], ph, abort, a.status)) return false;
         tc_fence_after();
-        const float mj = m_hist[jo & 1];
+        const float mj = (jo & 1) ? m_hist1 : m_hist0;
         const float corr = exp2f(m_prev_o - mj);   // 0 on the first fold
         const uint32_t ta = tO + lane_addr + (uint32_t)(ob * DH);
 #pragma unroll
@@ -351,25 +360,33 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         ++s_it;
         const int k0 = j * kBKV;
         const bool needs_mask = k0 + kBKV > full_keys;
-        float tmax = -INFINITY;
+        // s stays unscaled (masked keys -inf); the running max m, the
+        // second best m2 and the references are in scaled (log2) units.
+        // Scaling by a positive constant commutes with the max, rounding
+        // included, so the tile max is scaled once.
+        float tmax;
         if (track) {
+          tmax = -INFINITY;
 #pragma unroll
           for (int c = 0; c < kBKV; ++c) {
-            float v = s[c] * scale_log2;
+            float v = s[c];
             if (needs_mask && k0 + c >= limit) v = -INFINITY;
             s[c] = v;
-            m2 = fmaxf(m2, fminf(fmaxf(m, tmax), v));
-            tmax = fmaxf(tmax, v);
+            const float vs = v * scale_log2;
+            m2 = fmaxf(m2, fminf(fmaxf(m, tmax), vs));
+            tmax = fmaxf(tmax, vs);
           }
         } else {
           // no near tie possible for this row: the second-best score is not needed
+          float traw = -INFINITY;
 #pragma unroll
           for (int c = 0; c < kBKV; ++c) {
-            float v = s[c] * scale_log2;
+            float v = s[c];
             if (needs_mask && k0 + c >= limit) v = -INFINITY;
             s[c] = v;
-            tmax = fmaxf(tmax, v);
+            traw = fmaxf(traw, v);
           }
+          tmax = traw * scale_log2;
         }
         const float mn = fmaxf(m, tmax);
         // A row with no visible key in this tile keeps its max; its
@@ -377,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const float mref = mn == -INFINITY ? 0.f : mn;
         l *= exp2f(m - mref);
         m = mn;
-        m_hist[j & 1] = mref;
+        if (j & 1) m_hist1 = mref; else m_hist0 = mref;
         // P_j into the (hi, lo) swizzled operand buffer.
         const int pb = (int)((s_it - 1) & 1);
         if (!mbar_wait(&p_empty[pb], (uint32_t)((((s_it - 1) >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
@@ -388,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           float p8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            p8[e] = exp2f(s[c8 * 8 + e] - mref);
+            // one rounding: 2^(s scale - mref), flushed to 0 below 2^-126
+            p8[e] = ex2_ftz(fmaf(s[c8 * 8 + e], scale_log2, -mref));
             l += p8[e];
           }
           uint4 hv, lv;
