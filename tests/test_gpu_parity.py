@@ -106,6 +106,20 @@ def test_layered_rows_over_several_n_tiles(dtype, d, H, dff, L, batch, scale):
     _check(make_inputs(s, seed=4, input_scale=scale), "layered")
 
 
+@pytest.mark.parametrize("dtype,d,H,L,batch", [
+    ("f16", 64, 8, 40, 3),     # head_dim 8: four heads per 32-column chunk
+    ("bf16", 64, 16, 33, 2),   # head_dim 4
+    ("f16", 64, 32, 17, 2),    # head_dim 2
+    ("bf16", 128, 4, 70, 2),   # head_dim 32: one chunk per head
+])
+@pytest.mark.parametrize("scale", [1.0, 1e3])
+def test_layered_qkv_head_widths(dtype, d, H, L, batch, scale):
+    """The head-major QKV epilogue for every head width it handles."""
+    s = tiny_shape(dtype=dtype, batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=2 * d, n_layers=2)
+    _check(make_inputs(s, seed=6, input_scale=scale), "layered")
+
+
 @pytest.mark.parametrize("scale", INPUT_SCALES)
 def test_long_d64_reduced_length(scale):
     # Same layer as the 100k-token workload, 3000 tokens (ragged tail) so the

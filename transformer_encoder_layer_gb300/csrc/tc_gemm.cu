@@ -90,6 +90,71 @@ __device__ __forceinline__ void store_row32(T* dst, size_t at, const float (&v)[
   for (int j = 0; j < 4; ++j) hd[j] = hv[j];
 }
 
+// W consecutive values of one row as (hi, lo) 16-bit planes, 16-byte stores
+// (W a multiple of 8, `at` a multiple of 8 elements).
+template <typename T, int W>
+__device__ __forceinline__ void store_row_pair(T* hi, T* lo, size_t at, const float* v) {
+#pragma unroll
+  for (int q = 0; q < W / 8; ++q) {
+    uint4 hv, lv;
+    T* hp = reinterpret_cast<T*>(&hv);
+    T* lp = reinterpret_cast<T*>(&lv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) Split<T>::go(v[8 * q + j], hp[j], lp[j]);
+    reinterpret_cast<uint4*>(hi + at)[q] = hv;
+    reinterpret_cast<uint4*>(lo + at)[q] = lv;
+  }
+}
+
+// QKV epilogue for one row's 32-column chunk starting at column n0 of
+// [q | k | v]: head pieces of W = min(dh, 32) columns (dh divides 32 or is a
+// multiple of it).  Q and K go to
+// [B, H, L, dh] planes, V to the transposed [B, H, dh, Lp] planes (a lane
+// per row, so each V^T store covers consecutive positions).  kn2 carries
+// |k|^2 of the head being written across chunks (dh > 32); the head's |k|
+// goes to the plane maximum used by the near-tie test.
+template <typename T, int W>
+__device__ __forceinline__ void qkv_scatter(const float (&v)[32], const TcGemmArgs& a, int row, int n0,
+                                            float& kn2) {
+  const int d = a.H * a.dh;
+  const int b = row / a.L, i = row % a.L;
+#pragma unroll
+  for (int j0 = 0; j0 < 32; j0 += W) {
+    const int n = n0 + j0;
+    const int which = n / d, h = (n % d) / a.dh, c0 = n % a.dh;
+    const size_t bh = (size_t)b * a.H + h;
+    if (which < 2) {
+      T* hi = reinterpret_cast<T*>(which == 0 ? a.q_hi : a.k_hi);
+      T* lo = reinterpret_cast<T*>(which == 0 ? a.q_lo : a.k_lo);
+      const size_t at = (bh * a.L + i) * a.dh + c0;
+      if constexpr (W % 8 == 0) {
+        store_row_pair<T, W>(hi, lo, at, v + j0);
+      } else {
+#pragma unroll
+        for (int j = 0; j < W; ++j) store_pair(hi, lo, at + j, v[j0 + j]);
+      }
+      if (which == 1 && a.kmax) {
+#pragma unroll
+        for (int j = 0; j < W; ++j) kn2 = fmaf(v[j0 + j], v[j0 + j], kn2);
+        if (c0 + W == a.dh) {
+          atomicMax(a.kmax + bh, __float_as_int(sqrtf(kn2)));
+          kn2 = 0.f;
+        }
+      }
+    } else {
+      T* vt_hi = reinterpret_cast<T*>(a.vt_hi);
+      T* vt_lo = reinterpret_cast<T*>(a.vt_lo);
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const size_t vr = (bh * a.dh + c0 + j) * a.Lp;
+        store_pair(vt_hi, vt_lo, vr + i, v[j0 + j]);
+        if (i == a.L - 1)  // zero the pitch padding: keys beyond L read as 0
+          for (int z = a.L; z < a.Lp; ++z) store_pair(vt_hi, vt_lo, vr + z, 0.f);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -267,39 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) v[j] += __ldg(a.bias + n0 + j);
           if (EPI == TC_EPI_QKV) {
             if (row_ok) {
-              const int d = a.H * a.dh;
-              const int b = row / a.L, i = row % a.L;
-              // a 32-column chunk covers whole heads (dh = 16) or part of one
-              for (int j0 = 0; j0 < 32; j0 += (a.dh < 32 ? a.dh : 32)) {
-                const int n = n0 + j0;
-                const int which = n / d, h = (n % d) / a.dh, c0 = n % a.dh;
-                const int w = a.dh < 32 ? a.dh : 32;
-                const size_t bh = (size_t)b * a.H + h;
-                if (which < 2) {
-                  T* hi = which == 0 ? q_hi : k_hi;
-                  T* lo = which == 0 ? q_lo : k_lo;
-                  const size_t at = (bh * a.L + i) * a.dh + c0;
-                  if (w == 32) {
-                    store_row32_pair(hi, lo, at, v);
-                  } else {
-                    for (int j = 0; j < w; ++j) store_pair(hi, lo, at + j, v[j0 + j]);
-                  }
-                  if (which == 1 && a.kmax) {  // |k_j| of this head, for the near-tie test
-                    for (int j = 0; j < w; ++j) kn2 = fmaf(v[j0 + j], v[j0 + j], kn2);
-                    if (c0 + w == a.dh) {
-                      atomicMax(a.kmax + bh, __float_as_int(sqrtf(kn2)));
-                      kn2 = 0.f;
-                    }
-                  }
-                } else {
-                  for (int j = 0; j < w; ++j) {
-                    const size_t vr = (bh * a.dh + c0 + j) * a.Lp;
-                    store_pair(vt_hi, vt_lo, vr + i, v[j0 + j]);
-                    if (i == a.L - 1)  // zero the pitch padding: keys beyond L read as 0
-                      for (int z = a.L; z < a.Lp; ++z) store_pair(vt_hi, vt_lo, vr + z, 0.f);
-                  }
-                }
-              }
+              // a 32-column chunk covers part of one head (dh >= 32) or 32/dh
+              // whole heads; the head width is a template constant so the
+              // chunk stays in registers
+              if (a.dh >= 32) qkv_scatter<T, 32>(v, a, row, n0, kn2);
+              else if (a.dh == 16) qkv_scatter<T, 16>(v, a, row, n0, kn2);
+              else if (a.dh == 8) qkv_scatter<T, 8>(v, a, row, n0, kn2);
+              else if (a.dh == 4) qkv_scatter<T, 4>(v, a, row, n0, kn2);
+              else if (a.dh == 2) qkv_scatter<T, 2>(v, a, row, n0, kn2);
+              else qkv_scatter<T, 1>(v, a, row, n0, kn2);
             }
           } else if (EPI == TC_EPI_GELU) {
             if (row_ok) {
