@@ -391,7 +391,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "layered", "mega", "dag"])
-    ap.add_argument("--cpu-seqs", type=int, default=1024,
+    ap.add_argument("--cpu-seqs", type=int, default=4096,
                     help="sequences in the bounded CPU-oracle sample")
     ap.add_argument("--ref-seqs", type=int, default=64,
                     help="sequences per step of the reference (oracle) arm")
