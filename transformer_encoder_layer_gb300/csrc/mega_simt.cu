@@ -10,7 +10,11 @@
 // sequence, the layer input X [L, d], Q, K, V head-major [H, L, dh], K
 // transposed per head [H, dh, L] (conflict-free scores), the context / LN1
 // output C [L, d], the pre-LayerNorm rows R [L, d] and the FFN hidden
-// HB [L, d_ff].  Weights are read through L1 (16-byte loads).  Per layer:
+// HB [L, d_ff].  When they fit, every layer's weights are copied into shared
+// memory at kernel start (cp.async, one group per layer, rows padded by 16
+// bytes so that neighbouring output columns hit different banks), and layer
+// l waits only for its own group; otherwise they are read through L1.  Per
+// layer:
 //   X -> Q, K, V (+ b_qkv)          GEMM, one output column x 8 rows a thread
 //   attention rows                   4 threads per (head, query row), online
 //                                    softmax in registers; the top two scores
@@ -30,7 +34,6 @@ namespace tl {
 namespace {
 
 constexpr int kThreads = 256, kWarps = kThreads / 32;
-constexpr int kRB = 8;  // output rows per GEMM task
 
 struct Smem {
   float *X, *Q, *K, *V, *Kt, *C, *R, *HB;
@@ -38,10 +41,18 @@ struct Smem {
   int* nflag;
   int* flags;  // queued (head, row) entries for the fp64 fix-up
   double* fix;
+  float* W;    // staged weights, n_layers x layer_w_floats (or null)
   size_t bytes;
 };
 
-__host__ __device__ inline Smem carve(unsigned char* base, int L, int d, int dh, int dff) {
+// Floats of one layer's staged weights: W_qkv [3d][d+4], W_o [d][d+4],
+// W_1 [dff][d+4], W_2 [d][dff+4].
+__host__ __device__ inline size_t layer_w_floats(int d, int dff) {
+  return (size_t)4 * d * (d + 4) + (size_t)dff * (d + 4) + (size_t)d * (dff + 4);
+}
+
+__host__ __device__ inline Smem carve(unsigned char* base, int L, int d, int dh, int dff,
+                                      int w_layers) {
   Smem s;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -57,31 +68,65 @@ __host__ __device__ inline Smem carve(unsigned char* base, int L, int d, int dh,
   s.nflag = (int*)take(16);
   s.flags = (int*)take((size_t)(d / dh) * L * sizeof(int));
   s.fix = (double*)take((size_t)kWarps * (dh + d) * sizeof(double));
+  s.W = w_layers ? (float*)take((size_t)w_layers * layer_w_floats(d, dff) * sizeof(float)) : nullptr;
   s.bytes = off;
   return s;
 }
 
-// out(t, n) = sum_k A[t][k] W[n][k] for t < L, n < N, handed to epi; A is a
-// dense [L, K] shared-memory array, W [N, K] in global memory, K % 4 == 0.
-// A task is one column n for kRB rows; its weight row is loaded 8 x 16 bytes
-// at a time, all in flight together, so a K-long row costs K / 32 memory
-// latencies instead of K / 4.
-template <typename Epi>
-__device__ __forceinline__ void gemm(const float* A, int K, const float* W, int N, int L, Epi epi) {
-  const int groups = (L + kRB - 1) / kRB;
+// 16-byte asynchronous copy global -> shared, and its group bookkeeping.
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// Wait until at most n of this thread's groups are pending (n <= 7).
+__device__ __forceinline__ void cp_wait_n(int n) {
+  switch (n) {
+    case 0: cp_wait<0>(); break;
+    case 1: cp_wait<1>(); break;
+    case 2: cp_wait<2>(); break;
+    case 3: cp_wait<3>(); break;
+    case 4: cp_wait<4>(); break;
+    case 5: cp_wait<5>(); break;
+    case 6: cp_wait<6>(); break;
+    default: cp_wait<7>(); break;
+  }
+}
+
+// W [N, K] (global, K % 4 == 0) -> dst [N][K + 4] in shared memory.
+__device__ __forceinline__ void stage_w(float* dst, const float* W, int N, int K) {
+  const int K4 = K / 4;
+  for (int i = threadIdx.x; i < N * K4; i += kThreads) {
+    const int n = i / K4, k4 = i - n * K4;
+    cp16(dst + (size_t)n * (K + 4) + 4 * k4, W + (size_t)n * K + 4 * k4);
+  }
+}
+
+// out(t, n) = sum_k A[t][k] W[n][k] for t < L, n < N; A is a dense [L, K]
+// shared-memory array, W [N, K] with row pitch ldw, in shared memory (SW) or
+// global memory, K % 4 == 0.  A task is one column n for RB rows; its weight
+// row is read 8 x 16 bytes at a time, all in flight together.  The epilogue
+// gets the task's rows at once: epi(t0, rows, n, acc[RB]).
+template <int RB, bool SW, typename Epi>
+__device__ __forceinline__ void gemm(const float* A, int K, const float* W, int ldw, int N, int L,
+                                     Epi epi) {
+  const int groups = (L + RB - 1) / RB;
   for (int task = threadIdx.x; task < N * groups; task += kThreads) {
-    const int n = task % N, t0 = (task / N) * kRB;
-    float acc[kRB];
+    const int n = task % N, t0 = (task / N) * RB;
+    float acc[RB];
 #pragma unroll
-    for (int r = 0; r < kRB; ++r) acc[r] = 0.f;
-    const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)n * K);
+    for (int r = 0; r < RB; ++r) acc[r] = 0.f;
+    const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)n * ldw);
     const int K4 = K / 4;
     for (int kb = 0; kb < K4; kb += 8) {
       float4 w[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) w[u] = kb + u < K4 ? __ldg(w4 + kb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 8; ++u)
+        w[u] = kb + u < K4 ? (SW ? w4[kb + u] : __ldg(w4 + kb + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int r = 0; r < kRB; ++r) {
+      for (int r = 0; r < RB; ++r) {
         const float* arow = A + (size_t)min(t0 + r, L - 1) * K + 4 * kb;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -95,26 +140,53 @@ __device__ __forceinline__ void gemm(const float* A, int K, const float* W, int 
         }
       }
     }
-#pragma unroll
-    for (int r = 0; r < kRB; ++r)
-      if (t0 + r < L) epi(t0 + r, n, acc[r]);
+    epi(t0, min(RB, L - t0), n, acc);
   }
 }
 
+// The GEMM with 8-row tasks, or 4-row tasks when 8-row ones would leave
+// threads idle.
+template <bool SW, typename Epi>
+__device__ __forceinline__ void gemm_rows(const float* A, int K, const float* W, int ldw, int N, int L,
+                                          Epi epi) {
+  if (N * ((L + 7) / 8) >= kThreads) gemm<8, SW>(A, K, W, ldw, N, L, epi);
+  else gemm<4, SW>(A, K, W, ldw, N, L, epi);
+}
+
 // Rows of R -> (r - mean) / sqrt(var + 1e-5) * g + b into out (row stride d),
-// two-pass in fp32, a warp per row; d <= 64.
+// two-pass in fp32; 8 lanes per row (columns lane, lane + 8, ...), 4 rows per
+// warp at once; d <= 64.
 __device__ __forceinline__ void layernorm_rows(const float* R, const float* g, const float* be,
                                                float* out, int L, int d) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int t = warp; t < L; t += kWarps) {
-    const float* x = R + (size_t)t * d;
-    const float v0 = lane < d ? x[lane] : 0.f;
-    const float v1 = lane + 32 < d ? x[lane + 32] : 0.f;
-    const float mean = warp_sum(v0 + v1) / d;
-    const float d0 = lane < d ? v0 - mean : 0.f, d1 = lane + 32 < d ? v1 - mean : 0.f;
-    const float rstd = rsqrtf(warp_sum(fmaf(d0, d0, d1 * d1)) / d + 1e-5f);
-    if (lane < d) out[(size_t)t * d + lane] = d0 * rstd * g[lane] + be[lane];
-    if (lane + 32 < d) out[(size_t)t * d + lane + 32] = d1 * rstd * g[lane + 32] + be[lane + 32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, sub = lane & 7;
+  for (int t0 = 4 * warp; t0 < L; t0 += 4 * kWarps) {
+    const int t = t0 + (lane >> 3);
+    const bool ok = t < L;
+    float v[8], sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int col = sub + 8 * c;
+      v[c] = ok && col < d ? R[(size_t)t * d + col] : 0.f;
+      sum += v[c];
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mean = sum / d;
+    float q = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float dv = sub + 8 * c < d ? v[c] - mean : 0.f;
+      v[c] = dv;
+      q = fmaf(dv, dv, q);
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = rsqrtf(q / d + 1e-5f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int col = sub + 8 * c;
+      if (ok && col < d) out[(size_t)t * d + col] = v[c] * rstd * g[col] + be[col];
+    }
   }
 }
 
@@ -122,12 +194,25 @@ template <int DH>
 __global__ void __launch_bounds__(kThreads) mega_simt_kernel(const __grid_constant__ MegaSimtArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int L = a.L, d = a.d, H = a.H, dh = DH, dff = a.dff;
-  const Smem sm = carve(smem_raw, L, d, dh, dff);
+  const Smem sm = carve(smem_raw, L, d, dh, dff, a.w_stage ? a.n_layers : 0);
   const int seq = blockIdx.x, tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   int vl = a.vl[seq];
   if (vl < 1 || vl > L) {
     if (tid == 0) set_status(a.status, TL_ERR_BAD_VALID_LEN);
     vl = vl < 1 ? 1 : L;
+  }
+  const size_t lw = layer_w_floats(d, dff);
+  if (a.w_stage) {
+    // every layer's weights into shared memory, one cp.async group per layer
+    for (int l = 0; l < a.n_layers; ++l) {
+      const tl_layer_dev& P = a.layers[l];
+      float* w = sm.W + l * lw;
+      stage_w(w, (const float*)P.w_qkv, 3 * d, d);
+      stage_w(w + 3 * d * (d + 4), (const float*)P.w_o, d, d);
+      stage_w(w + 4 * d * (d + 4), (const float*)P.w_1, dff, d);
+      stage_w(w + 4 * d * (d + 4) + (size_t)dff * (d + 4), (const float*)P.w_2, d, dff);
+      cp_commit();
+    }
   }
   // Every layer's parameters into L2 first: the steps below then wait on L2,
   // not on HBM, for their first touches.
@@ -139,21 +224,34 @@ __global__ void __launch_bounds__(kThreads) mega_simt_kernel(const __grid_consta
   for (int l = 0; l < a.n_layers; ++l) {
     const tl_layer_dev& P = a.layers[l];
     if (tid < H) sm.kmax[tid] = 0;
+    if (a.w_stage) cp_wait_n(a.n_layers - 1 - l);  // this layer's weights have landed
     __syncthreads();
+    // This layer's weights and their row pitches, staged or in global memory.
+    const float* wl = sm.W + l * lw;
+    const bool sw = a.w_stage != 0;
+    const float* Wq = sw ? wl : (const float*)P.w_qkv;
+    const float* Wo = sw ? wl + 3 * d * (d + 4) : (const float*)P.w_o;
+    const float* W1 = sw ? wl + 4 * d * (d + 4) : (const float*)P.w_1;
+    const float* W2 = sw ? wl + 4 * d * (d + 4) + (size_t)dff * (d + 4) : (const float*)P.w_2;
+    const int ldd = sw ? d + 4 : d, ldf = sw ? dff + 4 : dff;
     // ---- QKV projection, head-major (K also transposed)
-    gemm(sm.X, d, (const float*)P.w_qkv, 3 * d, L, [&](int t, int n, float acc) {
-      const float v = acc + P.b_qkv[n];
+    auto qkv_epi = [&](int t0, int nr, int n, const auto& acc) {
+      constexpr int rb = sizeof(acc) / sizeof(float);
+      const float b = P.b_qkv[n];
       const int which = n / d, w = n % d, h = w / dh, c = w % dh;
-      const size_t hm = ((size_t)h * L + t) * dh + c;
-      if (which == 0) {
-        sm.Q[hm] = v;
-      } else if (which == 1) {
-        sm.K[hm] = v;
-        sm.Kt[((size_t)h * dh + c) * L + t] = v;
-      } else {
-        sm.V[hm] = v;
+      float* dst = which == 0 ? sm.Q : (which == 1 ? sm.K : sm.V);
+#pragma unroll
+      for (int r = 0; r < rb; ++r) {
+        if (r < nr) {
+          const int t = t0 + r;
+          const float v = acc[r] + b;
+          dst[((size_t)h * L + t) * dh + c] = v;
+          if (which == 1) sm.Kt[((size_t)h * dh + c) * L + t] = v;
+        }
       }
-    });
+    };
+    if (sw) gemm_rows<true>(sm.X, d, Wq, ldd, 3 * d, L, qkv_epi);
+    else gemm_rows<false>(sm.X, d, Wq, ldd, 3 * d, L, qkv_epi);
     __syncthreads();
     // the largest |k| of each head (near-tie error scale)
     for (int i = tid; i < H * L; i += kThreads) {
@@ -252,20 +350,38 @@ __global__ void __launch_bounds__(kThreads) mega_simt_kernel(const __grid_consta
     }
     __syncthreads();
     // ---- out-projection + b_o + residual, LayerNorm 1 into C
-    gemm(sm.C, d, (const float*)P.w_o, d, L, [&](int t, int n, float acc) {
-      sm.R[(size_t)t * d + n] = acc + P.b_o[n] + sm.X[(size_t)t * d + n];
-    });
+    auto out_epi = [&](int t0, int nr, int n, const auto& acc) {
+      constexpr int rb = sizeof(acc) / sizeof(float);
+      const float b = P.b_o[n];
+#pragma unroll
+      for (int r = 0; r < rb; ++r)
+        if (r < nr) sm.R[(size_t)(t0 + r) * d + n] = acc[r] + b + sm.X[(size_t)(t0 + r) * d + n];
+    };
+    if (sw) gemm_rows<true>(sm.C, d, Wo, ldd, d, L, out_epi);
+    else gemm_rows<false>(sm.C, d, Wo, ldd, d, L, out_epi);
     __syncthreads();
     layernorm_rows(sm.R, P.ln1_g, P.ln1_b, sm.C, L, d);
     __syncthreads();
     // ---- FFN
-    gemm(sm.C, d, (const float*)P.w_1, dff, L, [&](int t, int n, float acc) {
-      sm.HB[(size_t)t * dff + n] = gelu_erf(acc + P.b_1[n]);
-    });
+    auto ffn1_epi = [&](int t0, int nr, int n, const auto& acc) {
+      constexpr int rb = sizeof(acc) / sizeof(float);
+      const float b = P.b_1[n];
+#pragma unroll
+      for (int r = 0; r < rb; ++r)
+        if (r < nr) sm.HB[(size_t)(t0 + r) * dff + n] = gelu_erf(acc[r] + b);
+    };
+    if (sw) gemm_rows<true>(sm.C, d, W1, ldd, dff, L, ffn1_epi);
+    else gemm_rows<false>(sm.C, d, W1, ldd, dff, L, ffn1_epi);
     __syncthreads();
-    gemm(sm.HB, dff, (const float*)P.w_2, d, L, [&](int t, int n, float acc) {
-      sm.R[(size_t)t * d + n] = acc + P.b_2[n] + sm.C[(size_t)t * d + n];
-    });
+    auto ffn2_epi = [&](int t0, int nr, int n, const auto& acc) {
+      constexpr int rb = sizeof(acc) / sizeof(float);
+      const float b = P.b_2[n];
+#pragma unroll
+      for (int r = 0; r < rb; ++r)
+        if (r < nr) sm.R[(size_t)(t0 + r) * d + n] = acc[r] + b + sm.C[(size_t)(t0 + r) * d + n];
+    };
+    if (sw) gemm_rows<true>(sm.HB, dff, W2, ldf, d, L, ffn2_epi);
+    else gemm_rows<false>(sm.HB, dff, W2, ldf, d, L, ffn2_epi);
     __syncthreads();
     const bool last = l + 1 == a.n_layers;
     layernorm_rows(sm.R, P.ln2_g, P.ln2_b, last ? a.out + (size_t)seq * L * d : sm.X, L, d);
@@ -273,7 +389,11 @@ __global__ void __launch_bounds__(kThreads) mega_simt_kernel(const __grid_consta
   }
 }
 
-size_t smem_bytes(int L, int d, int dh, int dff) { return carve(nullptr, L, d, dh, dff).bytes; }
+size_t smem_bytes(int L, int d, int dh, int dff, int w_layers) {
+  return carve(nullptr, L, d, dh, dff, w_layers).bytes;
+}
+
+constexpr size_t kSmemBudget = 200 * 1024;
 
 }  // namespace
 
@@ -281,12 +401,14 @@ bool mega_simt_supported(int d, int H, int dff, int L, int n_layers, tl_dtype t)
   if (t != TL_F32 || H < 1 || d % H || H > 64 || n_layers < 1 || n_layers > kMegaSimtMaxLayers) return false;
   const int dh = d / H;
   return d <= 64 && d % 4 == 0 && (dh == 8 || dh == 16 || dh == 32) && L <= 64 && dff <= 256 &&
-         dff % 4 == 0 && smem_bytes(L, d, dh, dff) <= 200 * 1024;
+         dff % 4 == 0 && smem_bytes(L, d, dh, dff, 0) <= kSmemBudget;
 }
 
 template <int DH>
-static cudaError_t launch(const MegaSimtArgs& a, cudaStream_t s) {
-  const size_t smem = smem_bytes(a.L, a.d, DH, a.dff);
+static cudaError_t launch(MegaSimtArgs a, cudaStream_t s) {
+  // Stage the weights when every layer's fit beside the activations.
+  a.w_stage = smem_bytes(a.L, a.d, DH, a.dff, a.n_layers) <= kSmemBudget ? 1 : 0;
+  const size_t smem = smem_bytes(a.L, a.d, DH, a.dff, a.w_stage ? a.n_layers : 0);
   cudaError_t e = set_max_dyn_smem((const void*)mega_simt_kernel<DH>, smem);
   if (e != cudaSuccess) return e;
   mega_simt_kernel<DH><<<a.B, kThreads, smem, s>>>(a);

@@ -17,6 +17,7 @@ struct MegaSimtArgs {
   const int32_t* vl;   // [B]
   int* status;
   int B, L, d, H, dh, dff;
+  int w_stage;         // 1: every layer's weights staged in shared memory (set by the launcher)
 };
 
 bool mega_simt_supported(int d, int H, int dff, int L, int n_layers, tl_dtype t);
