@@ -15,12 +15,19 @@
 //              3-deep ring
 //   warp 1     TMEM owner; one thread issues S = Q K^T into one of two TMEM
 //              score buffers, then O_j = P_j V_j into one of two TMEM output
-//              buffers once the softmax warps have written P_j
+//              buffers once the softmax warps have written P_j.  At head_dim
+//              16, where the softmax's instruction issue is the bound, each
+//              V^T tile carries 16 extra rows after its head_dim rows (a row
+//              of ones in the hi plane, zeros otherwise, written once at
+//              start; TMA fills only the first head_dim rows), so the same
+//              MMAs also produce the row sum of P_j in output column
+//              head_dim and the softmax adds no probabilities itself; at
+//              larger heads the wider MMA costs more than it saves.
 //   warps 2-5  softmax: thread = query row.  Reads its 64 scores, masks,
-//              updates the running max/sum, writes P_j as (hi, lo) into the
+//              updates the running max, writes P_j as (hi, lo) into the
 //              swizzled shared-memory operand, and folds the previous tile's
-//              O_{j-1} into its fp32 register accumulator with the
-//              online-softmax correction.
+//              O_{j-1} and row sum into its fp32 register accumulators with
+//              the online-softmax correction.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -78,13 +85,23 @@ __device__ __forceinline__ int swz_offset(int r, int c_bytes, int row_bytes) {
   return o ^ (((o >> 7) & ((row_bytes >> 4) - 1)) << 4);
 }
 
+// Row sums of P from the P.V MMAs (a ones row appended to V^T) instead of
+// one add per probability: only where the softmax issue rate binds.
+template <int DH>
+__host__ __device__ constexpr bool row_sum_by_mma() { return DH == 16; }
+
 template <typename T, int DH>
 struct Layout {
   static constexpr int kQBytes = kBQ * DH * 2;      // one Q plane
   static constexpr int kKBytes = kBKV * DH * 2;     // one K plane tile
-  static constexpr int kVBytes = DH * kBKV * 2;     // one V^T plane tile
+  static constexpr int kXRows = row_sum_by_mma<DH>() ? 16 : 0;  // a ones row and 15 zero rows
+  static constexpr int kVRows = DH + kXRows;        // V^T rows
+  static constexpr int kVBytes = kVRows * kBKV * 2; // one V^T plane buffer
+  static constexpr int kVTx = DH * kBKV * 2;        // bytes TMA writes into it
   static constexpr int kPBytes = kBQ * kBKV * 2;    // one P plane (16 KB)
   static constexpr int kStageBytes = 2 * kKBytes + 2 * kVBytes;
+  static constexpr int kStageTx = 2 * kKBytes + 2 * kVTx;  // TMA bytes per stage
+  static constexpr int kOCols = (DH + kXRows + 31) / 32 * 32;  // TMEM columns per O buffer
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
   static constexpr int kPOff = kKVOff + kStages * kStageBytes;
@@ -122,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int planes = a.B * a.H;
   const int nqt = (a.L + kBQ - 1) / kBQ;
   const int n_items = planes * nqt;
-  constexpr uint32_t kTmemCols = 256;  // S: 2 x 64, O: 2 x DH (<= 128)
+  // S: 2 x 64 columns, O: 2 x kOCols (head_dim outputs + the row sum)
+  constexpr uint32_t kTmemCols = 2 * kBKV + 2 * Lay::kOCols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -144,6 +162,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+  if (row_sum_by_mma<DH>() && warp >= 2) {
+    // The V^T buffers' 16 extra rows, never touched by TMA: row head_dim of
+    // the hi plane all ones (its product with P is the row sum), the rest 0.
+    // A row of equal values is the same under the 128-byte swizzle.
+    T ones[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ones[e] = from_f32<T>(1.f);
+    const uint4 one4 = *reinterpret_cast<const uint4*>(ones);
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    const int t = threadIdx.x - 64;  // 128 threads, one 16-byte chunk of a 2 KB extension each
+    for (int st = 0; st < kStages; ++st)
+      for (int pl = 0; pl < 2; ++pl) {
+        unsigned char* ext = base + Lay::kKVOff + st * Lay::kStageBytes + 2 * Lay::kKBytes +
+                             pl * Lay::kVBytes + DH * kBKV * 2;
+        reinterpret_cast<uint4*>(ext)[t] = (pl == 0 && t < 8) ? one4 : zero4;
+      }
+    fence_proxy_async();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -182,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           const uint32_t ph = (uint32_t)((kv_it / kStages) & 1);
           if (!mbar_wait(&kv_empty[st], ph ^ 1, abort, a.status)) { ok = false; break; }
           unsigned char* sb = base + Lay::kKVOff + st * Lay::kStageBytes;
-          mbar_arrive_expect_tx(&kv_full[st], Lay::kStageBytes);
+          mbar_arrive_expect_tx(&kv_full[st], Lay::kStageTx);
           const int krow = plane * a.L + j * kBKV;
           tma_load_2d(sb, &mkh, &kv_full[st], 0, krow);
           tma_load_2d(sb + Lay::kKBytes, &mkl, &kv_full[st], 0, krow);
@@ -201,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     // ---------------------------------------------------------------- MMA
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc_s = idesc_f16(kBQ, kBKV, kBf);
-    const uint32_t idesc_o = idesc_f16(kBQ, DH, kBf);
+    const uint32_t idesc_o = idesc_f16(kBQ, DH + Lay::kXRows, kBf);  // head_dim outputs (+ the row sum)
     long long kv_it = 0, s_it = 0, o_it = 0, n_done = 0;
     bool ok = true;
     const uint32_t q_addr = smem_u32(base + Lay::kQOff);
@@ -217,8 +253,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const uint32_t vh = sb + 2 * Lay::kKBytes, vl_ = vh + Lay::kVBytes;
         const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * 2 * Lay::kPBytes);
         const uint32_t pl_ = ph_ + Lay::kPBytes;
-        const uint32_t d = tO + (uint32_t)(pb * DH);
-        // O = Ph.Vh + Ph.Vl + Pl.Vh over 64 keys (4 steps of K = 16)
+        const uint32_t d = tO + (uint32_t)(pb * Lay::kOCols);
+        // O = Ph.Vh + Ph.Vl + Pl.Vh over 64 keys (4 steps of K = 16); with
+        // the extra rows, column DH = sum of Ph + Pl (the ones row of Vh)
         const uint32_t as[3] = {ph_, ph_, pl_};
         const uint32_t bs[3] = {vh, vl_, vh};
 #pragma unroll
@@ -327,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         tc_fence_after();
         const float mj = (jo & 1) ? m_hist1 : m_hist0;
         const float corr = exp2f(m_prev_o - mj);   // 0 on the first fold
-        const uint32_t ta = tO + lane_addr + (uint32_t)(ob * DH);
+        const uint32_t ta = tO + lane_addr + (uint32_t)(ob * Lay::kOCols);
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 16) {
           uint32_t rr[16];
@@ -341,6 +378,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
           for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(acc[c0 + c], corr, __uint_as_float(rr[c]));
+        }
+        if constexpr (row_sum_by_mma<DH>()) {  // the row sum of P_jo, column DH
+          uint32_t rl;
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rl) : "r"(ta + DH));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          l = fmaf(l, corr, __uint_as_float(rl));
         }
         m_prev_o = mj;
         tc_fence_before();
@@ -392,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         // A row with no visible key in this tile keeps its max; its
         // probabilities are exactly 0 below.
         const float mref = mn == -INFINITY ? 0.f : mn;
-        l *= exp2f(m - mref);
+        if constexpr (!row_sum_by_mma<DH>()) l *= exp2f(m - mref);
         m = mn;
         if (j & 1) m_hist1 = mref; else m_hist0 = mref;
         // P_j into the (hi, lo) swizzled operand buffer.
@@ -404,10 +447,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         for (int c8 = 0; c8 < kBKV / 8; ++c8) {
           float p8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            // one rounding: 2^(s scale - mref), flushed to 0 below 2^-126
+          for (int e = 0; e < 8; ++e)  // one rounding: 2^(s scale - mref), flushed below 2^-126
             p8[e] = ex2_ftz(fmaf(s[c8 * 8 + e], scale_log2, -mref));
-            l += p8[e];
+          if constexpr (!row_sum_by_mma<DH>()) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l += p8[e];
           }
           uint4 hv, lv;
           split8(p8, hv, lv, T());
