@@ -137,7 +137,14 @@ __device__ __forceinline__ void qkv_scatter(const float (&v)[32], const TcGemmAr
 #pragma unroll
         for (int j = 0; j < W; ++j) kn2 = fmaf(v[j0 + j], v[j0 + j], kn2);
         if (c0 + W == a.dh) {
-          atomicMax(a.kmax + bh, __float_as_int(sqrtf(kn2)));
+          // one atomic per (sequence, head) present in the warp: the lanes
+          // sharing a plane reduce first (non-negative floats order like
+          // their bit patterns)
+          const unsigned lane = threadIdx.x & 31u;
+          const unsigned mask = __activemask();
+          const unsigned grp = __match_any_sync(mask, (unsigned long long)bh);
+          const unsigned mx = __reduce_max_sync(grp, (unsigned)__float_as_int(sqrtf(kn2)));
+          if ((grp & ((1u << lane) - 1u)) == 0u) atomicMax(a.kmax + bh, (int)mx);
           kn2 = 0.f;
         }
       }
