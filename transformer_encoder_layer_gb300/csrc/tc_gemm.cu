@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (EPI == TC_EPI_GELU) {
             if (row_ok) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+              for (int j = 0; j < 32; ++j) v[j] = gelu_as7128(v[j]);
               store_row32_pair(o_hi, o_lo, (size_t)row * a.N + n0, v);
             }
           } else {  // LN pass 1: r = acc + bias + residual, chunk stats
