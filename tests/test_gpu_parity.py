@@ -274,6 +274,43 @@ def test_forward_host_slices_are_bit_identical(path, dtype, d, H, dff, L, batch,
     enc.close()
 
 
+@pytest.mark.parametrize("path,dtype,d,H,dff,L,batch", [
+    ("mega", "f16", 128, 4, 512, 64, 6),
+    ("mega", "f32", 32, 2, 128, 32, 4),
+    ("layered", "bf16", 512, 8, 1024, 70, 2),   # d > 256: GEMM + LayerNorm apply pass
+    ("layered", "f16", 64, 4, 256, 200, 2),     # head_dim 16 attention
+    ("dag", "f32", 64, 2, 256, 40, 2),          # counter memset + one launch
+    ("simt", "f32", 64, 4, 128, 33, 3),
+])
+def test_forward_captures_in_a_cuda_graph(path, dtype, d, H, dff, L, batch):
+    """forward() neither allocates nor synchronises, so it records into a CUDA
+    graph as it is; the replay gives the eager forward's bits."""
+    from transformer_encoder_layer_gb300 import binding
+    s = tiny_shape(dtype=dtype, batch=batch, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                   n_heads=H, d_ff=dff, n_layers=2)
+    inp = make_inputs(s, seed=12)
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    enc.set_path(path)
+    assert enc.plan(batch, L) == path
+    x = torch.from_numpy(to_storage(inp.x, dtype)).cuda()
+    vl = torch.from_numpy(inp.valid_len.astype(np.int32)).cuda()
+    ws = torch.empty(max(enc.workspace_size(batch, L), 256), dtype=torch.uint8, device="cuda")
+    ref = enc.forward(x, vl, workspace=ws)  # eager, also sets the kernels' attributes
+    out = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+        enc.forward(x, vl, out=out, workspace=ws, stream=side, check=False)
+    out.view(torch.uint8).fill_(0xFF)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+    assert enc.get_status() == 0
+    enc.close()
+
+
 def test_host_chunks_setting_is_checked():
     from transformer_encoder_layer_gb300 import binding
     s = SHAPES["short_d128_L64_B4096"].with_(batch=4)
