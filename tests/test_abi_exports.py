@@ -46,3 +46,18 @@ def test_status_strings_without_gpu():
     assert lib.tl_encoder_create(None, 1, 128, 4, 512, 1, ctypes.byref(h)) == 1
     assert lib.tl_encoder_workspace_size(None, 1, 1, None) == 1
     assert lib.tl_encoder_forward(None, None, 1, 1, None, None, None, 0, None) == 1
+    assert lib.tl_encoder_forward_host(None, None, 1, 1, None, None, None, 0, None) == 1
+    assert lib.tl_encoder_host_workspace_size(None, 1, 1, None) == 1
+    assert lib.tl_encoder_set_path(None, 0) == 1
+    assert lib.tl_encoder_set_host_chunks(None, 0) == 1
+    assert lib.tl_encoder_plan(None, 1, 1, None) == 1
+    # Shape checks at create time also come before any CUDA call (the weight
+    # pointers are not read when the shape is refused).
+    dummy = ctypes.create_string_buffer(12 * 8)
+    for d_model, heads, d_ff, dtype, want in [(100, 4, 512, 1, 2),   # d_model % 16
+                                              (2048, 16, 512, 1, 2),  # d_model > 1024
+                                              (128, 3, 512, 1, 2),    # heads do not divide
+                                              (128, 4, 520, 1, 2),    # d_ff % 16
+                                              (128, 4, 512, 7, 1),    # no such dtype
+                                              (8, 1, 512, 1, 1)]:     # d_model < 16
+        assert lib.tl_encoder_create(dummy, 1, d_model, heads, d_ff, dtype, ctypes.byref(h)) == want

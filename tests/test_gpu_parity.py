@@ -211,6 +211,88 @@ def test_causal_and_padding_invariance_bitwise():
         assert changed[b, s.seq_len - 1] and changed.sum() == 1
 
 
+@pytest.mark.parametrize("shape_name,batch", [("short_d128_L64_B4096", 9), ("wide_d1024_L1024_B32", 3),
+                                              ("batch1_d256_L512", 1), ("tiny_d32_L32", 4)])
+def test_layer_by_layer(shape_name, batch):
+    """Each layer alone: a one-layer encoder built from layer k's weights,
+    fed the oracle's layer k-1 output rounded to the I/O dtype, against the
+    oracle's one-layer result on that same input."""
+    import dataclasses
+    from transformer_encoder_layer_gb300.inputs import round_to_dtype
+    s = SHAPES[shape_name]
+    L = min(s.seq_len, 256)
+    s = s.with_(seq_len=L, vl_lo=min(s.vl_lo, L), vl_hi=L)
+    inp = make_inputs(s, seed=3, batch=batch)
+    h = inp.x
+    for k, p in enumerate(inp.layers):
+        one = dataclasses.replace(inp, shape=inp.shape.with_(n_layers=1), x=h, layers=[p])
+        got = _run(one)
+        ref = oracle.encoder_forward(h, inp.valid_len, [p], s.n_heads)
+        ok, util, idx = gate(got, ref)
+        assert ok, f"{shape_name} layer {k}: envelope {util:.3f} at {idx}"
+        h = round_to_dtype(ref, s.dtype)
+
+
+@pytest.mark.parametrize("shape_name", ["short_d128_L64_B4096", "wide_d1024_L1024_B32"])
+def test_batch_permutation_permutes_outputs(shape_name):
+    """Sequences are independent: permuting the batch permutes the output rows
+    bit for bit."""
+    s = SHAPES[shape_name]
+    batch = 6 if shape_name.startswith("short") else 3
+    inp = make_inputs(s, seed=5, batch=batch)
+    base = _run(inp)
+    perm = np.random.default_rng(7).permutation(batch)
+    inp2 = make_inputs(s, seed=5, batch=batch)
+    inp2.x = inp.x[perm].copy()
+    inp2.valid_len = inp.valid_len[perm].copy()
+    out = _run(inp2)
+    assert np.array_equal(out, base[perm])
+
+
+def test_argument_errors_with_a_handle():
+    """Host-side checks on a live handle return a status before any launch."""
+    import ctypes
+    from transformer_encoder_layer_gb300 import binding
+    s = tiny_shape(dtype="f16", batch=2, seq_len=40, vl_lo=1, vl_hi=40, d_model=64, n_heads=4,
+                   d_ff=256)
+    inp = make_inputs(s, seed=0)
+    enc = binding.Encoder(inp.layers, 64, 4, 256, "f16")
+    enc.set_path("layered")
+    lib, h = enc.lib, enc.handle
+    x = torch.from_numpy(to_storage(inp.x, "f16")).cuda()
+    vl = torch.from_numpy(inp.valid_len.astype(np.int32)).cuda()
+    out = torch.empty_like(x)
+    need = enc.workspace_size(2, 40)
+    assert need > 0
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    fwd = lambda xp, B, op, wsp, nb: lib.tl_encoder_forward(h, xp, B, 40, vl.data_ptr(), op, wsp, nb, None)
+    assert fwd(x.data_ptr(), 2, out.data_ptr(), ws.data_ptr(), need - 1) == 5      # workspace too small
+    assert fwd(x.data_ptr(), 2, x.data_ptr(), ws.data_ptr(), need) == 1           # out overlaps x
+    assert fwd(x.data_ptr() + 2, 2, out.data_ptr(), ws.data_ptr(), need) == 1     # x not 16-byte aligned
+    assert fwd(x.data_ptr(), 2, out.data_ptr(), ws.data_ptr() + 16, need) == 1    # workspace misaligned
+    assert fwd(x.data_ptr(), 0, out.data_ptr(), ws.data_ptr(), need) == 1         # B = 0
+    assert fwd(x.data_ptr(), 2, out.data_ptr(), ws.data_ptr(), need) == 0
+    assert lib.tl_encoder_set_path(h, 99) == 1
+    # a forced path that is not built for the shape: the megakernel needs d = 128
+    enc.set_path("mega")
+    with pytest.raises(binding.TLError):
+        enc.plan(2, 40)
+    assert fwd(x.data_ptr(), 2, out.data_ptr(), ws.data_ptr(), need) == 2
+    enc.set_path("auto")
+    # host-buffer forward: workspace below the reported size
+    hn = enc.host_workspace_size(2, 40)
+    xh, vh = x.cpu().pin_memory(), vl.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    hws = torch.empty(hn, dtype=torch.uint8, device="cuda")
+    assert lib.tl_encoder_forward_host(h, xh.data_ptr(), 2, 40, vh.data_ptr(), oh.data_ptr(),
+                                       hws.data_ptr(), hn - 1, None) == 5
+    assert lib.tl_encoder_forward_host(h, xh.data_ptr(), 2, 40, vh.data_ptr(), oh.data_ptr(),
+                                       hws.data_ptr(), hn, None) == 0
+    torch.cuda.synchronize()
+    assert enc.get_status() == 0
+    enc.close()
+
+
 def test_bad_valid_len_is_reported_and_clamped():
     from transformer_encoder_layer_gb300 import binding
     s = tiny_shape(dtype="f16", batch=2, seq_len=16, vl_lo=16, vl_hi=16, d_model=32)
