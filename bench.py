@@ -180,6 +180,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest of every rank's `value` (the job ends when its slowest
+    rank does); `value` itself when not distributed."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world_size, tokens_per_rank, ms_per_step):
+    """Weak scaling: every rank runs its own batch of the workload, so the job
+    processes world_size x tokens_per_rank tokens per step."""
+    return world_size * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def run_reference(args, shape):
     """The fp64 CPU oracle as the reference arm: each step is a bounded
     sample of the same workload (the first `ref_seqs` sequences)."""
@@ -298,15 +315,11 @@ def run_ours(args, shape):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
     per_kernel = enc.read_timing()
     enc.enable_timing(False)
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     if enc.get_status() != 0:
         raise RuntimeError("device status error in the timed region")
     ms_per_step = total_ms / args.steps
-    value = ws * shape.tokens / (ms_per_step / 1e3)
+    value = whole_job_tokens_per_s(ws, shape.tokens, ms_per_step)
     launches = sum(n for _, n in per_kernel.values())
 
     # End to end: the C-ABI host-buffer call (H2D of x and valid_len, the
@@ -319,7 +332,7 @@ def run_ours(args, shape):
         t0 = time.perf_counter()
         enc.forward_host(x_host, vl_host, out_host, workspace=hws)
         e2e_t.append(time.perf_counter() - t0)
-    e2e_s = statistics.mean(e2e_t)
+    e2e_s = max_over_ranks(statistics.mean(e2e_t), dist, dev)
     if not torch.equal(out_host, out.cpu()):
         raise RuntimeError("host-buffer forward disagrees with the device forward")
 
@@ -371,7 +384,7 @@ def run_ours(args, shape):
         "per_kernel_ms": {k: v[0] / args.steps for k, v in per_kernel.items()},
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
-        "e2e": {"value": ws * shape.tokens / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(ws, shape.tokens, 1e3 * e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size() + vl_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
         "clocks": clk.summary(),
