@@ -95,8 +95,8 @@ def kernel_work(cls, shape, counts):
         "dag": ("alu", counts["flops"]),
         "megakernel_simt": ("alu", counts["flops"]),
         # per launch, averaged over the 2 per layer: read the fp32 pre-LN rows
-        # and row stats, write fp32 + (hi, lo) planes (the last: the output)
-        "ln_apply": ("hbm", ((2 * shape.n_layers - 1) * (T * d * 12 + T * 8) + (T * d * 6 + T * 8))
+        # and row stats, write (hi, lo) planes (the last: the 16-bit output)
+        "ln_apply": ("hbm", ((2 * shape.n_layers - 1) * (T * d * 8 + T * 8) + (T * d * 6 + T * 8))
                      / (2 * shape.n_layers)),
     }
     return table.get(cls)

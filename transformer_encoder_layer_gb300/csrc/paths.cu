@@ -126,7 +126,7 @@ bool layered_supported(const tl_encoder* h) {
 
 struct LayeredWs {
   void *xh, *xl, *qh, *ql, *kh, *kl, *vth, *vtl, *ch, *cl, *yh, *yl, *hh, *hl;
-  float *x32, *y32, *rs;
+  float* rs;
   float2* stats;  // per-row (mean, rstd) of the LN GEMMs when d spans several N tiles
   int* ties;
   int* kmax;
@@ -151,7 +151,6 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   o[8] = take(T * d * e); o[9] = take(T * d * e);                          // ctx
   o[10] = take(T * d * e); o[11] = take(T * d * e);                        // y
   o[12] = take(T * h->dff * e); o[13] = take(T * h->dff * e);              // ffn hidden
-  o[14] = take(T * d * 4); o[15] = take(T * d * 4);                        // x32, y32
   o[16] = take(d > 256 ? T * d * 4 : 4);                                   // LN scratch
   const size_t ost = take(d > 256 ? T * 8 : 8);                            // LN row stats
   size_t ot = take((1 + T * h->H) * 4);
@@ -159,7 +158,7 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   void** p[14] = {&w.xh, &w.xl, &w.qh, &w.ql, &w.kh, &w.kl, &w.vth, &w.vtl, &w.ch, &w.cl,
                   &w.yh, &w.yl, &w.hh, &w.hl};
   for (int i = 0; i < 14; ++i) *p[i] = b + o[i];
-  w.x32 = (float*)(b + o[14]); w.y32 = (float*)(b + o[15]); w.rs = (float*)(b + o[16]);
+  w.rs = (float*)(b + o[16]);
   w.stats = (float2*)(b + ost);
   w.ties = (int*)(b + ot);
   w.kmax = (int*)(b + ok_);
@@ -235,8 +234,10 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
     {
       TcGemmArgs g{};
       g.M = M; g.N = d; g.K = d; g.BN = pick_bn(d); g.n_parts = 2; g.bias = P.b_o;
-      g.resid = first ? x : (const void*)w.x32; g.resid_kind = first ? 1 : 0;
-      g.gamma = P.ln1_g; g.beta = P.ln1_b; g.o32 = w.y32; g.o_hi = w.yh; g.o_lo = w.yl;
+      // residual: the stack input, then the previous layer's (hi, lo) output
+      g.resid = first ? x : (const void*)w.xh; g.resid_lo = first ? nullptr : w.xl;
+      g.resid_kind = first ? 1 : 2;
+      g.gamma = P.ln1_g; g.beta = P.ln1_b; g.o_hi = w.yh; g.o_lo = w.yl;
       g.rscratch = w.rs; g.status = h->status;
       if (d > g.BN) g.row_stats = w.stats;
       if (!amaps(w.ch, w.cl, M, d) || !make_tmap_2d(&mw, P.w_o, bf, d, d, d, 64, g.BN, 128))
@@ -261,11 +262,11 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
     {
       TcGemmArgs g{};
       g.M = M; g.N = d; g.K = dff; g.BN = pick_bn(d); g.n_parts = 2; g.bias = P.b_2;
-      g.resid = w.y32; g.resid_kind = 0; g.gamma = P.ln2_g; g.beta = P.ln2_b;
+      g.resid = w.yh; g.resid_lo = w.yl; g.resid_kind = 2; g.gamma = P.ln2_g; g.beta = P.ln2_b;
       if (last) {
         g.o_final = out;
       } else {
-        g.o32 = w.x32; g.o_hi = w.xh; g.o_lo = w.xl;
+        g.o_hi = w.xh; g.o_lo = w.xl;
       }
       g.rscratch = w.rs; g.status = h->status;
       if (d > g.BN) g.row_stats = w.stats;

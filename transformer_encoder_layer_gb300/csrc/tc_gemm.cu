@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float4 r = r4[j];
                   v[4 * j] += r.x; v[4 * j + 1] += r.y; v[4 * j + 2] += r.z; v[4 * j + 3] += r.w;
                 }
-              } else {
+              } else if (a.resid_kind == 1) {
                 const uint4* r4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.resid) + at);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -373,6 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const T* rt = reinterpret_cast<const T*>(&r);
 #pragma unroll
                   for (int e = 0; e < 8; ++e) v[8 * j + e] += to_f32<T>(rt[e]);
+                }
+              } else {  // (hi, lo) pair: the residual is hi + lo
+                const uint4* h4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.resid) + at);
+                const uint4* l4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.resid_lo) + at);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 rh = h4[j], rl = l4[j];
+                  const T* ht = reinterpret_cast<const T*>(&rh);
+                  const T* lt = reinterpret_cast<const T*>(&rl);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[8 * j + e] += to_f32<T>(ht[e]) + to_f32<T>(lt[e]);
                 }
               }
             }

@@ -27,7 +27,10 @@ struct TcGemmArgs {
   // TC_EPI_GELU: (hi, lo) planes [M, N].  TC_EPI_LN: optional (hi, lo) out.
   void *o_hi, *o_lo;
   // TC_EPI_LN
-  const void* resid;  // [M, N], fp32 (resid_kind 0) or the 16-bit type (1)
+  // [M, N]: fp32 (resid_kind 0), the 16-bit type (1), or the hi plane of a
+  // (hi, lo) pair of the 16-bit type whose lo plane is resid_lo (2)
+  const void* resid;
+  const void* resid_lo;
   int resid_kind;
   const float *gamma, *beta;
   float* o32;         // optional fp32 [M, N]
