@@ -151,8 +151,10 @@ tl_status tl_encoder_forward_host(tl_encoder *h, const void *x_host, int B, int 
 
 /* Batch slices tl_encoder_forward_host pipelines: 0 (the default) picks them
  * from the batch's size and path (slices of at least 8 MiB, at most 8; at
- * most 2 on the layered path; 1 on the task-graph path), 1 turns the pipeline
- * off, 2..64 asks for that many (capped at B).  TL_ERR_INVALID_ARG outside
+ * most 2 on the layered path; 1 on the task-graph path; with 4 or more, a
+ * quarter slice is also cut off each end so that the first upload and the
+ * last download are short), 1 turns the pipeline off, 2..64 asks for that
+ * many equal slices (capped at B).  TL_ERR_INVALID_ARG outside
  * 0..64. */
 tl_status tl_encoder_set_host_chunks(tl_encoder *h, int chunks);
 

@@ -393,6 +393,24 @@ def test_forward_captures_in_a_cuda_graph(path, dtype, d, H, dff, L, batch):
     enc.close()
 
 
+def test_forward_host_automatic_slices_with_ramp():
+    """A batch large enough for the automatic plan to pipeline (4+ slices of
+    8 MiB, with quarter slices at both ends) still gives the device forward's
+    bits."""
+    from transformer_encoder_layer_gb300 import binding
+    s = SHAPES["short_d128_L64_B4096"].with_(batch=2048)
+    inp = make_inputs(s, seed=8)
+    enc = binding.Encoder(inp.layers, s.d_model, s.n_heads, s.d_ff, s.dtype)
+    xh = torch.from_numpy(to_storage(inp.x, "f16")).pin_memory()
+    vh = torch.from_numpy(inp.valid_len.astype(np.int32)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    oh.view(torch.uint8).fill_(0xFF)
+    enc.forward_host(xh, vh, oh)
+    od = enc.forward(xh.cuda(), vh.cuda()).cpu()
+    assert torch.equal(oh.view(torch.uint8), od.view(torch.uint8))
+    enc.close()
+
+
 def test_host_chunks_setting_is_checked():
     from transformer_encoder_layer_gb300 import binding
     s = SHAPES["short_d128_L64_B4096"].with_(batch=4)

@@ -94,7 +94,8 @@ constexpr int kMaxHostChunks = 64;
 // path is the one chosen for the whole batch and every slice runs it.
 struct HostPlan {
   tl_path p;
-  int chunks, bc;  // slices and sequences per slice (the last may be shorter)
+  int chunks, bc;  // slices, and the most sequences in one slice
+  int start[kMaxHostChunks + 3];  // slice c holds sequences [start[c], start[c + 1])
   size_t row;      // bytes of one sequence of x or out
   size_t io;       // bytes of the device copy of x (and of out), padded
   size_t fw;       // forward workspace of one slice, padded
@@ -120,6 +121,22 @@ tl_status host_plan(const tl_encoder* h, int B, int L, HostPlan* hp) {
   hp->p = p;
   hp->chunks = (B + bc - 1) / bc;  // no empty slice
   hp->bc = bc;
+  int k = 0;
+  for (int c = 0; c <= hp->chunks; ++c) hp->start[k++] = std::min(c * bc, B);
+  if (h->host_chunks == 0 && hp->chunks >= 4 && bc >= 4) {
+    // Automatic plans also cut a quarter slice off each end: the first
+    // upload and the last download, which nothing overlaps, shrink 4x.
+    const int first = bc / 4, last = (B - hp->start[hp->chunks - 1]) / 4;
+    int s2[kMaxHostChunks + 3], m = 0;
+    s2[m++] = 0;
+    s2[m++] = first;
+    for (int c = 1; c < hp->chunks; ++c) s2[m++] = hp->start[c];
+    if (last >= 1) s2[m++] = B - last;
+    s2[m++] = B;
+    for (int i = 0; i < m; ++i) hp->start[i] = s2[i];
+    k = m;
+  }
+  hp->chunks = k - 1;
   hp->row = row;
   hp->io = align_up((size_t)B * row, 256);
   hp->fw = align_up(path_workspace_bytes(h, p, bc, L), 256);
@@ -352,12 +369,12 @@ tl_status tl_encoder_forward_host(tl_encoder* h, const void* x_host, int B, int 
   // buffers (whose downloads return only when done) slice c still computes
   // while slice c - 1 is copied back.
   auto down = [&](int c) {
-    const size_t off = (size_t)c * hp.bc * hp.row;
-    const size_t bytes = (size_t)std::min(hp.bc, B - c * hp.bc) * hp.row;
+    const size_t off = (size_t)hp.start[c] * hp.row;
+    const size_t bytes = (size_t)(hp.start[c + 1] - hp.start[c]) * hp.row;
     return cudaMemcpyAsync(oh + off, od + off, bytes, cudaMemcpyDeviceToHost, ss[c & 1]);
   };
   for (int c = 0; c < hp.chunks && e == cudaSuccess; ++c) {
-    const int b0 = c * hp.bc, bn = std::min(hp.bc, B - b0);
+    const int b0 = hp.start[c], bn = hp.start[c + 1] - b0;
     const size_t off = (size_t)b0 * hp.row, bytes = (size_t)bn * hp.row;
     cudaStream_t sc = ss[c & 1];
     if ((e = cudaMemcpyAsync(xd + off, xh + off, bytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess ||
