@@ -129,6 +129,27 @@ def test_k7_brute_force_tiny(scale):
     np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-11)
 
 
+def test_k7_brute_force_random_shapes():
+    """K7 over randomly drawn tiny shapes: batch, length, heads, widths,
+    layer count, valid lengths (including 1 and L), seed and input scale."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=30, deadline=None, derandomize=True)
+    @hyp.given(batch=st.integers(1, 3), seq_len=st.integers(1, 8), heads=st.sampled_from([1, 2, 4]),
+               dh=st.sampled_from([1, 2, 3]), d_ff=st.sampled_from([4, 8, 12]),
+               n_layers=st.integers(1, 2), seed=st.integers(0, 1000),
+               scale=st.sampled_from(list(SCALES)), vl_lo=st.integers(1, 8))
+    def check(batch, seq_len, heads, dh, d_ff, n_layers, seed, scale, vl_lo):
+        vl_lo = min(vl_lo, seq_len)
+        inp = _inputs(seed=seed, scale=scale, batch=batch, seq_len=seq_len, d_model=heads * dh,
+                      n_heads=heads, d_ff=d_ff, n_layers=n_layers, vl_lo=vl_lo, vl_hi=seq_len)
+        got = oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, heads)
+        np.testing.assert_allclose(got, brute_force_stack(inp), rtol=1e-10, atol=1e-10)
+
+    check()
+
+
 # -------------------------------------------------------- K2 / K3 invariances
 @pytest.mark.parametrize("scale", SCALES)
 def test_k2_causal_invariance(scale):
