@@ -61,3 +61,25 @@ def test_status_strings_without_gpu():
                                               (128, 4, 512, 7, 1),    # no such dtype
                                               (8, 1, 512, 1, 1)]:     # d_model < 16
         assert lib.tl_encoder_create(dummy, 1, d_model, heads, d_ff, dtype, ctypes.byref(h)) == want
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    """The boundary header is plain C99 (no C++ or CUDA types leak into it)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        import pytest
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "tl_encoder.h"\n'
+                   "int main(void) {\n"
+                   "  tl_layer_weights w = {0};\n"
+                   "  tl_encoder *h = 0;\n"
+                   "  (void)w;\n"
+                   "  return tl_encoder_destroy(h) == TL_OK ? 0 : 1;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src),
+                        "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
