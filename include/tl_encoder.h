@@ -124,7 +124,9 @@ tl_status tl_encoder_workspace_size(const tl_encoder *h, int B, int L, size_t *b
  * (right padding: tokens valid_len[b] .. L-1 of sequence b are padding).
  * workspace is caller-owned device scratch of at least
  * tl_encoder_workspace_size() bytes, 256-byte aligned.  The call only
- * enqueues work on stream: it neither allocates nor synchronises. */
+ * enqueues work on stream: it neither allocates nor synchronises.  B * L is
+ * at most 2^30 tokens (and B * L * n_heads below 2^31); a larger batch
+ * returns TL_ERR_UNSUPPORTED_SHAPE and is to be split by the caller. */
 tl_status tl_encoder_forward(tl_encoder *h, const void *x, int B, int L,
                              const int32_t *valid_len, void *out, void *workspace,
                              size_t workspace_bytes, void *stream);

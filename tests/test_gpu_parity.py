@@ -273,6 +273,11 @@ def test_argument_errors_with_a_handle():
     assert fwd(x.data_ptr(), 0, out.data_ptr(), ws.data_ptr(), need) == 1         # B = 0
     assert fwd(x.data_ptr(), 2, out.data_ptr(), ws.data_ptr(), need) == 0
     assert lib.tl_encoder_set_path(h, 99) == 1
+    # more tokens than the kernels' int row counts allow: refused, nothing allocated
+    with pytest.raises(binding.TLError):
+        enc.plan(1 << 20, 1 << 11)
+    with pytest.raises(binding.TLError):
+        enc.workspace_size(1 << 20, 1 << 11)
     # a forced path that is not built for the shape: the megakernel needs d = 128
     enc.set_path("mega")
     with pytest.raises(binding.TLError):

@@ -398,7 +398,10 @@ bool mega_ok(const tl_encoder* h, int L) {
 }
 
 tl_path choose_path(const tl_encoder* h, int B, int L) {
-  (void)B; (void)L;
+  // Row counts (B * L) and row-by-head counts are int in the kernels and
+  // their launch arithmetic; refuse token counts that could overflow them.
+  if ((long long)B * L > (1LL << 30) || (long long)B * L * h->H > (1LL << 31) - 1)
+    return TL_PATH_AUTO;
   switch (h->path) {
     case TL_PATH_SIMT:
       return TL_PATH_SIMT;
