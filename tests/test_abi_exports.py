@@ -83,3 +83,20 @@ def test_header_compiles_as_plain_c(tmp_path):
                         "-I", os.path.join(ROOT, "include"), "-c", str(src),
                         "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_no_cpu_fallback_without_a_gpu():
+    """Without a CUDA device the product path raises; nothing computes on the
+    host in its place."""
+    import pytest
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    from transformer_encoder_layer_gb300.inputs import make_inputs, tiny_shape
+    s = tiny_shape(dtype="f16", batch=1, seq_len=4, vl_lo=4, vl_hi=4, d_model=32)
+    inp = make_inputs(s, seed=0)
+    with pytest.raises(binding.TLError) as e:
+        binding.Encoder(inp.layers, 32, 2, 128, "f16")
+    assert e.value.code == 3  # TL_ERR_CUDA
+    with pytest.raises(Exception):
+        binding.run_forward(inp)
