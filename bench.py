@@ -76,7 +76,35 @@ def algorithmic_counts(shape, valid_len):
         "flops": nl * sum(per_layer.values()),
         "hbm_bytes": 2 * T * d * es + weights + 4 * shape.batch,
         "visible_keys": keys,
+        # transcendental evaluations: one exponential per visible score, one
+        # erf per FFN hidden value
+        "sfu_ops": nl * (keys * shape.n_heads + T * dff),
     }
+
+
+# SFU results per SM per clock (nominal: 4 per SM sub-partition).
+SFU_PER_SM_CLK = 16
+
+
+def step_fractions(counts, ms_per_step, peaks, sms, dtype):
+    """The whole step's algorithmic work over each roofline: tensor (16-bit
+    I/O only; measured sustained bf16 peak), FP32 ALU (SMs x 128 lanes x 2 x
+    max clock), HBM (measured copy bandwidth) and SFU (SMs x 16 x max clock).
+    The largest is the binding one."""
+    t = ms_per_step / 1e3
+    clk = peaks.get("sm_max_mhz", 2070.0) * 1e6
+    f = {
+        "tensor": None if dtype == "f32" else counts["flops"] / t / (peaks["bf16_tflops_sustained"] * 1e12),
+        "fp32_alu": counts["flops"] / t / (sms * 128 * 2 * clk),
+        "hbm": counts["hbm_bytes"] / t / (peaks["hbm_gbs"] * 1e9),
+        "sfu": counts["sfu_ops"] / t / (sms * SFU_PER_SM_CLK * clk),
+    }
+    # fp32 I/O runs on the CUDA cores, 16-bit I/O on the tensor cores: the
+    # arithmetic roofline that applies is the one the path uses
+    arith = "fp32_alu" if dtype == "f32" else "tensor"
+    candidates = {k: v for k, v in f.items() if v is not None and k in (arith, "hbm", "sfu")}
+    f["binding"] = max(candidates, key=candidates.get)
+    return f
 
 
 # Kernel class -> (bound, algorithmic work per launch) for the roofline line.
@@ -380,6 +408,9 @@ def run_ours(args, shape):
                    "l2": "flushed between timed steps (256 MB write)"},
         "valid_tokens_per_s": ws * int(inp.valid_len.sum()) / (ms_per_step / 1e3),
         "algorithmic_tflop_per_s": counts["flops"] / (ms_per_step / 1e3) / 1e12,
+        "step_fractions": step_fractions(counts, ms_per_step, peaks,
+                                         torch.cuda.get_device_properties(dev).multi_processor_count,
+                                         "f32" if shape.dtype == "f32" else shape.dtype),
         "roofline": roof,
         "per_kernel_ms": {k: v[0] / args.steps for k, v in per_kernel.items()},
         "gpu_launches": launches,
