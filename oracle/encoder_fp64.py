@@ -21,8 +21,7 @@ library primitives).  The layer, as the three pages describe the task
   erf failed a tolerance measured against exact erf);
 * second residual add and LayerNorm.  Post-LN order, no dropout.
 
-Readings where the pages are silent (each one is listed in the design notes):
-attention scale 1/sqrt(dh); LayerNorm eps 1e-5 with the biased variance and an
+Readings taken where the pages are silent: attention scale 1/sqrt(dh); LayerNorm eps 1e-5 with the biased variance and an
 affine gamma/beta; every linear has a bias; W_qkv rows are Q, K, V blocks in
 that order and head h owns rows h*dh .. (h+1)*dh-1 of each block; key j is
 visible to query i iff j <= i and j < valid_len (so padded query rows attend to
@@ -75,45 +74,45 @@ def allowed_keys(i, valid_len):
     return np.minimum(np.asarray(i) + 1, valid_len)
 
 
-def attention_row(q_i: np.ndarray, k: np.ndarray, v: np.ndarray, n_keys: int,
-                  check: bool = True) -> np.ndarray:
-    """Exact two-pass softmax attention of one query row over keys
-    0 .. n_keys-1 (the keys the mask allows).  q_i [dh]; k, v [L, dh]."""
-    dh = q_i.shape[-1]
-    s = (k[:n_keys] @ q_i) / math.sqrt(dh)
-    m = s.max()
-    e = np.exp(s - m)
-    p = e / e.sum()
-    if check:
-        assert abs(p.sum() - 1.0) < 1e-12
-    return p @ v[:n_keys]
-
-
 def masked_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                      valid_len: Sequence[int], row_block: int = 256,
-                     check: bool = True) -> np.ndarray:
-    """Causal + key-padding multi-head attention.  q, k, v [B, H, L, dh]
-    -> context [B, L, H*dh].
+                     check: bool = True, rows: np.ndarray | None = None) -> np.ndarray:
+    """Causal + key-padding multi-head attention.  k, v [B, H, L, dh];
+    q [B, H, R, dh] holds the query rows at positions ``rows[b]`` ([B, R],
+    increasing; default: every position, R = L).  Returns the context
+    [B, R, H*dh].
 
-    Query rows are independent, so they are taken in blocks of ``row_block``
-    rows (this only bounds memory for 100k-token sequences; every row's
-    scores, max, exponentials and sums are those of :func:`attention_row`).
-    Within a block, entries of keys the mask hides are set to -inf before the
-    max, so their exponentials are exactly 0."""
-    B, H, L, dh = q.shape
+    Each query row i takes an exact two-pass softmax over the keys the mask
+    leaves visible, j < min(i + 1, valid_len).  Rows are independent; they are
+    evaluated in blocks of the positions [r0, r0 + row_block), which only
+    bounds memory for 100k-token sequences.  A block's score matrix spans the
+    keys its last position may see; entries of keys hidden from a row are
+    set to -inf before the max, so their exponentials are exactly 0.  A
+    subset of rows is evaluated in the same blocks as the full set, so every
+    selected row goes through the same operations as in the full result."""
+    B, H, R, dh = q.shape
+    L = k.shape[2]
+    if rows is None:
+        rows = np.broadcast_to(np.arange(L), (B, L))
+    rows = np.asarray(rows)
+    assert rows.shape == (B, R)
     out = np.empty_like(q)
     scale = 1.0 / math.sqrt(dh)
     for b in range(B):
         vl = int(valid_len[b])
         assert 1 <= vl <= L
+        pos = rows[b]
+        assert np.all(np.diff(pos) > 0) and pos[0] >= 0 and pos[-1] < L
         for r0 in range(0, L, row_block):
             r1 = min(L, r0 + row_block)
-            rows = np.arange(r0, r1)
-            n_keys = allowed_keys(rows, vl)            # visible prefix per row
-            kmax = int(n_keys.max())
+            sel = np.nonzero((pos >= r0) & (pos < r1))[0]  # entries of q in this block
+            if sel.size == 0:
+                continue
+            n_keys = allowed_keys(pos[sel], vl)        # visible prefix per row
+            kmax = int(allowed_keys(r1 - 1, vl))       # the block's widest prefix
             hidden = np.arange(kmax)[None, :] >= n_keys[:, None]
             for h in range(H):
-                s = (q[b, h, r0:r1] @ k[b, h, :kmax].T) * scale
+                s = (q[b, h, sel] @ k[b, h, :kmax].T) * scale
                 s[hidden] = -np.inf
                 m = s.max(axis=1, keepdims=True)
                 e = np.exp(s - m)
@@ -121,7 +120,7 @@ def masked_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                 p = e / den
                 if check:
                     assert np.all(np.abs(p.sum(axis=1) - 1.0) < 1e-12)
-                out[b, h, r0:r1] = p @ v[b, h, :kmax]
+                out[b, h, sel] = p @ v[b, h, :kmax]
     return merge_heads(out)
 
 
@@ -141,14 +140,24 @@ def gelu_erf(u: np.ndarray) -> np.ndarray:
 
 
 def encoder_layer(x: np.ndarray, valid_len: Sequence[int], p: Dict[str, np.ndarray],
-                  n_heads: int, row_block: int = 256, check: bool = True) -> np.ndarray:
+                  n_heads: int, row_block: int = 256, check: bool = True,
+                  rows: np.ndarray | None = None) -> np.ndarray:
     """One post-LN encoder layer, no dropout:
         y  = LN1(x + MHA(x) W_o^T + b_o)
-        x' = LN2(y + gelu(y W_1^T + b_1) W_2^T + b_2)."""
+        x' = LN2(y + gelu(y W_1^T + b_1) W_2^T + b_2).
+    With ``rows`` ([B, R] increasing positions per sequence) only those
+    query rows are evaluated and [B, R, d] is returned; the keys and values
+    still come from every position."""
     q, k, v = qkv_projection(x, p["w_qkv"], p["b_qkv"], n_heads)
-    ctx = masked_attention(q, k, v, valid_len, row_block=row_block, check=check)
+    xr = x
+    if rows is not None:
+        rows = np.asarray(rows)
+        bi = np.arange(x.shape[0])[:, None]
+        q = q[bi[:, :, None], np.arange(n_heads)[None, :, None], rows[:, None, :]]
+        xr = x[bi, rows]
+    ctx = masked_attention(q, k, v, valid_len, row_block=row_block, check=check, rows=rows)
     a = ctx @ p["w_o"].T + p["b_o"]
-    y = layer_norm(x + a, p["ln1_g"], p["ln1_b"])
+    y = layer_norm(xr + a, p["ln1_g"], p["ln1_b"])
     f = gelu_erf(y @ p["w_1"].T + p["b_1"])
     g = f @ p["w_2"].T + p["b_2"]
     return layer_norm(y + g, p["ln2_g"], p["ln2_b"])
@@ -181,24 +190,3 @@ def first_row_closed_form(x0: np.ndarray, layers: List[Dict[str, np.ndarray]]
         f = gelu_erf(y @ p["w_1"].T + p["b_1"])
         h = layer_norm(y + f @ p["w_2"].T + p["b_2"], p["ln2_g"], p["ln2_b"])
     return h
-
-
-def layer1_top2_gap(x: np.ndarray, valid_len: Sequence[int], p: Dict[str, np.ndarray],
-                    n_heads: int) -> np.ndarray:
-    """Diagnostic: for every (b, h, i) of the first layer, the gap in logits
-    between the largest and second-largest visible score (inf for rows with
-    one visible key).  Small gaps at large input scales are the rows whose
-    softmax is ill-conditioned."""
-    q, k, _ = qkv_projection(x, p["w_qkv"], p["b_qkv"], n_heads)
-    B, H, L, dh = q.shape
-    gap = np.full((B, H, L), np.inf)
-    for b in range(B):
-        vl = int(valid_len[b])
-        for h in range(H):
-            s = (q[b, h] @ k[b, h, :vl].T) / math.sqrt(dh)
-            for i in range(L):
-                n = int(allowed_keys(i, vl))
-                if n >= 2:
-                    top = np.partition(s[i, :n], n - 2)[n - 2:]
-                    gap[b, h, i] = top[1] - top[0]
-    return gap

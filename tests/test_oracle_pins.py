@@ -282,6 +282,44 @@ def test_row_blocking_does_not_change_rows():
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_row_selection_matches_full_result(seed):
+    """Evaluating only some query rows (the sampled gate of the 100k-token
+    workload) gives those rows of the full evaluation.  The two runs group
+    the same sums differently (BLAS picks its kernels by the number of rows),
+    so they agree to rounding, 1e-13 of the output's scale, not bit for bit;
+    a wrong row, key range or residual row would be off by O(1)."""
+    rng = np.random.default_rng(100 + seed)
+    B, L = int(rng.integers(1, 4)), int(rng.integers(2, 60))
+    H = int(rng.choice([1, 2, 4]))
+    d = H * int(rng.choice([1, 2, 4, 8]))
+    scale = float(rng.choice(SCALES))
+    inp = _inputs(seed=seed, scale=scale, batch=B, seq_len=L, vl_lo=1, vl_hi=L, d_model=d,
+                  n_heads=H, d_ff=2 * d, n_layers=1)
+    rb = int(rng.integers(1, 16))
+    full = oracle.encoder_layer(inp.x, inp.valid_len, inp.layers[0], H, row_block=rb)
+    n = int(rng.integers(min(L, 5), L + 1))  # rows per sequence
+    rows = []
+    for b in range(B):
+        vl = int(inp.valid_len[b])
+        # always the first and last rows and those around the padding boundary
+        pick = {0, L - 1, max(vl - 2, 0), vl - 1, min(vl, L - 1)}
+        for r in rng.permutation(L):
+            if len(pick) >= n:
+                break
+            pick.add(int(r))
+        rows.append(sorted(pick)[:n] if len(pick) > n else sorted(pick))
+    rows = np.array(rows)
+    sel = oracle.encoder_layer(inp.x, inp.valid_len, inp.layers[0], H, row_block=rb, rows=rows)
+    ref = full[np.arange(B)[:, None], rows]
+    assert sel.shape == (B, n, d)
+    np.testing.assert_allclose(sel, ref, rtol=0, atol=1e-13 * np.max(np.abs(ref)))
+    # every row: the selection of all positions is the full evaluation itself
+    allr = np.broadcast_to(np.arange(L), (B, L))
+    assert np.array_equal(
+        oracle.encoder_layer(inp.x, inp.valid_len, inp.layers[0], H, row_block=rb, rows=allr), full)
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """Plant plausible mistakes in the oracle (on the CPU) and check that the
     library pin K8 rejects each of them."""
