@@ -182,10 +182,12 @@ tl_status tl_encoder_destroy(tl_encoder *h);
  * that the library declares statically: every GPU that loads the library
  * holds it until the process exits.  A shape whose workspace
  * (tl_encoder_workspace_size) exceeds it is rejected with
- * TL_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The first call on
- * a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current and caches it, so make that first call before any
- * stream capture.  Every call on a device shares the one array and it keeps
+ * TL_ERR_WORKSPACE_TOO_SMALL before anything is launched.  tl_encoder_create
+ * looks up the array's device address (cudaGetSymbolAddress) with the
+ * handle's device current and keeps it in the handle, so the address lives
+ * and dies with the same context as the handle's weights; this call itself
+ * neither allocates nor looks anything up (TL_ERR_CUDA if that lookup failed
+ * at create).  Every call on a device shares the one array and it keeps
  * the last call's contents (the forward zeroes what it needs zeroed itself);
  * calls that overlap on the GPU -- on two streams, or from two handles --
  * race on it, so serialise them.  Otherwise as tl_encoder_forward (x, out,

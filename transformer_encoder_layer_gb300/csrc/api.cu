@@ -211,6 +211,10 @@ tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d
     delete h;
     return TL_ERR_CUDA;
   }
+  // The static scratch array's address in this device's context, for
+  // tl_encoder_forward_static (null if the lookup fails; that entry point
+  // then returns TL_ERR_CUDA and every other call is unaffected).
+  h->static_scratch = static_scratch_address();
   const size_t es = dtype_size(dtype);
   std::vector<LayerOffsets> offs;
   size_t total = 0;

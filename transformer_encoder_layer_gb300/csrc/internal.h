@@ -66,6 +66,9 @@ struct tl_encoder {
   tl_layer_dev* layers = nullptr;  // host array of n_layers
   tl_timing* timing = nullptr;     // non-null while per-kernel timing is on
   const void* mega_layers = nullptr;  // device array of MegaLayer (megakernel path)
+  // Device address of the library's static scratch array in this handle's
+  // context (tl_encoder_forward_static), looked up at create.
+  void* static_scratch = nullptr;
   // Host-buffer forward: batch slices per call (0 = automatic) and the two
   // non-blocking streams plus fork/join events its copy/compute pipeline uses
   // (created on first use).
@@ -82,6 +85,8 @@ struct KernelTimer {
   tl_encoder* h; int k; cudaStream_t s; int slot;
 };
 void timing_destroy(tl_encoder* h);
+// Device address of the static scratch array in the current context, or null.
+void* static_scratch_address();
 }  // namespace tl
 
 namespace tl {

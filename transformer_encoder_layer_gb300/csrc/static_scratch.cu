@@ -3,14 +3,15 @@
 // for callers that may not allocate device memory at the point of the call.
 //
 // The array is TL_STATIC_SCRATCH_BYTES (32 MiB) of file-scope __device__
-// memory, created when the library's module loads on a device and held until
-// the process exits.  Host code cannot hand the array's name to a kernel (on
-// the host it is only a stand-in symbol), so the first call on each device
-// looks up its device address with cudaGetSymbolAddress, with that device
-// current, and caches it; later calls reuse the cached address.
+// memory, created when the library's module loads in a device's context and
+// held until the process exits.  Host code cannot hand the array's name to a
+// kernel (on the host it is only a stand-in symbol), so tl_encoder_create
+// looks up its device address with cudaGetSymbolAddress, with the handle's
+// device current, and keeps it in the handle.  The address then belongs to
+// the same context as the handle's packed weights: a context that is torn
+// down and re-created (cudaDeviceReset) invalidates both together, and a
+// handle created afterwards looks the address up afresh.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -23,27 +24,22 @@ static_assert(kStaticScratchBytes == TL_STATIC_SCRATCH_BYTES, "header and librar
 
 static __device__ __align__(256) unsigned char tl_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
+}  // namespace
 
-// Device address of the static array on the current device (set up once per
-// device).  Returns null if the lookup fails.
-void* scratch_on_current_device(int dev) {
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, tl_static_scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = p;
+namespace tl {
+
+// Device address of the static array in the current context, or null if the
+// lookup fails (the error is cleared).
+void* static_scratch_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, tl_static_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  return p;
 }
 
-}  // namespace
+}  // namespace tl
 
 extern "C" tl_status tl_encoder_forward_static(tl_encoder* h, const void* x, int B, int L,
                                                const int32_t* valid_len, void* out, void* stream) {
@@ -55,7 +51,7 @@ extern "C" tl_status tl_encoder_forward_static(tl_encoder* h, const void* x, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TL_ERR_CUDA;
   if (dev != h->device) return TL_ERR_INVALID_ARG;
-  void* ws = scratch_on_current_device(dev);
+  void* ws = h->static_scratch;  // looked up by tl_encoder_create
   if (!ws) return TL_ERR_CUDA;
   return tl_encoder_forward(h, x, B, L, valid_len, out, need ? ws : nullptr, need, stream);
 }
