@@ -4,8 +4,9 @@ Every comparison is element by element under the pages' gate
 (|err| <= 0.002 OR |err| <= 0.02 |ref|, NaN/Inf fail), on seeded inputs, over
 seeds and the input-scale sweep 1e-3 .. 1e3.  Sizes the oracle finishes in
 seconds are checked in full; full-size workloads are checked on sampled
-sequences (sequences are independent) or, for the 100k-token workload, on a
-causal prefix (rows < P depend only on tokens < P when P <= valid_len).
+sequences (sequences are independent) or, for the 100k-token workload, layer
+by layer on 4096 sampled query rows of every sequence, and as a whole stack
+on a causal prefix (rows < P depend only on tokens < P when P <= valid_len).
 """
 import numpy as np
 import pytest
@@ -150,8 +151,58 @@ def test_short_d128_full_size_sampled(scale):
     _sampled_sequences("short_d128_L64_B4096", 48, scale=scale)
 
 
-def test_wide_d1024_full_size_sampled():
-    _sampled_sequences("wide_d1024_L1024_B32", 2)
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_wide_d1024_full_size_sampled(scale):
+    _sampled_sequences("wide_d1024_L1024_B32", 4, scale=scale)
+
+
+@pytest.fixture(scope="module")
+def oracle_pool():
+    import oracle_workers
+    pool = oracle_workers.make_pool()
+    yield pool
+    pool.close()
+    pool.join()
+
+
+def _gate_rows(L, vl, n, rng):
+    """n increasing query positions of a sequence: a seeded uniform sample
+    that always holds rows 0, 1, vl-2, vl-1, vl (when vl < L) and L-1."""
+    must = {0, 1, vl - 2, vl - 1, L - 1} | ({vl} if vl < L else set())
+    rest = np.setdiff1d(np.arange(L), np.array(sorted(must)))
+    extra = rng.choice(rest, size=n - len(must), replace=False)
+    return np.sort(np.concatenate([np.array(sorted(must)), extra]))
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+@pytest.mark.parametrize("layer", [0, 1])
+def test_long_d64_full_length_sampled_rows(layer, scale, oracle_pool):
+    """Each layer of the 100k-token workload at full size (8 sequences of
+    100,000 tokens) as a one-layer encoder on the seeded input: every element
+    of 4096 seeded query rows per sequence against the oracle, which
+    evaluates just those rows (keys and values from all 100,000 positions).
+    The sample reaches the longest key ranges, the padding boundary and the
+    padded rows past it."""
+    import dataclasses
+    s = SHAPES["long_d64_L100k_B8"]
+    inp = make_inputs(s, seed=0, input_scale=scale)
+    p = inp.layers[layer]
+    one = dataclasses.replace(inp, shape=s.with_(n_layers=1), layers=[p])
+    got = _run(one)
+    assert got.shape == (s.batch, s.seq_len, s.d_model)
+    rng = np.random.default_rng(1000 + 10 * layer + INPUT_SCALES.index(scale))
+    rows = [_gate_rows(s.seq_len, int(inp.valid_len[b]), 4096, rng) for b in range(s.batch)]
+    jobs = [(inp.x[b:b + 1], inp.valid_len[b:b + 1], p, s.n_heads, rows[b][None])
+            for b in range(s.batch)]
+    import oracle_workers
+    refs = oracle_pool.map(oracle_workers.layer_rows, jobs)
+    worst = 0.0
+    for b in range(s.batch):
+        ok, util, where = gate(got[b, rows[b]], refs[b][0])
+        assert ok, f"layer {layer} scale {scale} sequence {b}: envelope {util:.3f} at " \
+                   f"row {rows[b][where[0]]} col {where[1]}"
+        worst = max(worst, util)
+    assert np.all(np.isfinite(got))
 
 
 def test_long_d64_full_size_prefix_and_first_row():
@@ -298,19 +349,36 @@ def test_argument_errors_with_a_handle():
     enc.close()
 
 
-def test_bad_valid_len_is_reported_and_clamped():
+@pytest.mark.parametrize("path,dtype,d,H,dff,L", [
+    ("simt", "f16", 32, 2, 128, 16),
+    ("layered", "f16", 64, 4, 256, 16),     # tcgen05 attention, head_dim 16
+    ("layered", "bf16", 128, 2, 256, 40),   # tcgen05 attention, head_dim 64
+    ("mega", "f16", 128, 4, 512, 64),       # tensor-core megakernel
+    ("mega", "f32", 32, 2, 128, 32),        # CUDA-core megakernel
+    ("dag", "f32", 64, 2, 256, 40),         # task graph
+])
+def test_bad_valid_len_is_reported_and_clamped(path, dtype, d, H, dff, L):
+    """Every path clamps a valid_len outside [1, L] and reports it through
+    the status word; the result equals a run with the clamped lengths."""
     from transformer_encoder_layer_gb300 import binding
-    s = tiny_shape(dtype="f16", batch=2, seq_len=16, vl_lo=16, vl_hi=16, d_model=32)
+    s = tiny_shape(dtype=dtype, batch=2, seq_len=L, vl_lo=L, vl_hi=L, d_model=d, n_heads=H,
+                   d_ff=dff)
     inp = make_inputs(s, seed=0)
-    enc = binding.Encoder(inp.layers, 32, 2, 128, "f16")
-    x = torch.from_numpy(to_storage(inp.x, "f16")).cuda()
-    vl = torch.tensor([0, 17], dtype=torch.int32, device="cuda")
+    enc = binding.Encoder(inp.layers, d, H, dff, dtype)
+    enc.set_path(path)
+    assert enc.plan(2, L) == path
+    st = to_storage(inp.x, dtype)
+    x = (torch.from_numpy(st.view(np.int16)).view(torch.bfloat16) if dtype == "bf16"
+         else torch.from_numpy(st)).cuda()
+    vl = torch.tensor([0, L + 1], dtype=torch.int32, device="cuda")
     out = enc.forward(x, vl, check=False)
     assert enc.get_status() == 6  # TL_ERR_BAD_VALID_LEN
     assert enc.get_status() == 0  # cleared by the read
-    # Clamped to [1, L]: equal to running with valid_len = [1, 16].
-    ref = enc.forward(x, torch.tensor([1, 16], dtype=torch.int32, device="cuda"))
-    assert torch.equal(out, ref)
+    # Clamped to [1, L]: equal to running with valid_len = [1, L].
+    ref = enc.forward(x, torch.tensor([1, L], dtype=torch.int32, device="cuda"))
+    assert torch.equal(out.view(torch.uint8) if dtype == "bf16" else out,
+                       ref.view(torch.uint8) if dtype == "bf16" else ref)
+    assert enc.get_status() == 0
     enc.close()
 
 

@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+  // A valid_len outside [1, L] is clamped where it is read (key_tiles); the
+  // first CTA records it in the status word, once per offending sequence.
+  if (blockIdx.x == 0 && warp >= 2)
+    for (int b = threadIdx.x - 64; b < a.B; b += kThreads - 64) load_valid_len(a.valid_len, b, a.L, a.status);
   if (row_sum_by_mma<DH>() && warp >= 2) {
     // The V^T buffers' 16 extra rows, never touched by TMA: row head_dim of
     // the hi plane all ones (its product with P is the row sum), the rest 0.
