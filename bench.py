@@ -4,8 +4,12 @@
 One step = one forward of the whole stack (every layer: fused QKV, masked
 attention, out-projection + residual + LayerNorm, FFN with exact GELU,
 residual + LayerNorm) over one batch of synthetic inputs already resident in
-HBM.  The default workload is the 4-layer d_model=128 encoder on 4096
-sequences of 64 tokens, fp16 I/O.  Prints ONE JSON line (rank 0).
+HBM.  The headline workload is the 4-layer d_model=128 encoder on 4096
+sequences of 64 tokens, fp16 I/O.  Prints ONE JSON line (rank 0); its
+``per_workload`` object times the same forward on every one of the five
+synthetic workloads (configs of the pages' task), each with its dominant
+kernel's roofline fraction and the gate's envelope utilisation on a sample of
+the timed output.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -32,6 +36,11 @@ import numpy as np  # noqa: E402
 
 METRIC = "encoder forward tokens/s on 1 GB300 (masked); % of tensor/HBM roofline"
 DEFAULT_WORKLOAD = "short_d128_L64_B4096"
+WORKLOADS = ("tiny_d32_L32", "short_d128_L64_B4096", "batch1_d256_L512",
+             "wide_d1024_L1024_B32", "long_d64_L100k_B8")
+# Timed steps per workload in the per-workload table (the headline uses --steps).
+PER_WORKLOAD_STEPS = {"tiny_d32_L32": 50, "short_d128_L64_B4096": 30, "batch1_d256_L512": 50,
+                      "wide_d1024_L1024_B32": 20, "long_d64_L100k_B8": 5}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -86,24 +95,28 @@ def algorithmic_counts(shape, valid_len):
 SFU_PER_SM_CLK = 16
 
 
+def fp32_alu_tflops(peaks, sms):
+    """FP32 FMA peak derived from unit counts: SMs x 128 lanes x 2 flops x
+    max SM clock."""
+    return sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
 def step_fractions(counts, ms_per_step, peaks, sms, dtype):
-    """The whole step's algorithmic work over each roofline: tensor (16-bit
-    I/O only; measured sustained bf16 peak), FP32 ALU (SMs x 128 lanes x 2 x
-    max clock), HBM (measured copy bandwidth) and SFU (SMs x 16 x max clock).
-    The largest is the binding one."""
+    """The whole step's algorithmic work over the rooflines that apply to the
+    path: the tensor cores (16-bit I/O; measured bf16 burst peak, fp16 dense
+    runs at the same rate) or the FP32 ALUs (fp32 I/O runs on the CUDA
+    cores), HBM (measured copy bandwidth) and the SFU (SMs x 16 x max
+    clock).  The largest is the binding one."""
     t = ms_per_step / 1e3
     clk = peaks.get("sm_max_mhz", 2070.0) * 1e6
-    f = {
-        "tensor": None if dtype == "f32" else counts["flops"] / t / (peaks["bf16_tflops_sustained"] * 1e12),
-        "fp32_alu": counts["flops"] / t / (sms * 128 * 2 * clk),
-        "hbm": counts["hbm_bytes"] / t / (peaks["hbm_gbs"] * 1e9),
-        "sfu": counts["sfu_ops"] / t / (sms * SFU_PER_SM_CLK * clk),
-    }
-    # fp32 I/O runs on the CUDA cores, 16-bit I/O on the tensor cores: the
-    # arithmetic roofline that applies is the one the path uses
-    arith = "fp32_alu" if dtype == "f32" else "tensor"
-    candidates = {k: v for k, v in f.items() if v is not None and k in (arith, "hbm", "sfu")}
-    f["binding"] = max(candidates, key=candidates.get)
+    f = {}
+    if dtype == "f32":
+        f["fp32_alu"] = counts["flops"] / t / (fp32_alu_tflops(peaks, sms) * 1e12)
+    else:
+        f["tensor"] = counts["flops"] / t / (peaks["bf16_tflops"] * 1e12)
+    f["hbm"] = counts["hbm_bytes"] / t / (peaks["hbm_gbs"] * 1e9)
+    f["sfu"] = counts["sfu_ops"] / t / (sms * SFU_PER_SM_CLK * clk)
+    f["binding"] = max(f, key=f.get)
     return f
 
 
@@ -149,6 +162,31 @@ def traffic_from_profiles(cls, workload):
     return e["dram_bytes_per_launch"] if sha == e["source_sha"] else None
 
 
+def kernel_roofline(per_kernel, shape, counts, peaks, sms, total_ms):
+    """The dominant kernel's algorithmic work per launch over its average
+    event-timed launch duration, against the peak of the unit that bounds it
+    (tensor: measured bf16 burst peak; HBM: measured copy bandwidth; FP32
+    ALU: derived from unit counts and the max clock)."""
+    if not per_kernel:
+        return None
+    dom = max(per_kernel, key=lambda k: per_kernel[k][0])
+    ms, n = per_kernel[dom]
+    bound, work = kernel_work(dom, shape, counts) or ("tensor", counts["flops"])
+    avg_s = ms / n / 1e3
+    if bound == "hbm":
+        achieved, peak, unit, src = work / avg_s / 1e9, peaks["hbm_gbs"], "GB/s", peaks["source"]
+    elif bound == "alu":
+        achieved, peak, unit = work / avg_s / 1e12, fp32_alu_tflops(peaks, sms), "TFLOP/s"
+        src = "derived: SMs x 128 FP32 lanes x 2 x max SM clock"
+    else:
+        achieved, peak, unit = work / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        src = peaks["source"] + " bf16 burst (fp16 dense runs at the bf16 rate)"
+    return {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic_from_profiles(dom, shape.name),
+            "peak_source": src, "share_of_step": ms / total_ms if total_ms else None,
+            "launches": n, "avg_launch_ms": ms / n}
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -183,7 +221,7 @@ class ClockSampler:
     def summary(self):
         if not getattr(self, "lines", None):
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -192,13 +230,17 @@ class ClockSampler:
                 mx.append(float(f[1]))
             except (ValueError, IndexError):
                 continue
+            try:
+                pw.append(float(f[2]))
+            except (ValueError, IndexError):
+                pass
             for n, v in zip(names, f[3:7]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons)}
 
 
 def dist_env():
@@ -223,6 +265,10 @@ def whole_job_tokens_per_s(world_size, tokens_per_rank, ms_per_step):
     """Weak scaling: every rank runs its own batch of the workload, so the job
     processes world_size x tokens_per_rank tokens per step."""
     return world_size * tokens_per_rank / (ms_per_step / 1e3)
+
+
+def percentile(v, q):
+    return float(np.percentile(np.asarray(v, dtype=np.float64), q))
 
 
 def run_reference(args, shape):
@@ -273,6 +319,171 @@ def cpu_baseline(shape, n_seqs):
                       f"{dt:.1f} s"}
 
 
+def envelope_on_sample(inp, out_np):
+    """The gate's envelope utilisation of a timed output against the oracle,
+    on a sample the oracle finishes in seconds: whole sequences where the
+    workload allows (sequences are independent), else, at 100k tokens, the
+    causal prefix of 2048 rows (rows < P see only tokens < P when every
+    valid_len > P)."""
+    import oracle
+    from transformer_encoder_layer_gb300.gate import gate
+    s = inp.shape
+    if s.seq_len > 8192:
+        P = 2048
+        assert int(inp.valid_len.min()) > P
+        ref = oracle.encoder_forward(inp.x[:, :P], np.full(s.batch, P), inp.layers, s.n_heads,
+                                     check=False)
+        ok, util, _ = gate(out_np[:, :P], ref)
+        return {"utilisation": util, "passed": ok,
+                "sample": f"rows < {P} of all {s.batch} sequences (causal prefix)"}
+    n = max(1, min(s.batch, 16, (1 << 16) // (s.seq_len * max(1, s.d_model // 64))))
+    ref = oracle.encoder_forward(inp.x[:n], inp.valid_len[:n], inp.layers, s.n_heads, check=False)
+    ok, util, _ = gate(out_np[:n], ref)
+    return {"utilisation": util, "passed": ok, "sample": f"first {n} of {s.batch} sequences"}
+
+
+class Workload:
+    """One workload's encoder, device buffers and pinned host copies."""
+
+    def __init__(self, shape, seed, dev, path="auto"):
+        import torch
+        from transformer_encoder_layer_gb300 import binding
+        from transformer_encoder_layer_gb300.inputs import make_inputs, to_storage
+        self.shape = shape
+        self.inp = make_inputs(shape, seed=seed, input_scale=1.0)
+        self.counts = algorithmic_counts(shape, self.inp.valid_len)
+        self.enc = binding.Encoder(self.inp.layers, shape.d_model, shape.n_heads, shape.d_ff,
+                                   shape.dtype)
+        if path != "auto":
+            self.enc.set_path(path)
+        self.path = self.enc.plan(shape.batch, shape.seq_len)
+        xs = to_storage(self.inp.x, shape.dtype)
+        if shape.dtype == "bf16":
+            x_host = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16)
+        else:
+            x_host = torch.from_numpy(xs)
+        self.x_host = x_host.contiguous().pin_memory()
+        self.vl_host = torch.from_numpy(self.inp.valid_len.astype(np.int32)).pin_memory()
+        self.x = self.x_host.to(dev)
+        self.vl = self.vl_host.to(dev)
+        self.out = torch.empty_like(self.x)
+        wsz = self.enc.workspace_size(shape.batch, shape.seq_len)
+        self.work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+
+    def step(self, stream):
+        self.enc.forward(self.x, self.vl, out=self.out, workspace=self.work, stream=stream, check=False)
+
+    def out_f64(self):
+        import torch
+        from transformer_encoder_layer_gb300.inputs import from_storage
+        o = self.out.cpu()
+        if self.shape.dtype == "bf16":
+            return from_storage(o.view(torch.int16).numpy().view(np.uint16), "bf16")
+        return from_storage(o.numpy(), self.shape.dtype)
+
+    def close(self):
+        self.enc.close()
+
+
+def time_steps(w, steps, warmup, flush, stream, dist=None, clock_index=None):
+    """W warm-up steps, then K timed steps with an L2 flush (a 256 MB write)
+    before each, timed by CUDA events on the launch stream, with the
+    library's per-launch event timer on.  Returns per-step ms, per-kernel
+    (ms, launches), the host wall time of the timed region and the clocks
+    sampled during it."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        w.step(stream)
+    torch.cuda.synchronize()
+    if w.enc.get_status() != 0:
+        raise RuntimeError(f"{w.shape.name}: device status error during warm-up")
+    w.enc.enable_timing(True, capacity=max(4096, 64 * steps * w.shape.n_layers))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(clock_index) if clock_index is not None else None
+    if clk:
+        clk.__enter__()
+    t_wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        starts[i].record(stream)
+        w.step(stream)
+        stops[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if clk:
+        clk.__exit__(None, None, None)
+    if dist:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    per_kernel = w.enc.read_timing()
+    w.enc.enable_timing(False)
+    if w.enc.get_status() != 0:
+        raise RuntimeError(f"{w.shape.name}: device status error in the timed region")
+    return step_ms, per_kernel, t_wall, (clk.summary() if clk else None)
+
+
+def first_calls(workloads):
+    """First-call time of each workload in a fresh process (the pages' harness
+    runs every measurement in a new process): create the encoder, then the
+    host wall time of its first forward up to the stream synchronisation.
+    Workloads run in the given order in one child process, so the first entry
+    also pays the library's module load."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--first-call-probe", ",".join(workloads)]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        for ln in r.stdout.splitlines()[::-1]:
+            if ln.startswith("{"):
+                return json.loads(ln)
+    except (subprocess.TimeoutExpired, OSError, ValueError):
+        pass
+    return None
+
+
+def first_call_probe(names):
+    import torch
+    from transformer_encoder_layer_gb300.inputs import SHAPES
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    out = {}
+    for name in names.split(","):
+        w = Workload(SHAPES[name], 0, dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        w.step(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        out[name] = 1e3 * (time.perf_counter() - t0)
+        w.close()
+    print(json.dumps(out), flush=True)
+
+
+def per_workload_entry(w, step_ms, per_kernel, peaks, sms, env, first_ms):
+    s = w.shape
+    med = statistics.median(step_ms)
+    total = sum(step_ms)
+    return {
+        "path": w.path, "steps": len(step_ms),
+        "ms_per_forward": {"median": med, "p10": percentile(step_ms, 10),
+                           "p90": percentile(step_ms, 90), "mean": statistics.mean(step_ms)},
+        "tokens_per_s": s.tokens / (med / 1e3),
+        "valid_tokens_per_s": int(w.inp.valid_len.sum()) / (med / 1e3),
+        "algorithmic_tflop_per_s": w.counts["flops"] / (med / 1e3) / 1e12,
+        "roofline": kernel_roofline(per_kernel, s, w.counts, peaks, sms, total),
+        "step_fractions": step_fractions(w.counts, med, peaks, sms, s.dtype),
+        "per_kernel_ms": {k: v[0] / len(step_ms) for k, v in per_kernel.items()},
+        "gpu_launches_per_forward": sum(n for _, n in per_kernel.values()) / len(step_ms),
+        "envelope": env,
+        "first_call_ms": first_ms,
+        "config": {"n_layers": s.n_layers, "d_model": s.d_model, "n_heads": s.n_heads,
+                   "d_ff": s.d_ff, "batch": s.batch, "seq_len": s.seq_len, "io_dtype": s.dtype,
+                   "valid_len": f"U[{s.vl_lo},{s.vl_hi}]"},
+    }
+
+
 def run_ours(args, shape):
     import torch
     ws, rank, local = dist_env()
@@ -285,141 +496,91 @@ def run_ours(args, shape):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     from transformer_encoder_layer_gb300 import binding, build
-    from transformer_encoder_layer_gb300.inputs import make_inputs, to_storage
+    from transformer_encoder_layer_gb300.inputs import SHAPES
 
     if rank == 0 or not os.path.exists(binding.LIB_PATH):
         build.build()
     if dist:
         dist.barrier()
-    inp = make_inputs(shape, seed=rank, input_scale=1.0)
-    counts = algorithmic_counts(shape, inp.valid_len)
-    enc = binding.Encoder(inp.layers, shape.d_model, shape.n_heads, shape.d_ff, shape.dtype)
-    if args.path != "auto":
-        enc.set_path(args.path)
-    path = enc.plan(shape.batch, shape.seq_len)
-    xs = to_storage(inp.x, shape.dtype)
-    tdt = binding.torch_dtype(shape.dtype)
-    if shape.dtype == "bf16":
-        x_host = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16)
-    else:
-        x_host = torch.from_numpy(xs)
-    x_host = x_host.contiguous().pin_memory()
-    vl_host = torch.from_numpy(inp.valid_len.astype(np.int32)).pin_memory()
-    x = x_host.to(dev)
-    vl = vl_host.to(dev)
-    out = torch.empty_like(x)
-    wsz = enc.workspace_size(shape.batch, shape.seq_len)
-    work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        enc.forward(x, vl, out=out, workspace=work, stream=stream, check=False)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    if enc.get_status() != 0:
-        raise RuntimeError("device status error during warm-up")
-
-    enc.enable_timing(True, capacity=max(4096, 64 * args.steps * shape.n_layers))
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps (outside the events)
-            starts[i].record(stream)
-            step()
-            stops[i].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        if dist:
-            dist.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
-    per_kernel = enc.read_timing()
-    enc.enable_timing(False)
+    # ---- headline: the chosen workload, K timed steps
+    w = Workload(shape, rank, dev, args.path)
+    step_ms, per_kernel, t_wall, clocks = time_steps(w, args.steps, args.warmup, flush, stream,
+                                                     dist, dev.index)
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
-    if enc.get_status() != 0:
-        raise RuntimeError("device status error in the timed region")
     ms_per_step = total_ms / args.steps
     value = whole_job_tokens_per_s(ws, shape.tokens, ms_per_step)
     launches = sum(n for _, n in per_kernel.values())
 
     # End to end: the C-ABI host-buffer call (H2D of x and valid_len, the
     # forward, D2H of out, stream sync) timed by the host clock.
-    out_host = torch.empty_like(x_host).pin_memory()
-    hws = torch.empty(enc.host_workspace_size(shape.batch, shape.seq_len), dtype=torch.uint8, device=dev)
-    enc.forward_host(x_host, vl_host, out_host, workspace=hws)
+    out_host = torch.empty_like(w.x_host).pin_memory()
+    hws = torch.empty(w.enc.host_workspace_size(shape.batch, shape.seq_len), dtype=torch.uint8,
+                      device=dev)
+    w.enc.forward_host(w.x_host, w.vl_host, out_host, workspace=hws)
     e2e_t = []
     for _ in range(max(3, min(args.steps, 10))):
         t0 = time.perf_counter()
-        enc.forward_host(x_host, vl_host, out_host, workspace=hws)
+        w.enc.forward_host(w.x_host, w.vl_host, out_host, workspace=hws)
         e2e_t.append(time.perf_counter() - t0)
     e2e_s = max_over_ranks(statistics.mean(e2e_t), dist, dev)
-    if not torch.equal(out_host, out.cpu()):
+    if not torch.equal(out_host, w.out.cpu()):
         raise RuntimeError("host-buffer forward disagrees with the device forward")
 
     if rank != 0:
+        w.close()
         if dist:
             dist.destroy_process_group()
         return
 
-    peaks = load_peaks()
-    roof = None
-    if per_kernel:
-        dom = max(per_kernel, key=lambda k: per_kernel[k][0])
-        ms, n = per_kernel[dom]
-        bound, work_per_launch = kernel_work(dom, shape, counts) or ("tensor", counts["flops"])
-        if dom == "megakernel":
-            n_launch_work = work_per_launch
-        else:
-            n_launch_work = work_per_launch
-        avg_s = ms / n / 1e3
-        if bound == "hbm":
-            achieved, peak, unit = n_launch_work / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
-        elif bound == "alu":
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-            achieved, unit = n_launch_work / avg_s / 1e12, "TFLOP/s"
-        else:
-            achieved, peak, unit = (n_launch_work / avg_s / 1e12,
-                                    peaks["bf16_tflops_sustained"], "TFLOP/s")
-        roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic_from_profiles(dom, shape.name),
-                "peak_source": peaks["source"] + (" (fp32 FMA: SMs x 128 lanes x 2 x max clock)"
-                                                  if bound == "alu" else ""),
-                "share_of_step": ms / total_ms if total_ms else None,
-                "launches": n, "avg_launch_ms": ms / n}
+    head_env = envelope_on_sample(w.inp, w.out_f64())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if shape.dtype == "f32" else shape.dtype, "data": "synthetic",
+        "dtype": shape.dtype, "data": "synthetic",
         "config": {"workload": shape.name, "n_layers": shape.n_layers, "d_model": shape.d_model,
                    "n_heads": shape.n_heads, "d_ff": shape.d_ff, "batch_per_gpu": shape.batch,
                    "global_batch": ws * shape.batch, "seq_len": shape.seq_len,
                    "io_dtype": shape.dtype, "valid_len": f"U[{shape.vl_lo},{shape.vl_hi}]",
-                   "input_scale": 1.0, "path": path, "parallelism": f"dp{ws}" if ws > 1 else "single",
+                   "input_scale": 1.0, "path": w.path,
+                   "parallelism": f"dp{ws}" if ws > 1 else "single",
                    "l2": "flushed between timed steps (256 MB write)"},
-        "valid_tokens_per_s": ws * int(inp.valid_len.sum()) / (ms_per_step / 1e3),
-        "algorithmic_tflop_per_s": counts["flops"] / (ms_per_step / 1e3) / 1e12,
-        "step_fractions": step_fractions(counts, ms_per_step, peaks,
-                                         torch.cuda.get_device_properties(dev).multi_processor_count,
-                                         "f32" if shape.dtype == "f32" else shape.dtype),
-        "roofline": roof,
+        "ms_per_step_p10": percentile(step_ms, 10), "ms_per_step_p90": percentile(step_ms, 90),
+        "valid_tokens_per_s": ws * int(w.inp.valid_len.sum()) / (ms_per_step / 1e3),
+        "algorithmic_tflop_per_s": w.counts["flops"] / (ms_per_step / 1e3) / 1e12,
+        "step_fractions": step_fractions(w.counts, ms_per_step, peaks, sms, shape.dtype),
+        "roofline": kernel_roofline(per_kernel, shape, w.counts, peaks, sms, total_ms),
         "per_kernel_ms": {k: v[0] / args.steps for k, v in per_kernel.items()},
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
+        "envelope": head_env,
         "e2e": {"value": whole_job_tokens_per_s(ws, shape.tokens, 1e3 * e2e_s), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size() + vl_host.numel() * 4),
+                "h2d_bytes_per_step": int(w.x_host.numel() * w.x_host.element_size() +
+                                          w.vl_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    w.close()
+    del hws, out_host
+
+    # ---- every workload: a short timed loop each, same method
+    if ws == 1 and not args.no_per_workload:
+        firsts = first_calls(WORKLOADS) or {}
+        table = {}
+        for name in WORKLOADS:
+            s = SHAPES[name]
+            wk = Workload(s, 0, dev)
+            k = min(args.steps, PER_WORKLOAD_STEPS[name])
+            sm, pk, _, _ = time_steps(wk, k, args.warmup, flush, stream)
+            env = envelope_on_sample(wk.inp, wk.out_f64())
+            table[name] = per_workload_entry(wk, sm, pk, peaks, sms, env, firsts.get(name))
+            wk.close()
+        line["per_workload"] = table
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, args.cpu_seqs)
     print(json.dumps(line), flush=True)
@@ -440,9 +601,15 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=64,
                     help="sequences per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time the headline workload only (profiling runs)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling)")
+    ap.add_argument("--first-call-probe", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.first_call_probe:
+        first_call_probe(args.first_call_probe)
+        return
     if args.warmup < 3:
         args.warmup = 3
     from transformer_encoder_layer_gb300.inputs import SHAPES
