@@ -114,6 +114,22 @@ tl_status tl_encoder_set_path(tl_encoder *h, tl_path path);
 /* The path forward() would run for a batch of B sequences of length L. */
 tl_status tl_encoder_plan(const tl_encoder *h, int B, int L, tl_path *path);
 
+/* Split-K attention on the layered tensor-core path (KernelForge, section
+ * "What's next": partition the key range and merge partial softmax states).
+ * When a batch has too few (sequence, head, 128-query tile) items to keep
+ * every SM busy behind the longest causal rows (batch 1, long sequences),
+ * each tile's key range is cut into chunks of key_tiles x 64 keys that run
+ * as separate work items; their partial states (unnormalised output, running
+ * max, row sum) go to the workspace and the last chunk to finish merges
+ * them.  key_tiles = -1 (the default) chooses per shape, 0 never splits,
+ * k in 1..4096 forces chunks of k tiles.  Host-only; the workspace size
+ * depends on it.  TL_ERR_INVALID_ARG outside -1..4096. */
+tl_status tl_encoder_set_attention_split(tl_encoder *h, int key_tiles);
+
+/* The chunk size (in 64-key tiles) forward() would use for B x L: 0 when
+ * the attention runs unsplit (or the path has no tensor-core attention). */
+tl_status tl_encoder_attention_split(const tl_encoder *h, int B, int L, int *key_tiles);
+
 /* Bytes of scratch device memory forward() needs for B sequences of length
  * L on the path it would choose.  0 is possible (then workspace may be NULL). */
 tl_status tl_encoder_workspace_size(const tl_encoder *h, int B, int L, size_t *bytes);

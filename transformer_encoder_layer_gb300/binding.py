@@ -31,6 +31,8 @@ SIGNATURES = {
     "tl_encoder_set_path": (_i, [_vp, _i]),
     "tl_encoder_set_host_chunks": (_i, [_vp, _i]),
     "tl_encoder_plan": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
+    "tl_encoder_set_attention_split": (_i, [_vp, _i]),
+    "tl_encoder_attention_split": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_workspace_size": (_i, [_vp, _i, _i, ctypes.POINTER(_sz)]),
     "tl_encoder_forward": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "tl_encoder_host_workspace_size": (_i, [_vp, _i, _i, ctypes.POINTER(_sz)]),
@@ -150,6 +152,17 @@ class Encoder:
         p = ctypes.c_int()
         _check(self.lib.tl_encoder_plan(self.handle, B, L, ctypes.byref(p)), "tl_encoder_plan")
         return PATH_NAMES[p.value]
+
+    def set_attention_split(self, key_tiles: int):
+        """-1 automatic (default), 0 never, k > 0 chunks of k 64-key tiles."""
+        _check(self.lib.tl_encoder_set_attention_split(self.handle, key_tiles),
+               "tl_encoder_set_attention_split")
+
+    def attention_split(self, B: int, L: int) -> int:
+        k = ctypes.c_int()
+        _check(self.lib.tl_encoder_attention_split(self.handle, B, L, ctypes.byref(k)),
+               "tl_encoder_attention_split")
+        return k.value
 
     def workspace_size(self, B: int, L: int) -> int:
         n = ctypes.c_size_t()

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "paths.h"
+#include "tc_attention.h"
 
 using namespace tl;
 
@@ -287,6 +288,22 @@ tl_status tl_encoder_create(const tl_layer_weights* weights, int n_layers, int d
 tl_status tl_encoder_set_path(tl_encoder* h, tl_path path) {
   if (!h || path < TL_PATH_AUTO || path > TL_PATH_DAG) return TL_ERR_INVALID_ARG;
   h->path = path;
+  return TL_OK;
+}
+
+tl_status tl_encoder_set_attention_split(tl_encoder* h, int key_tiles) {
+  if (!h || key_tiles < -1 || key_tiles > 4096) return TL_ERR_INVALID_ARG;
+  h->attn_split = key_tiles;
+  return TL_OK;
+}
+
+tl_status tl_encoder_attention_split(const tl_encoder* h, int B, int L, int* key_tiles) {
+  if (!h || !key_tiles || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  *key_tiles = 0;
+  if (p == TL_PATH_LAYERED && tc_attention_supported(h->dh) && !h->simt_attention)
+    *key_tiles = tc_attention_split_plan(B, h->H, L, h->dh, h->num_sms, h->attn_split).kc;
   return TL_OK;
 }
 

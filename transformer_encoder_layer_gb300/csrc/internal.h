@@ -58,6 +58,9 @@ struct tl_encoder {
   tl_path path = TL_PATH_AUTO;
   bool simt_attention = false;  // layered path: CUDA-core attention instead of tcgen05
   bool dag_inject_stall = false;  // task-graph path: make the first wait time out (tests)
+  // Split-K attention on the layered path: -1 automatic, 0 never, k > 0
+  // chunks of k 64-key tiles (tl_encoder_set_attention_split).
+  int attn_split = -1;
   int device = 0;
   int num_sms = 0;
   void* wbuf = nullptr;      // one allocation holding every packed parameter

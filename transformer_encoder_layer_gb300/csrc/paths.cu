@@ -130,6 +130,8 @@ struct LayeredWs {
   float2* stats;  // per-row (mean, rstd) of the LN GEMMs when d spans several N tiles
   int* ties;
   int* kmax;
+  void* att_part;  // split-K attention: partial states and arrival counters
+  void* att_cnt;
   int Lp;
   size_t bytes;
 };
@@ -155,6 +157,11 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   const size_t ost = take(d > 256 ? T * 8 : 8);                            // LN row stats
   size_t ot = take((1 + T * h->H) * 4);
   size_t ok_ = take((size_t)B * h->H * 4);
+  const TcAttnSplit sp = tc_attention_supported(h->dh) && !h->simt_attention
+                             ? tc_attention_split_plan(B, h->H, L, h->dh, h->num_sms, h->attn_split)
+                             : TcAttnSplit{};
+  size_t oap = take(sp.part_bytes ? sp.part_bytes : 4);
+  size_t oac = take(sp.cnt_bytes ? sp.cnt_bytes : 4);
   void** p[14] = {&w.xh, &w.xl, &w.qh, &w.ql, &w.kh, &w.kl, &w.vth, &w.vtl, &w.ch, &w.cl,
                   &w.yh, &w.yl, &w.hh, &w.hl};
   for (int i = 0; i < 14; ++i) *p[i] = b + o[i];
@@ -162,6 +169,8 @@ LayeredWs layered_layout(const tl_encoder* h, int B, int L, void* base) {
   w.stats = (float2*)(b + ost);
   w.ties = (int*)(b + ot);
   w.kmax = (int*)(b + ok_);
+  w.att_part = b + oap;
+  w.att_cnt = b + oac;
   w.bytes = off;
   return w;
 }
@@ -212,7 +221,8 @@ cudaError_t run_layered(tl_encoder* h, const void* x, int B, int L, const int32_
       TcAttnArgs ta{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, w.ch, w.cl, vl, w.kmax, ties,
                     B, H, L, w.Lp, dh, d, h->status};
       KernelTimer t(h, KC_TC_ATTENTION, s);
-      if ((e = tc_attention(ta, bf, h->num_sms, s)) != cudaSuccess) return e;
+      if ((e = tc_attention(ta, bf, h->num_sms, h->attn_split, w.att_part, w.att_cnt, s)) != cudaSuccess)
+        return e;
     } else {
       AttnIO io{w.qh, w.ql, w.kh, w.kl, w.vth, w.vtl, 1, w.Lp, w.ch, w.cl};
       KernelTimer t(h, KC_SIMT_ATTENTION, s);

@@ -28,10 +28,26 @@
 //              swizzled shared-memory operand, and folds the previous tile's
 //              O_{j-1} and row sum into its fp32 register accumulators with
 //              the online-softmax correction.
+//
+// Split-K over keys ("KernelForge", section "What's next": partition the key
+// range and merge partial softmax states).  When few (plane, query tile)
+// items would leave most CTAs idle behind the longest causal rows, the host
+// plan cuts every query tile's key range into chunks of kc 64-key tiles and
+// makes each chunk its own work item.  A chunk's softmax warps write, per
+// row, the unnormalised output, the running max and second-best score (log2
+// units), the row sum and |q|^2 to the partial buffer, then count the chunk
+// in the tile's arrival counters (one per warp of 32 rows); the warp whose
+// chunk arrives last for its rows merges the tile's chunks (out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
+// with M = max_c m_c) and writes the context.  No CTA ever waits for
+// another: the merge is done by whoever finishes last.  A chunk past the
+// sequence's valid keys (the plan assumes valid_len = L) loads nothing and
+// arrives with an empty state.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
+#include <vector>
 
 #include "common.cuh"
 #include "neartie.cuh"
@@ -110,6 +126,48 @@ struct Layout {
   static constexpr int kRowBytes = DH * 2;          // Q/K rows: 32, 64, 128
 };
 
+// 64-key tiles query tile qt sees at most (every valid_len = L), and the
+// chunks the split plan cuts them into (1 without a split).
+__host__ __device__ inline int nkt_bound(int qt, int L) {
+  const int kend = qt * kBQ + kBQ < L ? qt * kBQ + kBQ : L;
+  return (kend + kBKV - 1) / kBKV;
+}
+__host__ __device__ inline int chunks_of(int qt, int L, int kc) {
+  return kc ? (nkt_bound(qt, L) + kc - 1) / kc : 1;
+}
+
+// Work item w -> (plane, query tile, chunk).  Items run heaviest query tile
+// first: order index o covers query tile nqt-1-o, whose planes x chunks
+// items are numbered chunk-major.  Each role walks its CTA's increasing item
+// indices with its own cursor, so the decoding is amortised O(1).
+struct ItemCursor {
+  int o = 0, base = 0;
+  __device__ __forceinline__ void decode(int w, int planes, int nqt, int L, int kc, int& plane,
+                                         int& qt, int& c, int& nch) {
+    if (kc == 0) {
+      qt = nqt - 1 - w / planes;
+      plane = w % planes;
+      c = 0;
+      nch = 1;
+      return;
+    }
+    while (true) {
+      const int q = nqt - 1 - o;
+      const int n = chunks_of(q, L, kc);
+      if (w < base + planes * n) {
+        const int r = w - base;
+        qt = q;
+        c = r / planes;
+        plane = r % planes;
+        nch = n;
+        return;
+      }
+      base += planes * n;
+      ++o;
+    }
+  }
+};
+
 template <typename T, int DH>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     tc_attention_kernel(const __grid_constant__ CUtensorMap mqh, const __grid_constant__ CUtensorMap mql,
@@ -138,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int planes = a.B * a.H;
   const int nqt = (a.L + kBQ - 1) / kBQ;
-  const int n_items = planes * nqt;
+  const int n_items = a.kc ? a.n_items : planes * nqt;
+  const int kc = a.kc;
   // S: 2 x 64 columns, O: 2 x kOCols (head_dim outputs + the row sum)
   constexpr uint32_t kTmemCols = 2 * kBKV + 2 * Lay::kOCols <= 256 ? 256 : 512;
 
@@ -191,33 +250,36 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   volatile int* abort = abort_flag;
   const uint32_t tS = tmem, tO = tmem + 2 * kBKV;
 
-  // Work item w -> (plane, query tile), heaviest query tiles first.
-  auto item = [&](int w, int& plane, int& qt) {
-    qt = nqt - 1 - w / planes;
-    plane = w % planes;
-  };
   auto key_tiles = [&](int plane, int qt, int& vl) {
     vl = a.valid_len[plane / a.H];
     vl = vl < 1 ? 1 : (vl > a.L ? a.L : vl);
     const int kend = min(qt * kBQ + kBQ, vl);  // keys any row of the tile sees
     return (kend + kBKV - 1) / kBKV;
   };
+  // Key tiles [j0, j1) of chunk c of a tile with nkt visible key tiles.
+  auto key_range = [&](int c, int nkt, int& j0, int& j1) {
+    j0 = kc ? c * kc : 0;
+    j1 = kc ? min(j0 + kc, nkt) : nkt;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      long long kv_it = 0, n_items_done = 0;
+      long long kv_it = 0, n_items_done = 0;  // items with keys (Q loaded)
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_items_done) {
-        int plane, qt, vl;
-        item(w, plane, qt);
-        const int nkt = key_tiles(plane, qt, vl);
+      ItemCursor cur;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        int plane, qt, c, nch, vl, j0, j1;
+        cur.decode(w, planes, nqt, a.L, kc, plane, qt, c, nch);
+        key_range(c, key_tiles(plane, qt, vl), j0, j1);
+        if (j0 >= j1) continue;  // a chunk past the valid keys loads nothing
         if (!mbar_wait(q_empty, (uint32_t)(n_items_done & 1) ^ 1, abort, a.status)) break;
+        ++n_items_done;
         mbar_arrive_expect_tx(q_full, 2 * Lay::kQBytes);
         const int qrow = plane * a.L + qt * kBQ;
         tma_load_2d(base + Lay::kQOff, &mqh, q_full, 0, qrow);
         tma_load_2d(base + Lay::kQOff + Lay::kQBytes, &mql, q_full, 0, qrow);
-        for (int j = 0; j < nkt; ++j, ++kv_it) {
+        for (int j = j0; j < j1; ++j, ++kv_it) {
           const int st = (int)(kv_it % kStages);
           const uint32_t ph = (uint32_t)((kv_it / kStages) & 1);
           if (!mbar_wait(&kv_empty[st], ph ^ 1, abort, a.status)) { ok = false; break; }
@@ -275,13 +337,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       __syncwarp();
       return true;
     };
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_done) {
-      int plane, qt, vl;
-      item(w, plane, qt);
-      const int nkt = key_tiles(plane, qt, vl);
+    ItemCursor cur;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int plane, qt, c, nch, vl, j0, j1;
+      cur.decode(w, planes, nqt, a.L, kc, plane, qt, c, nch);
+      key_range(c, key_tiles(plane, qt, vl), j0, j1);
+      if (j0 >= j1) continue;
+      const int nkt = j1 - j0;  // key tiles of this item
       if (!mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) break;
+      ++n_done;
       tc_fence_after();
-      for (int j = 0; j < nkt; ++j) {
+      for (int j = 0; j < nkt; ++j) {  // j: position within the item's key tiles
         const long long it = kv_it + j;
         const int st = (int)(it % kStages);
         if (!mbar_wait(&kv_full[st], (uint32_t)((it / kStages) & 1), abort, a.status)) { ok = false; break; }
@@ -329,10 +395,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     const float scale_log2 = rsqrtf((float)DH) * 1.4426950408889634f;
     long long s_it = 0, o_it = 0, n_done = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n_done) {
-      int plane, qt, vl;
-      item(w, plane, qt);
-      const int nkt = key_tiles(plane, qt, vl);
+    ItemCursor cur;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int plane, qt, cidx, nch, vl, j0, j1;
+      cur.decode(w, planes, nqt, a.L, kc, plane, qt, cidx, nch);
+      key_range(cidx, key_tiles(plane, qt, vl), j0, j1);
+      const bool has_keys = j0 < j1;
       const int i = qt * kBQ + r;                    // query position in the sequence
       const int limit = min(i + 1, vl);              // keys [0, limit) visible
       const int full_keys = min(qt * kBQ + 1, vl);   // keys every row of the tile sees
@@ -343,7 +411,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       float m_hist0 = -INFINITY, m_hist1 = -INFINITY;  // running max after tile j (by parity)
       // |q_i| for the near-tie test, from the (hi, lo) Q tile in shared memory.
       float qn2 = 0.f;
-      if (mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) {
+      if (!has_keys) {
+        // nothing loaded for this chunk: only its (empty) partial state is due
+      } else if (mbar_wait(q_full, (uint32_t)(n_done & 1), abort, a.status)) {
+        ++n_done;
         const unsigned char* qh = base + Lay::kQOff;
 #pragma unroll
         for (int c = 0; c < DH; ++c) {
@@ -359,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       }
       // The second-best score matters only where fp32 scores can be off.
       const float kmax_plane = __int_as_float(a.kmax[plane]);
-      const bool track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
+      bool track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
       // Fold O_{jo} (computed against the running max after tile jo) into acc.
       auto fold_o = [&](int jo) -> bool {
         const int ob = (int)(o_it & 1);
@@ -395,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         ++o_it;
         return true;
       };
-      for (int j = 0; j < nkt && ok; ++j) {
+      for (int j = j0; j < j1 && ok; ++j) {
         const int sbuf = (int)(s_it & 1);
         if (!mbar_wait(&s_full[sbuf], (uint32_t)((s_it >> 1) & 1), abort, a.status)) { ok = false; break; }
         tc_fence_after();
@@ -465,10 +536,63 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         }
         fence_proxy_async();
         mbar_arrive(&p_full[pb]);
-        if (j > 0 && !fold_o(j - 1)) { ok = false; break; }
+        if (j > j0 && !fold_o(j - 1)) { ok = false; break; }
       }
       if (!ok) break;
-      if (!fold_o(nkt - 1)) { ok = false; break; }
+      if (has_keys && !fold_o(j1 - 1)) { ok = false; break; }
+      if (nch > 1) {
+        // ---- split-K: publish this chunk's partial state, count the chunk
+        // in, and merge the tile if it is the last to arrive.
+        const int cols = DH + 4;
+        float* mine = a.part + (size_t)w * kBQ * cols + r;  // column-major: [col][row]
+#pragma unroll
+        for (int e = 0; e < DH; ++e) mine[(size_t)e * kBQ] = acc[e];
+        mine[(size_t)DH * kBQ] = m;
+        mine[(size_t)(DH + 1) * kBQ] = m2;
+        mine[(size_t)(DH + 2) * kBQ] = l;
+        mine[(size_t)(DH + 3) * kBQ] = has_keys ? qn2 : -1.f;
+        // Each warp counts its own 32 rows in (no barrier across warps, so
+        // no wait that could outlive a failed peer): the last warp of the
+        // tile's chunks to arrive for these rows merges them.
+        __threadfence();
+        __syncwarp();
+        int before = 0;
+        if (lane == 0) before = atomicAdd(&a.cnt[(plane * nqt + qt) * 4 + qd], 1);
+        before = __shfl_sync(0xffffffffu, before, 0);
+        if (before != nch - 1) continue;
+        __threadfence();
+        // The tile's items are numbered first_w + c * planes (chunk-major).
+        const int first_w = w - cidx * planes;
+        float mmax = m, top1 = m, top2 = m2;
+        for (int c2 = 0; c2 < nch; ++c2) {
+          if (c2 == cidx) continue;
+          const float* o = a.part + (size_t)(first_w + c2 * planes) * kBQ * cols + r;
+          const float mc = __ldcg(o + (size_t)DH * kBQ), m2c = __ldcg(o + (size_t)(DH + 1) * kBQ);
+          const float qc = __ldcg(o + (size_t)(DH + 3) * kBQ);
+          mmax = fmaxf(mmax, mc);
+          if (qc >= 0.f) qn2 = qc;  // |q|^2 from any chunk that loaded Q
+          // top two of the union of the chunks' (best, second best)
+          if (mc > top1) { top2 = fmaxf(top1, m2c); top1 = mc; }
+          else top2 = fmaxf(top2, mc);
+        }
+        // every row sees key 0, which lies in chunk 0: mmax is finite
+        const float wown = exp2f(m - mmax);
+        float lsum = l * wown;
+#pragma unroll
+        for (int e = 0; e < DH; ++e) acc[e] *= wown;
+        for (int c2 = 0; c2 < nch; ++c2) {
+          if (c2 == cidx) continue;
+          const float* o = a.part + (size_t)(first_w + c2 * planes) * kBQ * cols + r;
+          const float wc = exp2f(__ldcg(o + (size_t)DH * kBQ) - mmax);
+          lsum = fmaf(wc, __ldcg(o + (size_t)(DH + 2) * kBQ), lsum);
+#pragma unroll
+          for (int e = 0; e < DH; ++e) acc[e] = fmaf(wc, __ldcg(o + (size_t)e * kBQ), acc[e]);
+        }
+        l = lsum;
+        m = top1;
+        m2 = top2;
+        track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
+      }
       if (i < a.L) {
         const float inv = 1.f / l;
         const size_t at = ((size_t)(plane / a.H) * a.L + i) * a.d + (size_t)(plane % a.H) * DH;
@@ -511,9 +635,74 @@ cudaError_t launch_dh(const TcAttnArgs& a, const CUtensorMap* maps, int grid, cu
 
 bool tc_attention_supported(int dh) { return dh == 16 || dh == 32 || dh == 64; }
 
-cudaError_t tc_attention(const TcAttnArgs& a, bool bf16, int num_sms, cudaStream_t s) {
+TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, int force_kc) {
+  TcAttnSplit p;
+  if (!tc_attention_supported(dh) || B < 1 || H < 1 || L < 1 || force_kc == 0) return p;
+  const long long planes = (long long)B * H;
+  const int nqt = (L + kBQ - 1) / kBQ;
+  const long long items0 = planes * nqt;
+  const int slots = num_sms * (dh == 16 ? ctas_per_sm<16>() : 1);
+  // The item index is an int and the decoding walks the query tiles; keep
+  // the split to shapes whose (plane, query tile) count is modest.
+  if (nqt > 4096 || items0 * ((nkt_bound(nqt - 1, L) + 1) / 2) > (1LL << 28)) return p;
+  auto items_of = [&](int kc) {
+    long long n = 0;
+    for (int qt = 0; qt < nqt; ++qt) n += planes * chunks_of(qt, L, kc);
+    return n;
+  };
+  int kc = 0;
+  if (force_kc > 0) {
+    kc = force_kc;
+  } else {
+    if (items0 >= 4LL * slots) return p;  // enough items to fill every CTA
+    // Model of the persistent grid: CTA g takes items g, g + slots, ... in
+    // the kernel's order; an item costs its key tiles plus ~2 tiles of set-up
+    // (Q load, pipeline fill), a chunk one more for its partial state.
+    auto makespan = [&](int kcc) {
+      std::vector<double> load(slots, 0.0);
+      long long w = 0;
+      for (int o = 0; o < nqt; ++o) {
+        const int qt = nqt - 1 - o, nkt = nkt_bound(qt, L), nch = chunks_of(qt, L, kcc);
+        for (int c = 0; c < nch; ++c) {
+          const int t = kcc ? std::min(kcc, nkt - c * kcc) : nkt;
+          for (long long pl = 0; pl < planes; ++pl, ++w) load[w % slots] += t + 2.0 + (nch > 1 ? 1.0 : 0.0);
+        }
+      }
+      return *std::max_element(load.begin(), load.end());
+    };
+    double best = makespan(0);
+    const double base = best;
+    for (int cand : {64, 32, 16, 8, 4}) {
+      const double m = makespan(cand);
+      if (m < best) { best = m; kc = cand; }
+    }
+    if (kc && best > 0.9 * base) kc = 0;  // not worth the partial traffic
+  }
+  if (!kc) return p;
+  const long long n = items_of(kc);
+  if (n > (1LL << 30)) return TcAttnSplit{};
+  p.kc = kc;
+  p.n_items = (int)n;
+  p.part_bytes = (size_t)n * kBQ * (dh + 4) * sizeof(float);
+  p.cnt_bytes = (size_t)planes * nqt * 4 * sizeof(int);
+  return p;
+}
+
+cudaError_t tc_attention(const TcAttnArgs& a_in, bool bf16, int num_sms, int force_kc, void* ws_part,
+                         void* ws_cnt, cudaStream_t s) {
+  TcAttnArgs a = a_in;
   const int dh = a.dh;
   if (!tc_attention_supported(dh) || a.L < 1 || a.Lp % 8 || a.Lp < a.L) return cudaErrorInvalidValue;
+  const TcAttnSplit plan = tc_attention_split_plan(a.B, a.H, a.L, dh, num_sms, force_kc);
+  a.kc = plan.kc;
+  a.n_items = plan.n_items;
+  a.part = (float*)ws_part;
+  a.cnt = (int*)ws_cnt;
+  if (plan.kc) {
+    if (!ws_part || !ws_cnt) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(ws_cnt, 0, plan.cnt_bytes, s);
+    if (e != cudaSuccess) return e;
+  }
   const uint64_t rows = (uint64_t)a.B * a.H * a.L;
   CUtensorMap maps[6];
   bool ok = make_tmap_2d(&maps[0], a.q_hi, bf16, rows, dh, dh, dh, kBQ, dh * 2) &&
@@ -523,8 +712,8 @@ cudaError_t tc_attention(const TcAttnArgs& a, bool bf16, int num_sms, cudaStream
             make_tmap_2d(&maps[4], a.vt_hi, bf16, (uint64_t)a.B * a.H * dh, a.Lp, a.Lp, kBKV, dh, 128) &&
             make_tmap_2d(&maps[5], a.vt_lo, bf16, (uint64_t)a.B * a.H * dh, a.Lp, a.Lp, kBKV, dh, 128);
   if (!ok) return cudaErrorInvalidValue;
-  const int items = a.B * a.H * ((a.L + kBQ - 1) / kBQ);
-  const int grid = items < num_sms ? items : num_sms;  // per resident CTA slot (launch_dh scales)
+  const long long items = plan.kc ? plan.n_items : (long long)a.B * a.H * ((a.L + kBQ - 1) / kBQ);
+  const int grid = items < num_sms ? (int)items : num_sms;  // per resident CTA slot (launch_dh scales)
   if (bf16) {
     if (dh == 16) return launch_dh<__nv_bfloat16, 16>(a, maps, grid, s);
     if (dh == 32) return launch_dh<__nv_bfloat16, 32>(a, maps, grid, s);
