@@ -111,7 +111,11 @@ tl_status tl_encoder_create(const tl_layer_weights *weights, int n_layers, int d
 /* Force an execution path (default TL_PATH_AUTO).  Host-only, no device work. */
 tl_status tl_encoder_set_path(tl_encoder *h, tl_path path);
 
-/* The path forward() would run for a batch of B sequences of length L. */
+/* The path forward() would run for a batch of B sequences of length L.
+ * Under TL_PATH_AUTO a shape listed in the library's frozen plan table
+ * (KernelForge, section "What it does": candidates proven against the gate,
+ * then timed, the winner frozen) takes the table's path; other shapes take
+ * fixed rules by dtype, d_model, head width, sequence length and tokens. */
 tl_status tl_encoder_plan(const tl_encoder *h, int B, int L, tl_path *path);
 
 /* Split-K attention on the layered tensor-core path (KernelForge, section
@@ -121,9 +125,11 @@ tl_status tl_encoder_plan(const tl_encoder *h, int B, int L, tl_path *path);
  * each tile's key range is cut into chunks of key_tiles x 64 keys that run
  * as separate work items; their partial states (unnormalised output, running
  * max, row sum) go to the workspace and the last chunk to finish merges
- * them.  key_tiles = -1 (the default) chooses per shape, 0 never splits,
- * k in 1..4096 forces chunks of k tiles.  Host-only; the workspace size
- * depends on it.  TL_ERR_INVALID_ARG outside -1..4096. */
+ * them.  key_tiles = -1 (the default) chooses per shape: the frozen plan
+ * table's setting when the shape is in it (see tl_encoder_plan), else a
+ * model of the persistent grid's load; 0 never splits, k in 1..4096 forces
+ * chunks of k tiles.  Host-only; the workspace size depends on it.
+ * TL_ERR_INVALID_ARG outside -1..4096. */
 tl_status tl_encoder_set_attention_split(tl_encoder *h, int key_tiles);
 
 /* The chunk size (in 64-key tiles) forward() would use for B x L: 0 when
@@ -146,6 +152,23 @@ tl_status tl_encoder_workspace_size(const tl_encoder *h, int B, int L, size_t *b
 tl_status tl_encoder_forward(tl_encoder *h, const void *x, int B, int L,
                              const int32_t *valid_len, void *out, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/* Graph mode (KernelForge, section "What we built": the launches of a
+ * forward captured in a CUDA graph).  With enable = 1, a forward on the
+ * layered path (several launches per layer) whose stream is not itself being
+ * captured runs as follows: the first call for a given (B, L, x, valid_len,
+ * out, workspace) launches the kernels as usual and also records them into a
+ * CUDA graph on an internal stream; later calls with the same shape and
+ * buffers launch that graph instead (the kernels read their buffers through
+ * the recorded pointers, so the caller changes the contents, not the
+ * addresses).  One graph is kept per handle; a new shape or buffer set
+ * replaces it.  The recording call creates a stream and a graph (host and
+ * device allocations by the driver), so unlike the plain forward it is not
+ * allocation-free; replays are.  Other paths, per-kernel timing and a stream
+ * under capture bypass it.  enable = 0 (the default) frees the graph. */
+tl_status tl_encoder_set_graphs(tl_encoder *h, int enable);
+/* How many graphs graph mode recorded and how many forwards replayed one. */
+tl_status tl_encoder_graph_stats(const tl_encoder *h, long long *captures, long long *replays);
 
 /* Bytes of device workspace tl_encoder_forward_host() needs: device copies of
  * x, valid_len and out, plus the forward's own scratch for one batch slice

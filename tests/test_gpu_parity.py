@@ -519,13 +519,17 @@ def test_mega_shapes(dtype, L, dff, n_layers, batch, scale):
 
 
 def test_mega_matches_layered_closely():
-    # Two tensor-core paths over the same split-operand arithmetic: they
-    # differ only in summation order, so their difference is far inside the gate.
+    # Two tensor-core paths over the same function: the layered path keeps
+    # every (hi, lo) operand, the fp16 megakernel rounds P and the FFN hidden
+    # to one 16-bit value; both pass the gate against the oracle, and they
+    # are within twice the gate's absolute bound of each other.
     s = SHAPES["short_d128_L64_B4096"].with_(batch=64)
     inp = make_inputs(s, seed=4)
     a = _run(inp, "mega")
     b = _run(inp, "layered")
-    assert np.max(np.abs(a - b)) < 2e-3
+    ref = oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, s.n_heads)
+    assert gate(a, ref)[0] and gate(b, ref)[0]
+    assert np.max(np.abs(a - b)) < 4e-3
 
 
 # ------------------------------------------------------ task-graph path

@@ -84,10 +84,13 @@ def test_batch1_other_head_widths(dtype, d, H, L, vl_lo, vl_hi, batch):
     ref = oracle.encoder_forward(inp.x, inp.valid_len, inp.layers, H, check=False)
     ok, util, idx = gate(got, ref)
     assert ok, f"envelope {util:.3f} at {idx}"
-    # against the unsplit kernel: the same function summed in another order
+    # against the unsplit kernel: the same function summed in another order,
+    # so the outputs differ at most by the I/O rounding of a value next to a
+    # rounding boundary (one unit in the last place)
     base, kc0 = _run(inp, 0)
     assert kc0 == 0
-    assert np.max(np.abs(got - base)) < 2e-3
+    ulp = 2.0 ** (-8 if dtype == "bf16" else -11) * np.abs(base)
+    assert np.all(np.abs(got - base) <= np.maximum(2 * ulp, 1e-3))
 
 
 @pytest.mark.parametrize("kc", [1, 2, 3, 5])

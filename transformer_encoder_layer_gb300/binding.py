@@ -32,6 +32,9 @@ SIGNATURES = {
     "tl_encoder_set_host_chunks": (_i, [_vp, _i]),
     "tl_encoder_plan": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_set_attention_split": (_i, [_vp, _i]),
+    "tl_encoder_set_graphs": (_i, [_vp, _i]),
+    "tl_encoder_graph_stats": (_i, [_vp, ctypes.POINTER(ctypes.c_longlong),
+                                    ctypes.POINTER(ctypes.c_longlong)]),
     "tl_encoder_attention_split": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_workspace_size": (_i, [_vp, _i, _i, ctypes.POINTER(_sz)]),
     "tl_encoder_forward": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
@@ -157,6 +160,15 @@ class Encoder:
         """-1 automatic (default), 0 never, k > 0 chunks of k 64-key tiles."""
         _check(self.lib.tl_encoder_set_attention_split(self.handle, key_tiles),
                "tl_encoder_set_attention_split")
+
+    def set_graphs(self, enable: bool):
+        _check(self.lib.tl_encoder_set_graphs(self.handle, int(enable)), "tl_encoder_set_graphs")
+
+    def graph_stats(self):
+        c, r = ctypes.c_longlong(), ctypes.c_longlong()
+        _check(self.lib.tl_encoder_graph_stats(self.handle, ctypes.byref(c), ctypes.byref(r)),
+               "tl_encoder_graph_stats")
+        return c.value, r.value
 
     def attention_split(self, B: int, L: int) -> int:
         k = ctypes.c_int()

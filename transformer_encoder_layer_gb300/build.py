@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 
 def _headers():
-    hs = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+    hs = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+          glob.glob(os.path.join(CSRC, "*.inc")))
     hs += glob.glob(os.path.join(PKG, "..", "include", "*.h"))
     return hs
 

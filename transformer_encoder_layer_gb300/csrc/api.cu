@@ -160,6 +160,45 @@ bool host_streams(tl_encoder* h) {
   return true;
 }
 
+void drop_graph(tl_encoder* h) {
+  if (h->graph_exec) cudaGraphExecDestroy(h->graph_exec);
+  h->graph_exec = nullptr;
+  h->graph_key = tl_encoder::GraphKey{};
+}
+
+// Record the path's launch sequence for these buffers into a CUDA graph on
+// the handle's own stream (thread-local capture, so other threads' CUDA
+// calls are unaffected) and keep its executable instance in the handle.
+cudaError_t capture_graph(tl_encoder* h, tl_path p, const void* x, int B, int L, const int32_t* vl,
+                          void* out, void* ws) {
+  drop_graph(h);
+  cudaError_t e = cudaSuccess;
+  if (!h->capture_stream &&
+      (e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking)) != cudaSuccess) {
+    h->capture_stream = nullptr;
+    return e;
+  }
+  if ((e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
+    return e;
+  const cudaError_t er = run_path(h, p, x, B, L, vl, out, ws, h->capture_stream);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(h->capture_stream, &g);
+  if (er != cudaSuccess || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return er != cudaSuccess ? er : e;
+  }
+  e = cudaGraphInstantiateWithFlags(&h->graph_exec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) {
+    h->graph_exec = nullptr;
+    cudaGetLastError();
+    return e;
+  }
+  ++h->graph_captures;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,7 +342,8 @@ tl_status tl_encoder_attention_split(const tl_encoder* h, int B, int L, int* key
   if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
   *key_tiles = 0;
   if (p == TL_PATH_LAYERED && tc_attention_supported(h->dh) && !h->simt_attention)
-    *key_tiles = tc_attention_split_plan(B, h->H, L, h->dh, h->num_sms, h->attn_split).kc;
+    *key_tiles =
+        tc_attention_split_plan(B, h->H, L, h->dh, h->num_sms, attention_split_setting(h, B, L)).kc;
   return TL_OK;
 }
 
@@ -335,8 +375,40 @@ tl_status tl_encoder_forward(tl_encoder* h, const void* x, int B, int L, const i
   size_t need = path_workspace_bytes(h, p, B, L);
   if (workspace_bytes < need) return TL_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && (!workspace || !aligned(workspace, 256))) return TL_ERR_INVALID_ARG;
-  cudaError_t e = run_path(h, p, x, B, L, valid_len, out, workspace, (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->graphs && p == TL_PATH_LAYERED && !h->timing) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return TL_ERR_CUDA;
+    if (cs == cudaStreamCaptureStatusNone) {
+      const tl_encoder::GraphKey key{(int)p, B, L, h->attn_split, x, valid_len, out, workspace};
+      if (h->graph_exec && h->graph_key == key) {
+        ++h->graph_replays;
+        return cudaGraphLaunch(h->graph_exec, st) == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+      }
+      // A new (shape, buffers): run it as usual, and record the same launch
+      // sequence on the handle's capture stream for the next call.
+      cudaError_t e = run_path(h, p, x, B, L, valid_len, out, workspace, st);
+      if (e != cudaSuccess) return TL_ERR_CUDA;
+      if (capture_graph(h, p, x, B, L, valid_len, out, workspace) == cudaSuccess) h->graph_key = key;
+      return TL_OK;
+    }
+  }
+  cudaError_t e = run_path(h, p, x, B, L, valid_len, out, workspace, st);
   return e == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
+tl_status tl_encoder_set_graphs(tl_encoder* h, int enable) {
+  if (!h || enable < 0 || enable > 1) return TL_ERR_INVALID_ARG;
+  h->graphs = enable != 0;
+  if (!h->graphs) drop_graph(h);
+  return TL_OK;
+}
+
+tl_status tl_encoder_graph_stats(const tl_encoder* h, long long* captures, long long* replays) {
+  if (!h || !captures || !replays) return TL_ERR_INVALID_ARG;
+  *captures = h->graph_captures;
+  *replays = h->graph_replays;
+  return TL_OK;
 }
 
 tl_status tl_encoder_set_host_chunks(tl_encoder* h, int chunks) {
@@ -438,6 +510,8 @@ tl_status tl_encoder_destroy(tl_encoder* h) {
     if (x) cudaStreamDestroy(x);
   for (cudaEvent_t& x : h->host_event)
     if (x) cudaEventDestroy(x);
+  drop_graph(h);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->wbuf) cudaFree(h->wbuf);
   if (h->status) cudaFree(h->status);
   delete[] h->layers;

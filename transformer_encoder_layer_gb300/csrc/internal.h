@@ -78,6 +78,20 @@ struct tl_encoder {
   int host_chunks = 0;
   cudaStream_t host_stream[2] = {nullptr, nullptr};
   cudaEvent_t host_event[3] = {nullptr, nullptr, nullptr};
+  // Graph mode of the layered path (tl_encoder_set_graphs): the launch
+  // sequence of the last (shape, buffers) seen, captured once and replayed.
+  bool graphs = false;
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  struct GraphKey {
+    int path, B, L, attn_split;
+    const void *x, *vl, *out, *ws;
+    bool operator==(const GraphKey& o) const {
+      return path == o.path && B == o.B && L == o.L && attn_split == o.attn_split && x == o.x &&
+             vl == o.vl && out == o.out && ws == o.ws;
+    }
+  } graph_key{};
+  long long graph_captures = 0, graph_replays = 0;
 };
 
 namespace tl {

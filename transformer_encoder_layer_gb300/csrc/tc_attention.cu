@@ -575,13 +575,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           if (mc > top1) { top2 = fmaxf(top1, m2c); top1 = mc; }
           else top2 = fmaxf(top2, mc);
         }
-        // every row sees key 0, which lies in chunk 0: mmax is finite
-        const float wown = exp2f(m - mmax);
-        float lsum = l * wown;
+        // Every row sees key 0, which lies in chunk 0, so mmax is finite.
+        // The chunks are summed in chunk order whichever warp merges, so
+        // the result does not depend on which chunk finished last.
+        float own[DH];
 #pragma unroll
-        for (int e = 0; e < DH; ++e) acc[e] *= wown;
+        for (int e = 0; e < DH; ++e) {
+          own[e] = acc[e];
+          acc[e] = 0.f;
+        }
+        float lsum = 0.f;
         for (int c2 = 0; c2 < nch; ++c2) {
-          if (c2 == cidx) continue;
+          if (c2 == cidx) {
+            const float wc = exp2f(m - mmax);
+            lsum = fmaf(wc, l, lsum);
+#pragma unroll
+            for (int e = 0; e < DH; ++e) acc[e] = fmaf(wc, own[e], acc[e]);
+            continue;
+          }
           const float* o = a.part + (size_t)(first_w + c2 * planes) * kBQ * cols + r;
           const float wc = exp2f(__ldcg(o + (size_t)DH * kBQ) - mmax);
           lsum = fmaf(wc, __ldcg(o + (size_t)(DH + 2) * kBQ), lsum);
@@ -654,10 +665,15 @@ TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, in
   if (force_kc > 0) {
     kc = force_kc;
   } else {
-    if (items0 >= 4LL * slots) return p;  // enough items to fill every CTA
+    if (items0 >= 2LL * slots) return p;  // enough items to keep every CTA busy
     // Model of the persistent grid: CTA g takes items g, g + slots, ... in
-    // the kernel's order; an item costs its key tiles plus ~2 tiles of set-up
-    // (Q load, pipeline fill), a chunk one more for its partial state.
+    // the kernel's order.  An item costs its 64-key tiles plus about 4 tiles
+    // of fixed cost (Q load, pipeline fill and drain); a chunk also pays for
+    // its partial state and its share of the merge, about half a tile per
+    // chunk of its query tile.  Both constants are fitted to GB300 timings
+    // of chunk sizes 4..32 at head_dim 16 and 64 (batch 1 and 2, 2k-32k
+    // tokens), which the model then ranks as measured; with two or more
+    // items per CTA the unsplit grid was already the fastest.
     auto makespan = [&](int kcc) {
       std::vector<double> load(slots, 0.0);
       long long w = 0;
@@ -665,18 +681,19 @@ TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, in
         const int qt = nqt - 1 - o, nkt = nkt_bound(qt, L), nch = chunks_of(qt, L, kcc);
         for (int c = 0; c < nch; ++c) {
           const int t = kcc ? std::min(kcc, nkt - c * kcc) : nkt;
-          for (long long pl = 0; pl < planes; ++pl, ++w) load[w % slots] += t + 2.0 + (nch > 1 ? 1.0 : 0.0);
+          const double cost = t + 4.0 + (nch > 1 ? 0.5 * nch : 0.0);
+          for (long long pl = 0; pl < planes; ++pl, ++w) load[w % slots] += cost;
         }
       }
       return *std::max_element(load.begin(), load.end());
     };
     double best = makespan(0);
     const double base = best;
-    for (int cand : {64, 32, 16, 8, 4}) {
+    for (int cand : {64, 32, 16, 8}) {
       const double m = makespan(cand);
       if (m < best) { best = m; kc = cand; }
     }
-    if (kc && best > 0.9 * base) kc = 0;  // not worth the partial traffic
+    if (kc && best > 0.9 * base) kc = 0;  // not worth the partial states
   }
   if (!kc) return p;
   const long long n = items_of(kc);

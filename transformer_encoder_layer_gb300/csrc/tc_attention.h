@@ -38,8 +38,8 @@ struct TcAttnSplit {
   size_t part_bytes = 0, cnt_bytes = 0;
 };
 // force_kc < 0: choose by a model of the persistent CTAs' static item
-// assignment (split only where it shortens the busiest CTA's key-tile count
-// by a tenth or more); 0: never split; > 0: chunks of force_kc key tiles.
+// assignment (split only where it shortens the busiest CTA's work by 10% or
+// more); 0: never split; > 0: chunks of force_kc key tiles.
 TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, int force_kc);
 
 bool tc_attention_supported(int dh);
