@@ -143,10 +143,10 @@ def kernel_work(cls, shape, counts):
     return table.get(cls)
 
 
-def traffic_from_profiles(cls, workload):
-    """DRAM bytes per launch of kernel class `cls` on `workload` from the
-    committed ncu summary (an entry "cls@workload", else "cls"), if it was
-    taken on the current kernel source; else None."""
+def traffic_entry(cls, workload):
+    """The committed ncu DRAM figures of kernel class `cls` on `workload`
+    (an entry "cls@workload", else "cls"), if they were taken on the current
+    kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -159,7 +159,13 @@ def traffic_from_profiles(cls, workload):
     if not os.path.exists(src):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return e["dram_bytes_per_launch"] if sha == e["source_sha"] else None
+    return e if sha == e["source_sha"] else None
+
+
+def traffic_from_profiles(cls, workload):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch, or None."""
+    e = traffic_entry(cls, workload)
+    return e["dram_bytes_per_launch"] if e else None
 
 
 def kernel_roofline(per_kernel, shape, counts, peaks, sms, total_ms):
@@ -181,8 +187,11 @@ def kernel_roofline(per_kernel, shape, counts, peaks, sms, total_ms):
     else:
         achieved, peak, unit = work / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
         src = peaks["source"] + " bf16 burst (fp16 dense runs at the bf16 rate)"
+    te = traffic_entry(dom, shape.name)
     return {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": traffic_from_profiles(dom, shape.name),
+            "frac": achieved / peak, "traffic": te["dram_bytes_per_launch"] if te else None,
+            # output bytes the kernel leaves dirty in L2 reach DRAM after it ends
+            "traffic_with_l2_writeback": te.get("dram_bytes_with_writeback") if te else None,
             "peak_source": src, "share_of_step": ms / total_ms if total_ms else None,
             "launches": n, "avg_launch_ms": ms / n}
 

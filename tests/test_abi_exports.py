@@ -54,6 +54,7 @@ def test_status_strings_without_gpu():
     assert lib.tl_encoder_set_attention_split(None, 0) == 1
     assert lib.tl_encoder_attention_split(None, 1, 1, None) == 1
     assert lib.tl_encoder_set_graphs(None, 1) == 1
+    assert lib.tl_encoder_set_gemm_pairs(None, 1) == 1
     assert lib.tl_encoder_graph_stats(None, None, None) == 1
     # Shape checks at create time also come before any CUDA call (the weight
     # pointers are not read when the shape is refused).

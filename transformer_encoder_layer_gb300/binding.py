@@ -33,6 +33,7 @@ SIGNATURES = {
     "tl_encoder_plan": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_set_attention_split": (_i, [_vp, _i]),
     "tl_encoder_set_graphs": (_i, [_vp, _i]),
+    "tl_encoder_set_gemm_pairs": (_i, [_vp, _i]),
     "tl_encoder_graph_stats": (_i, [_vp, ctypes.POINTER(ctypes.c_longlong),
                                     ctypes.POINTER(ctypes.c_longlong)]),
     "tl_encoder_attention_split": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
@@ -160,6 +161,10 @@ class Encoder:
         """-1 automatic (default), 0 never, k > 0 chunks of k 64-key tiles."""
         _check(self.lib.tl_encoder_set_attention_split(self.handle, key_tiles),
                "tl_encoder_set_attention_split")
+
+    def set_gemm_pairs(self, enable: bool):
+        _check(self.lib.tl_encoder_set_gemm_pairs(self.handle, int(enable)),
+               "tl_encoder_set_gemm_pairs")
 
     def set_graphs(self, enable: bool):
         _check(self.lib.tl_encoder_set_graphs(self.handle, int(enable)), "tl_encoder_set_graphs")

@@ -336,6 +336,12 @@ tl_status tl_encoder_set_attention_split(tl_encoder* h, int key_tiles) {
   return TL_OK;
 }
 
+tl_status tl_encoder_set_gemm_pairs(tl_encoder* h, int enable) {
+  if (!h || enable < 0 || enable > 1) return TL_ERR_INVALID_ARG;
+  h->gemm_pairs = enable;
+  return TL_OK;
+}
+
 tl_status tl_encoder_attention_split(const tl_encoder* h, int B, int L, int* key_tiles) {
   if (!h || !key_tiles || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
   tl_path p = choose_path(h, B, L);
@@ -380,7 +386,8 @@ tl_status tl_encoder_forward(tl_encoder* h, const void* x, int B, int L, const i
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return TL_ERR_CUDA;
     if (cs == cudaStreamCaptureStatusNone) {
-      const tl_encoder::GraphKey key{(int)p, B, L, h->attn_split, x, valid_len, out, workspace};
+      const tl_encoder::GraphKey key{(int)p, B, L, h->attn_split * 2 + h->gemm_pairs, x, valid_len, out,
+                                     workspace};
       if (h->graph_exec && h->graph_key == key) {
         ++h->graph_replays;
         return cudaGraphLaunch(h->graph_exec, st) == cudaSuccess ? TL_OK : TL_ERR_CUDA;

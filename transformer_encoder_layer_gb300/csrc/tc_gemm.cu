@@ -14,6 +14,19 @@
 //   warps 2-5  epilogue: thread = output row (TMEM lane), 32 columns at a
 //              time with tcgen05.ld; two TMEM accumulators let the epilogue
 //              of one tile overlap the main loop of the next
+//
+// CTA-pair variant (PAIR, launched as clusters of two): the pair owns a
+// 256-row block.  Each CTA loads its own 128 rows of A and its half (BN/2
+// rows) of the W tile -- no data is multicast -- with both CTAs' loads
+// completing on the leader's (rank 0) ring barrier; the leader alone issues
+// tcgen05.mma.cta_group::2 with M = 256, which reads A and B from both
+// CTAs' shared memory and writes each CTA's rows into its own tensor memory,
+// and commits both CTAs' ring and accumulator barriers.  One MMA instruction
+// thus covers 256 rows: half the instructions per row of the single-CTA
+// kernel, and half the W bytes staged per CTA.  The epilogue is unchanged;
+// the peer's epilogue warps release the accumulator on the leader's barrier.
+// Both CTAs hand each other a bounded "done" signal before freeing tensor
+// memory and exiting, so neither leaves while the other may still signal it.
 // Epilogues (the pages' fused steps: "KernelForge", section "What we
 // built" -- fused QKV projection, fused add + LayerNorm; the megakernel
 // page, section "Hybrid" -- QKV GEMM with the head-major transpose fused):
@@ -50,6 +63,7 @@ struct Smem {
   uint64_t* acc_full;   // [2]
   uint64_t* acc_empty;  // [2]
   uint64_t* mma_done;   // [1]
+  uint64_t* done;       // [1] pair: the peer has finished signalling this CTA
   uint32_t* tmem_base;
   int* abort;
 };
@@ -176,7 +190,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <typename T, int EPI>
+template <typename T, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                    const __grid_constant__ CUtensorMap map_w, const TcGemmArgs args) {
@@ -186,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const int BN = a.BN;
-  const int stage_bytes = a.n_parts * kATileBytes + BN * kBK * 2;
+  const int w_rows = PAIR ? BN / 2 : BN;  // rows of the W tile this CTA stages
+  const int stage_bytes = a.n_parts * kATileBytes + w_rows * kBK * 2;
   unsigned char* bar_base = base + (size_t)a.stages * stage_bytes;
   Smem sm;
   sm.full = reinterpret_cast<uint64_t*>(bar_base);
@@ -194,8 +209,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.acc_full = sm.empty + a.stages;
   sm.acc_empty = sm.acc_full + 2;
   sm.mma_done = sm.acc_empty + 2;
-  sm.tmem_base = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
+  sm.done = sm.mma_done + 1;
+  sm.tmem_base = reinterpret_cast<uint32_t*>(sm.done + 1);
   sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
+  // Pair: rank 0 leads (issues the MMAs); the peer is the other CTA.
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int rows_per_unit = PAIR ? 2 * kBM : kBM;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   T* const q_hi = reinterpret_cast<T*>(a.q_hi);
   T* const q_lo = reinterpret_cast<T*>(a.q_lo);
@@ -208,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   T* const o_final = reinterpret_cast<T*>(a.o_final);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const bool ln_rows = (EPI == TC_EPI_LN);
-  // Work units: LN -> one 128-row block with all its N tiles; else one tile.
+  // Work units: LN -> one row block (128 rows, or 256 for a pair) with all
+  // its N tiles; else one tile.  a.m_blocks counts row blocks of that size.
   const int n_units = ln_rows ? a.m_blocks : a.m_blocks * a.n_tiles;
   const int tiles_per_unit = ln_rows ? a.n_tiles : 1;
   const int k_blocks = (a.K + kBK - 1) / kBK;
@@ -220,9 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.acc_full[s], 1);
-      mbar_init(&sm.acc_empty[s], 128);
+      // pair leader: its own 128 epilogue threads plus one arrival per peer
+      // epilogue warp
+      mbar_init(&sm.acc_empty[s], PAIR ? 128 + 4 : 128);
     }
     mbar_init(sm.mma_done, 1);
+    mbar_init(sm.done, 1);
     *sm.abort = 0;
     fence_barrier_init();
   }
@@ -231,9 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.n_parts > 1) tma_prefetch_desc(&map_a1);
     tma_prefetch_desc(&map_w);
   }
-  if (warp == 1) tmem_alloc(sm.tmem_base, a.tmem_cols);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(sm.tmem_base, a.tmem_cols);
+    else tmem_alloc(sm.tmem_base, a.tmem_cols);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_base;
   volatile int* abort = sm.abort;
@@ -244,19 +274,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      const uint32_t tx = (uint32_t)stage_bytes;
+      // a pair's loads of both CTAs complete on the leader's barrier
+      const uint32_t tx = (uint32_t)stage_bytes * (PAIR ? 2u : 1u);
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < n_units && ok; u += unit_step) {
         for (int t = 0; t < tiles_per_unit && ok; ++t) {
           const int m_blk = ln_rows ? u : u / a.n_tiles;
           const int n_tile = ln_rows ? t : u % a.n_tiles;
+          const int arow = m_blk * rows_per_unit + (int)rank * kBM;
+          const int wrow = n_tile * BN + (int)rank * w_rows;
           for (int kb = 0; kb < k_blocks; ++kb) {
             if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort, a.status)) { ok = false; break; }
             unsigned char* st = base + (size_t)stage * stage_bytes;
-            mbar_arrive_expect_tx(&sm.full[stage], tx);
-            tma_load_2d(st, &map_a0, &sm.full[stage], kb * kBK, m_blk * kBM);
-            if (a.n_parts > 1) tma_load_2d(st + kATileBytes, &map_a1, &sm.full[stage], kb * kBK, m_blk * kBM);
-            tma_load_2d(st + a.n_parts * kATileBytes, &map_w, &sm.full[stage], kb * kBK, n_tile * BN);
+            if constexpr (PAIR) {
+              const uint32_t fb = map_to_rank(smem_u32(&sm.full[stage]), 0);
+              if (leader) mbar_arrive_expect_tx(&sm.full[stage], tx);
+              tma_load_2d_pair(st, &map_a0, fb, kb * kBK, arow);
+              if (a.n_parts > 1) tma_load_2d_pair(st + kATileBytes, &map_a1, fb, kb * kBK, arow);
+              tma_load_2d_pair(st + a.n_parts * kATileBytes, &map_w, fb, kb * kBK, wrow);
+            } else {
+              mbar_arrive_expect_tx(&sm.full[stage], tx);
+              tma_load_2d(st, &map_a0, &sm.full[stage], kb * kBK, arow);
+              if (a.n_parts > 1) tma_load_2d(st + kATileBytes, &map_a1, &sm.full[stage], kb * kBK, arow);
+              tma_load_2d(st + a.n_parts * kATileBytes, &map_w, &sm.full[stage], kb * kBK, wrow);
+            }
             ++issued;
             if (++stage == a.stages) { stage = 0; phase ^= 1; }
           }
@@ -264,52 +305,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every load issued must have landed before the CTA exits: wait (with
       // a bound, ignoring the abort flag) on the last `stages` full phases.
-      for (long long r = 1; r <= issued && r <= a.stages; ++r) {
-        const long long idx = issued - r;
-        mbar_wait_bounded(&sm.full[idx % a.stages], (uint32_t)((idx / a.stages) & 1), a.status);
-      }
+      // A pair's peer cannot see its loads' barrier; the leader's MMAs read
+      // them before the end-of-kernel handshake, which covers the peer.
+      if (!PAIR || leader)
+        for (long long r = 1; r <= issued && r <= a.stages; ++r) {
+          const long long idx = issued - r;
+          mbar_wait_bounded(&sm.full[idx % a.stages], (uint32_t)((idx / a.stages) & 1), a.status);
+        }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      for (int t = 0; t < tiles_per_unit && ok; ++t) {
-        if (!mbar_wait(&sm.acc_empty[acc], acc_phase ^ 1, abort, a.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&sm.full[stage], phase, abort, a.status)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            unsigned char* st = base + (size_t)stage * stage_bytes;
-            const uint32_t w_addr = smem_u32(st + a.n_parts * kATileBytes);
-            for (int p = 0; p < a.n_parts; ++p) {
-              const uint32_t a_addr = smem_u32(st + p * kATileBytes);
-#pragma unroll
-              for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                mma_f16(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
-                        a.idesc, (kb | p | k16) != 0);
-              }
-            }
-            mma_commit(&sm.empty[stage]);
-          }
-          __syncwarp();
-          if (++stage == a.stages) { stage = 0; phase ^= 1; }
+    if (!PAIR || leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      // commit to this CTA's barrier and, for a pair, to the peer's copy
+      auto commit_both = [&](uint64_t* bar) {
+        if constexpr (PAIR) {
+          mma_commit_pair(smem_u32(bar));
+          mma_commit_pair(map_to_rank(smem_u32(bar), 1));
+        } else {
+          mma_commit(bar);
         }
-        if (lane == 0) mma_commit(&sm.acc_full[acc]);
-        __syncwarp();
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+      };
+      for (int u = unit0; u < n_units && ok; u += unit_step) {
+        for (int t = 0; t < tiles_per_unit && ok; ++t) {
+          if (!mbar_wait(&sm.acc_empty[acc], acc_phase ^ 1, abort, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait(&sm.full[stage], phase, abort, a.status)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+              unsigned char* st = base + (size_t)stage * stage_bytes;
+              const uint32_t w_addr = smem_u32(st + a.n_parts * kATileBytes);
+              for (int p = 0; p < a.n_parts; ++p) {
+                const uint32_t a_addr = smem_u32(st + p * kATileBytes);
+#pragma unroll
+                for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                  if constexpr (PAIR)
+                    mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
+                                 a.idesc, (kb | p | k16) != 0);
+                  else
+                    mma_f16(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
+                            a.idesc, (kb | p | k16) != 0);
+                }
+              }
+              commit_both(&sm.empty[stage]);
+            }
+            __syncwarp();
+            if (++stage == a.stages) { stage = 0; phase ^= 1; }
+          }
+          if (lane == 0) commit_both(&sm.acc_full[acc]);
+          __syncwarp();
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
       }
+      // All issued MMAs complete before TMEM is released.
+      if (lane == 0) {
+        if constexpr (PAIR) mma_commit_pair(smem_u32(sm.mma_done));
+        else mma_commit(sm.mma_done);
+      }
+      __syncwarp();
+      mbar_wait_bounded(sm.mma_done, 0, a.status);
     }
-    // All issued MMAs complete before TMEM is released.
-    if (lane == 0) mma_commit(sm.mma_done);
-    __syncwarp();
-    mbar_wait_bounded(sm.mma_done, 0, a.status);
   } else {
     // ----------------------------------------------------------- epilogue
     const int qd = warp & 3;
@@ -319,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     const int n_chunks = BN / 32;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = unit0; u < n_units && ok; u += unit_step) {
       const int m_blk = ln_rows ? u : u / a.n_tiles;
-      const int row = m_blk * kBM + row_in_tile;
+      const int row = m_blk * rows_per_unit + (int)rank * kBM + row_in_tile;
       const bool row_ok = row < a.M;
       // LayerNorm running statistics over the row (Chan's parallel merge).
       float ln_n = 0.f, ln_mean = 0.f, ln_m2 = 0.f;
@@ -444,7 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&sm.acc_empty[acc]);
+        if (PAIR && !leader) {
+          // the leader reuses the accumulator: one arrival per warp on its barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&sm.acc_empty[acc]), 0));
+        } else {
+          mbar_arrive(&sm.acc_empty[acc]);
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
@@ -452,34 +520,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // Each CTA has finished every signal it sends the other (the leader's
+    // MMA commits completed before its mma_done wait; the peer's releases
+    // happened in its epilogue).  Tell the peer, and wait (bounded) for the
+    // peer to say the same before freeing the pair's tensor memory.
+    if (threadIdx.x == 0) {
+      mbar_arrive_cluster(map_to_rank(smem_u32(sm.done), rank ^ 1u));
+      mbar_wait_bounded(sm.done, 0, a.status);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, a.tmem_cols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, a.tmem_cols);
+    else tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
-template <typename T, int EPI>
+template <typename T, int EPI, bool PAIR>
 cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& mw,
                    const TcGemmArgs& a, int grid, size_t smem, cudaStream_t s) {
-  auto k = tc_gemm_kernel<T, EPI>;
+  auto k = tc_gemm_kernel<T, EPI, PAIR>;
   cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(m0, m1, mw, a);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, m0, m1, mw, a);
+  } else {
+    k<<<grid, kThreads, smem, s>>>(m0, m1, mw, a);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
-int tc_gemm_stages(int BN, int n_parts) {
-  const int stage = n_parts * kATileBytes + BN * kBK * 2;
+int tc_gemm_stages(int BN, int n_parts, bool pair) {
+  const int stage = n_parts * kATileBytes + (pair ? BN / 2 : BN) * kBK * 2;
   int st = (kTcGemmSmemBudget - 2048) / stage;
   return st > 6 ? 6 : st;
 }
 
-size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages) {
-  const int stage = n_parts * kATileBytes + BN * kBK * 2;
-  return 1024 + (size_t)stages * stage + 256;
+size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages, bool pair) {
+  const int stage = n_parts * kATileBytes + (pair ? BN / 2 : BN) * kBK * 2;
+  // pair: slack of one more half W tile after the ring, so that no operand
+  // read of the last stage can reach past the allocation
+  return 1024 + (size_t)stages * stage + 256 + (pair ? (size_t)(BN / 2) * kBK * 2 : 0);
 }
+
+bool tc_gemm_pair_ok(int M, int BN) { return M > kBM && BN >= 64 && BN <= 256 && BN % 32 == 0; }
 
 cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const CUtensorMap& map_w,
                     TcGemmArgs a, bool bf16, int epi, int num_sms, cudaStream_t s) {
@@ -488,28 +588,36 @@ cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const 
   if (a.BN % 32 || a.BN < 32 || a.BN > 256 || a.N % a.BN || a.K < 16 || a.K % 8 ||
       a.n_parts < 1 || a.n_parts > 2 || a.M < 1)
     return cudaErrorInvalidValue;
+  if (a.pair && !tc_gemm_pair_ok(a.M, a.BN)) return cudaErrorInvalidValue;
+  const bool pair = a.pair != 0;
+  const int rows = pair ? 2 * kBM : kBM;
   a.n_tiles = a.N / a.BN;
-  a.m_blocks = (a.M + kBM - 1) / kBM;
-  a.stages = tc_gemm_stages(a.BN, a.n_parts);
+  a.m_blocks = (a.M + rows - 1) / rows;
+  a.stages = tc_gemm_stages(a.BN, a.n_parts, pair);
   int cols = 32;
   while (cols < 2 * a.BN) cols <<= 1;
   a.tmem_cols = cols;
-  a.idesc = idesc_f16(kBM, a.BN, bf16);
+  a.idesc = idesc_f16(rows, a.BN, bf16);
   const int units = epi == TC_EPI_LN ? a.m_blocks : a.m_blocks * a.n_tiles;
-  const int grid = units < num_sms ? units : num_sms;
-  const size_t smem = tc_gemm_smem_bytes(a.BN, a.n_parts, a.stages);
+  const int slots = pair ? num_sms / 2 : num_sms;  // CTAs (pairs) resident at once
+  const int grid = (units < slots ? units : slots) * (pair ? 2 : 1);
+  const size_t smem = tc_gemm_smem_bytes(a.BN, a.n_parts, a.stages, pair);
+#define TL_GEMM_LAUNCH(T_, E_)                                                      \
+  return pair ? launch<T_, E_, true>(map_a0, map_a1, map_w, a, grid, smem, s)       \
+              : launch<T_, E_, false>(map_a0, map_a1, map_w, a, grid, smem, s)
   if (bf16) {
     switch (epi) {
-      case TC_EPI_QKV: return launch<__nv_bfloat16, TC_EPI_QKV>(map_a0, map_a1, map_w, a, grid, smem, s);
-      case TC_EPI_GELU: return launch<__nv_bfloat16, TC_EPI_GELU>(map_a0, map_a1, map_w, a, grid, smem, s);
-      default: return launch<__nv_bfloat16, TC_EPI_LN>(map_a0, map_a1, map_w, a, grid, smem, s);
+      case TC_EPI_QKV: TL_GEMM_LAUNCH(__nv_bfloat16, TC_EPI_QKV);
+      case TC_EPI_GELU: TL_GEMM_LAUNCH(__nv_bfloat16, TC_EPI_GELU);
+      default: TL_GEMM_LAUNCH(__nv_bfloat16, TC_EPI_LN);
     }
   }
   switch (epi) {
-    case TC_EPI_QKV: return launch<__half, TC_EPI_QKV>(map_a0, map_a1, map_w, a, grid, smem, s);
-    case TC_EPI_GELU: return launch<__half, TC_EPI_GELU>(map_a0, map_a1, map_w, a, grid, smem, s);
-    default: return launch<__half, TC_EPI_LN>(map_a0, map_a1, map_w, a, grid, smem, s);
+    case TC_EPI_QKV: TL_GEMM_LAUNCH(__half, TC_EPI_QKV);
+    case TC_EPI_GELU: TL_GEMM_LAUNCH(__half, TC_EPI_GELU);
+    default: TL_GEMM_LAUNCH(__half, TC_EPI_LN);
   }
+#undef TL_GEMM_LAUNCH
 }
 
 }  // namespace tl

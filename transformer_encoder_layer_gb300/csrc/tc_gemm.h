@@ -17,6 +17,8 @@ struct TcGemmArgs {
   int M, N, K;
   int BN;        // N tile: a multiple of 32 in [32, 256] dividing N
   int n_parts;   // A planes: 1 (exact 16-bit input) or 2 (hi, lo)
+  int pair;      // 1: CTA pairs on 256-row blocks (tcgen05 cta_group::2); the
+                 // W map's box is then BN/2 rows (tc_gemm_pair_ok must hold)
   int n_tiles, m_blocks, stages, tmem_cols;  // (set by tc_gemm)
   uint32_t idesc;                            // (set by tc_gemm)
   const float* bias;  // [N]
@@ -43,11 +45,14 @@ struct TcGemmArgs {
   int* status;
 };
 
-int tc_gemm_stages(int BN, int n_parts);
-size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages);
+int tc_gemm_stages(int BN, int n_parts, bool pair);
+size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages, bool pair);
+// Whether the CTA-pair variant can run M rows with N tile BN.
+bool tc_gemm_pair_ok(int M, int BN);
 
 // map_a0/map_a1: A planes [M, K] (box 64 x 128), map_w: W [N, K] (box
-// 64 x BN), all 128-byte swizzled.  map_a1 is ignored when n_parts == 1.
+// 64 x BN, or 64 x BN/2 with pair), all 128-byte swizzled.  map_a1 is
+// ignored when n_parts == 1.
 cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const CUtensorMap& map_w,
                     TcGemmArgs a, bool bf16, int epi, int num_sms, cudaStream_t s);
 
