@@ -354,7 +354,8 @@ def envelope_on_sample(inp, out_np):
 class Workload:
     """One workload's encoder, device buffers and pinned host copies."""
 
-    def __init__(self, shape, seed, dev, path="auto"):
+    def __init__(self, shape, seed, dev, path="auto", attention_split=-1, gemm_pairs=-1,
+                 graphs=False):
         import torch
         from transformer_encoder_layer_gb300 import binding
         from transformer_encoder_layer_gb300.inputs import make_inputs, to_storage
@@ -365,7 +366,12 @@ class Workload:
                                    shape.dtype)
         if path != "auto":
             self.enc.set_path(path)
+        self.enc.set_attention_split(attention_split)
+        self.enc.set_gemm_pairs(gemm_pairs)
+        self.enc.set_graphs(graphs)
+        self.graphs = bool(graphs)
         self.path = self.enc.plan(shape.batch, shape.seq_len)
+        self.attention_split = self.enc.attention_split(shape.batch, shape.seq_len)
         xs = to_storage(self.inp.x, shape.dtype)
         if shape.dtype == "bf16":
             x_host = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16)
@@ -407,7 +413,9 @@ def time_steps(w, steps, warmup, flush, stream, dist=None, clock_index=None):
     torch.cuda.synchronize()
     if w.enc.get_status() != 0:
         raise RuntimeError(f"{w.shape.name}: device status error during warm-up")
-    w.enc.enable_timing(True, capacity=max(4096, 64 * steps * w.shape.n_layers))
+    # (graph mode replays whole forwards; the per-launch timer would bypass it)
+    if not w.graphs:
+        w.enc.enable_timing(True, capacity=max(4096, 64 * steps * w.shape.n_layers))
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if dist:
@@ -429,7 +437,7 @@ def time_steps(w, steps, warmup, flush, stream, dist=None, clock_index=None):
     if dist:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
-    per_kernel = w.enc.read_timing()
+    per_kernel = {} if w.graphs else w.enc.read_timing()
     w.enc.enable_timing(False)
     if w.enc.get_status() != 0:
         raise RuntimeError(f"{w.shape.name}: device status error in the timed region")
@@ -517,7 +525,7 @@ def run_ours(args, shape):
     stream = torch.cuda.current_stream()
 
     # ---- headline: the chosen workload, K timed steps
-    w = Workload(shape, rank, dev, args.path)
+    w = Workload(shape, rank, dev, args.path, args.attention_split, args.gemm_pairs, args.graphs)
     step_ms, per_kernel, t_wall, clocks = time_steps(w, args.steps, args.warmup, flush, stream,
                                                      dist, dev.index)
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -556,7 +564,8 @@ def run_ours(args, shape):
                    "n_heads": shape.n_heads, "d_ff": shape.d_ff, "batch_per_gpu": shape.batch,
                    "global_batch": ws * shape.batch, "seq_len": shape.seq_len,
                    "io_dtype": shape.dtype, "valid_len": f"U[{shape.vl_lo},{shape.vl_hi}]",
-                   "input_scale": 1.0, "path": w.path,
+                   "input_scale": 1.0, "path": w.path, "attention_split": w.attention_split,
+                   "gemm_pairs": args.gemm_pairs, "graphs": bool(args.graphs),
                    "parallelism": f"dp{ws}" if ws > 1 else "single",
                    "l2": "flushed between timed steps (256 MB write)"},
         "ms_per_step_p10": percentile(step_ms, 10), "ms_per_step_p90": percentile(step_ms, 90),
@@ -614,6 +623,13 @@ def main():
                     help="time the headline workload only (profiling runs)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small cases for profiling)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the workload's sequence length (valid lengths scaled with it)")
+    ap.add_argument("--attention-split", type=int, default=-1,
+                    help="split-K attention chunk in 64-key tiles (-1 per shape, 0 off)")
+    ap.add_argument("--gemm-pairs", type=int, default=-1, choices=[-1, 0, 1],
+                    help="layered GEMMs on CTA pairs: -1 where measured faster, 0 none, 1 all")
+    ap.add_argument("--graphs", action="store_true", help="layered path in graph mode")
     ap.add_argument("--first-call-probe", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.first_call_probe:
@@ -625,6 +641,10 @@ def main():
     shape = SHAPES[args.workload]
     if args.batch:
         shape = shape.with_(batch=args.batch)
+    if args.seq_len:
+        f = args.seq_len / shape.seq_len
+        shape = shape.with_(seq_len=args.seq_len, vl_lo=max(1, int(shape.vl_lo * f)),
+                            vl_hi=max(1, min(args.seq_len, int(shape.vl_hi * f))))
     if args.impl == "reference":
         run_reference(args, shape)
     else:

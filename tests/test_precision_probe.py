@@ -5,7 +5,8 @@ precision plan, pinned here so that its conclusions are reproducible:
   above, bf16 everywhere);
 * a (hi, lo) pair for every activation operand passes with a wide margin;
 * with fp16, dropping the lo part of P (the Pl.Vh product) and of the FFN
-  hidden (FFN2 on h_hi) still passes: the megakernel's fp16 plan;
+  hidden (FFN2 on h_hi) still passes: the megakernel's fp16 plan; P alone is
+  the layered fp16 attention's plan;
 * with bf16 the same removal fails, so bf16 keeps every lo part.
 
 The measured GPU envelopes agree with the probe's all-split prediction
@@ -50,6 +51,16 @@ def test_fp16_d128_plans(scale):
     assert e["mega"] < 0.8, e
     if scale >= 10.0:
         assert e["plain"] > 1.0, e
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])
+def test_fp16_long_sequence_layer_without_pl(scale):
+    """The 100k-token workload's layer (fp16, head_dim 16) on 2 sequences of
+    1000 tokens: P without its lo part (the layered fp16 attention's plan)
+    stays far inside the gate."""
+    s = SHAPES["long_d64_L100k_B8"].with_(seq_len=1000, vl_lo=900, vl_hi=1000)
+    e = _envelopes(s, 2, scale, {"split": pp.ALL_SPLIT, "p_hi": pp.Plan(p_lo=False)})
+    assert e["p_hi"] < 0.6, e
 
 
 @pytest.mark.parametrize("scale", [1e-3, 1.0, 1e3])

@@ -162,7 +162,8 @@ class Encoder:
         _check(self.lib.tl_encoder_set_attention_split(self.handle, key_tiles),
                "tl_encoder_set_attention_split")
 
-    def set_gemm_pairs(self, enable: bool):
+    def set_gemm_pairs(self, enable):
+        """-1 automatic (default), 0 / False none, 1 / True every GEMM."""
         _check(self.lib.tl_encoder_set_gemm_pairs(self.handle, int(enable)),
                "tl_encoder_set_gemm_pairs")
 

@@ -337,7 +337,7 @@ tl_status tl_encoder_set_attention_split(tl_encoder* h, int key_tiles) {
 }
 
 tl_status tl_encoder_set_gemm_pairs(tl_encoder* h, int enable) {
-  if (!h || enable < 0 || enable > 1) return TL_ERR_INVALID_ARG;
+  if (!h || enable < -1 || enable > 1) return TL_ERR_INVALID_ARG;
   h->gemm_pairs = enable;
   return TL_OK;
 }
@@ -386,7 +386,7 @@ tl_status tl_encoder_forward(tl_encoder* h, const void* x, int B, int L, const i
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return TL_ERR_CUDA;
     if (cs == cudaStreamCaptureStatusNone) {
-      const tl_encoder::GraphKey key{(int)p, B, L, h->attn_split * 2 + h->gemm_pairs, x, valid_len, out,
+      const tl_encoder::GraphKey key{(int)p, B, L, h->attn_split * 4 + h->gemm_pairs + 1, x, valid_len, out,
                                      workspace};
       if (h->graph_exec && h->graph_key == key) {
         ++h->graph_replays;

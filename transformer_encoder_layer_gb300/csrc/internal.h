@@ -61,9 +61,10 @@ struct tl_encoder {
   // Split-K attention on the layered path: -1 automatic, 0 never, k > 0
   // chunks of k 64-key tiles (tl_encoder_set_attention_split).
   int attn_split = -1;
-  // Layered-path GEMMs on CTA pairs (tcgen05 cta_group::2): 0 off (the
-  // default), 1 on where the shape allows (tl_encoder_set_gemm_pairs).
-  int gemm_pairs = 0;
+  // Layered-path GEMMs on CTA pairs (tcgen05 cta_group::2): -1 automatic
+  // (the default: the FFN2 GEMM of large shapes), 0 off, 1 every GEMM the
+  // shape allows (tl_encoder_set_gemm_pairs).
+  int gemm_pairs = -1;
   int device = 0;
   int num_sms = 0;
   void* wbuf = nullptr;      // one allocation holding every packed parameter

@@ -241,28 +241,6 @@ __host__ __device__ constexpr bool p_hi_only() { return std::is_same<T, __half>:
 template <typename T>
 __host__ __device__ constexpr bool h_hi_only() { return std::is_same<T, __half>::value; }
 
-// Eight fp32 values rounded to 16 bits (the hi part alone) in one 16-byte chunk.
-__device__ __forceinline__ uint4 pack8_hi(const float* v, __half) {
-  uint4 r;
-  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __half2 h = __float22half2_rn(make_float2(v[2 * e], v[2 * e + 1]));
-    w[e] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return r;
-}
-__device__ __forceinline__ uint4 pack8_hi(const float* v, __nv_bfloat16) {
-  uint4 r;
-  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(v[2 * e], v[2 * e + 1]));
-    w[e] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return r;
-}
-
 // The (hi, lo) slots of P for row rr and key kk of the row's own sequence.
 __device__ __forceinline__ void p_slot(int rr, int kk, int& hi_off, int& lo_off) {
   const int off = sw128(rr, kk >> 3) + (kk & 7) * 2;

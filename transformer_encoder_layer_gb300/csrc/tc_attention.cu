@@ -101,6 +101,14 @@ __device__ __forceinline__ int swz_offset(int r, int c_bytes, int row_bytes) {
   return o ^ (((o >> 7) & ((row_bytes >> 4) - 1)) << 4);
 }
 
+// fp16: the probabilities enter P.V as one 16-bit value (O = Ph.Vh + Ph.Vl,
+// no Pl.Vh product, no lo plane of P to compute).  The CPU rounding-emulation
+// probe (tests/precision_probe.py) puts the gate's envelope of this plan at
+// 0.05-0.13 on the 100k-token workload's layer (0.024 with the lo part) over
+// input scales 1e-3 .. 1e3; with bf16 it fails the gate, so bf16 keeps Pl.
+template <typename T>
+__host__ __device__ constexpr bool p_hi_only() { return std::is_same<T, __half>::value; }
+
 // Row sums of P from the P.V MMAs (a ones row appended to V^T) instead of
 // one add per probability: only where the softmax issue rate binds.
 template <int DH>
@@ -136,17 +144,24 @@ __host__ __device__ inline int chunks_of(int qt, int L, int kc) {
   return kc ? (nkt_bound(qt, L) + kc - 1) / kc : 1;
 }
 
-// Work item w -> (plane, query tile, chunk).  Items run heaviest query tile
-// first: order index o covers query tile nqt-1-o, whose planes x chunks
-// items are numbered chunk-major.  Each role walks its CTA's increasing item
-// indices with its own cursor, so the decoding is amortised O(1).
+// Work item w -> (plane, query tile, chunk).  Without a split, planes go in
+// groups of `group` planes whose K/V fit in L2 together, and within a group
+// the items run heaviest query tile first (plane fastest): the CTAs working
+// at one time then stream the keys of a few planes, which stay in L2, and the
+// causal triangle's long rows still start first.  With a split, order index
+// o covers query tile nqt-1-o, whose planes x chunks items are numbered
+// chunk-major.  Each role walks its CTA's increasing item indices with its
+// own cursor, so the decoding is amortised O(1).
 struct ItemCursor {
   int o = 0, base = 0;
-  __device__ __forceinline__ void decode(int w, int planes, int nqt, int L, int kc, int& plane,
-                                         int& qt, int& c, int& nch) {
+  __device__ __forceinline__ void decode(int w, int planes, int nqt, int L, int kc, int group,
+                                         int& plane, int& qt, int& c, int& nch) {
     if (kc == 0) {
-      qt = nqt - 1 - w / planes;
-      plane = w % planes;
+      const int per_group = group * nqt;
+      const int g = w / per_group, i = w - g * per_group;
+      const int gp = min(group, planes - g * group);  // planes in this (maybe last) group
+      qt = nqt - 1 - i / gp;
+      plane = g * group + i % gp;
       c = 0;
       nch = 1;
       return;
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       ItemCursor cur;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         int plane, qt, c, nch, vl, j0, j1;
-        cur.decode(w, planes, nqt, a.L, kc, plane, qt, c, nch);
+        cur.decode(w, planes, nqt, a.L, kc, a.group, plane, qt, c, nch);
         key_range(c, key_tiles(plane, qt, vl), j0, j1);
         if (j0 >= j1) continue;  // a chunk past the valid keys loads nothing
         if (!mbar_wait(q_empty, (uint32_t)(n_items_done & 1) ^ 1, abort, a.status)) break;
@@ -320,12 +335,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * 2 * Lay::kPBytes);
         const uint32_t pl_ = ph_ + Lay::kPBytes;
         const uint32_t d = tO + (uint32_t)(pb * Lay::kOCols);
-        // O = Ph.Vh + Ph.Vl + Pl.Vh over 64 keys (4 steps of K = 16); with
-        // the extra rows, column DH = sum of Ph + Pl (the ones row of Vh)
+        // O = Ph.Vh + Ph.Vl (+ Pl.Vh with bf16) over 64 keys (4 steps of
+        // K = 16); with the extra rows, column DH = the sum of the P values
+        // used (the ones row of Vh)
         const uint32_t as[3] = {ph_, ph_, pl_};
         const uint32_t bs[3] = {vh, vl_, vh};
+        constexpr int kProducts = p_hi_only<T>() ? 2 : 3;
 #pragma unroll
-        for (int t = 0; t < 3; ++t)
+        for (int t = 0; t < kProducts; ++t)
 #pragma unroll
           for (int k = 0; k < kBKV / 16; ++k)
             mma_f16(d, sdesc_rows(as[t] + k * 32, 128), sdesc_rows(bs[t] + k * 32, 128), idesc_o,
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     ItemCursor cur;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int plane, qt, c, nch, vl, j0, j1;
-      cur.decode(w, planes, nqt, a.L, kc, plane, qt, c, nch);
+      cur.decode(w, planes, nqt, a.L, kc, a.group, plane, qt, c, nch);
       key_range(c, key_tiles(plane, qt, vl), j0, j1);
       if (j0 >= j1) continue;
       const int nkt = j1 - j0;  // key tiles of this item
@@ -398,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     ItemCursor cur;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int plane, qt, cidx, nch, vl, j0, j1;
-      cur.decode(w, planes, nqt, a.L, kc, plane, qt, cidx, nch);
+      cur.decode(w, planes, nqt, a.L, kc, a.group, plane, qt, cidx, nch);
       key_range(cidx, key_tiles(plane, qt, vl), j0, j1);
       const bool has_keys = j0 < j1;
       const int i = qt * kBQ + r;                    // query position in the sequence
@@ -524,15 +541,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
 #pragma unroll
           for (int e = 0; e < 8; ++e)  // one rounding: 2^(s scale - mref), flushed below 2^-126
             p8[e] = ex2_ftz(fmaf(s[c8 * 8 + e], scale_log2, -mref));
+          const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
           if constexpr (!row_sum_by_mma<DH>()) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) l += p8[e];
           }
-          uint4 hv, lv;
-          split8(p8, hv, lv, T());
-          const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(ph + off) = hv;
-          *reinterpret_cast<uint4*>(pl + off) = lv;
+          if constexpr (p_hi_only<T>()) {
+            *reinterpret_cast<uint4*>(ph + off) = pack8_hi(p8, T());
+          } else {
+            uint4 hv, lv;
+            split8(p8, hv, lv, T());
+            *reinterpret_cast<uint4*>(ph + off) = hv;
+            *reinterpret_cast<uint4*>(pl + off) = lv;
+          }
         }
         fence_proxy_async();
         mbar_arrive(&p_full[pb]);
@@ -713,6 +734,11 @@ cudaError_t tc_attention(const TcAttnArgs& a_in, bool bf16, int num_sms, int for
   const TcAttnSplit plan = tc_attention_split_plan(a.B, a.H, a.L, dh, num_sms, force_kc);
   a.kc = plan.kc;
   a.n_items = plan.n_items;
+  // Planes whose K and V (hi, lo) fit together in half the L2 (64 MB).
+  const size_t kv_plane = (size_t)a.L * dh * 2 * 2 * 2;
+  const size_t g = ((size_t)64 << 20) / (kv_plane ? kv_plane : 1);
+  const int planes = a.B * a.H;
+  a.group = (int)std::max<size_t>(1, std::min<size_t>(g, (size_t)planes));
   a.part = (float*)ws_part;
   a.cnt = (int*)ws_cnt;
   if (plan.kc) {

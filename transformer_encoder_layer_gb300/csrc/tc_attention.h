@@ -21,6 +21,7 @@ struct TcAttnArgs {
   // chunk (0 = no split), the work-item count, the partial-state buffer and
   // the per-(plane, query tile) arrival counters (zeroed by tc_attention).
   int kc = 0, n_items = 0;
+  int group = 1;  // planes per L2-resident group of unsplit items (set by tc_attention)
   float* part = nullptr;
   int* cnt = nullptr;
 };

@@ -304,5 +304,27 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo, __n
   }
 }
 
+// Eight fp32 values rounded to 16 bits (the hi part alone) in one 16-byte chunk.
+__device__ __forceinline__ uint4 pack8_hi(const float* v, __half) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2 h = __float22half2_rn(make_float2(v[2 * e], v[2 * e + 1]));
+    w[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return r;
+}
+__device__ __forceinline__ uint4 pack8_hi(const float* v, __nv_bfloat16) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(make_float2(v[2 * e], v[2 * e + 1]));
+    w[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return r;
+}
+
 }  // namespace tc
 }  // namespace tl
