@@ -144,6 +144,20 @@ tl_status tl_encoder_set_attention_split(tl_encoder *h, int key_tiles);
  * outside -1..1. */
 tl_status tl_encoder_set_gemm_pairs(tl_encoder *h, int enable);
 
+/* Assisting CTAs for the sequence-resident megakernel ("Hyper-optimized
+ * megakernel-hybrid transformer inference", section "Problem decomposition":
+ * extra CTAs take part of the resident CTAs' work when the batch alone leaves
+ * SMs idle).  When the batch's 128-row tiles fill at most half the SMs (and
+ * d_ff >= 256), each tile runs on a cluster of two CTAs: the resident one and
+ * a helper that computes half the heads' attention and half the FFN chunks,
+ * handing context, FFN partial sums and activations over through distributed
+ * shared memory.  enable = 1 uses it wherever possible; -1 (the default,
+ * automatic) and 0 do not: on GB300 it measured slower than one CTA per
+ * tile.  Host-only.  TL_ERR_INVALID_ARG outside -1..1. */
+tl_status tl_encoder_set_mega_assist(tl_encoder *h, int enable);
+/* *assisted = 1 when forward() on B x L runs the megakernel assisted. */
+tl_status tl_encoder_mega_assisted(const tl_encoder *h, int B, int L, int *assisted);
+
 /* The chunk size (in 64-key tiles) forward() would use for B x L: 0 when
  * the attention runs unsplit (or the path has no tensor-core attention). */
 tl_status tl_encoder_attention_split(const tl_encoder *h, int B, int L, int *key_tiles);

@@ -55,6 +55,8 @@ def test_status_strings_without_gpu():
     assert lib.tl_encoder_attention_split(None, 1, 1, None) == 1
     assert lib.tl_encoder_set_graphs(None, 1) == 1
     assert lib.tl_encoder_set_gemm_pairs(None, 1) == 1
+    assert lib.tl_encoder_set_mega_assist(None, 1) == 1
+    assert lib.tl_encoder_mega_assisted(None, 1, 1, None) == 1
     assert lib.tl_encoder_graph_stats(None, None, None) == 1
     # Shape checks at create time also come before any CUDA call (the weight
     # pointers are not read when the shape is refused).

@@ -34,6 +34,8 @@ SIGNATURES = {
     "tl_encoder_set_attention_split": (_i, [_vp, _i]),
     "tl_encoder_set_graphs": (_i, [_vp, _i]),
     "tl_encoder_set_gemm_pairs": (_i, [_vp, _i]),
+    "tl_encoder_set_mega_assist": (_i, [_vp, _i]),
+    "tl_encoder_mega_assisted": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
     "tl_encoder_graph_stats": (_i, [_vp, ctypes.POINTER(ctypes.c_longlong),
                                     ctypes.POINTER(ctypes.c_longlong)]),
     "tl_encoder_attention_split": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
@@ -166,6 +168,17 @@ class Encoder:
         """-1 automatic (default), 0 / False none, 1 / True every GEMM."""
         _check(self.lib.tl_encoder_set_gemm_pairs(self.handle, int(enable)),
                "tl_encoder_set_gemm_pairs")
+
+    def set_mega_assist(self, enable: int):
+        """-1 automatic (default), 0 never, 1 wherever possible."""
+        _check(self.lib.tl_encoder_set_mega_assist(self.handle, int(enable)),
+               "tl_encoder_set_mega_assist")
+
+    def mega_assisted(self, B: int, L: int) -> bool:
+        v = ctypes.c_int()
+        _check(self.lib.tl_encoder_mega_assisted(self.handle, B, L, ctypes.byref(v)),
+               "tl_encoder_mega_assisted")
+        return bool(v.value)
 
     def set_graphs(self, enable: bool):
         _check(self.lib.tl_encoder_set_graphs(self.handle, int(enable)), "tl_encoder_set_graphs")

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "paths.h"
+#include "mega.h"
 #include "tc_attention.h"
 
 using namespace tl;
@@ -339,6 +340,21 @@ tl_status tl_encoder_set_attention_split(tl_encoder* h, int key_tiles) {
 tl_status tl_encoder_set_gemm_pairs(tl_encoder* h, int enable) {
   if (!h || enable < -1 || enable > 1) return TL_ERR_INVALID_ARG;
   h->gemm_pairs = enable;
+  return TL_OK;
+}
+
+tl_status tl_encoder_set_mega_assist(tl_encoder* h, int enable) {
+  if (!h || enable < -1 || enable > 1) return TL_ERR_INVALID_ARG;
+  h->mega_assist = enable;
+  return TL_OK;
+}
+
+tl_status tl_encoder_mega_assisted(const tl_encoder* h, int B, int L, int* assisted) {
+  if (!h || !assisted || B < 1 || L < 1) return TL_ERR_INVALID_ARG;
+  tl_path p = choose_path(h, B, L);
+  if (p == TL_PATH_AUTO) return TL_ERR_UNSUPPORTED_SHAPE;
+  *assisted = p == TL_PATH_MEGA && h->dtype != TL_F32 &&
+              mega_assisted(B, L, h->dff, h->num_sms, h->mega_assist);
   return TL_OK;
 }
 

@@ -65,6 +65,10 @@ struct tl_encoder {
   // (the default: the FFN2 GEMM of large shapes), 0 off, 1 every GEMM the
   // shape allows (tl_encoder_set_gemm_pairs).
   int gemm_pairs = -1;
+  // Megakernel assisted mode (a helper CTA per tile when the tiles fill at
+  // most half the SMs): -1 automatic (off: measured slower), 0 off, 1 on
+  // where possible (tl_encoder_set_mega_assist).
+  int mega_assist = -1;
   int device = 0;
   int num_sms = 0;
   void* wbuf = nullptr;      // one allocation holding every packed parameter

@@ -55,6 +55,25 @@
 // (8 significant bits) either removal fails the gate, so bf16 keeps them.
 // That is 48 of the 264 MMAs of a layer and tile.
 //
+// Assisted mode (small batches; "Hyper-optimized megakernel-hybrid
+// transformer inference", section "Problem decomposition": extra CTAs take
+// part of the resident CTAs' work when the tiles alone leave SMs idle).
+// Launched as clusters of two CTAs per tile: the resident CTA R (rank 0)
+// and its helper H (rank 1) split each layer --
+//   QKV      R the weight boxes of heads 0, 1; H those of heads 2, 3
+//   heads    R heads 0, 1; H heads 2, 3, whose context H writes into R's
+//            ctx buffer (distributed shared memory) once R's own P and V
+//            buffers there are free
+//   out-proj R alone (all of ctx), LayerNorm 1 -> y, which R also writes
+//            into H's X buffer once H's attention no longer reads it
+//   FFN      R the first half of the d_ff chunks, H the second half; H's
+//            FFN2 partial sum goes (fp32) into R's P/ctx area
+//   LN 2     R adds H's partial, normalises, and writes the next layer's
+//            input to its own X buffer and tensor memory and into H's X
+//            buffer (once H's FFN1 no longer reads y there)
+// Every hand-over is a remote mbarrier arrive (release, cluster scope)
+// after the data, and a bounded cluster-scope acquire wait on the other side.
+//
 // Near ties (see neartie.cuh) are corrected in place: a flagged (row, head)
 // has its probabilities recomputed in fp64 from the layer input and the
 // weights, by the group-0 warp that owns the row, before the P . V product.
@@ -103,7 +122,7 @@ constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max pa
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
 constexpr int kBars = kVec + (384 + kMaxDff) * 4;
-constexpr int kNumBars = 32;
+constexpr int kNumBars = 40;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
 // mbarrier indices
@@ -112,7 +131,15 @@ enum {
   B_QKV_DONE, B_QKVH_READY,
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
-  B_MMA_DONE, B_SYNC, B_COUNT
+  B_MMA_DONE, B_SYNC,
+  // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster):
+  B_PEER_CTX,     // R: H's 8 context warps wrote heads 2, 3 into R's ctx buffer
+  B_PEER_XFREE,   // R: H's 16 compute warps no longer read H's X buffer (twice a layer)
+  B_PEER_PART,    // R: H's 16 compute warps wrote their FFN2 partial into R's P/ctx area
+  B_PEER_PBFREE,  // H: R's 16 compute warps finished with R's P/V area (H may write ctx)
+  B_PEER_Y,       // H: R's 16 compute warps wrote y into H's X buffer
+  B_PEER_X,       // H: R's 16 compute warps wrote the next layer's input into H's X buffer
+  B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget");
@@ -341,7 +368,7 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
 // of 16384 / 5 / 32 registers); setmaxnreg then moves them from the control
 // warpgroup (64 each) to the compute warps (104 each): 128 x 64 + 512 x 104
 // = 61440 = 640 x 96, and per sub-partition 32 x (64 + 4 x 104) <= 16384.
-template <typename T, int L>
+template <typename T, int L, bool ASSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     mega_kernel(const __grid_constant__ CUtensorMap map_x, const MegaArgs a) {
   extern __shared__ __align__(1024) unsigned char dyn_smem[];
@@ -356,6 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (a.B + S - 1) / S;
   const int n_chunks = a.dff / 128;  // 128-wide FFN chunks
   const int T_rows = a.B * L;
+  // Assisted mode: rank 0 = resident R, rank 1 = helper H (see above).
+  const uint32_t rank = ASSIST ? cluster_rank() : 0u;
+  const bool helper = ASSIST && rank == 1;
+  const uint32_t peer = rank ^ 1u;
+  const int nb0 = helper ? 1 : 0, nb1 = ASSIST ? nb0 + 2 : 3;    // QKV weight boxes [nb0, nb1)
+  const int h0 = helper ? 2 : 0, h1 = ASSIST ? h0 + 2 : kH;      // heads [h0, h1)
+  const int half = (n_chunks + 1) / 2;
+  const int c0 = helper ? half : 0, c1 = ASSIST && !helper ? half : n_chunks;  // FFN chunks [c0, c1)
+  // tile loop: a cluster shares one tile sequence (unsigned special registers)
+#define TL_T0 (ASSIST ? (blockIdx.x >> 1) : blockIdx.x)
+#define TL_TSTEP (ASSIST ? (gridDim.x >> 1) : gridDim.x)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
@@ -369,6 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         case B_S_DONE:
           cnt = 2;  // the S commit + a release arrive of the MMA thread
           break;
+        case B_PEER_CTX:
+          cnt = 8;  // H's context warps (groups 2, 3)
+          break;
+        case B_PEER_XFREE: case B_PEER_PART: case B_PEER_PBFREE: case B_PEER_Y: case B_PEER_X:
+          cnt = 16;  // one arrive per compute warp of the other CTA
+          break;
         default: break;
       }
       mbar_init(bar + i, cnt);
@@ -379,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(tmem_holder, 512);
   tc_fence_before();
   __syncthreads();
+  if constexpr (ASSIST) cluster_sync_all();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   volatile int* abort = abort_flag;
@@ -407,21 +452,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         used |= 1u << st;
         return true;
       };
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles_done) {
+      for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP, ++tiles_done) {
         if (!mbar_wait(bar + B_XA_FREE, (uint32_t)(tiles_done & 1) ^ 1, abort, status)) break;
         mbar_arrive_expect_tx(bar + B_X_FULL, 2 * kTile16);
         tma_load_2d(sm + kXA, &map_x, bar + B_X_FULL, 0, t * 128);
         tma_load_2d(sm + kXA + kTile16, &map_x, bar + B_X_FULL, 64, t * 128);
         for (int l = 0; l < a.n_layers && ok; ++l) {
           const MegaLayer& P = a.layers[l];
-          for (int nb = 0; nb < 3 && ok; ++nb)
+          for (int nb = nb0; nb < nb1 && ok; ++nb)
             for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16, false);
-          for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
+          if (!helper)
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
           ffn_it = 0;  // at least three FFN boxes per layer: slot 2 is used, OUT_DONE waited once
-          for (int c = 0; c <= n_chunks && ok; ++c) {
-            if (c < n_chunks)  // W_1 rows [128c, 128c + 128): two 128 x 64 boxes
+          for (int c = c0; c <= c1 && ok; ++c) {
+            if (c < c1)  // W_1 rows [128c, 128c + 128): two 128 x 64 boxes
               for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_1, 64 * kh, 128 * c, kTile16, true);
-            if (c >= 1)  // W_2 columns [128(c-1), 128c): two 128 x 64 boxes
+            if (c > c0)  // W_2 columns [128(c-1), 128c): two 128 x 64 boxes
               for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_2, 128 * (c - 1) + 64 * kh, 0, kTile16, true);
           }
         }
@@ -498,16 +544,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     long long c_x = 0, c_a = 0, c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
               c_hfree[2] = {0, 0}, c_hr = 0;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    long long c_pctx = 0;  // assisted R: phases of B_PEER_CTX waited
+    for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
       for (int l = 0; l < a.n_layers && ok; ++l) {
         // ---- QKV (the first layer's input is exact in its hi plane)
         ok = l == 0 ? wait(B_X_FULL, c_x) : wait(B_A_READY, c_a);
         // layer 0: x from shared memory (exact in its hi plane); later layers:
-        // the (hi, lo) input LayerNorm 2 also left in TMEM [384, 512)
-        for (int nb = 0; nb < 3 && ok; ++nb)
+        // the (hi, lo) input LayerNorm 2 also left in TMEM [384, 512) (the
+        // helper has it in its X buffer, written by R)
+        for (int nb = nb0; nb < nb1 && ok; ++nb)
           for (int kh = 0; kh < 2 && ok; ++kh)
             ok = l == 0 ? wbox(tmem + 128 * nb, xa + kh * kTile16, 0u, id128, kh == 0, false)
-                        : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
+                 : helper ? wbox(tmem + 128 * nb, xa + kh * kTile16, 2u * kTile16, id128, kh == 0, false)
+                          : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
         if (!ok) break;
         commit(B_QKV_DONE);
         // ---- attention: S_0, then per head h: S_{h+1} as soon as head h+1's
@@ -531,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           commit(B_S_DONE);
           return true;
         };
-        ok = issue_s(0);
-        for (int h = 0; h < kH && ok; ++h) {
-          if (h + 1 < kH && !(ok = issue_s(h + 1))) break;
+        ok = issue_s(h0);
+        for (int h = h0; h < h1 && ok; ++h) {
+          if (h + 1 < h1 && !(ok = issue_s(h + 1))) break;
           ok = wait(B_P_READY, c_p);
           if (!ok) break;
           if (lane == 0) {
@@ -554,31 +603,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           commit(B_O_DONE);
         }
         if (!ok) break;
-        // ---- out-projection
-        ok = wait(B_CTX_READY, c_ctx);
-        for (int kh = 0; kh < 2 && ok; ++kh)
-          ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
-        if (!ok) break;
-        commit(B_OUT_DONE);
+        if (helper) {
+          // no out-projection here: OUT_DONE marks the end of this CTA's
+          // attention products (the loader's borrowed FFN slots wait on it)
+          commit(B_OUT_DONE);
+        } else {
+          // ---- out-projection (assisted: also heads 2, 3 from the helper)
+          ok = wait(B_CTX_READY, c_ctx);
+          if (ok && ASSIST) {
+            ok = mbar_wait_cluster(bar + B_PEER_CTX, (uint32_t)(c_pctx & 1), abort, status);
+            ++c_pctx;
+            // H's context (generic stores into this CTA's shared memory) is
+            // read by the MMAs below through the async proxy
+            fence_proxy_async();
+            tc_fence_after();
+          }
+          for (int kh = 0; kh < 2 && ok; ++kh)
+            ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
+          if (!ok) break;
+          commit(B_OUT_DONE);
+        }
         // ---- FFN in 128-wide chunks; chunk c uses TMEM buffer c % 2 for its
         // FFN1 accumulator and then, rewritten by GELU, as FFN2's A operand
         ok = wait(B_Y_READY, c_y);
         ffn_it = 0;
-        for (int c = 0; c <= n_chunks && ok; ++c) {
-          if (c < n_chunks) {
+        for (int c = c0; c <= c1 && ok; ++c) {
+          if (c < c1) {
             const int buf = c & 1;
             // the buffer's last reader, FFN2 of chunk c - 2, must be done
-            if (c >= 2) ok = wait(B_H_FREE + buf, c_hfree[buf]);
+            if (c >= c0 + 2) ok = wait(B_H_FREE + buf, c_hfree[buf]);
+            // A = y: tensor memory, or (helper) the (hi, lo) copy R wrote
+            // into this CTA's X buffer
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox_ta(tmem + kTF + 128 * buf, kTY + 32 * kh, 64, id128, kh == 0, true);
+              ok = helper ? wbox(tmem + kTF + 128 * buf, xa + kh * kTile16, 2u * kTile16, id128, kh == 0, true)
+                          : wbox_ta(tmem + kTF + 128 * buf, kTY + 32 * kh, 64, id128, kh == 0, true);
             if (!ok) break;
             commit(B_F1_DONE + buf);
           }
-          if (c >= 1) {
+          if (c > c0) {
             const int hb = (c - 1) & 1;
             ok = wait(B_H_READY, c_hr);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox_ta(tmem, kTF + 128 * hb + 32 * kh, 64, id128, c == 1 && kh == 0, true,
+              ok = wbox_ta(tmem, kTF + 128 * hb + 32 * kh, 64, id128, c == c0 + 1 && kh == 0, true,
                            h_hi_only<T>() ? 1 : 2);
             if (!ok) break;
             commit(B_H_FREE + hb);
@@ -588,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(B_F2_DONE);
         // keep the per-buffer release counts in step: the last two chunks'
         // releases were not waited for in the loop
-        for (int c = (n_chunks >= 2 ? n_chunks - 2 : 0); c < n_chunks && ok; ++c)
+        for (int c = (c1 - c0 >= 2 ? c1 - 2 : c0); c < c1 && ok; ++c)
           ok = wait(B_H_FREE + (c & 1), c_hfree[c & 1]);
         if (!ok) break;
       }
@@ -617,7 +683,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NM = L / 32;  // own 8-key chunks of a row per group
     int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_f2 = 0,
         c_sync = 0;  // completed phases per barrier (parity = count & 1)
+    // assisted mode: phases of the barriers the other CTA arrives on
+    int c_pbfree = 0, c_py = 0, c_px = 0, c_xfree = 0, c_part = 0;
     bool ok = true;
+    // Wait for a hand-over from the other CTA of the cluster.
+    auto wait_peer = [&](int b, int& n) -> bool {
+      const uint32_t par = (uint32_t)(n & 1);
+      ++n;
+      if (!mbar_wait_cluster(bar + b, par, abort, status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    // This warp's hand-over to the other CTA: its writes (made visible at
+    // cluster scope) first, then one release arrive on the peer's barrier.
+    auto signal_peer = [&](int b) {
+      fence_cluster();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(bar + b), peer));
+      __syncwarp();
+    };
+    // 32 values of row r, columns [32g, 32g + 32), as (hi, lo) 16-bit pairs
+    // into the peer's X-buffer layout (the A-operand layout of this CTA's XA).
+    auto put_peer_xa = [&](const float* v) {
+      const int kh = g >> 1;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint4 hv, lv;
+        split8(v + 8 * cc, hv, lv, T());
+        const int off = sw128(r, (g & 1) * 4 + cc);
+        st_cluster_v4(map_to_rank(smem_u32(xa + kh * kTile16 + off), peer), hv);
+        st_cluster_v4(map_to_rank(smem_u32(xa + (2 + kh) * kTile16 + off), peer), lv);
+      }
+    };
     auto wait = [&](int b, int& n) -> bool {
       const uint32_t par = (uint32_t)(n & 1);
       ++n;
@@ -686,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (the X buffer): per-group (mean, M2) over 32 columns, merged through
     // the exchange with Chan's formula, (01)(23) then the two pairs.
     auto layernorm = [&](uint32_t tcol, const float* bias, const float* gam, const float* bet,
-                         bool resid_lo, bool resid_tmem, float* v) {
+                         bool resid_lo, bool resid_tmem, float* v, const float* part = nullptr) {
       tmem_ld32_nw(trow + tcol + 32 * g, v);
       if (resid_tmem) {
         // the residual y: (hi, lo) words [16g, 16g + 16) of TMEM columns kTY, kTY + 64
@@ -709,6 +806,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           get8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), resid_lo, x8);
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[cc * 8 + e] += x8[e];
+        }
+      }
+      if (part) {  // the helper's FFN2 partial sum: fp32 [128 rows][128 columns]
+        const float4* p4 = reinterpret_cast<const float4*>(part + r * 128 + 32 * g);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 q = p4[c4];
+          v[4 * c4] += q.x; v[4 * c4 + 1] += q.y; v[4 * c4 + 2] += q.z; v[4 * c4 + 3] += q.w;
         }
       }
       add_vec<32>(v, bias + 32 * g);
@@ -746,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * gg.w + e.w;
       }
     };
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
       const int seq = t * S + sq;
       const bool row_valid = seq < a.B;
       int vl = row_valid ? a.valid_len[seq] : 1;
@@ -771,10 +876,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               k < 384 ? P.b_qkv[((k % 96) >> 5) * 128 + (k / 96) * 32 + (k & 31)]  // head-grouped order
                       : P.b_1[k - 384];
         bar_compute();
-        convert_qk(0, P);
-        convert_v(0, P);
+        convert_qk(h0, P);
+        convert_v(h0, P);
         arrive(B_QKVH_READY);
-        for (int h = 0; h < kH && ok; ++h) {
+        for (int h = h0; h < h1 && ok; ++h) {
           // ---- softmax of S = Q_h K_h^T over the row's visible keys; this
           // group holds own chunks g + 4m (keys 8 (g + 4m) .. + 8)
           if (!wait(B_S_DONE, c_s)) { ok = false; break; }
@@ -787,8 +892,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P is single-buffered: P_{h-1} V_{h-1} must be done before this head
           // writes P (it is, since S_h completed after it; this also keeps the
           // O_DONE barrier at most one phase ahead of this thread's waits)
-          if (h >= 1 && !wait(B_O_DONE, c_o)) { ok = false; break; }
-          if (h + 1 < kH) {
+          if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+          if (h + 1 < h1) {
             // head h+1's Q, K (their buffers' reader S_h is done) and V (its
             // buffer's reader P_{h-1} V_{h-1} was just waited for), so that
             // S_{h+1} runs during this softmax
@@ -878,7 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
         // sequence s are in TMEM columns 96g + 32s
         if (!wait(B_O_DONE, c_o)) { ok = false; break; }
-        {
+        // assisted R: its P and V buffers are free, H may write there
+        if (ASSIST && !helper) signal_peer(B_PEER_PBFREE);
+        if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
           float o[32];
           tmem_ld32_nw(trow + 96 * g + 32 * sq, o);
           tmem_wait_ld();
@@ -888,14 +995,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] *= inv;
           const int kh = g >> 1;
+          if (helper) {
+            // heads 2, 3 into R's ctx buffer, once R's P and V are done there
+            if (!wait_peer(B_PEER_PBFREE, c_pbfree)) { ok = false; break; }
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), o + 8 * cc);
+            for (int cc = 0; cc < 4; ++cc) {
+              uint4 hv, lv;
+              split8(o + 8 * cc, hv, lv, T());
+              const int off = sw128(r, (g & 1) * 4 + cc);
+              st_cluster_v4(map_to_rank(smem_u32(pbuf + kh * kTile16 + off), peer), hv);
+              st_cluster_v4(map_to_rank(smem_u32(pbuf + (2 + kh) * kTile16 + off), peer), lv);
+            }
+            signal_peer(B_PEER_CTX);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), o + 8 * cc);
+          }
         }
-        arrive(B_CTX_READY);
-        // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
-        if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
-        {
+        if (helper) {
+          // H's X buffer is no longer read (its QKV products and every
+          // fix-up of its heads are done): R may write y there
+          signal_peer(B_PEER_XFREE);
+          if (!wait_peer(B_PEER_Y, c_py)) { ok = false; break; }
+        } else {
+          arrive(B_CTX_READY);
+          // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
+          if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
           float y[32];
           layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, false, y);
           // y -> TMEM [128, 256) as (hi, lo) words: group g holds K columns
@@ -908,11 +1034,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(trow + kTY + 16 * g, hw);
           tmem_st16(trow + kTY + 64 + 16 * g, lw);
           tmem_wait_st();
+          if (ASSIST) {
+            // y into H's X buffer, the A operand of its FFN1 chunks
+            if (!wait_peer(B_PEER_XFREE, c_xfree)) { ok = false; break; }
+            put_peer_xa(y);
+            signal_peer(B_PEER_Y);
+          }
         }
         arrive(B_Y_READY);
         // ---- FFN chunks (128 wide): h_c = gelu(acc1 + b_1) replaces acc1 in
         // its TMEM buffer as (hi, lo) words, the A operand of FFN2
-        for (int c = 0; c < n_chunks && ok; ++c) {
+        for (int c = c0; c < c1 && ok; ++c) {
           const int buf = c & 1;
           const uint32_t tb = kTF + 128 * buf;
           if (!wait(B_F1_DONE + buf, c_f1[buf])) { ok = false; break; }
@@ -950,12 +1082,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           arrive(B_H_READY);
         }
         if (!ok) break;
+        // assisted H: every FFN1 product of its chunks is done, so y in its X
+        // buffer is no longer read; R may write the next layer's input there
+        if (helper) signal_peer(B_PEER_XFREE);
         // ---- FFN2 + b_2 + residual y, LayerNorm 2
         if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
-        {
+        if (helper) {
+          // the partial FFN2 sum over this CTA's chunks -> R's P/ctx area
+          // (fp32 [row][128 columns]); R adds it before LayerNorm 2
+          float v[32];
+          tmem_ld32_nw(trow + 32 * g, v);
+          tmem_wait_ld();
+          const uint32_t dst = map_to_rank(smem_u32(pbuf + (size_t)(r * 128 + 32 * g) * 4), peer);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            st_cluster_v4(dst + 16 * c4, make_uint4(__float_as_uint(v[4 * c4]), __float_as_uint(v[4 * c4 + 1]),
+                                                    __float_as_uint(v[4 * c4 + 2]), __float_as_uint(v[4 * c4 + 3])));
+          signal_peer(B_PEER_PART);
+          if (l + 1 < a.n_layers) {
+            // the next layer's input, written by R into this CTA's X buffer
+            if (!wait_peer(B_PEER_X, c_px)) { ok = false; break; }
+            tc_fence_before();
+            arrive(B_A_READY);
+          }
+        } else {
+          if (ASSIST && !wait_peer(B_PEER_PART, c_part)) { ok = false; break; }
           float xo[32];
-          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo);
+          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo,
+                    ASSIST ? reinterpret_cast<const float*>(pbuf) : nullptr);
           const int kh = g >> 1;
+          if (ASSIST) {
+            // H's FFN1 no longer reads its X buffer (every layer, so that the
+            // phase counts stay in step); then the next layer's input there
+            if (!wait_peer(B_PEER_XFREE, c_xfree)) { ok = false; break; }
+            if (l + 1 < a.n_layers) {
+              put_peer_xa(xo);
+              signal_peer(B_PEER_X);
+            }
+          }
           if (l + 1 < a.n_layers) {
             // the next layer's input: X buffer (residual, fix-up) and TMEM
             // [384, 512) as (hi, lo) words, the A operand of its QKV product
@@ -993,16 +1157,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+#undef TL_T0
+#undef TL_TSTEP
 }
 
-template <typename T, int L>
+template <typename T, int L, bool ASSIST>
 cudaError_t launch_l(const CUtensorMap& mx, const MegaArgs& a, int grid, cudaStream_t s) {
-  auto k = mega_kernel<T, L>;
+  auto k = mega_kernel<T, L, ASSIST>;
   const size_t smem = kSmemBytes + 1024;
   cudaError_t e = set_max_dyn_smem((const void*)k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(mx, a);
-  return cudaGetLastError();
+  if constexpr (ASSIST) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, mx, a);
+  } else {
+    k<<<grid, kThreads, smem, s>>>(mx, a);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
@@ -1012,16 +1194,28 @@ bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
          L == 64 && dt != TL_F32;
 }
 
+bool mega_assisted(int B, int L, int dff, int num_sms, int setting) {
+  const int tiles = (B + (128 / L) - 1) / (128 / L);
+  const bool possible = dff >= 256 && 2 * tiles <= num_sms;  // every CTA gets a helper
+  // Automatic (-1) is off: on GB300 the assisted forward measured slower
+  // (0.158 vs 0.142 ms for 1-152 sequences of the d128 workload).
+  return possible && setting == 1;
+}
+
 cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int num_sms, cudaStream_t s) {
   CUtensorMap mx;
   if (!make_tmap_2d(&mx, x, bf16, (uint64_t)a.B * L, kD, kD, 64, 128, 128)) return cudaErrorInvalidValue;
   const int S = 128 / L;
   const int tiles = (a.B + S - 1) / S;
+  if (mega_assisted(a.B, L, a.dff, num_sms, a.assist)) {
+    const int grid = 2 * tiles;  // one cluster (resident + helper) per tile
+    return bf16 ? launch_l<__nv_bfloat16, 64, true>(mx, a, grid, s) : launch_l<__half, 64, true>(mx, a, grid, s);
+  }
   const int grid = tiles < num_sms ? tiles : num_sms;
   if (bf16) {
-    return launch_l<__nv_bfloat16, 64>(mx, a, grid, s);
+    return launch_l<__nv_bfloat16, 64, false>(mx, a, grid, s);
   }
-  return launch_l<__half, 64>(mx, a, grid, s);
+  return launch_l<__half, 64, false>(mx, a, grid, s);
 }
 
 }  // namespace tl

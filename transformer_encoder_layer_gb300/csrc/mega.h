@@ -25,9 +25,14 @@ struct MegaArgs {
   const int32_t* valid_len;
   void* out;
   int* status;
+  // Assisted mode (a helper CTA per tile, clusters of two) for batches whose
+  // tiles fill at most half the SMs: -1 automatic, 0 never (mega_assisted).
+  int assist = -1;
 };
 
 bool mega_supported(int d, int H, int dff, int L, tl_dtype dt);
+// Whether a forward of B sequences runs assisted (setting: -1 auto, 0 off, 1 on).
+bool mega_assisted(int B, int L, int dff, int num_sms, int setting);
 cudaError_t mega_forward(const void* x, const MegaArgs& a, int L, bool bf16, int num_sms, cudaStream_t s);
 
 }  // namespace tl
