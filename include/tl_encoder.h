@@ -152,7 +152,7 @@ tl_status tl_encoder_set_gemm_pairs(tl_encoder *h, int enable);
  * a helper that computes half the heads' attention and half the FFN chunks,
  * handing context, FFN partial sums and activations over through distributed
  * shared memory.  enable = 1 uses it wherever possible; -1 (the default,
- * automatic) and 0 do not: on GB300 it measured slower than one CTA per
+ * automatic) and 0 do not: on GB300 it measured within 2% of one CTA per
  * tile.  Host-only.  TL_ERR_INVALID_ARG outside -1..1. */
 tl_status tl_encoder_set_mega_assist(tl_encoder *h, int enable);
 /* *assisted = 1 when forward() on B x L runs the megakernel assisted. */

@@ -66,7 +66,7 @@ struct tl_encoder {
   // shape allows (tl_encoder_set_gemm_pairs).
   int gemm_pairs = -1;
   // Megakernel assisted mode (a helper CTA per tile when the tiles fill at
-  // most half the SMs): -1 automatic (off: measured slower), 0 off, 1 on
+  // most half the SMs): -1 automatic (off: no measured gain), 0 off, 1 on
   // where possible (tl_encoder_set_mega_assist).
   int mega_assist = -1;
   int device = 0;

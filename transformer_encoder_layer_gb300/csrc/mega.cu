@@ -71,8 +71,11 @@
 //   LN 2     R adds H's partial, normalises, and writes the next layer's
 //            input to its own X buffer and tensor memory and into H's X
 //            buffer (once H's FFN1 no longer reads y there)
-// Every hand-over is a remote mbarrier arrive (release, cluster scope)
-// after the data, and a bounded cluster-scope acquire wait on the other side.
+// Each data hand-over is staged in the sender's own shared memory and moved
+// by one bulk copy (cp.async.bulk shared::cta -> shared::cluster) that
+// completes on the receiver's mbarrier, whose expected bytes the receiver
+// registers; "buffer free" signals are single remote arrives (release,
+// cluster scope); every wait is a bounded cluster-scope acquire.
 //
 // Near ties (see neartie.cuh) are corrected in place: a flagged (row, head)
 // has its probabilities recomputed in fp64 from the layer input and the
@@ -132,13 +135,14 @@ enum {
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC,
-  // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster):
-  B_PEER_CTX,     // R: H's 8 context warps wrote heads 2, 3 into R's ctx buffer
-  B_PEER_XFREE,   // R: H's 16 compute warps no longer read H's X buffer (twice a layer)
-  B_PEER_PART,    // R: H's 16 compute warps wrote their FFN2 partial into R's P/ctx area
-  B_PEER_PBFREE,  // H: R's 16 compute warps finished with R's P/V area (H may write ctx)
-  B_PEER_Y,       // H: R's 16 compute warps wrote y into H's X buffer
-  B_PEER_X,       // H: R's 16 compute warps wrote the next layer's input into H's X buffer
+  // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster);
+  // data hand-overs are bulk copies completing on the receiver's barrier
+  B_PEER_CTX,     // R: H's context of heads 2, 3 has landed in R's ctx buffer
+  B_PEER_XFREE,   // R: H no longer reads its X buffer (twice a layer)
+  B_PEER_PART,    // R: H's FFN2 partial has landed in R's P/ctx area
+  B_PEER_PBFREE,  // H: R is done with its P/V area (H may send the context)
+  B_PEER_Y,       // H: y has landed in H's X buffer
+  B_PEER_X,       // H: the next layer's input has landed in H's X buffer
   B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
@@ -407,13 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         case B_S_DONE:
           cnt = 2;  // the S commit + a release arrive of the MMA thread
           break;
-        case B_PEER_CTX:
-          cnt = 8;  // H's context warps (groups 2, 3)
-          break;
-        case B_PEER_XFREE: case B_PEER_PART: case B_PEER_PBFREE: case B_PEER_Y: case B_PEER_X:
-          cnt = 16;  // one arrive per compute warp of the other CTA
-          break;
-        default: break;
+        default: break;  // the peer barriers: one arrive (or expect-tx arrive) per phase
       }
       mbar_init(bar + i, cnt);
     }
@@ -611,11 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // ---- out-projection (assisted: also heads 2, 3 from the helper)
           ok = wait(B_CTX_READY, c_ctx);
           if (ok && ASSIST) {
+            // H's context (two 16 KB planes) arrives by bulk copy
+            if (lane == 0) mbar_arrive_expect_tx(bar + B_PEER_CTX, 2 * kTile16);
+            __syncwarp();
             ok = mbar_wait_cluster(bar + B_PEER_CTX, (uint32_t)(c_pctx & 1), abort, status);
             ++c_pctx;
-            // H's context (generic stores into this CTA's shared memory) is
-            // read by the MMAs below through the async proxy
-            fence_proxy_async();
             tc_fence_after();
           }
           for (int kh = 0; kh < 2 && ok; ++kh)
@@ -694,26 +692,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return true;
     };
-    // This warp's hand-over to the other CTA: its writes (made visible at
-    // cluster scope) first, then one release arrive on the peer's barrier.
-    auto signal_peer = [&](int b) {
-      fence_cluster();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(bar + b), peer));
-      __syncwarp();
-    };
-    // 32 values of row r, columns [32g, 32g + 32), as (hi, lo) 16-bit pairs
-    // into the peer's X-buffer layout (the A-operand layout of this CTA's XA).
-    auto put_peer_xa = [&](const float* v) {
-      const int kh = g >> 1;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint4 hv, lv;
-        split8(v + 8 * cc, hv, lv, T());
-        const int off = sw128(r, (g & 1) * 4 + cc);
-        st_cluster_v4(map_to_rank(smem_u32(xa + kh * kTile16 + off), peer), hv);
-        st_cluster_v4(map_to_rank(smem_u32(xa + (2 + kh) * kTile16 + off), peer), lv);
-      }
+    // One thread of the compute warps handles the bulk copies and signals.
+    const bool elected = threadIdx.x == kCtrlWarps * 32;
+    auto peer_addr = [&](const void* p) { return map_to_rank(smem_u32(p), peer); };
+    // A "buffer free" signal to the other CTA (release at cluster scope).
+    auto signal_peer = [&](int b) { mbar_arrive_cluster(peer_addr(bar + b)); };
+    // Send `bytes` of this CTA's shared memory at src to the same offset in
+    // the other CTA, completing on its barrier b (after every compute thread
+    // staged its part: callers fence and bar_compute first).
+    auto send_peer = [&](const void* src, uint32_t bytes, int b) {
+      bulk_copy_to_cta(peer_addr(src), src, bytes, peer_addr(bar + b));
     };
     auto wait = [&](int b, int& n) -> bool {
       const uint32_t par = (uint32_t)(n & 1);
@@ -983,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
         // sequence s are in TMEM columns 96g + 32s
         if (!wait(B_O_DONE, c_o)) { ok = false; break; }
-        // assisted R: its P and V buffers are free, H may write there
-        if (ASSIST && !helper) signal_peer(B_PEER_PBFREE);
+        // assisted R: its P and V buffers are free, H may send its context
+        if (ASSIST && !helper && elected) signal_peer(B_PEER_PBFREE);
         if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
           float o[32];
           tmem_ld32_nw(trow + 96 * g + 32 * sq, o);
@@ -995,28 +983,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] *= inv;
           const int kh = g >> 1;
-          if (helper) {
-            // heads 2, 3 into R's ctx buffer, once R's P and V are done there
-            if (!wait_peer(B_PEER_PBFREE, c_pbfree)) { ok = false; break; }
+          // (H stages heads 2, 3 at the same place in its own buffer, which
+          // its attention no longer uses, and sends both planes below)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              uint4 hv, lv;
-              split8(o + 8 * cc, hv, lv, T());
-              const int off = sw128(r, (g & 1) * 4 + cc);
-              st_cluster_v4(map_to_rank(smem_u32(pbuf + kh * kTile16 + off), peer), hv);
-              st_cluster_v4(map_to_rank(smem_u32(pbuf + (2 + kh) * kTile16 + off), peer), lv);
-            }
-            signal_peer(B_PEER_CTX);
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-              put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), o + 8 * cc);
-          }
+          for (int cc = 0; cc < 4; ++cc)
+            put8<T>(pbuf + kh * kTile16, pbuf + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), o + 8 * cc);
         }
         if (helper) {
-          // H's X buffer is no longer read (its QKV products and every
-          // fix-up of its heads are done): R may write y there
-          signal_peer(B_PEER_XFREE);
+          fence_proxy_async();  // the staged context is read by the bulk copy
+          bar_compute();
+          if (elected) {
+            // once R is done with its P/V area: the hi and lo planes of
+            // columns 64..127 into R's ctx buffer
+            if (!wait_peer(B_PEER_PBFREE, c_pbfree)) { ok = false; break; }
+            send_peer(pbuf + kTile16, kTile16, B_PEER_CTX);
+            send_peer(pbuf + 3 * kTile16, kTile16, B_PEER_CTX);
+            // H's X buffer is no longer read (its QKV products and every
+            // fix-up of its heads are done): R may send y there
+            signal_peer(B_PEER_XFREE);
+            mbar_arrive_expect_tx(bar + B_PEER_Y, 4 * kTile16);
+          }
           if (!wait_peer(B_PEER_Y, c_py)) { ok = false; break; }
         } else {
           arrive(B_CTX_READY);
@@ -1035,10 +1021,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(trow + kTY + 64 + 16 * g, lw);
           tmem_wait_st();
           if (ASSIST) {
-            // y into H's X buffer, the A operand of its FFN1 chunks
+            // y into H's X buffer, the A operand of its FFN1 chunks: staged
+            // in this CTA's X buffer (its residual x was read above, by this
+            // same thread) and sent once H no longer reads its own
+            const int kh = g >> 1;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              put8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), y + 8 * cc);
+            fence_proxy_async();
+            bar_compute();
             if (!wait_peer(B_PEER_XFREE, c_xfree)) { ok = false; break; }
-            put_peer_xa(y);
-            signal_peer(B_PEER_Y);
+            if (elected) send_peer(xa, 4 * kTile16, B_PEER_Y);
           }
         }
         arrive(B_Y_READY);
@@ -1084,42 +1077,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // assisted H: every FFN1 product of its chunks is done, so y in its X
         // buffer is no longer read; R may write the next layer's input there
-        if (helper) signal_peer(B_PEER_XFREE);
+        if (helper && elected) signal_peer(B_PEER_XFREE);
         // ---- FFN2 + b_2 + residual y, LayerNorm 2
         if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
         if (helper) {
           // the partial FFN2 sum over this CTA's chunks -> R's P/ctx area
           // (fp32 [row][128 columns]); R adds it before LayerNorm 2
+          // staged in this CTA's P/ctx area (its context copy to R landed
+          // before R sent y), then one 64 KB copy to the same place in R
           float v[32];
           tmem_ld32_nw(trow + 32 * g, v);
           tmem_wait_ld();
-          const uint32_t dst = map_to_rank(smem_u32(pbuf + (size_t)(r * 128 + 32 * g) * 4), peer);
+          float4* dst = reinterpret_cast<float4*>(pbuf + (size_t)(r * 128 + 32 * g) * 4);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            st_cluster_v4(dst + 16 * c4, make_uint4(__float_as_uint(v[4 * c4]), __float_as_uint(v[4 * c4 + 1]),
-                                                    __float_as_uint(v[4 * c4 + 2]), __float_as_uint(v[4 * c4 + 3])));
-          signal_peer(B_PEER_PART);
+          for (int c4 = 0; c4 < 8; ++c4) dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+          fence_proxy_async();
+          bar_compute();
+          if (elected) {
+            send_peer(pbuf, 4 * kTile16, B_PEER_PART);
+            if (l + 1 < a.n_layers) mbar_arrive_expect_tx(bar + B_PEER_X, 4 * kTile16);
+          }
           if (l + 1 < a.n_layers) {
-            // the next layer's input, written by R into this CTA's X buffer
+            // the next layer's input, sent by R into this CTA's X buffer
             if (!wait_peer(B_PEER_X, c_px)) { ok = false; break; }
             tc_fence_before();
             arrive(B_A_READY);
           }
         } else {
-          if (ASSIST && !wait_peer(B_PEER_PART, c_part)) { ok = false; break; }
+          if (ASSIST) {
+            if (elected) mbar_arrive_expect_tx(bar + B_PEER_PART, 4 * kTile16);
+            if (!wait_peer(B_PEER_PART, c_part)) { ok = false; break; }
+          }
           float xo[32];
           layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo,
                     ASSIST ? reinterpret_cast<const float*>(pbuf) : nullptr);
           const int kh = g >> 1;
-          if (ASSIST) {
-            // H's FFN1 no longer reads its X buffer (every layer, so that the
-            // phase counts stay in step); then the next layer's input there
-            if (!wait_peer(B_PEER_XFREE, c_xfree)) { ok = false; break; }
-            if (l + 1 < a.n_layers) {
-              put_peer_xa(xo);
-              signal_peer(B_PEER_X);
-            }
-          }
+          // assisted: H's FFN1 no longer reads y -- so the copy of y out of
+          // this CTA's X buffer is complete and H's X buffer may take the
+          // next layer's input (waited every layer to keep the phases in step)
+          if (ASSIST && !wait_peer(B_PEER_XFREE, c_xfree)) { ok = false; break; }
           if (l + 1 < a.n_layers) {
             // the next layer's input: X buffer (residual, fix-up) and TMEM
             // [384, 512) as (hi, lo) words, the A operand of its QKV product
@@ -1132,6 +1128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(trow + kTX + 16 * g, hw);
             tmem_st16(trow + kTX + 64 + 16 * g, lw);
             tmem_wait_st();
+            if (ASSIST) {  // the same rows into H's X buffer
+              fence_proxy_async();
+              bar_compute();
+              if (elected) send_peer(xa, 4 * kTile16, B_PEER_X);
+            }
             arrive(B_A_READY);
           } else if (row_valid && grow < (size_t)T_rows) {
             T* dst = reinterpret_cast<T*>(a.out) + grow * kD + 32 * g;
@@ -1197,8 +1198,9 @@ bool mega_supported(int d, int H, int dff, int L, tl_dtype dt) {
 bool mega_assisted(int B, int L, int dff, int num_sms, int setting) {
   const int tiles = (B + (128 / L) - 1) / (128 / L);
   const bool possible = dff >= 256 && 2 * tiles <= num_sms;  // every CTA gets a helper
-  // Automatic (-1) is off: on GB300 the assisted forward measured slower
-  // (0.158 vs 0.142 ms for 1-152 sequences of the d128 workload).
+  // Automatic (-1) is off: on GB300 the assisted forward measured within
+  // 2% of one CTA per tile (0.140-0.142 vs 0.142-0.146 ms for 1-152
+  // sequences of the d128 workload), not worth a second SM per tile.
   return possible && setting == 1;
 }
 

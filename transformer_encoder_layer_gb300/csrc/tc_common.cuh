@@ -112,6 +112,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint4 v) {
                : "memory");
 }
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's (shared::cluster address), completing on the mbarrier at
+// `bar_cluster` in that CTA.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
 // Phase test with acquire at cluster scope: what the arriving threads of the
 // other CTA wrote before their (release) arrive is visible after it passes.
 __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
