@@ -355,7 +355,7 @@ class Workload:
     """One workload's encoder, device buffers and pinned host copies."""
 
     def __init__(self, shape, seed, dev, path="auto", attention_split=-1, gemm_pairs=-1,
-                 graphs=False):
+                 graphs=False, mega_assist=-1):
         import torch
         from transformer_encoder_layer_gb300 import binding
         from transformer_encoder_layer_gb300.inputs import make_inputs, to_storage
@@ -369,6 +369,7 @@ class Workload:
         self.enc.set_attention_split(attention_split)
         self.enc.set_gemm_pairs(gemm_pairs)
         self.enc.set_graphs(graphs)
+        self.enc.set_mega_assist(mega_assist)
         self.graphs = bool(graphs)
         self.path = self.enc.plan(shape.batch, shape.seq_len)
         self.attention_split = self.enc.attention_split(shape.batch, shape.seq_len)
@@ -525,7 +526,8 @@ def run_ours(args, shape):
     stream = torch.cuda.current_stream()
 
     # ---- headline: the chosen workload, K timed steps
-    w = Workload(shape, rank, dev, args.path, args.attention_split, args.gemm_pairs, args.graphs)
+    w = Workload(shape, rank, dev, args.path, args.attention_split, args.gemm_pairs, args.graphs,
+                 args.mega_assist)
     step_ms, per_kernel, t_wall, clocks = time_steps(w, args.steps, args.warmup, flush, stream,
                                                      dist, dev.index)
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -566,6 +568,7 @@ def run_ours(args, shape):
                    "io_dtype": shape.dtype, "valid_len": f"U[{shape.vl_lo},{shape.vl_hi}]",
                    "input_scale": 1.0, "path": w.path, "attention_split": w.attention_split,
                    "gemm_pairs": args.gemm_pairs, "graphs": bool(args.graphs),
+                   "mega_assisted": w.enc.mega_assisted(shape.batch, shape.seq_len),
                    "parallelism": f"dp{ws}" if ws > 1 else "single",
                    "l2": "flushed between timed steps (256 MB write)"},
         "ms_per_step_p10": percentile(step_ms, 10), "ms_per_step_p90": percentile(step_ms, 90),
@@ -630,6 +633,8 @@ def main():
     ap.add_argument("--gemm-pairs", type=int, default=-1, choices=[-1, 0, 1],
                     help="layered GEMMs on CTA pairs: -1 where measured faster, 0 none, 1 all")
     ap.add_argument("--graphs", action="store_true", help="layered path in graph mode")
+    ap.add_argument("--mega-assist", type=int, default=-1, choices=[-1, 0, 1],
+                    help="megakernel assisting CTAs: -1 automatic, 0 off, 1 on where possible")
     ap.add_argument("--first-call-probe", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.first_call_probe:
