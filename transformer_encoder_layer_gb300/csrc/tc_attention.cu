@@ -6,9 +6,12 @@
 // One CTA per SM, persistent over (plane, 128-query tile) work items taken
 // heaviest first (the causal triangle makes late query tiles longest).
 // Q, K and V arrive as (hi, lo) 16-bit planes; scores and probabilities are
-// products of split operands, S = Qh.Kh + Qh.Kl + Ql.Kh and O = Ph.Vh +
-// Ph.Vl + Pl.Vh (the lo.lo term is below fp32 rounding), accumulated in
-// fp32 in TMEM.
+// products of split operands, S = Qh.Kh + Qh.Kl + Ql.Kh (the lo.lo term is
+// below fp32 rounding) and O = P.Vh + P.Vl, accumulated in fp32 in TMEM.
+// V^T's hi and lo rows sit one after the other in shared memory, so one MMA
+// of width 2 x head_dim gives P.Vh and P.Vl side by side in TMEM (the softmax
+// adds the two halves): a tcgen05.mma of N <= 128 costs about the same issue
+// time whatever its N, and P.V is the larger part of a small head's MMAs.
 //
 // Warp roles (192 threads):
 //   warp 0     TMA: Q (once per work item) and K/V^T tiles of 64 keys into a
@@ -17,12 +20,12 @@
 //              score buffers, then O_j = P_j V_j into one of two TMEM output
 //              buffers once the softmax warps have written P_j.  At head_dim
 //              16, where the softmax's instruction issue is the bound, each
-//              V^T tile carries 16 extra rows after its head_dim rows (a row
-//              of ones in the hi plane, zeros otherwise, written once at
-//              start; TMA fills only the first head_dim rows), so the same
-//              MMAs also produce the row sum of P_j in output column
-//              head_dim and the softmax adds no probabilities itself; at
-//              larger heads the wider MMA costs more than it saves.
+//              V^T tile carries 16 extra rows after its 2 x head_dim (hi, lo)
+//              rows (a row of ones, then zeros, written once at start; TMA
+//              never touches them), so the same MMAs also produce the row sum
+//              of P_j in output column 2 x head_dim and the softmax adds no
+//              probabilities itself; at larger heads the wider MMA costs more
+//              than it saves.
 //   warps 2-5  softmax: thread = query row.  Reads its 64 scores, masks,
 //              updates the running max, writes P_j as (hi, lo) into the
 //              swizzled shared-memory operand, and folds the previous tile's
@@ -68,6 +71,24 @@ constexpr int kBQ = 128, kBKV = 64, kStages = 3;
 // the bound at that head size; larger heads keep one.
 template <int DH>
 constexpr int ctas_per_sm() { return DH == 16 ? 2 : 1; }
+
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 16 consecutive TMEM columns of this warp's 32 lanes (no wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 
 // 2^x by the SFU's approximate base-2 exponential with subnormal results
 // flushed to zero (a probability below 2^-126 of the row maximum's weight is
@@ -119,13 +140,14 @@ struct Layout {
   static constexpr int kQBytes = kBQ * DH * 2;      // one Q plane
   static constexpr int kKBytes = kBKV * DH * 2;     // one K plane tile
   static constexpr int kXRows = row_sum_by_mma<DH>() ? 16 : 0;  // a ones row and 15 zero rows
-  static constexpr int kVRows = DH + kXRows;        // V^T rows
-  static constexpr int kVBytes = kVRows * kBKV * 2; // one V^T plane buffer
-  static constexpr int kVTx = DH * kBKV * 2;        // bytes TMA writes into it
+  static constexpr int kVRows = 2 * DH + kXRows;    // V^T rows: hi, lo, extension
+  static constexpr int kVTx = DH * kBKV * 2;        // bytes of one V^T plane tile (TMA)
+  static constexpr int kVBytes = kVRows * kBKV * 2; // the V^T block of a stage
   static constexpr int kPBytes = kBQ * kBKV * 2;    // one P plane (16 KB)
-  static constexpr int kStageBytes = 2 * kKBytes + 2 * kVBytes;
+  static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
   static constexpr int kStageTx = 2 * kKBytes + 2 * kVTx;  // TMA bytes per stage
-  static constexpr int kOCols = (DH + kXRows + 31) / 32 * 32;  // TMEM columns per O buffer
+  static constexpr int kOCols = (kVRows + 31) / 32 * 32;  // TMEM columns per O buffer
+  static_assert(kVTx % 1024 == 0 && kStageBytes % 1024 == 0, "128-byte swizzle atoms stay aligned");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
   static constexpr int kPOff = kKVOff + kStages * kStageBytes;
@@ -213,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int nqt = (a.L + kBQ - 1) / kBQ;
   const int n_items = a.kc ? a.n_items : planes * nqt;
   const int kc = a.kc;
-  // S: 2 x 64 columns, O: 2 x kOCols (head_dim outputs + the row sum)
+  // S: 2 x 64 columns, O: 2 x kOCols (P.Vh, P.Vl and the row sum)
   constexpr uint32_t kTmemCols = 2 * kBKV + 2 * Lay::kOCols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
@@ -241,21 +263,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   if (blockIdx.x == 0 && warp >= 2)
     for (int b = threadIdx.x - 64; b < a.B; b += kThreads - 64) load_valid_len(a.valid_len, b, a.L, a.status);
   if (row_sum_by_mma<DH>() && warp >= 2) {
-    // The V^T buffers' 16 extra rows, never touched by TMA: row head_dim of
-    // the hi plane all ones (its product with P is the row sum), the rest 0.
-    // A row of equal values is the same under the 128-byte swizzle.
+    // The V^T blocks' 16 extra rows, never touched by TMA: the first all
+    // ones (its product with P is the row sum), the rest 0.  A row of equal
+    // values is the same under the 128-byte swizzle.
     T ones[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) ones[e] = from_f32<T>(1.f);
     const uint4 one4 = *reinterpret_cast<const uint4*>(ones);
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
     const int t = threadIdx.x - 64;  // 128 threads, one 16-byte chunk of a 2 KB extension each
-    for (int st = 0; st < kStages; ++st)
-      for (int pl = 0; pl < 2; ++pl) {
-        unsigned char* ext = base + Lay::kKVOff + st * Lay::kStageBytes + 2 * Lay::kKBytes +
-                             pl * Lay::kVBytes + DH * kBKV * 2;
-        reinterpret_cast<uint4*>(ext)[t] = (pl == 0 && t < 8) ? one4 : zero4;
-      }
+    for (int st = 0; st < kStages; ++st) {
+      unsigned char* ext = base + Lay::kKVOff + st * Lay::kStageBytes + 2 * Lay::kKBytes + 2 * Lay::kVTx;
+      reinterpret_cast<uint4*>(ext)[t] = t < 8 ? one4 : zero4;
+    }
     fence_proxy_async();
   }
   tc_fence_before();
@@ -304,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           tma_load_2d(sb, &mkh, &kv_full[st], 0, krow);
           tma_load_2d(sb + Lay::kKBytes, &mkl, &kv_full[st], 0, krow);
           tma_load_2d(sb + 2 * Lay::kKBytes, &mvh, &kv_full[st], j * kBKV, plane * DH);
-          tma_load_2d(sb + 2 * Lay::kKBytes + Lay::kVBytes, &mvl, &kv_full[st], j * kBKV, plane * DH);
+          tma_load_2d(sb + 2 * Lay::kKBytes + Lay::kVTx, &mvl, &kv_full[st], j * kBKV, plane * DH);
         }
       }
       // Drain: wait for the last loads issued into each ring slot and Q.
@@ -318,7 +338,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     // ---------------------------------------------------------------- MMA
     constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc_s = idesc_f16(kBQ, kBKV, kBf);
-    const uint32_t idesc_o = idesc_f16(kBQ, DH + Lay::kXRows, kBf);  // head_dim outputs (+ the row sum)
+    const uint32_t idesc_o = idesc_f16(kBQ, Lay::kVRows, kBf);  // P.Vh | P.Vl (| the row sum)
+    // bf16's Pl times Vh only, unless the row sum needs the ones row (then
+    // Pl.Vl, below fp32 rounding, rides along)
+    const uint32_t idesc_ol = idesc_f16(kBQ, row_sum_by_mma<DH>() ? Lay::kVRows : DH, kBf);
     long long kv_it = 0, s_it = 0, o_it = 0, n_done = 0;
     bool ok = true;
     const uint32_t q_addr = smem_u32(base + Lay::kQOff);
@@ -331,22 +354,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       if (lane == 0) {
         const int st = (int)(it_kv % kStages);
         const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
-        const uint32_t vh = sb + 2 * Lay::kKBytes, vl_ = vh + Lay::kVBytes;
+        const uint32_t vt = sb + 2 * Lay::kKBytes;  // rows: Vh^T, Vl^T (, extension)
         const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * 2 * Lay::kPBytes);
         const uint32_t pl_ = ph_ + Lay::kPBytes;
         const uint32_t d = tO + (uint32_t)(pb * Lay::kOCols);
-        // O = Ph.Vh + Ph.Vl (+ Pl.Vh with bf16) over 64 keys (4 steps of
-        // K = 16); with the extra rows, column DH = the sum of the P values
-        // used (the ones row of Vh)
-        const uint32_t as[3] = {ph_, ph_, pl_};
-        const uint32_t bs[3] = {vh, vl_, vh};
-        constexpr int kProducts = p_hi_only<T>() ? 2 : 3;
+        // O = Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
+        // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
+        // extension, column 2 DH = the sum of the P values used
 #pragma unroll
-        for (int t = 0; t < kProducts; ++t)
+        for (int k = 0; k < kBKV / 16; ++k)
+          mma_f16(d, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o, k != 0);
+        if constexpr (!p_hi_only<T>()) {
 #pragma unroll
           for (int k = 0; k < kBKV / 16; ++k)
-            mma_f16(d, sdesc_rows(as[t] + k * 32, 128), sdesc_rows(bs[t] + k * 32, 128), idesc_o,
-                    (t | k) != 0);
+            mma_f16(d, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
+        }
         mma_commit(&o_full[pb]);
         mma_commit(&p_empty[pb]);
         mma_commit(&kv_empty[st]);
@@ -457,25 +479,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const float mj = (jo & 1) ? m_hist1 : m_hist0;
         const float corr = exp2f(m_prev_o - mj);   // 0 on the first fold
         const uint32_t ta = tO + lane_addr + (uint32_t)(ob * Lay::kOCols);
+        // acc = acc corr + P.Vh + P.Vl, 16 columns of each half at a time
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 16) {
-          uint32_t rr[16];
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-              "%13,%14,%15}, [%16];"
-              : "=r"(rr[0]), "=r"(rr[1]), "=r"(rr[2]), "=r"(rr[3]), "=r"(rr[4]), "=r"(rr[5]),
-                "=r"(rr[6]), "=r"(rr[7]), "=r"(rr[8]), "=r"(rr[9]), "=r"(rr[10]), "=r"(rr[11]),
-                "=r"(rr[12]), "=r"(rr[13]), "=r"(rr[14]), "=r"(rr[15])
-              : "r"(ta + c0));
+          uint32_t rh[16], rl[16];
+          tmem_ld16(ta + c0, rh);
+          tmem_ld16(ta + DH + c0, rl);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(acc[c0 + c], corr, __uint_as_float(rr[c]));
+          for (int c = 0; c < 16; ++c)
+            acc[c0 + c] = fmaf(acc[c0 + c], corr, __uint_as_float(rh[c]) + __uint_as_float(rl[c]));
         }
-        if constexpr (row_sum_by_mma<DH>()) {  // the row sum of P_jo, column DH
-          uint32_t rl;
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rl) : "r"(ta + DH));
+        if constexpr (row_sum_by_mma<DH>()) {  // the row sum of P_jo, column 2 DH
+          uint32_t rs;
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs) : "r"(ta + 2 * DH));
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          l = fmaf(l, corr, __uint_as_float(rl));
+          l = fmaf(l, corr, __uint_as_float(rs));
         }
         m_prev_o = mj;
         tc_fence_before();
@@ -512,15 +531,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
             tmax = fmaxf(tmax, vs);
           }
         } else {
-          // no near tie possible for this row: the second-best score is not needed
+          // no near tie possible for this row: the second-best score is not
+          // needed, and the tile max takes one three-input max per two scores
+          if (needs_mask) {
+#pragma unroll
+            for (int c = 0; c < kBKV; ++c)
+              if (k0 + c >= limit) s[c] = -INFINITY;
+          }
           float traw = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kBKV; ++c) {
-            float v = s[c];
-            if (needs_mask && k0 + c >= limit) v = -INFINITY;
-            s[c] = v;
-            traw = fmaxf(traw, v);
-          }
+          for (int c = 0; c < kBKV; c += 2) traw = max3f(traw, s[c], s[c + 1]);
           tmax = traw * scale_log2;
         }
         const float mn = fmaxf(m, tmax);
