@@ -17,8 +17,9 @@
 //   warp 0     TMA: Q (once per work item) and K/V^T tiles of 64 keys into a
 //              3-deep ring
 //   warp 1     TMEM owner; one thread issues S = Q K^T into one of two TMEM
-//              score buffers, then O_j = P_j V_j into one of two TMEM output
-//              buffers once the softmax warps have written P_j.  At head_dim
+//              score buffers, then adds P_j V_j to the work item's O
+//              accumulator in TMEM once the softmax warps have written P_j
+//              (the item's first product overwrites it).  At head_dim
 //              16, where the softmax's instruction issue is the bound, each
 //              V^T tile carries 16 extra rows after its 2 x head_dim (hi, lo)
 //              rows (a row of ones, then zeros, written once at start; TMA
@@ -27,10 +28,15 @@
 //              probabilities itself; at larger heads the wider MMA costs more
 //              than it saves.
 //   warps 2-5  softmax: thread = query row.  Reads its 64 scores, masks,
-//              updates the running max, writes P_j as (hi, lo) into the
-//              swizzled shared-memory operand, and folds the previous tile's
-//              O_{j-1} and row sum into its fp32 register accumulators with
-//              the online-softmax correction.
+//              updates the running max and writes P_j = 2^(s - mr) (16-bit,
+//              hi and, with bf16, lo) into the swizzled shared-memory operand.
+//              The reference mr follows the running max lazily: only when the
+//              max passes it by more than 2^8 does the thread wait for the
+//              last product, scale its row of O (and the row sum) in TMEM by
+//              2^(mr_old - mr_new) and move mr.  So no key tile ends with a
+//              wait for P.V or a pass over O, the online-softmax correction is
+//              applied a few times per row, and the item's O is read once at
+//              its end.
 //
 // Split-K over keys ("KernelForge", section "What's next": partition the key
 // range and merge partial softmax states).  When few (plane, query tile)
@@ -90,6 +96,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// Store 16 consecutive TMEM columns of this warp's 32 lanes (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Multiply the first NCOLS columns of this warp's rows of the O accumulator
+// by the lane's factor, in place (warp-collective).
+template <int NCOLS>
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float corr) {
+  static_assert(NCOLS % 16 == 0, "whole 16-column loads");
+#pragma unroll
+  for (int c0 = 0; c0 < NCOLS; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(taddr + c0, v);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+    tmem_st16(taddr + c0, v);
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 2^x by the SFU's approximate base-2 exponential with subnormal results
 // flushed to zero (a probability below 2^-126 of the row maximum's weight is
 // below fp32 resolution of the row sum anyway); 2^-inf = 0.
@@ -135,6 +169,16 @@ __host__ __device__ constexpr bool p_hi_only() { return std::is_same<T, __half>:
 template <int DH>
 __host__ __device__ constexpr bool row_sum_by_mma() { return DH == 16; }
 
+// How far (log2 units) a row's maximum may pass the reference its
+// probabilities are taken against before O and the row sum are rescaled:
+// probabilities stay below 2^8, exact in either 16-bit type's range.
+constexpr float kLazy = 8.f;
+
+// Split-K partial state per row: output (head_dim), reference, second-best
+// score, row sum, |q|^2, best score.
+template <int DH>
+__host__ __device__ constexpr int kPartCols() { return DH + 5; }
+
 template <typename T, int DH>
 struct Layout {
   static constexpr int kQBytes = kBQ * DH * 2;      // one Q plane
@@ -146,12 +190,14 @@ struct Layout {
   static constexpr int kPBytes = kBQ * kBKV * 2;    // one P plane (16 KB)
   static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
   static constexpr int kStageTx = 2 * kKBytes + 2 * kVTx;  // TMA bytes per stage
-  static constexpr int kOCols = (kVRows + 31) / 32 * 32;  // TMEM columns per O buffer
+  static constexpr int kOUsed = kVRows;              // O columns the MMAs write
+  static constexpr int kOCols = (kVRows + 31) / 32 * 32;  // TMEM columns of the O accumulator
+  static constexpr int kPPlanes = p_hi_only<T>() ? 1 : 2;  // P planes: hi (, lo)
   static_assert(kVTx % 1024 == 0 && kStageBytes % 1024 == 0, "128-byte swizzle atoms stay aligned");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
   static constexpr int kPOff = kKVOff + kStages * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * 2 * kPBytes;
+  static constexpr int kBarOff = kPOff + 2 * kPPlanes * kPBytes;
   static constexpr int kBytes = kBarOff + 256;
   static constexpr int kRowBytes = DH * 2;          // Q/K rows: 32, 64, 128
 };
@@ -223,10 +269,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   uint64_t* s_full = kv_empty + kStages;   // [2]
   uint64_t* s_empty = s_full + 2;          // [2]
   uint64_t* p_full = s_empty + 2;          // [2]
-  uint64_t* p_empty = p_full + 2;          // [2]
-  uint64_t* o_full = p_empty + 2;          // [2]
-  uint64_t* o_empty = o_full + 2;          // [2]
-  uint64_t* mma_done = o_empty + 2;
+  uint64_t* p_empty = p_full + 2;          // [2]: P buffer free = its P.V complete
+  uint64_t* o_free = p_empty + 2;          // the item's O has been read
+  uint64_t* mma_done = o_free + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
@@ -235,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int nqt = (a.L + kBQ - 1) / kBQ;
   const int n_items = a.kc ? a.n_items : planes * nqt;
   const int kc = a.kc;
-  // S: 2 x 64 columns, O: 2 x kOCols (P.Vh, P.Vl and the row sum)
-  constexpr uint32_t kTmemCols = 2 * kBKV + 2 * Lay::kOCols <= 256 ? 256 : 512;
+  // S: 2 x 64 columns, O: kOCols (P.Vh, P.Vl and the row sum)
+  constexpr uint32_t kTmemCols = 2 * kBKV + Lay::kOCols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -250,9 +295,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       mbar_init(&s_empty[s], 128);
       mbar_init(&p_full[s], 128);
       mbar_init(&p_empty[s], 1);
-      mbar_init(&o_full[s], 1);
-      mbar_init(&o_empty[s], 128);
     }
+    mbar_init(o_free, 128);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -345,31 +389,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     long long kv_it = 0, s_it = 0, o_it = 0, n_done = 0;
     bool ok = true;
     const uint32_t q_addr = smem_u32(base + Lay::kQOff);
-    auto issue_pv = [&](long long it_kv, long long it_o) -> bool {
+    // P_{it_o}.V into the O accumulator; the item's first product overwrites
+    // it, once the softmax has read the previous item's O.
+    auto issue_pv = [&](long long it_kv, long long it_o, bool first) -> bool {
       const int pb = (int)(it_o & 1);
-      const uint32_t ph = (uint32_t)((it_o >> 1) & 1);
-      if (!mbar_wait(&p_full[pb], ph, abort, a.status)) return false;
-      if (!mbar_wait(&o_empty[pb], ph ^ 1, abort, a.status)) return false;
+      if (!mbar_wait(&p_full[pb], (uint32_t)((it_o >> 1) & 1), abort, a.status)) return false;
+      if (first && n_done > 1 && !mbar_wait(o_free, (uint32_t)((n_done - 2) & 1), abort, a.status))
+        return false;
       tc_fence_after();
       if (lane == 0) {
         const int st = (int)(it_kv % kStages);
         const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
         const uint32_t vt = sb + 2 * Lay::kKBytes;  // rows: Vh^T, Vl^T (, extension)
-        const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * 2 * Lay::kPBytes);
+        const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes);
         const uint32_t pl_ = ph_ + Lay::kPBytes;
-        const uint32_t d = tO + (uint32_t)(pb * Lay::kOCols);
-        // O = Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
+        // O += Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
         // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
         // extension, column 2 DH = the sum of the P values used
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k)
-          mma_f16(d, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o, k != 0);
+          mma_f16(tO, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o,
+                  !first || k != 0);
         if constexpr (!p_hi_only<T>()) {
 #pragma unroll
           for (int k = 0; k < kBKV / 16; ++k)
-            mma_f16(d, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
+            mma_f16(tO, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
         }
-        mma_commit(&o_full[pb]);
         mma_commit(&p_empty[pb]);
         mma_commit(&kv_empty[st]);
       }
@@ -412,12 +457,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         __syncwarp();
         ++s_it;
         if (j > 0) {
-          if (!issue_pv(kv_it + j - 1, o_it)) { ok = false; break; }
+          if (!issue_pv(kv_it + j - 1, o_it, j == 1)) { ok = false; break; }
           ++o_it;
         }
       }
       if (!ok) break;
-      if (!issue_pv(kv_it + nkt - 1, o_it)) { ok = false; break; }
+      if (!issue_pv(kv_it + nkt - 1, o_it, nkt == 1)) { ok = false; break; }
       ++o_it;
       kv_it += nkt;
     }
@@ -429,10 +474,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // row of the query tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    const uint32_t to = tO + lane_addr;  // this warp's rows of the O accumulator
     T* const ctx_hi = reinterpret_cast<T*>(a.ctx_hi);
     T* const ctx_lo = reinterpret_cast<T*>(a.ctx_lo);
     const float scale_log2 = rsqrtf((float)DH) * 1.4426950408889634f;
-    long long s_it = 0, o_it = 0, n_done = 0;
+    long long s_it = 0, n_done = 0;
     bool ok = true;
     ItemCursor cur;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -443,11 +489,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       const int i = qt * kBQ + r;                    // query position in the sequence
       const int limit = min(i + 1, vl);              // keys [0, limit) visible
       const int full_keys = min(qt * kBQ + 1, vl);   // keys every row of the tile sees
-      float acc[DH];
-#pragma unroll
-      for (int c = 0; c < DH; ++c) acc[c] = 0.f;
-      float m = -INFINITY, m2 = -INFINITY, l = 0.f, m_prev_o = -INFINITY;
-      float m_hist0 = -INFINITY, m_hist1 = -INFINITY;  // running max after tile j (by parity)
+      // m, m2: the row's best and second-best score so far (log2 units);
+      // mr: the reference the probabilities are taken against.  mr follows
+      // m lazily, only when m passes it by more than kLazy, so O (in TMEM)
+      // and the row sum are rescaled a few times per row instead of after
+      // every key tile; probabilities stay below 2^kLazy.
+      float m = -INFINITY, m2 = -INFINITY, mr = -INFINITY, l = 0.f;
       // |q_i| for the near-tie test, from the (hi, lo) Q tile in shared memory.
       float qn2 = 0.f;
       if (!has_keys) {
@@ -470,48 +517,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       // The second-best score matters only where fp32 scores can be off.
       const float kmax_plane = __int_as_float(a.kmax[plane]);
       bool track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
-      // Fold O_{jo} (computed against the running max after tile jo) into acc.
-      auto fold_o = [&](int jo) -> bool {
-        const int ob = (int)(o_it & 1);
-        const uint32_t ph = (uint32_t)((o_it >> 1) & 1);
-        if (!mbar_wait(&o_full[ob], ph, abort, a.status)) return false;
-        tc_fence_after();
-        const float mj = (jo & 1) ? m_hist1 : m_hist0;
-        const float corr = exp2f(m_prev_o - mj);   // 0 on the first fold
-        const uint32_t ta = tO + lane_addr + (uint32_t)(ob * Lay::kOCols);
-        // acc = acc corr + P.Vh + P.Vl, 16 columns of each half at a time
-#pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 16) {
-          uint32_t rh[16], rl[16];
-          tmem_ld16(ta + c0, rh);
-          tmem_ld16(ta + DH + c0, rl);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            acc[c0 + c] = fmaf(acc[c0 + c], corr, __uint_as_float(rh[c]) + __uint_as_float(rl[c]));
-        }
-        if constexpr (row_sum_by_mma<DH>()) {  // the row sum of P_jo, column 2 DH
-          uint32_t rs;
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs) : "r"(ta + 2 * DH));
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          l = fmaf(l, corr, __uint_as_float(rs));
-        }
-        m_prev_o = mj;
-        tc_fence_before();
-        mbar_arrive(&o_empty[ob]);
-        ++o_it;
-        return true;
-      };
       for (int j = j0; j < j1 && ok; ++j) {
-        const int sbuf = (int)(s_it & 1);
-        if (!mbar_wait(&s_full[sbuf], (uint32_t)((s_it >> 1) & 1), abort, a.status)) { ok = false; break; }
+        const long long it = s_it++;  // this CTA's key tile count
+        const int sbuf = (int)(it & 1);
+        if (!mbar_wait(&s_full[sbuf], (uint32_t)((it >> 1) & 1), abort, a.status)) { ok = false; break; }
         tc_fence_after();
         float s[kBKV];
         tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV), *reinterpret_cast<float(*)[32]>(&s[0]));
         tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV + 32), *reinterpret_cast<float(*)[32]>(&s[32]));
         tc_fence_before();
         mbar_arrive(&s_empty[sbuf]);
-        ++s_it;
         const int k0 = j * kBKV;
         const bool needs_mask = k0 + kBKV > full_keys;
         // s stays unscaled (masked keys -inf); the running max m, the
@@ -543,17 +558,36 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           for (int c = 0; c < kBKV; c += 2) traw = max3f(traw, s[c], s[c + 1]);
           tmax = traw * scale_log2;
         }
-        const float mn = fmaxf(m, tmax);
-        // A row with no visible key in this tile keeps its max; its
+        m = fmaxf(m, tmax);
+        // A row with no visible key so far keeps mr = -inf; its
         // probabilities are exactly 0 below.
-        const float mref = mn == -INFINITY ? 0.f : mn;
-        if constexpr (!row_sum_by_mma<DH>()) l *= exp2f(m - mref);
-        m = mn;
-        if (j & 1) m_hist1 = mref; else m_hist0 = mref;
-        // P_j into the (hi, lo) swizzled operand buffer.
-        const int pb = (int)((s_it - 1) & 1);
-        if (!mbar_wait(&p_empty[pb], (uint32_t)((((s_it - 1) >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
-        unsigned char* ph = base + Lay::kPOff + pb * 2 * Lay::kPBytes;
+        float corr = 1.f;
+        bool resc = false;
+        if (m > mr + kLazy) {
+          if (mr != -INFINITY) {
+            corr = exp2f(mr - m);
+            resc = true;
+          }
+          mr = m;
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds the products up to key tile it-1 against the old
+          // references: wait for the last of them, then scale this warp's
+          // rows in place (corr = 1 for rows that keep their reference).
+          if (!mbar_wait(&p_empty[(it - 1) & 1], (uint32_t)(((it - 1) >> 1) & 1), abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          rescale_o<Lay::kOUsed>(to, corr);
+          if constexpr (!row_sum_by_mma<DH>()) l *= corr;
+        }
+        const float mref = mr == -INFINITY ? 0.f : mr;
+        // P_it into the (hi, lo) swizzled operand buffer, once P.V_{it-2}
+        // has released it.
+        const int pb = sbuf;
+        if (!mbar_wait(&p_empty[pb], (uint32_t)(((it >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
+        unsigned char* ph = base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes;
         unsigned char* pl = ph + Lay::kPBytes;
 #pragma unroll
         for (int c8 = 0; c8 < kBKV / 8; ++c8) {
@@ -576,22 +610,49 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           }
         }
         fence_proxy_async();
+        tc_fence_before();  // orders a rescale's TMEM stores before P.V_it
         mbar_arrive(&p_full[pb]);
-        if (j > j0 && !fold_o(j - 1)) { ok = false; break; }
       }
       if (!ok) break;
-      if (has_keys && !fold_o(j1 - 1)) { ok = false; break; }
+      // The item's output (unnormalised, against mr) and row sum, once its
+      // last product is complete; then O is free for the next item.
+      float acc[DH];
+#pragma unroll
+      for (int c = 0; c < DH; ++c) acc[c] = 0.f;
+      if (has_keys) {
+        const long long last = s_it - 1;
+        if (!mbar_wait(&p_empty[last & 1], (uint32_t)((last >> 1) & 1), abort, a.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t rh[16], rl[16];
+          tmem_ld16(to + c0, rh);
+          tmem_ld16(to + DH + c0, rl);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int c = 0; c < 16; ++c) acc[c0 + c] = __uint_as_float(rh[c]) + __uint_as_float(rl[c]);
+        }
+        if constexpr (row_sum_by_mma<DH>()) {  // the row sum, column 2 DH
+          uint32_t rs;
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs) : "r"(to + 2 * DH));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          l = __uint_as_float(rs);
+        }
+        tc_fence_before();
+        mbar_arrive(o_free);
+      }
       if (nch > 1) {
         // ---- split-K: publish this chunk's partial state, count the chunk
         // in, and merge the tile if it is the last to arrive.
-        const int cols = DH + 4;
+        const int cols = kPartCols<DH>();
         float* mine = a.part + (size_t)w * kBQ * cols + r;  // column-major: [col][row]
 #pragma unroll
         for (int e = 0; e < DH; ++e) mine[(size_t)e * kBQ] = acc[e];
-        mine[(size_t)DH * kBQ] = m;
+        mine[(size_t)DH * kBQ] = mr;  // the reference acc and l are taken against
         mine[(size_t)(DH + 1) * kBQ] = m2;
         mine[(size_t)(DH + 2) * kBQ] = l;
         mine[(size_t)(DH + 3) * kBQ] = has_keys ? qn2 : -1.f;
+        mine[(size_t)(DH + 4) * kBQ] = m;
         // Each warp counts its own 32 rows in (no barrier across warps, so
         // no wait that could outlive a failed peer): the last warp of the
         // tile's chunks to arrive for these rows merges them.
@@ -604,19 +665,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         __threadfence();
         // The tile's items are numbered first_w + c * planes (chunk-major).
         const int first_w = w - cidx * planes;
-        float mmax = m, top1 = m, top2 = m2;
+        float mmax = mr, top1 = m, top2 = m2;
         for (int c2 = 0; c2 < nch; ++c2) {
           if (c2 == cidx) continue;
           const float* o = a.part + (size_t)(first_w + c2 * planes) * kBQ * cols + r;
-          const float mc = __ldcg(o + (size_t)DH * kBQ), m2c = __ldcg(o + (size_t)(DH + 1) * kBQ);
+          const float mc = __ldcg(o + (size_t)(DH + 4) * kBQ), m2c = __ldcg(o + (size_t)(DH + 1) * kBQ);
           const float qc = __ldcg(o + (size_t)(DH + 3) * kBQ);
-          mmax = fmaxf(mmax, mc);
+          mmax = fmaxf(mmax, __ldcg(o + (size_t)DH * kBQ));
           if (qc >= 0.f) qn2 = qc;  // |q|^2 from any chunk that loaded Q
           // top two of the union of the chunks' (best, second best)
           if (mc > top1) { top2 = fmaxf(top1, m2c); top1 = mc; }
           else top2 = fmaxf(top2, mc);
         }
-        // Every row sees key 0, which lies in chunk 0, so mmax is finite.
+        // Every row sees key 0, which lies in chunk 0, so mmax (the largest
+        // reference) is finite.
         // The chunks are summed in chunk order whichever warp merges, so
         // the result does not depend on which chunk finished last.
         float own[DH];
@@ -628,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         float lsum = 0.f;
         for (int c2 = 0; c2 < nch; ++c2) {
           if (c2 == cidx) {
-            const float wc = exp2f(m - mmax);
+            const float wc = exp2f(mr - mmax);
             lsum = fmaf(wc, l, lsum);
 #pragma unroll
             for (int e = 0; e < DH; ++e) acc[e] = fmaf(wc, own[e], acc[e]);
@@ -741,7 +803,7 @@ TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, in
   if (n > (1LL << 30)) return TcAttnSplit{};
   p.kc = kc;
   p.n_items = (int)n;
-  p.part_bytes = (size_t)n * kBQ * (dh + 4) * sizeof(float);
+  p.part_bytes = (size_t)n * kBQ * (dh + 5) * sizeof(float);
   p.cnt_bytes = (size_t)planes * nqt * 4 * sizeof(int);
   return p;
 }
