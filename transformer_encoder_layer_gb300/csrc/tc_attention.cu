@@ -70,7 +70,12 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 192;
-constexpr int kBQ = 128, kBKV = 64, kStages = 3;
+// Query rows and keys per tile; the MMA thread issues P.V of key tile
+// j - kPvLag after S of tile j, into kPvLag + 1 TMEM score buffers.  (A lag
+// of 2 keeps the next scores further ahead of the softmax but releases P
+// buffers later; with the MMA thread's issue the busiest role, a lag of 1
+// measured faster.)
+constexpr int kBQ = 128, kBKV = 64, kPvLag = 1, kSBufs = kPvLag + 1;
 
 // CTAs per SM: head_dim 16 fits two (about 97 KB of shared memory and 256
 // TMEM columns each), which doubles the softmax warps per SM sub-partition,
@@ -196,6 +201,12 @@ struct Layout {
   static_assert(kVTx % 1024 == 0 && kStageBytes % 1024 == 0, "128-byte swizzle atoms stay aligned");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
+  // K/V ring depth: what the shared memory left per CTA holds, up to 6
+  // (the TMA runs further ahead of the MMAs; K/V come from L2).
+  static constexpr int kFixedBytes = kKVOff + 2 * kPPlanes * kPBytes + 256;
+  static constexpr int kStages =
+      std::min(6, (232448 / ctas_per_sm<DH>() - 1024 - kFixedBytes) / kStageBytes);
+  static_assert(kStages >= 4, "K/V ring");
   static constexpr int kPOff = kKVOff + kStages * kStageBytes;
   static constexpr int kBarOff = kPOff + 2 * kPPlanes * kPBytes;
   static constexpr int kBytes = kBarOff + 256;
@@ -258,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
                         const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
                         const TcAttnArgs a) {
   using Lay = Layout<T, DH>;
+  constexpr int kStages = Lay::kStages;
   extern __shared__ __align__(1024) unsigned char dyn_smem[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -266,9 +278,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   uint64_t* q_empty = bars + 1;
   uint64_t* kv_full = bars + 2;            // [kStages]
   uint64_t* kv_empty = kv_full + kStages;  // [kStages]
-  uint64_t* s_full = kv_empty + kStages;   // [2]
-  uint64_t* s_empty = s_full + 2;          // [2]
-  uint64_t* p_full = s_empty + 2;          // [2]
+  uint64_t* s_full = kv_empty + kStages;   // [kSBufs]
+  uint64_t* s_empty = s_full + kSBufs;     // [kSBufs]
+  uint64_t* p_full = s_empty + kSBufs;     // [2]
   uint64_t* p_empty = p_full + 2;          // [2]: P buffer free = its P.V complete
   uint64_t* o_free = p_empty + 2;          // the item's O has been read
   uint64_t* mma_done = o_free + 1;
@@ -280,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int nqt = (a.L + kBQ - 1) / kBQ;
   const int n_items = a.kc ? a.n_items : planes * nqt;
   const int kc = a.kc;
-  // S: 2 x 64 columns, O: kOCols (P.Vh, P.Vl and the row sum)
-  constexpr uint32_t kTmemCols = 2 * kBKV + Lay::kOCols <= 256 ? 256 : 512;
+  // S: kSBufs x 64 columns, O: kOCols (P.Vh, P.Vl and the row sum)
+  constexpr uint32_t kTmemCols = kSBufs * kBKV + Lay::kOCols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -290,9 +302,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBufs; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], 128);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&p_full[s], 128);
       mbar_init(&p_empty[s], 1);
     }
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   volatile int* abort = abort_flag;
-  const uint32_t tS = tmem, tO = tmem + 2 * kBKV;
+  const uint32_t tS = tmem, tO = tmem + kSBufs * kBKV;
 
   auto key_tiles = [&](int plane, int qt, int& vl) {
     vl = a.valid_len[plane / a.H];
@@ -397,27 +411,26 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       if (first && n_done > 1 && !mbar_wait(o_free, (uint32_t)((n_done - 2) & 1), abort, a.status))
         return false;
       tc_fence_after();
-      if (lane == 0) {
-        const int st = (int)(it_kv % kStages);
-        const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
-        const uint32_t vt = sb + 2 * Lay::kKBytes;  // rows: Vh^T, Vl^T (, extension)
-        const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes);
-        const uint32_t pl_ = ph_ + Lay::kPBytes;
-        // O += Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
-        // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
-        // extension, column 2 DH = the sum of the P values used
+      // The whole warp builds the (uniform) descriptors; one elected lane issues.
+      const int st = (int)(it_kv % kStages);
+      const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
+      const uint32_t vt = sb + 2 * Lay::kKBytes;  // rows: Vh^T, Vl^T (, extension)
+      const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes);
+      const uint32_t pl_ = ph_ + Lay::kPBytes;
+      // O += Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
+      // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
+      // extension, column 2 DH = the sum of the P values used
+#pragma unroll
+      for (int k = 0; k < kBKV / 16; ++k)
+        mma_f16_elect(tO, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o,
+                      !first || k != 0);
+      if constexpr (!p_hi_only<T>()) {
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k)
-          mma_f16(tO, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o,
-                  !first || k != 0);
-        if constexpr (!p_hi_only<T>()) {
-#pragma unroll
-          for (int k = 0; k < kBKV / 16; ++k)
-            mma_f16(tO, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
-        }
-        mma_commit(&p_empty[pb]);
-        mma_commit(&kv_empty[st]);
+          mma_f16_elect(tO, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
       }
+      mma_commit_elect(&p_empty[pb]);
+      mma_commit_elect(&kv_empty[st]);
       __syncwarp();
       return true;
     };
@@ -435,10 +448,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const long long it = kv_it + j;
         const int st = (int)(it % kStages);
         if (!mbar_wait(&kv_full[st], (uint32_t)((it / kStages) & 1), abort, a.status)) { ok = false; break; }
-        const int sbuf = (int)(s_it & 1);
-        if (!mbar_wait(&s_empty[sbuf], (uint32_t)(((s_it >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
+        const int sbuf = (int)(s_it % kSBufs);
+        if (!mbar_wait(&s_empty[sbuf], (uint32_t)(((s_it / kSBufs) & 1) ^ 1), abort, a.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (lane == 0) {
+        {
           const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
           const uint32_t kh = sb, kl = sb + Lay::kKBytes;
           const uint32_t qh = q_addr, ql = q_addr + Lay::kQBytes;
@@ -449,24 +465,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           for (int t = 0; t < 3; ++t)
 #pragma unroll
             for (int k = 0; k < DH / 16; ++k)
-              mma_f16(d, sdesc_rows(as[t] + k * 32, Lay::kRowBytes),
-                      sdesc_rows(bs[t] + k * 32, Lay::kRowBytes), idesc_s, (t | k) != 0);
-          mma_commit(&s_full[sbuf]);
-          if (j == nkt - 1) mma_commit(q_empty);  // Q no longer read
+              mma_f16_elect(d, sdesc_rows(as[t] + k * 32, Lay::kRowBytes),
+                            sdesc_rows(bs[t] + k * 32, Lay::kRowBytes), idesc_s, (t | k) != 0);
+          mma_commit_elect(&s_full[sbuf]);
+          if (j == nkt - 1) mma_commit_elect(q_empty);  // Q no longer read
         }
         __syncwarp();
         ++s_it;
-        if (j > 0) {
-          if (!issue_pv(kv_it + j - 1, o_it, j == 1)) { ok = false; break; }
+        if (j >= kPvLag) {
+          if (!issue_pv(kv_it + j - kPvLag, o_it, j == kPvLag)) { ok = false; break; }
           ++o_it;
         }
       }
       if (!ok) break;
-      if (!issue_pv(kv_it + nkt - 1, o_it, nkt == 1)) { ok = false; break; }
-      ++o_it;
+      for (int j = nkt >= kPvLag ? nkt - kPvLag : 0; j < nkt && ok; ++j) {
+        if (!issue_pv(kv_it + j, o_it, j == 0)) { ok = false; break; }
+        ++o_it;
+      }
+      if (!ok) break;
       kv_it += nkt;
     }
-    if (lane == 0) mma_commit(mma_done);
+    mma_commit_elect(mma_done);
     __syncwarp();
     mbar_wait_bounded(mma_done, 0, a.status);
   } else {
@@ -519,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       bool track = neartie_err(sqrtf(qn2), kmax_plane, DH) > kTieErrMin;
       for (int j = j0; j < j1 && ok; ++j) {
         const long long it = s_it++;  // this CTA's key tile count
-        const int sbuf = (int)(it & 1);
-        if (!mbar_wait(&s_full[sbuf], (uint32_t)((it >> 1) & 1), abort, a.status)) { ok = false; break; }
+        const int sbuf = (int)(it % kSBufs);
+        if (!mbar_wait(&s_full[sbuf], (uint32_t)((it / kSBufs) & 1), abort, a.status)) { ok = false; break; }
         tc_fence_after();
         float s[kBKV];
         tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV), *reinterpret_cast<float(*)[32]>(&s[0]));
@@ -585,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const float mref = mr == -INFINITY ? 0.f : mr;
         // P_it into the (hi, lo) swizzled operand buffer, once P.V_{it-2}
         // has released it.
-        const int pb = sbuf;
+        const int pb = (int)(it & 1);
         if (!mbar_wait(&p_empty[pb], (uint32_t)(((it >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
         unsigned char* ph = base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes;
         unsigned char* pl = ph + Lay::kPBytes;

@@ -248,6 +248,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// mma_f16 from a converged warp: every lane passes the same (warp-uniform)
+// operands and one elected lane issues.  Keeping the issuing warp converged
+// lets the descriptors live in uniform registers.
+__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Pair MMA (issued by the pair's leader CTA only): M = 256 rows, the first
 // 128 of A from this CTA's shared memory and the other 128 from the peer's
 // at the same offset; B's N rows likewise split in halves between the two
@@ -274,6 +286,16 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar_cluster) {
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// mma_commit from a converged warp: the lane elect.sync picks (the same one
+// that issued the MMAs through mma_f16_elect) commits.
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
           smem_u32(bar))
       : "memory");
 }
