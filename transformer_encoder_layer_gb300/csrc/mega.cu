@@ -212,12 +212,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // D (+)= A . B^T with A read from tensor memory (128 lanes = rows, K packed
-// two 16-bit elements per 32-bit column) and B from a shared-memory descriptor.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
+// two 16-bit elements per 32-bit column) and B from a shared-memory
+// descriptor, issued from a converged warp: warp-uniform operands, one
+// elected lane issues (as mma_f16_elect).
+__device__ __forceinline__ void mma_f16_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -494,16 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
       par ^= 1u << st;
       tc_fence_after();
-      if (lane == 0) {
+      // the whole warp builds the (uniform) descriptors; one elected lane issues
+      {
         const uint32_t w = smem_u32(sm + wslot_off(st));
         const int parts = part_stride == 0 ? 1 : 2;
         for (int p = 0; p < parts; ++p) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(d, sdesc_sw128(a_base + p * part_stride + k * 32), sdesc_sw128(w + k * 32), idesc,
-                    (first && p == 0 && k == 0) ? 0u : 1u);
+            mma_f16_elect(d, sdesc_sw128(a_base + p * part_stride + k * 32), sdesc_sw128(w + k * 32),
+                          idesc, (first && p == 0 && k == 0) ? 0u : 1u);
         }
-        mma_commit(bar + B_W_EMPTY + st);
+        mma_commit_elect(bar + B_W_EMPTY + st);
       }
       __syncwarp();
       return true;
@@ -516,21 +519,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
       par ^= 1u << st;
       tc_fence_after();
-      if (lane == 0) {
+      {
         const uint32_t w = smem_u32(sm + wslot_off(st));
         for (int p = 0; p < parts; ++p) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16_ta(d, tmem + a_col + p * part_cols + 8 * k, sdesc_sw128(w + k * 32), idesc,
-                       (first && p == 0 && k == 0) ? 0u : 1u);
+            mma_f16_ta_elect(d, tmem + a_col + p * part_cols + 8 * k, sdesc_sw128(w + k * 32), idesc,
+                             (first && p == 0 && k == 0) ? 0u : 1u);
         }
-        mma_commit(bar + B_W_EMPTY + st);
+        mma_commit_elect(bar + B_W_EMPTY + st);
       }
       __syncwarp();
       return true;
     };
     auto commit = [&](int b) {
-      if (lane == 0) mma_commit(bar + b);
+      mma_commit_elect(bar + b);
       __syncwarp();
     };
     auto wait = [&](int b, long long& n, bool is_free = false) -> bool {
@@ -565,15 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Release what the compute threads wrote before QKVH_READY (norms,
           // the tile's max |k|) to whoever acquires S_DONE.
           if (lane == 0) mbar_arrive(bar + B_S_DONE);
-          if (lane == 0) {
+          __syncwarp();
+          {
             const uint32_t as[3] = {qb, qb, qb + 8192};
             const uint32_t bs[3] = {kb, kb + 8192, kb};
 #pragma unroll
             for (int c = 0; c < 3; ++c)
 #pragma unroll
               for (int k = 0; k < 2; ++k)
-                mma_f16(tmem + 384, desc_sw64(as[c] + k * 32), desc_sw64(bs[c] + k * 32), id128,
-                        (c | k) != 0);
+                mma_f16_elect(tmem + 384, desc_sw64(as[c] + k * 32), desc_sw64(bs[c] + k * 32), id128,
+                              (c | k) != 0);
           }
           commit(B_S_DONE);
           return true;
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (h + 1 < h1 && !(ok = issue_s(h + 1))) break;
           ok = wait(B_P_READY, c_p);
           if (!ok) break;
-          if (lane == 0) {
+          {
             // O_h = Ph.Vh + Ph.Vl (+ Pl.Vh with bf16) over the row's own 64
             // keys (4 steps): B holds both sequences' V side by side (N = 64),
             // so row r's result is in columns [96h + 32 s, +32) of its sequence s.
@@ -595,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kProducts; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f16(tmem + 96 * h, sdesc_sw128(as[c] + k * 32), sdesc_sw128(bs[c] + k * 32), id64,
-                        (c | k) != 0);
+                mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c] + k * 32), sdesc_sw128(bs[c] + k * 32),
+                              id64, (c | k) != 0);
           }
           commit(B_O_DONE);
         }

@@ -273,6 +273,22 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, ui
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// mma_f16_pair / mma_commit_pair from a converged warp (one elected lane).
+__device__ __forceinline__ void mma_f16_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar_cluster) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          bar_cluster)
+      : "memory");
+}
 // Arrive once on the mbarrier at shared::cluster address `bar_cluster` (this
 // CTA's or the peer's) when every pair MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar_cluster) {

@@ -326,12 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       // commit to this CTA's barrier and, for a pair, to the peer's copy
+      // (the whole warp takes part; one elected lane issues, as for the MMAs)
       auto commit_both = [&](uint64_t* bar) {
         if constexpr (PAIR) {
-          mma_commit_pair(smem_u32(bar));
-          mma_commit_pair(map_to_rank(smem_u32(bar), 1));
+          mma_commit_pair_elect(smem_u32(bar));
+          mma_commit_pair_elect(map_to_rank(smem_u32(bar), 1));
         } else {
-          mma_commit(bar);
+          mma_commit_elect(bar);
         }
       };
       for (int u = TL_UNIT0; u < n_units && ok; u += TL_USTEP) {
@@ -342,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < k_blocks; ++kb) {
             if (!mbar_wait(&sm.full[stage], phase, abort, a.status)) { ok = false; break; }
             tc_fence_after();
-            if (lane == 0) {
+            {
+              // warp-uniform descriptors; one elected lane issues
               unsigned char* st = base + (size_t)stage * stage_bytes;
               const uint32_t w_addr = smem_u32(st + a.n_parts * kATileBytes);
               for (int p = 0; p < a.n_parts; ++p) {
@@ -350,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k16 = 0; k16 < kBK / 16; ++k16) {
                   if constexpr (PAIR)
-                    mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
-                                 a.idesc, (kb | p | k16) != 0);
+                    mma_f16_pair_elect(d_tmem, sdesc_sw128(a_addr + k16 * 32),
+                                       sdesc_sw128(w_addr + k16 * 32), a.idesc, (kb | p | k16) != 0);
                   else
-                    mma_f16(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
-                            a.idesc, (kb | p | k16) != 0);
+                    mma_f16_elect(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
+                                  a.idesc, (kb | p | k16) != 0);
                 }
               }
               commit_both(&sm.empty[stage]);
@@ -362,17 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (++stage == a.stages) { stage = 0; phase ^= 1; }
           }
-          if (lane == 0) commit_both(&sm.acc_full[acc]);
+          commit_both(&sm.acc_full[acc]);
           __syncwarp();
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1;
         }
       }
       // All issued MMAs complete before TMEM is released.
-      if (lane == 0) {
-        if constexpr (PAIR) mma_commit_pair(smem_u32(sm.mma_done));
-        else mma_commit(sm.mma_done);
-      }
+      if constexpr (PAIR) mma_commit_pair_elect(smem_u32(sm.mma_done));
+      else mma_commit_elect(sm.mma_done);
       __syncwarp();
       mbar_wait_bounded(sm.mma_done, 0, a.status);
     }
