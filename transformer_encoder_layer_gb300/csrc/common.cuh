@@ -96,6 +96,36 @@ __device__ __forceinline__ float gelu_erf(float u) {
   return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
 }
 
+// ------------------------------------------------ paired fp32 arithmetic
+// Two fp32 values in one 64-bit register for sm_100+'s paired fp32
+// instructions (fma/mul/add .f32x2): each lane is rounded exactly as the
+// scalar instruction rounds it, so a paired evaluation gives the scalar
+// results bit for bit in half the instructions.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t splat2(float a) { return pk2(a, a); }
+
 // GELU with a branch-free erf: Abramowitz & Stegun, Handbook of
 // Mathematical Functions (1964), formula 7.1.28 (after Hastings):
 //   erf(x) = 1 - (1 + a1 x + a2 x^2 + ... + a6 x^6)^-16,  x >= 0,  |error| <= 3e-7.
@@ -104,23 +134,34 @@ __device__ __forceinline__ float gelu_erf(float u) {
 // amplifies the polynomial's rounding 16-fold, so the GELU error is at most
 // 0.5 |u| (3e-7 + 2.5e-6 r) + 2e-7 |gelu(u)| (r <= 1).  Every lane runs the same
 // instructions (one reciprocal, no exponential), which keeps long unrolled
-// epilogue loops free of divergent branches.  Its agreement with the erff
-// form is checked on the GPU over a dense grid (tl_eval_gelu).
-__device__ __forceinline__ float gelu_as7128(float u) {
-  const float x = fabsf(u) * 0.70710678118654752f;
-  float t = fmaf(x, 0.0000430638f, 0.0002765672f);
-  t = fmaf(x, t, 0.0001520143f);
-  t = fmaf(x, t, 0.0092705272f);
-  t = fmaf(x, t, 0.0422820123f);
-  t = fmaf(x, t, 0.0705230784f);
-  t = fmaf(x, t, 1.0f);
-  t = t * t;  // ^2
-  t = t * t;  // ^4
-  t = t * t;  // ^8
-  t = t * t;  // ^16
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
-  return u >= 0.f ? fmaf(-0.5f * u, r, u) : 0.5f * u * r;
+// epilogue loops free of divergent branches.  Two values at a time, on the
+// paired fp32 instructions: every operation is the scalar one, rounded the
+// same way.  Its agreement with the erff form is checked on the GPU over a
+// dense grid (tl_eval_gelu).
+__device__ __forceinline__ void gelu_as7128_x2(float& u0, float& u1) {
+  const uint64_t u = pk2(u0, u1);
+  const uint64_t x = mul2(pk2(fabsf(u0), fabsf(u1)), splat2(0.70710678118654752f));
+  uint64_t t = fma2(x, splat2(0.0000430638f), splat2(0.0002765672f));
+  t = fma2(x, t, splat2(0.0001520143f));
+  t = fma2(x, t, splat2(0.0092705272f));
+  t = fma2(x, t, splat2(0.0422820123f));
+  t = fma2(x, t, splat2(0.0705230784f));
+  t = fma2(x, t, splat2(1.0f));
+  t = mul2(t, t);  // ^2
+  t = mul2(t, t);  // ^4
+  t = mul2(t, t);  // ^8
+  t = mul2(t, t);  // ^16
+  float t0, t1, r0, r1;
+  upk2(t, t0, t1);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(t0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(t1));
+  const uint64_t m = mul2(u, splat2(-0.5f));  // exact
+  const uint64_t r = pk2(r0, r1);
+  float a0, a1, b0, b1;
+  upk2(fma2(m, r, u), a0, a1);  // u - 0.5 u r = 0.5 u (1 + erf), u >= 0
+  upk2(mul2(m, r), b0, b1);     // -0.5 u r; its negation is 0.5 u (1 + erf), u < 0
+  u0 = u0 >= 0.f ? a0 : -b0;
+  u1 = u1 >= 0.f ? a1 : -b1;
 }
 
 }  // namespace tl

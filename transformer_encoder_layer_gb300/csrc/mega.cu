@@ -120,7 +120,8 @@ constexpr int kMisc = kWR + kNW * kTile16;
 // misc (floats unless noted)
 constexpr int kQn2 = kMisc;                           // [2 head parity][2 group][128] partial |q_r|^2
 constexpr int kEx = kQn2 + 2 * 2 * 128 * 4;           // [2][4 group][128] exchange: (m1, m2) or (mean, M2)
-constexpr int kLs = kEx + 2 * 4 * 128 * 4;            // [4 head][4 group][128] partial softmax sums
+constexpr int kLs = kEx + 2 * 4 * 128 * 4;            // [4 head][4 group][128] partial softmax sums;
+                                                      // from the out-projection on: b_o, ln1 g, b, b_2, ln2 g, b
 constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max partial |k|^2 (float bits)
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
@@ -498,13 +499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the whole warp builds the (uniform) descriptors; one elected lane issues
       {
-        const uint32_t w = smem_u32(sm + wslot_off(st));
+        // descriptors built once; a k16 step or a part moves the start
+        // address field (bytes / 16), which no smem address overflows
+        const uint64_t dw = sdesc_sw128(smem_u32(sm + wslot_off(st)));
+        const uint64_t da = sdesc_sw128(a_base);
         const int parts = part_stride == 0 ? 1 : 2;
         for (int p = 0; p < parts; ++p) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16_elect(d, sdesc_sw128(a_base + p * part_stride + k * 32), sdesc_sw128(w + k * 32),
-                          idesc, (first && p == 0 && k == 0) ? 0u : 1u);
+            mma_f16_elect(d, da + ((p * part_stride + k * 32) >> 4), dw + 2 * k, idesc,
+                          (first && p == 0 && k == 0) ? 0u : 1u);
         }
         mma_commit_elect(bar + B_W_EMPTY + st);
       }
@@ -520,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       par ^= 1u << st;
       tc_fence_after();
       {
-        const uint32_t w = smem_u32(sm + wslot_off(st));
+        const uint64_t dw = sdesc_sw128(smem_u32(sm + wslot_off(st)));
         for (int p = 0; p < parts; ++p) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16_ta_elect(d, tmem + a_col + p * part_cols + 8 * k, sdesc_sw128(w + k * 32), idesc,
+            mma_f16_ta_elect(d, tmem + a_col + p * part_cols + 8 * k, dw + 2 * k, idesc,
                              (first && p == 0 && k == 0) ? 0u : 1u);
         }
         mma_commit_elect(bar + B_W_EMPTY + st);
@@ -576,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 3; ++c)
 #pragma unroll
               for (int k = 0; k < 2; ++k)
-                mma_f16_elect(tmem + 384, desc_sw64(as[c] + k * 32), desc_sw64(bs[c] + k * 32), id128,
+                mma_f16_elect(tmem + 384, desc_sw64(as[c]) + 2 * k, desc_sw64(bs[c]) + 2 * k, id128,
                               (c | k) != 0);
           }
           commit(B_S_DONE);
@@ -599,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kProducts; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c] + k * 32), sdesc_sw128(bs[c] + k * 32),
+                mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c]) + 2 * k, sdesc_sw128(bs[c]) + 2 * k,
                               id64, (c | k) != 0);
           }
           commit(B_O_DONE);
@@ -774,6 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // LayerNorm of acc (TMEM columns tcol + [32g, +32)) + bias + residual
     // (the X buffer): per-group (mean, M2) over 32 columns, merged through
     // the exchange with Chan's formula, (01)(23) then the two pairs.
+    // bias, gam, bet: the layer's vectors staged in shared memory
     auto layernorm = [&](uint32_t tcol, const float* bias, const float* gam, const float* bet,
                          bool resid_lo, bool resid_tmem, float* v, const float* part = nullptr) {
       tmem_ld32_nw(trow + tcol + 32 * g, v);
@@ -836,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* e4 = reinterpret_cast<const float4*>(bet + 32 * g);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 gg = __ldg(g4 + c4), e = __ldg(e4 + c4);
+        const float4 gg = g4[c4], e = e4[c4];
         v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * gg.x + e.x;
         v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * gg.y + e.y;
         v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * gg.z + e.z;
@@ -1009,11 +1014,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!wait_peer(B_PEER_Y, c_py)) { ok = false; break; }
         } else {
+          // The layer's six LayerNorm vectors (b_o, ln1 gamma, beta, b_2, ln2
+          // gamma, beta; 768 floats) go to the softmax-sum area, free once
+          // every thread has read its sums (CTX_READY precedes OUT_DONE): the
+          // global loads are issued now and land during the out-projection.
+          const int ct = threadIdx.x - kCtrlWarps * 32;
+          auto ln_vec = [&](int k) -> float {
+            const int v6 = k >> 7, e = k & 127;
+            const float* src = v6 == 0 ? P.b_o : v6 == 1 ? P.ln1_g : v6 == 2 ? P.ln1_b
+                             : v6 == 3 ? P.b_2 : v6 == 4 ? P.ln2_g : P.ln2_b;
+            return __ldg(src + e);
+          };
+          const float lv0 = ln_vec(ct), lv1 = ct < 256 ? ln_vec(ct + 512) : 0.f;
           arrive(B_CTX_READY);
           // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
           if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
+          l_s[ct] = lv0;
+          if (ct < 256) l_s[ct + 512] = lv1;
+          bar_compute();
           float y[32];
-          layernorm(128, P.b_o, P.ln1_g, P.ln1_b, !first, false, y);
+          layernorm(128, l_s, l_s + 128, l_s + 256, !first, false, y);
           // y -> TMEM [128, 256) as (hi, lo) words: group g holds K columns
           // [32g, 32g + 32).  Every group read its out-projection accumulator
           // (the same columns) before the LayerNorm's exchange barrier.
@@ -1057,10 +1077,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 b = b4[c4];
-            hv[4 * c4 + 0] = gelu_as7128(hv[4 * c4 + 0] + b.x);
-            hv[4 * c4 + 1] = gelu_as7128(hv[4 * c4 + 1] + b.y);
-            hv[4 * c4 + 2] = gelu_as7128(hv[4 * c4 + 2] + b.z);
-            hv[4 * c4 + 3] = gelu_as7128(hv[4 * c4 + 3] + b.w);
+            hv[4 * c4 + 0] += b.x;
+            hv[4 * c4 + 1] += b.y;
+            hv[4 * c4 + 2] += b.z;
+            hv[4 * c4 + 3] += b.w;
+            gelu_as7128_x2(hv[4 * c4 + 0], hv[4 * c4 + 1]);
+            gelu_as7128_x2(hv[4 * c4 + 2], hv[4 * c4 + 3]);
           }
           // group g holds the chunk's K columns [32g, 32g + 32): words [16g, +16)
           uint32_t hw[16], lw[16];
@@ -1113,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_peer(B_PEER_PART, c_part)) { ok = false; break; }
           }
           float xo[32];
-          layernorm(0, P.b_2, P.ln2_g, P.ln2_b, true, true, xo,
+          layernorm(0, l_s + 384, l_s + 512, l_s + 640, true, true, xo,
                     ASSIST ? reinterpret_cast<const float*>(pbuf) : nullptr);
           const int kh = g >> 1;
           // assisted: H's FFN1 no longer reads y -- so the copy of y out of

@@ -420,14 +420,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       // O += Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
       // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
       // extension, column 2 DH = the sum of the P values used
+      // descriptors built once; a k16 step moves the start address field by 32 / 16
+      const uint64_t dph = sdesc_rows(ph_, 128), dvt = sdesc_rows(vt, 128);
 #pragma unroll
       for (int k = 0; k < kBKV / 16; ++k)
-        mma_f16_elect(tO, sdesc_rows(ph_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_o,
-                      !first || k != 0);
+        mma_f16_elect(tO, dph + 2 * k, dvt + 2 * k, idesc_o, !first || k != 0);
       if constexpr (!p_hi_only<T>()) {
+        const uint64_t dpl = sdesc_rows(pl_, 128);
 #pragma unroll
-        for (int k = 0; k < kBKV / 16; ++k)
-          mma_f16_elect(tO, sdesc_rows(pl_ + k * 32, 128), sdesc_rows(vt + k * 32, 128), idesc_ol, true);
+        for (int k = 0; k < kBKV / 16; ++k) mma_f16_elect(tO, dpl + 2 * k, dvt + 2 * k, idesc_ol, true);
       }
       mma_commit_elect(&p_empty[pb]);
       mma_commit_elect(&kv_empty[st]);
@@ -462,11 +463,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           const uint32_t as[3] = {qh, qh, ql};
           const uint32_t bs[3] = {kh, kl, kh};
 #pragma unroll
-          for (int t = 0; t < 3; ++t)
+          for (int t = 0; t < 3; ++t) {
+            const uint64_t da = sdesc_rows(as[t], Lay::kRowBytes), db = sdesc_rows(bs[t], Lay::kRowBytes);
 #pragma unroll
             for (int k = 0; k < DH / 16; ++k)
-              mma_f16_elect(d, sdesc_rows(as[t] + k * 32, Lay::kRowBytes),
-                            sdesc_rows(bs[t] + k * 32, Lay::kRowBytes), idesc_s, (t | k) != 0);
+              mma_f16_elect(d, da + 2 * k, db + 2 * k, idesc_s, (t | k) != 0);
+          }
           mma_commit_elect(&s_full[sbuf]);
           if (j == nkt - 1) mma_commit_elect(q_empty);  // Q no longer read
         }
@@ -602,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           if constexpr (!row_sum_by_mma<DH>()) l *= corr;
         }
         const float mref = mr == -INFINITY ? 0.f : mr;
+        const uint64_t sc2 = splat2(scale_log2), nm2 = splat2(-mref);
         // P_it into the (hi, lo) swizzled operand buffer, once P.V_{it-2}
         // has released it.
         const int pb = (int)(it & 1);
@@ -612,8 +615,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         for (int c8 = 0; c8 < kBKV / 8; ++c8) {
           float p8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)  // one rounding: 2^(s scale - mref), flushed below 2^-126
-            p8[e] = ex2_ftz(fmaf(s[c8 * 8 + e], scale_log2, -mref));
+          for (int e = 0; e < 8; e += 2) {  // 2^(s scale - mref), flushed below 2^-126
+            float a0, a1;  // the exponents, two at a time (paired fp32 fma)
+            upk2(fma2(pk2(s[c8 * 8 + e], s[c8 * 8 + e + 1]), sc2, nm2), a0, a1);
+            p8[e] = ex2_ftz(a0);
+            p8[e + 1] = ex2_ftz(a1);
+          }
           const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
           if constexpr (!row_sum_by_mma<DH>()) {
 #pragma unroll

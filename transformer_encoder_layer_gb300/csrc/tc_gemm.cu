@@ -346,17 +346,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
               // warp-uniform descriptors; one elected lane issues
               unsigned char* st = base + (size_t)stage * stage_bytes;
-              const uint32_t w_addr = smem_u32(st + a.n_parts * kATileBytes);
+              // a k16 step moves the descriptors' start address field by 32 / 16
+              const uint64_t dw = sdesc_sw128(smem_u32(st + a.n_parts * kATileBytes));
               for (int p = 0; p < a.n_parts; ++p) {
-                const uint32_t a_addr = smem_u32(st + p * kATileBytes);
+                const uint64_t da = sdesc_sw128(smem_u32(st + p * kATileBytes));
 #pragma unroll
                 for (int k16 = 0; k16 < kBK / 16; ++k16) {
                   if constexpr (PAIR)
-                    mma_f16_pair_elect(d_tmem, sdesc_sw128(a_addr + k16 * 32),
-                                       sdesc_sw128(w_addr + k16 * 32), a.idesc, (kb | p | k16) != 0);
+                    mma_f16_pair_elect(d_tmem, da + 2 * k16, dw + 2 * k16, a.idesc, (kb | p | k16) != 0);
                   else
-                    mma_f16_elect(d_tmem, sdesc_sw128(a_addr + k16 * 32), sdesc_sw128(w_addr + k16 * 32),
-                                  a.idesc, (kb | p | k16) != 0);
+                    mma_f16_elect(d_tmem, da + 2 * k16, dw + 2 * k16, a.idesc, (kb | p | k16) != 0);
                 }
               }
               commit_both(&sm.empty[stage]);
@@ -418,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (EPI == TC_EPI_GELU) {
             if (row_ok) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = gelu_as7128(v[j]);
+              for (int j = 0; j < 32; j += 2) gelu_as7128_x2(v[j], v[j + 1]);
               store_row32_pair(o_hi, o_lo, (size_t)row * a.N + n0, v);
             }
           } else {  // LN pass 1: r = acc + bias + residual, chunk stats
