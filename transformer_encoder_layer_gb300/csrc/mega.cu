@@ -212,19 +212,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// D (+)= A . B^T with A read from tensor memory (128 lanes = rows, K packed
-// two 16-bit elements per 32-bit column) and B from a shared-memory
-// descriptor, issued from a converged warp: warp-uniform operands, one
-// elected lane issues (as mma_f16_elect).
-__device__ __forceinline__ void mma_f16_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
 template <typename T>
 __device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int off, const float* v) {

@@ -70,18 +70,16 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 192;
-// Query rows and keys per tile; the MMA thread issues P.V of key tile
-// j - kPvLag after S of tile j, into kPvLag + 1 TMEM score buffers.  (A lag
-// of 2 keeps the next scores further ahead of the softmax but releases P
-// buffers later; with the MMA thread's issue the busiest role, a lag of 1
-// measured faster.)
-constexpr int kBQ = 128, kBKV = 64, kPvLag = 1, kSBufs = kPvLag + 1;
+// Query rows and keys per tile; the MMA thread issues P.V of key tile j - 1
+// after S of tile j, into two TMEM score buffers.  (Running S two tiles
+// ahead of P.V measured slower: the MMA thread's issue is the busiest role.)
+constexpr int kBQ = 128, kBKV = 64, kSBufs = 2, kPvLag = kSBufs - 1;
 
-// CTAs per SM: head_dim 16 fits two (about 97 KB of shared memory and 256
-// TMEM columns each), which doubles the softmax warps per SM sub-partition,
-// the bound at that head size; larger heads keep one.
+// CTAs per SM: two at every head size (256 TMEM columns each; P lives in
+// TMEM, so Q and the K/V ring are all the shared memory a CTA needs), so one
+// CTA's softmax overlaps the other's MMAs and loads.
 template <int DH>
-constexpr int ctas_per_sm() { return DH == 16 ? 2 : 1; }
+constexpr int ctas_per_sm() { return 2; }
 
 // max(a, b, c) in one instruction (sm_100 and later).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -192,23 +190,21 @@ struct Layout {
   static constexpr int kVRows = 2 * DH + kXRows;    // V^T rows: hi, lo, extension
   static constexpr int kVTx = DH * kBKV * 2;        // bytes of one V^T plane tile (TMA)
   static constexpr int kVBytes = kVRows * kBKV * 2; // the V^T block of a stage
-  static constexpr int kPBytes = kBQ * kBKV * 2;    // one P plane (16 KB)
   static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
   static constexpr int kStageTx = 2 * kKBytes + 2 * kVTx;  // TMA bytes per stage
   static constexpr int kOUsed = kVRows;              // O columns the MMAs write
   static constexpr int kOCols = (kVRows + 31) / 32 * 32;  // TMEM columns of the O accumulator
-  static constexpr int kPPlanes = p_hi_only<T>() ? 1 : 2;  // P planes: hi (, lo)
+  static_assert(kSBufs * kBKV + kOCols <= 256, "two CTAs per SM share the 512 TMEM columns");
   static_assert(kVTx % 1024 == 0 && kStageBytes % 1024 == 0, "128-byte swizzle atoms stay aligned");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = ((2 * kQBytes + 1023) / 1024) * 1024;
   // K/V ring depth: what the shared memory left per CTA holds, up to 6
   // (the TMA runs further ahead of the MMAs; K/V come from L2).
-  static constexpr int kFixedBytes = kKVOff + 2 * kPPlanes * kPBytes + 256;
+  static constexpr int kFixedBytes = kKVOff + 256;
   static constexpr int kStages =
       std::min(6, (232448 / ctas_per_sm<DH>() - 1024 - kFixedBytes) / kStageBytes);
-  static_assert(kStages >= 4, "K/V ring");
-  static constexpr int kPOff = kKVOff + kStages * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPPlanes * kPBytes;
+  static_assert(kStages >= 2, "K/V ring");
+  static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
   static constexpr int kBytes = kBarOff + 256;
   static constexpr int kRowBytes = DH * 2;          // Q/K rows: 32, 64, 128
 };
@@ -279,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   uint64_t* kv_full = bars + 2;            // [kStages]
   uint64_t* kv_empty = kv_full + kStages;  // [kStages]
   uint64_t* s_full = kv_empty + kStages;   // [kSBufs]
-  uint64_t* s_empty = s_full + kSBufs;     // [kSBufs]
-  uint64_t* p_full = s_empty + kSBufs;     // [2]
-  uint64_t* p_empty = p_full + 2;          // [2]: P buffer free = its P.V complete
+  uint64_t* s_empty = s_full + kSBufs;     // [kSBufs]: S/P buffer free = its P.V complete
+  uint64_t* p_full = s_empty + kSBufs;     // [2]: P written over S
+  uint64_t* p_empty = p_full + 2;          // [2]: the buffer's P.V complete (softmax side)
   uint64_t* o_free = p_empty + 2;          // the item's O has been read
   uint64_t* mma_done = o_free + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -292,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   const int nqt = (a.L + kBQ - 1) / kBQ;
   const int n_items = a.kc ? a.n_items : planes * nqt;
   const int kc = a.kc;
-  // S: kSBufs x 64 columns, O: kOCols (P.Vh, P.Vl and the row sum)
-  constexpr uint32_t kTmemCols = kSBufs * kBKV + Lay::kOCols <= 256 ? 256 : 512;
+  // S (then P over it): kSBufs x 64 columns, O: kOCols (P.Vh, P.Vl and the row sum)
+  constexpr uint32_t kTmemCols = 256;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -304,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
     }
     for (int s = 0; s < kSBufs; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
+      mbar_init(&s_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&p_full[s], 128);
@@ -415,22 +411,25 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       const int st = (int)(it_kv % kStages);
       const uint32_t sb = smem_u32(base + Lay::kKVOff + st * Lay::kStageBytes);
       const uint32_t vt = sb + 2 * Lay::kKBytes;  // rows: Vh^T, Vl^T (, extension)
-      const uint32_t ph_ = smem_u32(base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes);
-      const uint32_t pl_ = ph_ + Lay::kPBytes;
+      // P (A operand) in TMEM, over its S buffer: Ph in the first 32
+      // columns, Pl (bf16) in the next 32, two 16-bit values per column
+      const uint32_t tph = tS + (uint32_t)(pb * kBKV);
       // O += Ph.[Vh | Vl] (+ Pl.Vh with bf16) over 64 keys (4 steps of
-      // K = 16): columns [0, DH) take P.Vh, [DH, 2 DH) P.Vl; with the
-      // extension, column 2 DH = the sum of the P values used
-      // descriptors built once; a k16 step moves the start address field by 32 / 16
-      const uint64_t dph = sdesc_rows(ph_, 128), dvt = sdesc_rows(vt, 128);
+      // K = 16, 8 TMEM columns of P each): columns [0, DH) take P.Vh,
+      // [DH, 2 DH) P.Vl; with the extension, column 2 DH = the sum of the P
+      // values used.  The V descriptor is built once; a k16 step moves its
+      // start address field by 32 / 16.
+      const uint64_t dvt = sdesc_rows(vt, 128);
 #pragma unroll
       for (int k = 0; k < kBKV / 16; ++k)
-        mma_f16_elect(tO, dph + 2 * k, dvt + 2 * k, idesc_o, !first || k != 0);
+        mma_f16_ta_elect(tO, tph + 8 * k, dvt + 2 * k, idesc_o, !first || k != 0);
       if constexpr (!p_hi_only<T>()) {
-        const uint64_t dpl = sdesc_rows(pl_, 128);
 #pragma unroll
-        for (int k = 0; k < kBKV / 16; ++k) mma_f16_elect(tO, dpl + 2 * k, dvt + 2 * k, idesc_ol, true);
+        for (int k = 0; k < kBKV / 16; ++k)
+          mma_f16_ta_elect(tO, tph + 32 + 8 * k, dvt + 2 * k, idesc_ol, true);
       }
       mma_commit_elect(&p_empty[pb]);
+      mma_commit_elect(&s_empty[pb]);  // the S/P buffer may take S of tile it_o + 2
       mma_commit_elect(&kv_empty[st]);
       __syncwarp();
       return true;
@@ -546,8 +545,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         float s[kBKV];
         tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV), *reinterpret_cast<float(*)[32]>(&s[0]));
         tmem_ld32(tS + lane_addr + (uint32_t)(sbuf * kBKV + 32), *reinterpret_cast<float(*)[32]>(&s[32]));
-        tc_fence_before();
-        mbar_arrive(&s_empty[sbuf]);
         const int k0 = j * kBKV;
         const bool needs_mask = k0 + kBKV > full_keys;
         // s stays unscaled (masked keys -inf); the running max m, the
@@ -605,12 +602,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         }
         const float mref = mr == -INFINITY ? 0.f : mr;
         const uint64_t sc2 = splat2(scale_log2), nm2 = splat2(-mref);
-        // P_it into the (hi, lo) swizzled operand buffer, once P.V_{it-2}
-        // has released it.
+        // P_it over its own scores in TMEM (this thread's row).  P.V_{it-2},
+        // which read the buffer last, is complete (S_it was computed after
+        // it); the wait keeps this barrier's phases in step with the rescale
+        // and end-of-item waits on it.
         const int pb = (int)(it & 1);
         if (!mbar_wait(&p_empty[pb], (uint32_t)(((it >> 1) & 1) ^ 1), abort, a.status)) { ok = false; break; }
-        unsigned char* ph = base + Lay::kPOff + pb * Lay::kPPlanes * Lay::kPBytes;
-        unsigned char* pl = ph + Lay::kPBytes;
+        uint32_t pwh[32];
+        uint32_t pwl[p_hi_only<T>() ? 1 : 32];
 #pragma unroll
         for (int c8 = 0; c8 < kBKV / 8; ++c8) {
           float p8[8];
@@ -621,22 +620,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
             p8[e] = ex2_ftz(a0);
             p8[e + 1] = ex2_ftz(a1);
           }
-          const int off = r * 128 + ((c8 ^ (r & 7)) << 4);
           if constexpr (!row_sum_by_mma<DH>()) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) l += p8[e];
           }
           if constexpr (p_hi_only<T>()) {
-            *reinterpret_cast<uint4*>(ph + off) = pack8_hi(p8, T());
+            *reinterpret_cast<uint4*>(&pwh[4 * c8]) = pack8_hi(p8, T());
           } else {
-            uint4 hv, lv;
-            split8(p8, hv, lv, T());
-            *reinterpret_cast<uint4*>(ph + off) = hv;
-            *reinterpret_cast<uint4*>(pl + off) = lv;
+            split8(p8, *reinterpret_cast<uint4*>(&pwh[4 * c8]), *reinterpret_cast<uint4*>(&pwl[4 * c8]), T());
           }
         }
-        fence_proxy_async();
-        tc_fence_before();  // orders a rescale's TMEM stores before P.V_it
+        const uint32_t tp = tS + lane_addr + (uint32_t)(sbuf * kBKV);
+        tmem_st32(tp, pwh);
+        if constexpr (!p_hi_only<T>()) tmem_st32(tp + 32, *reinterpret_cast<uint32_t(*)[32]>(pwl));
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();  // orders P's (and a rescale's) TMEM stores before P.V_it
         mbar_arrive(&p_full[pb]);
       }
       if (!ok) break;
@@ -781,7 +779,7 @@ TcAttnSplit tc_attention_split_plan(int B, int H, int L, int dh, int num_sms, in
   const long long planes = (long long)B * H;
   const int nqt = (L + kBQ - 1) / kBQ;
   const long long items0 = planes * nqt;
-  const int slots = num_sms * (dh == 16 ? ctas_per_sm<16>() : 1);
+  const int slots = num_sms * ctas_per_sm<16>();  // every head size runs two CTAs per SM
   // The item index is an int and the decoding walks the query tiles; keep
   // the split to shapes whose (plane, query tile) count is modest.
   if (nqt > 4096 || items0 * ((nkt_bound(nqt - 1, L) + 1) / 2) > (1LL << 28)) return p;
