@@ -91,8 +91,11 @@ def algorithmic_counts(shape, valid_len):
     }
 
 
-# SFU results per SM per clock (nominal: 4 per SM sub-partition).
-SFU_PER_SM_CLK = 16
+# SFU base-2 exponentials per SM per clock on GB300: 32.  A throughput loop of
+# independent ex2.approx.ftz.f32 chains (608 blocks of 512 threads) ran
+# 9.48e12 per second on 152 SMs at about 2.0 GHz, 30 per SM per clock: twice
+# the 4 per SM sub-partition assumed before.
+SFU_PER_SM_CLK = 32
 
 
 def fp32_alu_tflops(peaks, sms):
@@ -105,7 +108,7 @@ def step_fractions(counts, ms_per_step, peaks, sms, dtype):
     """The whole step's algorithmic work over the rooflines that apply to the
     path: the tensor cores (16-bit I/O; measured bf16 burst peak, fp16 dense
     runs at the same rate) or the FP32 ALUs (fp32 I/O runs on the CUDA
-    cores), HBM (measured copy bandwidth) and the SFU (SMs x 16 x max
+    cores), HBM (measured copy bandwidth) and the SFU (SMs x 32 x max
     clock).  The largest is the binding one."""
     t = ms_per_step / 1e3
     clk = peaks.get("sm_max_mhz", 2070.0) * 1e6

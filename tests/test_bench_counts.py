@@ -33,7 +33,7 @@ def test_step_fractions_pick_the_path_roofline():
     f = bench.step_fractions(counts, 10.0, peaks, 100, "f16")   # 10 ms
     assert f["tensor"] == pytest.approx(1e14 / 1e15)
     assert f["hbm"] == pytest.approx(1e11 / 5e12)
-    assert f["sfu"] == pytest.approx(1e11 / (100 * 16 * 2e9))
+    assert f["sfu"] == pytest.approx(1e11 / (100 * bench.SFU_PER_SM_CLK * 2e9))
     assert "fp32_alu" not in f        # a 16-bit path runs on the tensor cores
     assert f["binding"] == "tensor"
     g = bench.step_fractions(counts, 10.0, peaks, 100, "f32")
