@@ -1,8 +1,10 @@
 // Second half of the add + LayerNorm epilogue for rows wider than one GEMM N
 // tile ("KernelForge", section "What we built": fused add + LayerNorm after
 // the projection GEMMs).  The GEMM's epilogue has already formed the
-// pre-normalisation rows r = x + a (bias and residual added) and each row's
-// (mean, 1/sqrt(var + eps)); this kernel applies
+// pre-normalisation rows r = x + a (bias and residual added) and, per row and
+// GEMM N tile, the (mean, M2) of the tile's columns; this kernel merges them
+// (equal counts c per block: mean = the blocks' mean, M2 = sum M2_b + c sum
+// (mean_b - mean)^2), takes rstd = 1/sqrt(M2 / N + eps) and applies
 //   y = (r - mean) * rstd * gamma + beta
 // and writes y as fp32 and/or (hi, lo) 16-bit planes, or as the stack's
 // output in the I/O dtype.  It is a plain streaming pass: each thread takes 8
@@ -31,7 +33,21 @@ __global__ void __launch_bounds__(256) ln_apply_kernel(const LnApplyArgs a) {
     const size_t at = (size_t)row * a.N + c0;
     const float4* rp = reinterpret_cast<const float4*>(a.r + at);
     const float4 r0 = __ldcs(rp), r1 = __ldcs(rp + 1);
-    const float2 st = a.stats[row];
+    float2 st;  // (mean, rstd) of the row from its blocks' statistics
+    {
+      const float2* ps = a.stats + (size_t)row * a.n_parts;
+      float msum = 0.f;
+      for (int k = 0; k < a.n_parts; ++k) msum += ps[k].x;
+      const float mean = msum / (float)a.n_parts;
+      float m2 = 0.f;
+      const float cnt = (float)(a.N / a.n_parts);
+      for (int k = 0; k < a.n_parts; ++k) {
+        const float2 p = ps[k];
+        const float dm = p.x - mean;
+        m2 += p.y + cnt * dm * dm;
+      }
+      st = make_float2(mean, rsqrtf(m2 / (float)a.N + 1e-5f));
+    }
     const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0));
     const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0) + 1);
     const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.beta + c0));
@@ -69,7 +85,8 @@ __global__ void __launch_bounds__(256) ln_apply_kernel(const LnApplyArgs a) {
 }  // namespace
 
 cudaError_t ln_apply(const LnApplyArgs& a, bool bf16, int num_sms, cudaStream_t s) {
-  if (a.M < 1 || a.N < 8 || a.N % 8 || !a.r || !a.stats || !a.gamma || !a.beta ||
+  if (a.M < 1 || a.N < 8 || a.N % 8 || a.n_parts < 1 || a.N % a.n_parts || !a.r || !a.stats ||
+      !a.gamma || !a.beta ||
       (!a.o32 && !a.o_hi && !a.o_final) || (a.o_hi && !a.o_lo))
     return cudaErrorInvalidValue;
   const long long work = (long long)a.M * (a.N / 8);

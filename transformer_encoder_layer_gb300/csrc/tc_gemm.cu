@@ -33,13 +33,15 @@
 //   QKV   + bias, scattered head-major: Q and K as [B, H, L, dh] and V as
 //         V^T [B, H, dh, Lp], each as (hi, lo) planes
 //   GELU  + bias, exact-erf GELU, (hi, lo) planes [M, N]
-//   LN    + bias + residual, LayerNorm over the full row (the CTA owns all
-//         N columns of its rows; per-32-column (mean, M2) merged with Chan's
-//         formula), written as fp32 and/or (hi, lo) planes, or as the final
-//         output in the I/O dtype.  A row wider than one N tile goes to a
-//         scratch row with its (mean, rstd); ln_apply.cu normalises those
-//         rows in a streaming pass while this kernel's tensor cores are free
-//         for the next launch.
+//   LN    + bias + residual, LayerNorm over the full row (per-32-column
+//         (mean, M2) merged with Chan's formula), written as fp32 and/or
+//         (hi, lo) planes, or as the final output in the I/O dtype.  When a
+//         row fits one N tile the CTA normalises it from TMEM.  A row wider
+//         than one N tile goes to a scratch row, each tile with the (mean,
+//         M2) of its columns (each tile a work unit of its own), and
+//         ln_apply.cu merges the statistics and normalises those rows in a
+//         streaming pass while this kernel's tensor cores are free for the
+//         next launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -233,9 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   T* const o_lo = reinterpret_cast<T*>(a.o_lo);
   T* const o_final = reinterpret_cast<T*>(a.o_final);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const bool ln_rows = (EPI == TC_EPI_LN);
-  // Work units: LN -> one row block (128 rows, or 256 for a pair) with all
-  // its N tiles; else one tile.  a.m_blocks counts row blocks of that size.
+  // Work units: an LN GEMM that normalises its rows itself -> one row block
+  // (128 rows, or 256 for a pair) with all its N tiles; else one tile (an LN
+  // GEMM whose rows span several tiles hands per-tile statistics to the
+  // apply pass, so its row blocks' tiles spread over the SMs: 4 x the units,
+  // fewer idle SMs in the last wave).  a.m_blocks counts row blocks.
+  const bool split_stats = EPI == TC_EPI_LN && a.n_tiles > 1 && a.row_stats;
+  const bool ln_rows = EPI == TC_EPI_LN && !split_stats;
   const int n_units = ln_rows ? a.m_blocks : a.m_blocks * a.n_tiles;
   const int tiles_per_unit = ln_rows ? a.n_tiles : 1;
   const int k_blocks = (a.K + kBK - 1) / kBK;
@@ -477,8 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the streaming apply pass when the rows went to scratch).
           const float mean = ln_mean;
           const float rstd = rsqrtf(ln_m2 / ln_n + 1e-5f);
-          if (a.n_tiles > 1 && a.row_stats) {
-            if (row_ok) a.row_stats[row] = make_float2(mean, rstd);
+          if (split_stats) {
+            // this tile's (mean, M2) over its BN columns, for the apply pass
+            if (row_ok) a.row_stats[(size_t)row * a.n_tiles + n_tile] = make_float2(ln_mean, ln_m2);
           } else for (int tt = 0; tt < a.n_tiles; ++tt) {
             for (int c = 0; c < n_chunks; ++c) {
               float v[32];
@@ -603,7 +610,9 @@ cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const 
   while (cols < 2 * a.BN) cols <<= 1;
   a.tmem_cols = cols;
   a.idesc = idesc_f16(rows, a.BN, bf16);
-  const int units = epi == TC_EPI_LN ? a.m_blocks : a.m_blocks * a.n_tiles;
+  // work units as the kernel counts them (see split_stats there)
+  const bool whole_rows = epi == TC_EPI_LN && !(a.n_tiles > 1 && a.row_stats);
+  const int units = whole_rows ? a.m_blocks : a.m_blocks * a.n_tiles;
   const int slots = pair ? num_sms / 2 : num_sms;  // CTAs (pairs) resident at once
   const int grid = (units < slots ? units : slots) * (pair ? 2 : 1);
   const size_t smem = tc_gemm_smem_bytes(a.BN, a.n_parts, a.stages, pair);

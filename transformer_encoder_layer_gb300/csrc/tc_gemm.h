@@ -38,10 +38,12 @@ struct TcGemmArgs {
   float* o32;         // optional fp32 [M, N]
   void* o_final;      // optional 16-bit [M, N] (the stack's output)
   float* rscratch;    // fp32 [M, N] pre-LN rows when N > BN
-  // When N > BN and row_stats is set, the epilogue stops after writing the
-  // pre-LN rows to rscratch and (mean, rstd) per row here; ln_apply then
-  // normalises (the outputs above are not written by the GEMM).
-  float2* row_stats;  // [M] or null
+  // When N > BN and row_stats is set, every (row block, N tile) is a work
+  // unit of its own: the epilogue writes the pre-LN rows to rscratch and,
+  // per row and N tile, the (mean, M2) of the tile's BN columns here;
+  // ln_apply merges them and normalises (the outputs above are not written
+  // by the GEMM).
+  float2* row_stats;  // [M][n_tiles] or null
   int* status;
 };
 
