@@ -406,8 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int n0 = n_tile * BN + c * 32;
+          {  // + bias: eight 16-byte loads (the same addresses in every lane)
+            const float4* b4 = reinterpret_cast<const float4*>(a.bias + n0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += __ldg(a.bias + n0 + j);
+            for (int j = 0; j < 8; ++j) {
+              const float4 bb = __ldg(b4 + j);
+              v[4 * j] += bb.x; v[4 * j + 1] += bb.y; v[4 * j + 2] += bb.z; v[4 * j + 3] += bb.w;
+            }
+          }
           if (EPI == TC_EPI_QKV) {
             if (row_ok) {
               // a 32-column chunk covers part of one head (dh >= 32) or 32/dh
