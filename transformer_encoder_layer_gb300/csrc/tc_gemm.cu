@@ -54,7 +54,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+// Threads per CTA: a TMA warp, an MMA warp and the epilogue warps.  The QKV
+// and GELU epilogues run on eight warps (two per TMEM lane quarter, each
+// taking half of a tile's columns): with four, a tile's epilogue (about 21K
+// cycles for 128 x 256 outputs on GB300) outlasted its MMAs (about 19K).
+// The LayerNorm epilogue keeps four (its row statistics run along the row).
+template <int EPI>
+constexpr int gemm_threads() { return EPI == TC_EPI_LN ? 192 : 320; }
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 
@@ -193,7 +199,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 
 template <typename T, int EPI, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                    const __grid_constant__ CUtensorMap map_w, const TcGemmArgs args) {
   extern __shared__ __align__(1024) unsigned char dyn_smem[];
@@ -255,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.acc_full[s], 1);
       // pair leader: its own 128 epilogue threads plus one arrival per peer
       // epilogue warp
-      mbar_init(&sm.acc_empty[s], PAIR ? 128 + 4 : 128);
+      // every epilogue thread, plus (pair) one remote arrival per peer epilogue warp
+      constexpr int kEpiWarps = gemm_threads<EPI>() / 32 - 2;
+      mbar_init(&sm.acc_empty[s], kEpiWarps * 32 + (PAIR ? kEpiWarps : 0));
     }
     mbar_init(sm.mma_done, 1);
     mbar_init(sm.done, 1);
@@ -389,6 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const int n_chunks = BN / 32;
+    // This warp's 32-column chunks of a tile: all of them with four epilogue
+    // warps; with eight, one half, split between whole heads (QKV with
+    // head_dim above 32 carries a head's |k|^2 across its chunks).
+    constexpr int kHalves = (gemm_threads<EPI>() / 32 - 2) / 4;
+    const int half = (warp - 2) / 4;
+    const int grp = (EPI == TC_EPI_QKV && a.dh > 32) ? a.dh / 32 : 1;
+    const int n_grp = n_chunks / grp;
+    const int c_lo = half * n_grp / kHalves * grp, c_hi = (half + 1) * n_grp / kHalves * grp;
     bool ok = true;
     for (int u = TL_UNIT0; u < n_units && ok; u += TL_USTEP) {
       const int m_blk = ln_rows ? u : u / a.n_tiles;
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tbase = tmem + lane_addr + (uint32_t)(acc * BN);
         float kn2 = 0.f;  // running |k|^2 of the head being written (QKV)
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int n0 = n_tile * BN + c * 32;
@@ -565,7 +581,7 @@ cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorM
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(gemm_threads<EPI>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -577,7 +593,7 @@ cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorM
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, m0, m1, mw, a);
   } else {
-    k<<<grid, kThreads, smem, s>>>(m0, m1, mw, a);
+    k<<<grid, gemm_threads<EPI>(), smem, s>>>(m0, m1, mw, a);
     return cudaGetLastError();
   }
 }
