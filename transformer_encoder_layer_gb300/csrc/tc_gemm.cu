@@ -54,13 +54,20 @@ namespace {
 
 using namespace tc;
 
-// Threads per CTA: a TMA warp, an MMA warp and the epilogue warps.  The QKV
-// and GELU epilogues run on eight warps (two per TMEM lane quarter, each
-// taking half of a tile's columns): with four, a tile's epilogue (about 21K
-// cycles for 128 x 256 outputs on GB300) outlasted its MMAs (about 19K).
-// The LayerNorm epilogue keeps four (its row statistics run along the row).
-template <int EPI>
-constexpr int gemm_threads() { return EPI == TC_EPI_LN ? 192 : 320; }
+// Threads per CTA: a TMA warp, an MMA warp and the epilogue warps, four per
+// half of a tile's columns (one per TMEM lane quarter).  Two halves: with
+// one, a tile's epilogue (about 21K cycles for 128 x 256 QKV or GELU outputs
+// on GB300, 33K with LayerNorm statistics) outlasted its MMAs (about 19K at
+// K = 1024).  The CTA-pair LayerNorm GEMM (the FFN2 over a long K, whose
+// MMAs outlast its epilogue) keeps one: the second half's warps slowed the
+// MMA warp they share a sub-partition with (0.599 -> 0.633 ms per d1024
+// forward).  A LayerNorm epilogue that normalises whole rows itself runs on
+// the first half (its statistics run along the row); with per-tile
+// statistics each half writes its own.
+template <int EPI, bool PAIR>
+constexpr int epi_halves() { return EPI == TC_EPI_LN && PAIR ? 1 : 2; }
+template <int EPI, bool PAIR>
+constexpr int gemm_threads() { return 64 + 128 * epi_halves<EPI, PAIR>(); }
 constexpr int kBM = 128, kBK = 64;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 
@@ -199,7 +206,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 
 template <typename T, int EPI, bool PAIR>
-__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
+__global__ void __launch_bounds__(gemm_threads<EPI, PAIR>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                    const __grid_constant__ CUtensorMap map_w, const TcGemmArgs args) {
   extern __shared__ __align__(1024) unsigned char dyn_smem[];
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       // pair leader: its own 128 epilogue threads plus one arrival per peer
       // epilogue warp
       // every epilogue thread, plus (pair) one remote arrival per peer epilogue warp
-      constexpr int kEpiWarps = gemm_threads<EPI>() / 32 - 2;
+      constexpr int kEpiWarps = gemm_threads<EPI, PAIR>() / 32 - 2;
       mbar_init(&sm.acc_empty[s], kEpiWarps * 32 + (PAIR ? kEpiWarps : 0));
     }
     mbar_init(sm.mma_done, 1);
@@ -400,11 +407,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     // This warp's 32-column chunks of a tile: all of them with four epilogue
     // warps; with eight, one half, split between whole heads (QKV with
     // head_dim above 32 carries a head's |k|^2 across its chunks).
-    constexpr int kHalves = (gemm_threads<EPI>() / 32 - 2) / 4;
     const int half = (warp - 2) / 4;
+    const int halves = ln_rows ? 1 : epi_halves<EPI, PAIR>();  // whole LN rows: the first half
     const int grp = (EPI == TC_EPI_QKV && a.dh > 32) ? a.dh / 32 : 1;
     const int n_grp = n_chunks / grp;
-    const int c_lo = half * n_grp / kHalves * grp, c_hi = (half + 1) * n_grp / kHalves * grp;
+    const int c_lo = half < halves ? half * n_grp / halves * grp : 0;
+    const int c_hi = half < halves ? (half + 1) * n_grp / halves * grp : 0;
     bool ok = true;
     for (int u = TL_UNIT0; u < n_units && ok; u += TL_USTEP) {
       const int m_blk = ln_rows ? u : u / a.n_tiles;
@@ -500,14 +508,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             }
           }
         }
-        if (EPI == TC_EPI_LN && t == tiles_per_unit - 1) {
+        if (EPI == TC_EPI_LN && t == tiles_per_unit - 1 && half < halves) {
           // LN pass 2: normalise and write (or hand the row statistics to
           // the streaming apply pass when the rows went to scratch).
           const float mean = ln_mean;
           const float rstd = rsqrtf(ln_m2 / ln_n + 1e-5f);
           if (split_stats) {
-            // this tile's (mean, M2) over its BN columns, for the apply pass
-            if (row_ok) a.row_stats[(size_t)row * a.n_tiles + n_tile] = make_float2(ln_mean, ln_m2);
+            // (mean, M2) of this warp's half of the tile, for the apply pass
+            if (row_ok)
+              a.row_stats[((size_t)row * a.n_tiles + n_tile) * halves + half] = make_float2(ln_mean, ln_m2);
           } else for (int tt = 0; tt < a.n_tiles; ++tt) {
             for (int c = 0; c < n_chunks; ++c) {
               float v[32];
@@ -581,7 +590,7 @@ cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorM
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(gemm_threads<EPI>());
+    cfg.blockDim = dim3(gemm_threads<EPI, PAIR>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -593,7 +602,7 @@ cudaError_t launch(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorM
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, m0, m1, mw, a);
   } else {
-    k<<<grid, gemm_threads<EPI>(), smem, s>>>(m0, m1, mw, a);
+    k<<<grid, gemm_threads<EPI, PAIR>(), smem, s>>>(m0, m1, mw, a);
     return cudaGetLastError();
   }
 }
@@ -614,6 +623,10 @@ size_t tc_gemm_smem_bytes(int BN, int n_parts, int stages, bool pair) {
 }
 
 bool tc_gemm_pair_ok(int M, int BN) { return M > kBM && BN >= 64 && BN <= 256 && BN % 32 == 0; }
+
+int tc_gemm_ln_parts(int N, int BN, bool pair) {
+  return BN > 0 && N > BN ? (N / BN) * (pair ? epi_halves<TC_EPI_LN, true>() : epi_halves<TC_EPI_LN, false>()) : 1;
+}
 
 cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const CUtensorMap& map_w,
                     TcGemmArgs a, bool bf16, int epi, int num_sms, cudaStream_t s) {

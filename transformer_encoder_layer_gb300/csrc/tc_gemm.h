@@ -40,10 +40,10 @@ struct TcGemmArgs {
   float* rscratch;    // fp32 [M, N] pre-LN rows when N > BN
   // When N > BN and row_stats is set, every (row block, N tile) is a work
   // unit of its own: the epilogue writes the pre-LN rows to rscratch and,
-  // per row and N tile, the (mean, M2) of the tile's BN columns here;
-  // ln_apply merges them and normalises (the outputs above are not written
-  // by the GEMM).
-  float2* row_stats;  // [M][n_tiles] or null
+  // per row, the (mean, M2) of each of tc_gemm_ln_parts(N, BN, pair) equal column
+  // blocks here; ln_apply merges them and normalises (the outputs above are
+  // not written by the GEMM).
+  float2* row_stats;  // [M][tc_gemm_ln_parts(N, BN, pair)] or null
   int* status;
 };
 
@@ -55,6 +55,10 @@ bool tc_gemm_pair_ok(int M, int BN);
 // map_a0/map_a1: A planes [M, K] (box 64 x 128), map_w: W [N, K] (box
 // 64 x BN, or 64 x BN/2 with pair), all 128-byte swizzled.  map_a1 is
 // ignored when n_parts == 1.
+// Column blocks per row whose (mean, M2) an LN GEMM with N > BN writes (on
+// CTA pairs or not).
+int tc_gemm_ln_parts(int N, int BN, bool pair);
+
 cudaError_t tc_gemm(const CUtensorMap& map_a0, const CUtensorMap& map_a1, const CUtensorMap& map_w,
                     TcGemmArgs a, bool bf16, int epi, int num_sms, cudaStream_t s);
 
