@@ -17,7 +17,7 @@
 //
 // CTA-pair variant (PAIR, launched as clusters of two): the pair owns a
 // 256-row block.  Each CTA loads its own 128 rows of A and its half (BN/2
-// rows) of the W tile -- no data is multicast -- with both CTAs' loads
+// rows) of the W tile -- every byte is loaded once, by one CTA -- with both CTAs' loads
 // completing on the leader's (rank 0) ring barrier; the leader alone issues
 // tcgen05.mma.cta_group::2 with M = 256, which reads A and B from both
 // CTAs' shared memory and writes each CTA's rows into its own tensor memory,
