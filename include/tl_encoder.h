@@ -136,8 +136,9 @@ tl_status tl_encoder_set_attention_split(tl_encoder *h, int key_tiles);
  * megakernel page, section "Problem decomposition", tried a 2-CTA cluster
  * variant).  A paired GEMM (at least 257 rows, an N tile of 64 or more) runs
  * on clusters of two CTAs that share one 256-row block: each CTA stages its
- * own 128 rows of the activation and half of the weight tile (nothing is
- * multicast), and one MMA instruction of the leader CTA covers all 256 rows.
+ * own 128 rows of the activation and half of the weight tile (each byte is
+ * loaded once, by one CTA), and one MMA instruction of the leader CTA covers
+ * all 256 rows.
  * enable = -1 (the default) pairs only the GEMM where GB300 measured a gain
  * (the FFN2 + LayerNorm GEMM over d_ff >= 2048 with 4096+ rows), 1 pairs
  * every GEMM the shape allows, 0 none.  Host-only.  TL_ERR_INVALID_ARG
