@@ -135,7 +135,7 @@ enum {
   B_QKV_DONE, B_QKVH_READY,
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
-  B_MMA_DONE, B_SYNC,
+  B_MMA_DONE, B_SYNC, B_SYNC_SM,
   // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster);
   // data hand-overs are bulk copies completing on the receiver's barrier
   B_PEER_CTX,     // R: H's context of heads 2, 3 has landed in R's ctx buffer
@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         case B_Y_READY: case B_F1_FREE: case B_F1_FREE1: case B_H_READY: case B_XA_FREE:
         case B_SYNC:
           cnt = kCompute;
+          break;
+        case B_SYNC_SM:
+          cnt = kCompute / 2;
           break;
         case B_S_DONE:
           cnt = 2;  // the S commit + a release arrive of the MMA thread
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
     constexpr int NM = L / 32;  // own 8-key chunks of a row per group
     int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_f2 = 0,
-        c_sync = 0;  // completed phases per barrier (parity = count & 1)
+        c_sync = 0, c_sync_sm = 0;  // completed phases per barrier (parity = count & 1)
     // assisted mode: phases of the barriers the other CTA arrives on
     int c_pbfree = 0, c_py = 0, c_px = 0, c_xfree = 0, c_part = 0;
     bool ok = true;
@@ -718,12 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++c_sync;
       mbar_wait(bar + B_SYNC, par, abort, status);
     };
-    // Groups 0, 1 write 16 columns each of Q_h (hi, lo) and a partial |q|^2;
-    // groups 2, 3 write K_h and the tile's largest partial |k|^2.
-    auto convert_qk = [&](int h, const MegaLayer& P) {
+    // The same for the 256 softmax threads (groups 0, 1) of the split heads.
+    auto bar_softmax = [&]() {
+      mbar_arrive(bar + B_SYNC_SM);
+      const uint32_t par = (uint32_t)(c_sync_sm & 1);
+      ++c_sync_sm;
+      mbar_wait(bar + B_SYNC_SM, par, abort, status);
+    };
+    // 16 columns (part 0 or 1) of Q_h (hi, lo) with a partial |q|^2, or of
+    // K_h with the tile's largest partial |k|^2.
+    auto convert_qk = [&](int h, bool isq, int part) {
       float v[16];
-      const bool isq = g < 2;
-      const int c0 = 16 * (g & 1);
+      const int c0 = 16 * part;
       const int col = 96 * h + (isq ? 0 : 32) + c0;  // head h's q | k | v columns
       tmem_ld16_nw(trow + col, v);
       tmem_wait_ld();
@@ -733,28 +742,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 16; ++c) n2 = fmaf(v[c], v[c], n2);
       unsigned char* dst = sm + (isq ? kQB : kKB);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) put8<T>(dst, dst + 8192, sw64(r, (2 * (g & 1) + cc) * 16), v + 8 * cc);
+      for (int cc = 0; cc < 2; ++cc) put8<T>(dst, dst + 8192, sw64(r, (2 * part + cc) * 16), v + 8 * cc);
       if (isq) {
-        qn2_s[((h & 1) * 2 + (g & 1)) * 128 + r] = n2;
+        qn2_s[((h & 1) * 2 + part) * 128 + r] = n2;
       } else {
         const float kn = warp_max(n2);
-        if (lane == 0) atomicMax(kmax_s + 2 * h + (g & 1), __float_as_int(kn));
+        if (lane == 0) atomicMax(kmax_s + 2 * h + part, __float_as_int(kn));
       }
     };
     // V_h^T (hi, lo) into buffer h % 2: the two sequences side by side, row
     // n = 32 s + dim, column = key position in sequence s.  This thread: key
-    // r (sequence r / 64, position r % 64), dims [8g, 8g + 8).
-    auto convert_v = [&](int h, const MegaLayer& P) {
+    // r (sequence r / 64, position r % 64), dims [8 vp, 8 vp + 8).
+    auto convert_v = [&](int h, int vp) {
       float v[8];
-      tmem_ld8_nw(trow + 96 * h + 64 + 8 * g, v);
+      tmem_ld8_nw(trow + 96 * h + 64 + 8 * vp, v);
       tmem_wait_ld();
-      add_vec<8>(v, vec_s + 96 * h + 64 + 8 * g);
+      add_vec<8>(v, vec_s + 96 * h + 64 + 8 * vp);
       const int sv = r >> 6, kc = r & 63;
       unsigned char* vh = sm + kPV + (h & 1) * kTile16;
       unsigned char* vlo = vh + kTile16 / 2;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const int dim = 32 * sv + 8 * g + c;
+        const int dim = 32 * sv + 8 * vp + c;
         const int off = dim * 128 + (((kc >> 3) ^ (dim & 7)) << 4) + (kc & 7) * 2;
         T hv, lv;
         Split<T>::go(v[c], hv, lv);
@@ -860,9 +869,124 @@ __global__ void __launch_bounds__(kThreads, 1)
               k < 384 ? P.b_qkv[((k % 96) >> 5) * 128 + (k / 96) * 32 + (k & 31)]  // head-grouped order
                       : P.b_1[k - 384];
         bar_compute();
-        convert_qk(h0, P);
-        convert_v(h0, P);
+        // the first head's Q, K, V: every group (groups 0, 1 Q, groups 2, 3 K)
+        convert_qk(h0, g < 2, g & 1);
+        convert_v(h0, g);
         arrive(B_QKVH_READY);
+        if constexpr (!ASSIST) {
+          // Heads on two warp roles at once: groups 0, 1 run the softmax of
+          // head h (32 keys of the row each) while groups 2, 3 convert head
+          // h + 1's Q, K, V; one role's barrier arrivals count twice, so the
+          // barriers keep their 512-thread counts.
+          const bool smx = g < 2;
+          const int gs = g & 1;
+          constexpr int NS = L / 16;  // own 8-key chunks gs + 2 m
+          for (int h = h0; h < h1 && ok; ++h) {
+            if (!wait(B_S_DONE, c_s)) { ok = false; break; }
+            if (!smx) {
+              // S_h has read the Q, K buffers; P_{h-1} V_{h-1} (waited below
+              // from the second head on) the V buffer head h + 1 takes
+              if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+              if (h + 1 < h1) {
+                convert_qk(h + 1, true, gs);
+                convert_qk(h + 1, false, gs);
+                convert_v(h + 1, 2 * gs);
+                convert_v(h + 1, 2 * gs + 1);
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive_n(bar + B_QKVH_READY, 2);
+              }
+              continue;
+            }
+            float s[8 * NS];
+#pragma unroll
+            for (int m = 0; m < NS; ++m) tmem_ld8_nw(trow + 384 + sq * L + 8 * (gs + 2 * m), s + 8 * m);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive_n(bar + B_S_FREE, 2);
+            // P is single-buffered: P_{h-1} V_{h-1} must be done first
+            if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+            const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
+            const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
+            const bool track = neartie_err(qn, kmx, kDH) > kTieErrMin;
+            float m1 = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+            for (int m = 0; m < NS; ++m)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int kk = 8 * (gs + 2 * m) + e;
+                const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
+                s[8 * m + e] = v;
+                m2 = fmaxf(m2, fminf(m1, v));
+                m1 = fmaxf(m1, v);
+              }
+            ex[gs * 128 + r] = m1;
+            ex[(4 + gs) * 128 + r] = m2;
+            if (track) {
+              // park the raw scores in this row's P slots for a possible fp64 fix-up
+#pragma unroll
+              for (int m = 0; m < NS; ++m) {
+                uint4 hv, lv;
+                uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
+                uint32_t* lw = reinterpret_cast<uint32_t*>(&lv);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const uint32_t b0 = __float_as_uint(s[8 * m + 2 * w]), b1 = __float_as_uint(s[8 * m + 2 * w + 1]);
+                  hw[w] = (b0 >> 16) | (b1 & 0xFFFF0000u);
+                  lw[w] = (b0 & 0xFFFFu) | (b1 << 16);
+                }
+                int ho, lo;
+                p_slot(r, 8 * (gs + 2 * m), ho, lo);
+                *reinterpret_cast<uint4*>(sm + ho) = hv;
+                *reinterpret_cast<uint4*>(sm + lo) = lv;
+              }
+            }
+            bar_softmax();
+            float M1 = -INFINITY, M2 = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float a1 = ex[k * 128 + r], a2 = ex[(4 + k) * 128 + r];
+              M2 = fmaxf(fmaxf(M2, a2), fminf(M1, a1));
+              M1 = fmaxf(M1, a1);
+            }
+            const bool flag = track && row_valid &&
+                              neartie_flag((M1 - M2) * 0.69314718055994531f, qn, kmx, kDH);
+            float lt = 0.f;
+            if (!flag) {
+#pragma unroll
+              for (int m = 0; m < NS; ++m) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  s[8 * m + e] = exp2f(s[8 * m + e] - M1);  // probabilities, in place
+                  lt += s[8 * m + e];
+                }
+                int ho, lo;
+                p_slot(r, 8 * (gs + 2 * m), ho, lo);
+                if constexpr (p_hi_only<T>())
+                  *reinterpret_cast<uint4*>(sm + ho) = pack8_hi(s + 8 * m, T());
+                else
+                  put8<T>(sm + ho, sm + lo, 0, s + 8 * m);
+              }
+            }
+            if (g == 0) {
+              // fp64 correction of this warp's flagged rows (rare)
+              unsigned fl = __ballot_sync(0xffffffffu, flag);
+              while (fl) {
+                const int src = __ffs(fl) - 1;
+                fl &= fl - 1;
+                const int rr = qd * 32 + src;
+                const float kmx_src = __shfl_sync(0xffffffffu, kmx, src);
+                const float lrow = fixup_row<T, L>(sm, P, rr, rr / L, h, first, lane, kmx_src);
+                if (lane == src) lt = lrow;
+              }
+            }
+            l_s[(h * 4 + gs) * 128 + r] = lt;
+            l_s[(h * 4 + gs + 2) * 128 + r] = 0.f;  // the context sums four slots
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive_n(bar + B_P_READY, 2);
+          }
+        } else
         for (int h = h0; h < h1 && ok; ++h) {
           // ---- softmax of S = Q_h K_h^T over the row's visible keys; this
           // group holds own chunks g + 4m (keys 8 (g + 4m) .. + 8)
@@ -881,8 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // head h+1's Q, K (their buffers' reader S_h is done) and V (its
             // buffer's reader P_{h-1} V_{h-1} was just waited for), so that
             // S_{h+1} runs during this softmax
-            convert_qk(h + 1, P);
-            convert_v(h + 1, P);
+            convert_qk(h + 1, g < 2, g & 1);
+            convert_v(h + 1, g);
             arrive(B_QKVH_READY);
           }
           const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
