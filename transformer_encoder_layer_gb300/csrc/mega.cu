@@ -909,19 +909,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
             const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
             const bool track = neartie_err(qn, kmx, kDH) > kTieErrMin;
+            // the second-best score only where a near tie can matter; a
+            // row's track flag is the same in both softmax groups, so the
+            // unused second-best slots are never merged into a used result
+            const bool wtrack = __any_sync(0xffffffffu, track);
             float m1 = -INFINITY, m2 = -INFINITY;
+            if (wtrack) {
 #pragma unroll
-            for (int m = 0; m < NS; ++m)
+              for (int m = 0; m < NS; ++m)
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int kk = 8 * (gs + 2 * m) + e;
-                const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
-                s[8 * m + e] = v;
-                m2 = fmaxf(m2, fminf(m1, v));
-                m1 = fmaxf(m1, v);
-              }
+                for (int e = 0; e < 8; ++e) {
+                  const int kk = 8 * (gs + 2 * m) + e;
+                  const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
+                  s[8 * m + e] = v;
+                  m2 = fmaxf(m2, fminf(m1, v));
+                  m1 = fmaxf(m1, v);
+                }
+              ex[(4 + gs) * 128 + r] = m2;
+            } else {
+#pragma unroll
+              for (int m = 0; m < NS; ++m)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int kk = 8 * (gs + 2 * m) + e;
+                  const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
+                  s[8 * m + e] = v;
+                  m1 = fmaxf(m1, v);
+                }
+            }
             ex[gs * 128 + r] = m1;
-            ex[(4 + gs) * 128 + r] = m2;
             if (track) {
               // park the raw scores in this row's P slots for a possible fp64 fix-up
 #pragma unroll
@@ -943,11 +959,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bar_softmax();
             float M1 = -INFINITY, M2 = -INFINITY;
+            if (wtrack) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const float a1 = ex[k * 128 + r], a2 = ex[(4 + k) * 128 + r];
-              M2 = fmaxf(fmaxf(M2, a2), fminf(M1, a1));
-              M1 = fmaxf(M1, a1);
+              for (int k = 0; k < 2; ++k) {
+                const float a1 = ex[k * 128 + r], a2 = ex[(4 + k) * 128 + r];
+                M2 = fmaxf(fmaxf(M2, a2), fminf(M1, a1));
+                M1 = fmaxf(M1, a1);
+              }
+            } else {
+              M1 = fmaxf(ex[r], ex[128 + r]);
             }
             const bool flag = track && row_valid &&
                               neartie_flag((M1 - M2) * 0.69314718055994531f, qn, kmx, kDH);
