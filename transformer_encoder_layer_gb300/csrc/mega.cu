@@ -126,13 +126,13 @@ constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max pa
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
 constexpr int kBars = kVec + (384 + kMaxDff) * 4;
-constexpr int kNumBars = 40;
+constexpr int kNumBars = 41;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
 // mbarrier indices
 enum {
   B_X_FULL = 0, B_W_FULL, B_W_EMPTY = B_W_FULL + kNSlot, B_A_READY = B_W_EMPTY + kNSlot,
-  B_QKV_DONE, B_QKVH_READY,
+  B_QKV_DONE, B_QKVH_READY, B_VH_READY, B_VH_READY1,
   B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC, B_SYNC_SM,
@@ -393,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
       switch (i) {
-        case B_A_READY: case B_QKVH_READY: case B_S_FREE: case B_P_READY: case B_CTX_READY:
+        case B_A_READY: case B_QKVH_READY: case B_VH_READY: case B_VH_READY1: case B_S_FREE:
+        case B_P_READY:
+        case B_CTX_READY:
         case B_Y_READY: case B_F1_FREE: case B_F1_FREE1: case B_H_READY: case B_XA_FREE:
         case B_SYNC:
           cnt = kCompute;
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return true;
     };
-    long long c_x = 0, c_a = 0, c_qkvh = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
+    long long c_x = 0, c_a = 0, c_qkvh = 0, c_vh0 = 0, c_vh1 = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
               c_hfree[2] = {0, 0}, c_hr = 0;
     long long c_pctx = 0;  // assisted R: phases of B_PEER_CTX waited
     for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
@@ -579,7 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = issue_s(h0);
         for (int h = h0; h < h1 && ok; ++h) {
           if (h + 1 < h1 && !(ok = issue_s(h + 1))) break;
-          ok = wait(B_P_READY, c_p);
+          // P_h, and V_h^T (published after Q_h, K_h: S_h does not wait for
+          // it), on one of two barriers by head parity: a barrier serves
+          // every other head, so it is never two phases ahead of this wait
+          ok = wait(B_P_READY, c_p) &&
+               ((h & 1) ? wait(B_VH_READY1, c_vh1) : wait(B_VH_READY, c_vh0));
           if (!ok) break;
           {
             // O_h = Ph.Vh + Ph.Vl (+ Pl.Vh with bf16) over the row's own 64
@@ -873,6 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         convert_qk(h0, g < 2, g & 1);
         convert_v(h0, g);
         arrive(B_QKVH_READY);
+        arrive(B_VH_READY + (h0 & 1));
         if constexpr (!ASSIST) {
           // Heads on two warp roles at once: groups 0, 1 run the softmax of
           // head h (32 keys of the row each) while groups 2, 3 convert head
@@ -884,17 +891,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = h0; h < h1 && ok; ++h) {
             if (!wait(B_S_DONE, c_s)) { ok = false; break; }
             if (!smx) {
-              // S_h has read the Q, K buffers; P_{h-1} V_{h-1} (waited below
-              // from the second head on) the V buffer head h + 1 takes
-              if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+              // S_h has read the Q, K buffers: head h + 1's Q, K first, so
+              // that S_{h+1} can start; then its V^T, once P_{h-1} V_{h-1}
+              // (waited from the second head on) has read that V buffer.
+              // That wait also means the MMA thread has taken the previous
+              // phase of this head parity's V barrier (V_{h-1}).
               if (h + 1 < h1) {
                 convert_qk(h + 1, true, gs);
                 convert_qk(h + 1, false, gs);
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive_n(bar + B_QKVH_READY, 2);
+              }
+              if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+              if (h + 1 < h1) {
                 convert_v(h + 1, 2 * gs);
                 convert_v(h + 1, 2 * gs + 1);
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive_n(bar + B_QKVH_READY, 2);
+                mbar_arrive_n(bar + B_VH_READY + ((h + 1) & 1), 2);
               }
               continue;
             }
@@ -1028,6 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             convert_qk(h + 1, g < 2, g & 1);
             convert_v(h + 1, g);
             arrive(B_QKVH_READY);
+            arrive(B_VH_READY + ((h + 1) & 1));
           }
           const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
           const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
