@@ -212,6 +212,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x by the SFU's approximate base-2 exponential, subnormal results flushed
+// to zero (a probability below 2^-126 of the row maximum's weight is below
+// the fp32 resolution of the row sum anyway).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
 template <typename T>
 __device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int off, const float* v) {
@@ -988,12 +997,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                               neartie_flag((M1 - M2) * 0.69314718055994531f, qn, kmx, kDH);
             float lt = 0.f;
             if (!flag) {
+              const uint64_t m12 = splat2(M1);
 #pragma unroll
               for (int m = 0; m < NS; ++m) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  s[8 * m + e] = exp2f(s[8 * m + e] - M1);  // probabilities, in place
-                  lt += s[8 * m + e];
+                for (int e = 0; e < 8; e += 2) {  // probabilities, in place (paired subtraction)
+                  float a0, a1;
+                  upk2(sub2(pk2(s[8 * m + e], s[8 * m + e + 1]), m12), a0, a1);
+                  s[8 * m + e] = ex2_approx(a0);
+                  s[8 * m + e + 1] = ex2_approx(a1);
+                  lt += s[8 * m + e] + s[8 * m + e + 1];
                 }
                 int ho, lo;
                 p_slot(r, 8 * (gs + 2 * m), ho, lo);
