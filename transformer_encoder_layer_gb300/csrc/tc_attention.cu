@@ -278,9 +278,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
   uint64_t* kv_full = bars + 2;            // [kStages]
   uint64_t* kv_empty = kv_full + kStages;  // [kStages]
   uint64_t* s_full = kv_empty + kStages;   // [kSBufs]
-  uint64_t* s_empty = s_full + kSBufs;     // [kSBufs]: S/P buffer free = its P.V complete
-  uint64_t* p_full = s_empty + kSBufs;     // [2]: P written over S
-  uint64_t* p_empty = p_full + 2;          // [2]: the buffer's P.V complete (softmax side)
+  uint64_t* p_full = s_full + kSBufs;      // [2]: P written over S
+  // [2]: the buffer's P.V complete; the softmax threads wait on it (P_{j+2}
+  // may follow, O may be rescaled or read) and so does the MMA thread (the
+  // S/P buffer may take S_{j+2}): one commit serves both
+  uint64_t* p_empty = p_full + 2;
+  static_assert(kSBufs == 2, "S and P buffers pair up one to one");
   uint64_t* o_free = p_empty + 2;          // the item's O has been read
   uint64_t* mma_done = o_free + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -301,10 +304,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < kSBufs; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 1);
-    }
+    for (int s = 0; s < kSBufs; ++s) mbar_init(&s_full[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&p_full[s], 128);
       mbar_init(&p_empty[s], 1);
@@ -432,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
           mma_f16_ta_elect(tO, tph + 32 + 8 * k, dvt + 2 * k, idesc_ol, true);
       }
       mma_commit_elect(&p_empty[pb]);
-      mma_commit_elect(&s_empty[pb]);  // the S/P buffer may take S of tile it_o + 2
       mma_commit_elect(&kv_empty[st]);
       __syncwarp();
       return true;
@@ -452,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<DH>())
         const int st = (int)(it % kStages);
         if (!mbar_wait(&kv_full[st], (uint32_t)((it / kStages) & 1), abort, a.status)) { ok = false; break; }
         const int sbuf = (int)(s_it % kSBufs);
-        if (!mbar_wait(&s_empty[sbuf], (uint32_t)(((s_it / kSBufs) & 1) ^ 1), abort, a.status)) {
+        if (!mbar_wait(&p_empty[sbuf], (uint32_t)(((s_it / kSBufs) & 1) ^ 1), abort, a.status)) {
           ok = false;
           break;
         }
