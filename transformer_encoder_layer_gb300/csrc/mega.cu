@@ -537,6 +537,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
+    // FFN2's A operand: the h words of FFN buffer column buf_col, box kh
+    // (K values [64 kh, 64 kh + 64)).  The compute group g that held K
+    // columns [32 g, 32 g + 32) wrote them over its own accumulator columns,
+    // hi in the upper 16, lo (bf16) in the lower 16: k16 step k of box kh is
+    // word 8 (k % 2) of group 2 kh + k / 2.
+    auto wbox_h = [&](uint32_t d, uint32_t buf_col, int kh, uint32_t idesc, bool first,
+                      int parts) -> bool {
+      const int st = ffn_it++ % kNSlot;
+      if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
+      par ^= 1u << st;
+      tc_fence_after();
+      {
+        const uint64_t dw = sdesc_sw128(smem_u32(sm + wslot_off(st)));
+        for (int p = 0; p < parts; ++p) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16_ta_elect(d, tmem + buf_col + 32 * (2 * kh + k / 2) + 8 * (k % 2) + (p == 0 ? 16 : 0),
+                             dw + 2 * k, idesc, (first && p == 0 && k == 0) ? 0u : 1u);
+        }
+        mma_commit_elect(bar + B_W_EMPTY + st);
+      }
+      __syncwarp();
+      return true;
+    };
     auto commit = [&](int b) {
       mma_commit_elect(bar + b);
       __syncwarp();
@@ -655,8 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hb = (c - 1) & 1;
             ok = wait(B_H_READY, c_hr);
             for (int kh = 0; kh < 2 && ok; ++kh)
-              ok = wbox_ta(tmem, kTF + 128 * hb + 32 * kh, 64, id128, c == c0 + 1 && kh == 0, true,
-                           h_hi_only<T>() ? 1 : 2);
+              ok = wbox_h(tmem, kTF + 128 * hb, kh, id128, c == c0 + 1 && kh == 0, h_hi_only<T>() ? 1 : 2);
             if (!ok) break;
             commit(B_H_FREE + hb);
           }
@@ -1228,11 +1251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           float hv[32];
           tmem_ld32_nw(trow + tb + 32 * g, hv);
           tmem_wait_ld();
-          // every group has read its accumulator columns before any h words
-          // (which span other groups' columns) are written
-          tc_fence_before();
-          bar_compute();
-          tc_fence_after();
           const float4* b4 = reinterpret_cast<const float4*>(vec_s + 384 + 128 * c + 32 * g);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
@@ -1244,18 +1262,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             gelu_as7128_x2(hv[4 * c4 + 0], hv[4 * c4 + 1]);
             gelu_as7128_x2(hv[4 * c4 + 2], hv[4 * c4 + 3]);
           }
-          // group g holds the chunk's K columns [32g, 32g + 32): words [16g, +16)
+          // group g holds the chunk's K columns [32g, 32g + 32) and writes
+          // their h words over its own accumulator columns (hi in the upper
+          // 16, lo in the lower 16): no group writes another's columns, so no
+          // barrier stands between the accumulator loads and these stores
           uint32_t hw[16], lw[16];
           if constexpr (h_hi_only<T>()) {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(hw + 4 * cc) = pack8_hi(hv + 8 * cc, T());
-            tmem_st16(trow + tb + 16 * g, hw);
+            tmem_st16(trow + tb + 32 * g + 16, hw);
           } else {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
               split8(hv + 8 * cc, *reinterpret_cast<uint4*>(hw + 4 * cc), *reinterpret_cast<uint4*>(lw + 4 * cc), T());
-            tmem_st16(trow + tb + 16 * g, hw);
-            tmem_st16(trow + tb + 64 + 16 * g, lw);
+            tmem_st16(trow + tb + 32 * g + 16, hw);
+            tmem_st16(trow + tb + 32 * g, lw);
           }
           tmem_wait_st();
           arrive(B_H_READY);
