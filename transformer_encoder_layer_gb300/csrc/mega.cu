@@ -221,6 +221,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3_f32(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 // Eight 16-bit (hi, lo) values into one 16-byte chunk of each plane.
 template <typename T>
 __device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int off, const float* v) {
@@ -848,13 +855,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       add_vec<32>(v, bias + 32 * g);
-      float mean = 0.f;
+      // sums over four interleaved accumulators (shorter dependency chains)
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mean += v[c];
-      mean *= (1.f / 32.f);
-      float m2v = 0.f;
+      for (int c = 0; c < 32; ++c) s4[c & 3] += v[c];
+      const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 32.f);
+      float q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) m2v = fmaf(v[c] - mean, v[c] - mean, m2v);
+      for (int c = 0; c < 32; ++c) q4[c & 3] = fmaf(v[c] - mean, v[c] - mean, q4[c & 3]);
+      const float m2v = (q4[0] + q4[1]) + (q4[2] + q4[3]);
       ex[g * 128 + r] = mean;
       ex[(4 + g) * 128 + r] = m2v;
       bar_compute();
@@ -974,15 +983,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               ex[(4 + gs) * 128 + r] = m2;
             } else {
+              // two independent three-input max chains (the maximum is exact
+              // in any order)
+              float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
               for (int m = 0; m < NS; ++m)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                   const int kk = 8 * (gs + 2 * m) + e;
-                  const float v = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
-                  s[8 * m + e] = v;
-                  m1 = fmaxf(m1, v);
+                  s[8 * m + e] = kk < limit ? s[8 * m + e] * scale_log2 : -INFINITY;
                 }
+#pragma unroll
+              for (int m = 0; m < NS; ++m) {
+                ma = max3_f32(ma, s[8 * m], s[8 * m + 1]);
+                mb = max3_f32(mb, s[8 * m + 2], s[8 * m + 3]);
+                ma = max3_f32(ma, s[8 * m + 4], s[8 * m + 5]);
+                mb = max3_f32(mb, s[8 * m + 6], s[8 * m + 7]);
+              }
+              m1 = fmaxf(ma, mb);
             }
             ex[gs * 128 + r] = m1;
             if (track) {
@@ -1021,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float lt = 0.f;
             if (!flag) {
               const uint64_t m12 = splat2(M1);
+              float la = 0.f, lb = 0.f;  // two partial row sums
 #pragma unroll
               for (int m = 0; m < NS; ++m) {
 #pragma unroll
@@ -1029,7 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   upk2(sub2(pk2(s[8 * m + e], s[8 * m + e + 1]), m12), a0, a1);
                   s[8 * m + e] = ex2_approx(a0);
                   s[8 * m + e + 1] = ex2_approx(a1);
-                  lt += s[8 * m + e] + s[8 * m + e + 1];
+                  la += s[8 * m + e];
+                  lb += s[8 * m + e + 1];
                 }
                 int ho, lo;
                 p_slot(r, 8 * (gs + 2 * m), ho, lo);
@@ -1038,6 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                   put8<T>(sm + ho, sm + lo, 0, s + 8 * m);
               }
+              lt = la + lb;
             }
             if (g == 0) {
               // fp64 correction of this warp's flagged rows (rare)
