@@ -134,18 +134,19 @@ __device__ __forceinline__ uint64_t splat2(float a) { return pk2(a, a); }
 // GELU with a branch-free erf: Abramowitz & Stegun, Handbook of
 // Mathematical Functions (1964), formula 7.1.28 (after Hastings):
 //   erf(x) = 1 - (1 + a1 x + a2 x^2 + ... + a6 x^6)^-16,  x >= 0,  |error| <= 3e-7.
-// For u < 0 the result 0.5 u (1 + erf(u / sqrt 2)) = 0.5 u r is taken from
-// r = (...)^-16 directly, without cancellation.  In fp32 the power
-// amplifies the polynomial's rounding 16-fold, so the GELU error is at most
-// 0.5 |u| (3e-7 + 2.5e-6 r) + 2e-7 |gelu(u)| (r <= 1).  Every lane runs the same
-// instructions (one reciprocal, no exponential), which keeps long unrolled
-// epilogue loops free of divergent branches.  Two values at a time, on the
-// paired fp32 instructions: every operation is the scalar one, rounded the
-// same way.  Its agreement with the erff form is checked on the GPU over a
-// dense grid (tl_eval_gelu).
+// With r = (...)^-16 at x = |u| / sqrt 2, 0.5 u (1 + erf(u / sqrt 2)) is
+// u - 0.5 u r for u >= 0 and 0.5 u r for u < 0 (no cancellation), i.e.
+// max(u, 0) - 0.5 |u| r for either sign: one fused multiply-add, no select.
+// In fp32 the power amplifies the polynomial's rounding 16-fold, so the GELU
+// error is at most 0.5 |u| (3e-7 + 2.5e-6 r) + 2e-7 |gelu(u)| (r <= 1).  Every
+// lane runs the same instructions (one reciprocal, no exponential), which
+// keeps long unrolled epilogue loops free of divergent branches.  Two values
+// at a time, on the paired fp32 instructions: every operation is the scalar
+// one, rounded the same way.  Its agreement with the erff form is checked on
+// the GPU over a dense grid (tl_eval_gelu).
 __device__ __forceinline__ void gelu_as7128_x2(float& u0, float& u1) {
-  const uint64_t u = pk2(u0, u1);
-  const uint64_t x = mul2(pk2(fabsf(u0), fabsf(u1)), splat2(0.70710678118654752f));
+  const uint64_t au = pk2(fabsf(u0), fabsf(u1));
+  const uint64_t x = mul2(au, splat2(0.70710678118654752f));
   uint64_t t = fma2(x, splat2(0.0000430638f), splat2(0.0002765672f));
   t = fma2(x, t, splat2(0.0001520143f));
   t = fma2(x, t, splat2(0.0092705272f));
@@ -160,13 +161,8 @@ __device__ __forceinline__ void gelu_as7128_x2(float& u0, float& u1) {
   upk2(t, t0, t1);
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(t0));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(t1));
-  const uint64_t m = mul2(u, splat2(-0.5f));  // exact
-  const uint64_t r = pk2(r0, r1);
-  float a0, a1, b0, b1;
-  upk2(fma2(m, r, u), a0, a1);  // u - 0.5 u r = 0.5 u (1 + erf), u >= 0
-  upk2(mul2(m, r), b0, b1);     // -0.5 u r; its negation is 0.5 u (1 + erf), u < 0
-  u0 = u0 >= 0.f ? a0 : -b0;
-  u1 = u1 >= 0.f ? a1 : -b1;
+  const uint64_t m = mul2(au, splat2(-0.5f));  // -0.5 |u|, exact
+  upk2(fma2(m, pk2(r0, r1), pk2(fmaxf(u0, 0.f), fmaxf(u1, 0.f))), u0, u1);
 }
 
 }  // namespace tl

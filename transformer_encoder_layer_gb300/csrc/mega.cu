@@ -266,8 +266,9 @@ __device__ __forceinline__ void add_vec(float* v, const float* vec) {
   const float4* b4 = reinterpret_cast<const float4*>(vec);
 #pragma unroll
   for (int c = 0; c < N / 4; ++c) {
-    const float4 b = b4[c];
-    v[4 * c] += b.x; v[4 * c + 1] += b.y; v[4 * c + 2] += b.z; v[4 * c + 3] += b.w;
+    const float4 b = b4[c];  // paired adds, rounded as the scalar ones
+    upk2(add2(pk2(v[4 * c], v[4 * c + 1]), pk2(b.x, b.y)), v[4 * c], v[4 * c + 1]);
+    upk2(add2(pk2(v[4 * c + 2], v[4 * c + 3]), pk2(b.z, b.w)), v[4 * c + 2], v[4 * c + 3]);
   }
 }
 
@@ -855,15 +856,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       add_vec<32>(v, bias + 32 * g);
-      // sums over four interleaved accumulators (shorter dependency chains)
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      // sums over four interleaved accumulators (shorter dependency chains),
+      // two of them at a time on the paired instructions
+      uint64_t sa = 0, sb = 0;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) s4[c & 3] += v[c];
-      const float mean = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 32.f);
-      float q4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < 32; c += 4) {
+        sa = add2(sa, pk2(v[c], v[c + 1]));
+        sb = add2(sb, pk2(v[c + 2], v[c + 3]));
+      }
+      float s0, s1, s2, s3;
+      upk2(sa, s0, s1);
+      upk2(sb, s2, s3);
+      const float mean = ((s0 + s1) + (s2 + s3)) * (1.f / 32.f);
+      const uint64_t mean2 = splat2(mean);
+      uint64_t qa = 0, qb = 0;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) q4[c & 3] = fmaf(v[c] - mean, v[c] - mean, q4[c & 3]);
-      const float m2v = (q4[0] + q4[1]) + (q4[2] + q4[3]);
+      for (int c = 0; c < 32; c += 4) {
+        const uint64_t da = sub2(pk2(v[c], v[c + 1]), mean2), db = sub2(pk2(v[c + 2], v[c + 3]), mean2);
+        qa = fma2(da, da, qa);
+        qb = fma2(db, db, qb);
+      }
+      upk2(qa, s0, s1);
+      upk2(qb, s2, s3);
+      const float m2v = (s0 + s1) + (s2 + s3);
       ex[g * 128 + r] = mean;
       ex[(4 + g) * 128 + r] = m2v;
       bar_compute();
@@ -882,13 +897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rstd = rsqrtf(var + 1e-5f);
       const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * g);
       const float4* e4 = reinterpret_cast<const float4*>(bet + 32 * g);
+      const uint64_t mu2 = splat2(mu), rs2 = splat2(rstd);
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
+      for (int c4 = 0; c4 < 8; ++c4) {  // (v - mu) rstd gamma + beta, paired
         const float4 gg = g4[c4], e = e4[c4];
-        v[4 * c4 + 0] = (v[4 * c4 + 0] - mu) * rstd * gg.x + e.x;
-        v[4 * c4 + 1] = (v[4 * c4 + 1] - mu) * rstd * gg.y + e.y;
-        v[4 * c4 + 2] = (v[4 * c4 + 2] - mu) * rstd * gg.z + e.z;
-        v[4 * c4 + 3] = (v[4 * c4 + 3] - mu) * rstd * gg.w + e.w;
+        upk2(fma2(mul2(sub2(pk2(v[4 * c4], v[4 * c4 + 1]), mu2), rs2), pk2(gg.x, gg.y), pk2(e.x, e.y)),
+             v[4 * c4], v[4 * c4 + 1]);
+        upk2(fma2(mul2(sub2(pk2(v[4 * c4 + 2], v[4 * c4 + 3]), mu2), rs2), pk2(gg.z, gg.w), pk2(e.z, e.w)),
+             v[4 * c4 + 2], v[4 * c4 + 3]);
       }
     };
     for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
@@ -1275,11 +1291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4* b4 = reinterpret_cast<const float4*>(vec_s + 384 + 128 * c + 32 * g);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 b = b4[c4];
-            hv[4 * c4 + 0] += b.x;
-            hv[4 * c4 + 1] += b.y;
-            hv[4 * c4 + 2] += b.z;
-            hv[4 * c4 + 3] += b.w;
+            const float4 b = b4[c4];  // + b_1 on the paired adds
+            upk2(add2(pk2(hv[4 * c4 + 0], hv[4 * c4 + 1]), pk2(b.x, b.y)), hv[4 * c4 + 0], hv[4 * c4 + 1]);
+            upk2(add2(pk2(hv[4 * c4 + 2], hv[4 * c4 + 3]), pk2(b.z, b.w)), hv[4 * c4 + 2], hv[4 * c4 + 3]);
             gelu_as7128_x2(hv[4 * c4 + 0], hv[4 * c4 + 1]);
             gelu_as7128_x2(hv[4 * c4 + 2], hv[4 * c4 + 3]);
           }
