@@ -236,28 +236,30 @@ __device__ __forceinline__ void put8(unsigned char* hi, unsigned char* lo, int o
   *reinterpret_cast<uint4*>(hi + off) = hv;
   *reinterpret_cast<uint4*>(lo + off) = lv;
 }
+// c + a for a 16-bit value a: one mixed-precision add (sm_100 and later),
+// a widened exactly, one rounding -- no separate conversion instruction.
+template <typename T> __device__ __forceinline__ float addw(float c, unsigned short a);
+template <> __device__ __forceinline__ float addw<__half>(float c, unsigned short a) {
+  float d;
+  asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(c));
+  return d;
+}
+template <> __device__ __forceinline__ float addw<__nv_bfloat16>(float c, unsigned short a) {
+  float d;
+  asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(c));
+  return d;
+}
+// v[0..8) += the eight 16-bit values of a 16-byte chunk (element 2e in the
+// low half of word e); with the lo plane added after the hi plane, a (hi, lo)
+// residual costs two adds per element.
 template <typename T>
-__device__ __forceinline__ void get8(const unsigned char* hi, const unsigned char* lo, int off,
-                                     bool use_lo, float* v) {
-  uint4 hv = *reinterpret_cast<const uint4*>(hi + off);
-  const T* hp = reinterpret_cast<const T*>(&hv);
-  if (use_lo) {
-    uint4 lv = *reinterpret_cast<const uint4*>(lo + off);
-    const T* lp = reinterpret_cast<const T*>(&lv);
+__device__ __forceinline__ void add8w(float* v, uint4 c) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]) + to_f32<T>(lp[e]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = to_f32<T>(hp[e]);
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = addw<T>(v[2 * e], (unsigned short)(w[e] & 0xFFFFu));
+    v[2 * e + 1] = addw<T>(v[2 * e + 1], (unsigned short)(w[e] >> 16));
   }
-}
-// The two 16-bit values packed in a 32-bit word (element 2e in the low half).
-template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
-template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
-template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
 }
 // v[0..N) += vec[0..N), N a multiple of 4, vec 16-byte aligned (shared or
 // global memory).
@@ -832,19 +834,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 a2 = unpack2<T>(hw[e]), b2 = unpack2<T>(lw[e]);
-          v[2 * e] += a2.x + b2.x;
-          v[2 * e + 1] += a2.y + b2.y;
+          v[2 * e] = addw<T>(addw<T>(v[2 * e], (unsigned short)(hw[e] & 0xFFFFu)), (unsigned short)(lw[e] & 0xFFFFu));
+          v[2 * e + 1] = addw<T>(addw<T>(v[2 * e + 1], (unsigned short)(hw[e] >> 16)), (unsigned short)(lw[e] >> 16));
         }
       } else {
         tmem_wait_ld();
         const int kh = g >> 1;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          float x8[8];
-          get8<T>(xa + kh * kTile16, xa + (2 + kh) * kTile16, sw128(r, (g & 1) * 4 + cc), resid_lo, x8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[cc * 8 + e] += x8[e];
+          const int off = sw128(r, (g & 1) * 4 + cc);
+          const uint4 hv = *reinterpret_cast<const uint4*>(xa + kh * kTile16 + off);
+          const uint4 lv = resid_lo ? *reinterpret_cast<const uint4*>(xa + (2 + kh) * kTile16 + off) : make_uint4(0, 0, 0, 0);
+          add8w<T>(v + 8 * cc, hv);
+          add8w<T>(v + 8 * cc, lv);
         }
       }
       if (part) {  // the helper's FFN2 partial sum: fp32 [128 rows][128 columns]
