@@ -126,14 +126,14 @@ constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max pa
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
 constexpr int kBars = kVec + (384 + kMaxDff) * 4;
-constexpr int kNumBars = 41;
+constexpr int kNumBars = 43;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
 // mbarrier indices
 enum {
   B_X_FULL = 0, B_W_FULL, B_W_EMPTY = B_W_FULL + kNSlot, B_A_READY = B_W_EMPTY + kNSlot,
   B_QKV_DONE, B_QKVH_READY, B_VH_READY, B_VH_READY1,
-  B_S_DONE, B_S_FREE, B_P_READY, B_O_DONE, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
+  B_S_DONE, B_S_FREE, B_P_READY, B_P_READY1, B_O_DONE, B_O_DONE1, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC, B_SYNC_SM,
   // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster);
@@ -281,11 +281,25 @@ __host__ __device__ constexpr bool p_hi_only() { return std::is_same<T, __half>:
 template <typename T>
 __host__ __device__ constexpr bool h_hi_only() { return std::is_same<T, __half>::value; }
 
-// The (hi, lo) slots of P for row rr and key kk of the row's own sequence.
-__device__ __forceinline__ void p_slot(int rr, int kk, int& hi_off, int& lo_off) {
+// P buffers: with fp16 I/O P has no lo part, so head h's P goes to buffer
+// h % 2 (the two 16 KB planes of the P area) and the softmax of head h + 1
+// does not wait for P_h V_h; bf16 keeps one (hi, lo) buffer.
+template <typename T>
+__host__ __device__ constexpr int p_bufs() { return p_hi_only<T>() ? 2 : 1; }
+// The (hi, lo) slots of P for row rr and key kk of the row's own sequence,
+// in P buffer b.  With two buffers the lo slots (only the fp64 fix-up's
+// parked score bits use them) are in the V spare area, free until the
+// out-projection.
+template <typename T>
+__device__ __forceinline__ void p_slot(int rr, int kk, int b, int& hi_off, int& lo_off) {
   const int off = sw128(rr, kk >> 3) + (kk & 7) * 2;
-  hi_off = kPB + off;
-  lo_off = kPB + kTile16 + off;
+  if constexpr (p_bufs<T>() == 2) {
+    hi_off = kPB + b * kTile16 + off;
+    lo_off = kVB + off;
+  } else {
+    hi_off = kPB + off;
+    lo_off = kPB + kTile16 + off;
+  }
 }
 
 // fp64 correction of one flagged (row rr, head h), done by a whole warp.
@@ -299,6 +313,7 @@ __device__ __forceinline__ void p_slot(int rr, int kk, int& hi_off, int& lo_off)
 template <typename T, int L>
 __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, int rr, int sq, int h,
                                         bool first, int lane, float kmx) {
+  const int pbuf = h & 1;
   constexpr int NK = L / 32;  // keys per lane
   const unsigned char* xa = sm + kXA;
   auto xval = [&](int row, int col) -> double {
@@ -312,7 +327,7 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
 #pragma unroll
   for (int m = 0; m < NK; ++m) {
     int ho, lo;
-    p_slot(rr, lane + 32 * m, ho, lo);
+    p_slot<T>(rr, lane + 32 * m, pbuf, ho, lo);
     const uint32_t bits = ((uint32_t)*reinterpret_cast<const uint16_t*>(sm + ho) << 16) |
                           (uint32_t)*reinterpret_cast<const uint16_t*>(sm + lo);
     sc[m] = __uint_as_float(bits) * 0.69314718055994531f;
@@ -368,7 +383,7 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
     T hv, lv;
     Split<T>::go((float)e, hv, lv);
     int ho, lo;
-    p_slot(rr, lane + 32 * m, ho, lo);
+    p_slot<T>(rr, lane + 32 * m, pbuf, ho, lo);
     *reinterpret_cast<T*>(sm + ho) = hv;
     *reinterpret_cast<T*>(sm + lo) = lv;
   }
@@ -413,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       switch (i) {
         case B_A_READY: case B_QKVH_READY: case B_VH_READY: case B_VH_READY1: case B_S_FREE:
-        case B_P_READY:
+        case B_P_READY: case B_P_READY1:
         case B_CTX_READY:
         case B_Y_READY: case B_F1_FREE: case B_F1_FREE1: case B_H_READY: case B_XA_FREE:
         case B_SYNC:
@@ -582,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return true;
     };
-    long long c_x = 0, c_a = 0, c_qkvh = 0, c_vh0 = 0, c_vh1 = 0, c_sfree = 0, c_p = 0, c_ctx = 0, c_y = 0,
+    long long c_x = 0, c_a = 0, c_qkvh = 0, c_vh0 = 0, c_vh1 = 0, c_sfree = 0, c_p0 = 0, c_p1 = 0, c_ctx = 0, c_y = 0,
               c_hfree[2] = {0, 0}, c_hr = 0;
     long long c_pctx = 0;  // assisted R: phases of B_PEER_CTX waited
     for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
@@ -627,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P_h, and V_h^T (published after Q_h, K_h: S_h does not wait for
           // it), on one of two barriers by head parity: a barrier serves
           // every other head, so it is never two phases ahead of this wait
-          ok = wait(B_P_READY, c_p) &&
+          ok = ((h & 1) ? wait(B_P_READY1, c_p1) : wait(B_P_READY, c_p0)) &&
                ((h & 1) ? wait(B_VH_READY1, c_vh1) : wait(B_VH_READY, c_vh0));
           if (!ok) break;
           {
@@ -635,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // keys (4 steps): B holds both sequences' V side by side (N = 64),
             // so row r's result is in columns [96h + 32 s, +32) of its sequence s.
             const uint32_t vbuf = pv + (uint32_t)((h & 1) * kTile16);
-            const uint32_t as[3] = {pb, pb, pb + kTile16};
+            const uint32_t pbh = pb + (uint32_t)((p_bufs<T>() == 2 ? h & 1 : 0) * kTile16);
+            const uint32_t as[3] = {pbh, pbh, pb + kTile16};
             const uint32_t bs[3] = {vbuf, vbuf + kTile16 / 2, vbuf};
             constexpr int kProducts = p_hi_only<T>() ? 2 : 3;
 #pragma unroll
@@ -645,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c]) + 2 * k, sdesc_sw128(bs[c]) + 2 * k,
                               id64, (c | k) != 0);
           }
-          commit(B_O_DONE);
+          commit(B_O_DONE + (h & 1));
         }
         if (!ok) break;
         if (helper) {
@@ -725,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* pbuf = sm + kPB;
     const float scale_log2 = rsqrtf((float)kDH) * 1.4426950408889634f;
     constexpr int NM = L / 32;  // own 8-key chunks of a row per group
-    int c_qkv = 0, c_s = 0, c_o = 0, c_out = 0, c_f1[2] = {0, 0}, c_f2 = 0,
+    int c_qkv = 0, c_s = 0, c_o0 = 0, c_o1 = 0, c_out = 0, c_f1[2] = {0, 0}, c_f2 = 0,
         c_sync = 0, c_sync_sm = 0;  // completed phases per barrier (parity = count & 1)
     // assisted mode: phases of the barriers the other CTA arrives on
     int c_pbfree = 0, c_py = 0, c_px = 0, c_xfree = 0, c_part = 0;
@@ -754,6 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n;
       if (!mbar_wait(bar + b, par, abort, status)) return false;
       tc_fence_after();
+      return true;
+    };
+    // O_h = P_h V_h done, on one of two barriers by head parity.  Every
+    // compute thread waits each head's phase once per layer, in head order
+    // (o_next: the first head not yet waited), and nothing completes a
+    // head's phase before every thread has waited the previous phase of
+    // that barrier (two heads earlier), so no wait sees two phases ahead.
+    int o_next = 0;
+    auto wait_o_upto = [&](int hl) -> bool {
+      for (; o_next <= hl; ++o_next)
+        if (!((o_next & 1) ? wait(B_O_DONE1, c_o1) : wait(B_O_DONE, c_o0))) return false;
       return true;
     };
     auto arrive = [&](int b) {
@@ -922,6 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int l = 0; l < a.n_layers && ok; ++l) {
         const MegaLayer& P = a.layers[l];
         const bool first = l == 0;
+        o_next = h0;
         if (!wait(B_QKV_DONE, c_qkv)) { ok = false; break; }
         // Every reader of the previous layer's maxima finished before the
         // QKV product could start.
@@ -962,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive_n(bar + B_QKVH_READY, 2);
               }
-              if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+              if (!wait_o_upto(h - 1)) { ok = false; break; }
               if (h + 1 < h1) {
                 convert_v(h + 1, 2 * gs);
                 convert_v(h + 1, 2 * gs + 1);
@@ -975,13 +1003,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             float s[8 * NS];
 #pragma unroll
             for (int m = 0; m < NS; ++m) tmem_ld8_nw(trow + 384 + sq * L + 8 * (gs + 2 * m), s + 8 * m);
+            // the row's |q| and the tile's max |k| of head h, read before S_FREE:
+            // the conversion of head h + 2 (which needs S_{h+1}, so S_FREE)
+            // reuses these |q|^2 slots
+            const float qn2a = qn2_s[((h & 1) * 2) * 128 + r], qn2b = qn2_s[((h & 1) * 2 + 1) * 128 + r];
+            const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive_n(bar + B_S_FREE, 2);
-            // P is single-buffered: P_{h-1} V_{h-1} must be done first
-            if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
-            const float qn = sqrtf(qn2_s[((h & 1) * 2) * 128 + r] + qn2_s[((h & 1) * 2 + 1) * 128 + r]);
-            const float kmx = sqrtf(__int_as_float(kmax_s[2 * h]) + __int_as_float(kmax_s[2 * h + 1]));
+            // every softmax thread is done with head h - 1 (its exchange
+            // slots and parked scores are reused); P_h's buffer was last read
+            // by P_{h - p_bufs} V
+            if (p_bufs<T>() == 2 && h > h0) bar_softmax();
+            if (!wait_o_upto(h - p_bufs<T>())) { ok = false; break; }
+            const float qn = sqrtf(qn2a + qn2b);
             const bool track = neartie_err(qn, kmx, kDH) > kTieErrMin;
             // the second-best score only where a near tie can matter; a
             // row's track flag is the same in both softmax groups, so the
@@ -1035,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   lw[w] = (b0 & 0xFFFFu) | (b1 << 16);
                 }
                 int ho, lo;
-                p_slot(r, 8 * (gs + 2 * m), ho, lo);
+                p_slot<T>(r, 8 * (gs + 2 * m), h & 1, ho, lo);
                 *reinterpret_cast<uint4*>(sm + ho) = hv;
                 *reinterpret_cast<uint4*>(sm + lo) = lv;
               }
@@ -1070,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   lb += s[8 * m + e + 1];
                 }
                 int ho, lo;
-                p_slot(r, 8 * (gs + 2 * m), ho, lo);
+                p_slot<T>(r, 8 * (gs + 2 * m), h & 1, ho, lo);
                 if constexpr (p_hi_only<T>())
                   *reinterpret_cast<uint4*>(sm + ho) = pack8_hi(s + 8 * m, T());
                 else
@@ -1094,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_s[(h * 4 + gs + 2) * 128 + r] = 0.f;  // the context sums four slots
             fence_proxy_async();
             tc_fence_before();
-            mbar_arrive_n(bar + B_P_READY, 2);
+            mbar_arrive_n(bar + B_P_READY + (h & 1), 2);
           }
         } else
         for (int h = h0; h < h1 && ok; ++h) {
@@ -1107,10 +1142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar + B_S_FREE);
-          // P is single-buffered: P_{h-1} V_{h-1} must be done before this head
-          // writes P (it is, since S_h completed after it; this also keeps the
-          // O_DONE barrier at most one phase ahead of this thread's waits)
-          if (h > h0 && !wait(B_O_DONE, c_o)) { ok = false; break; }
+          // P_{h-1} V_{h-1} done before this head writes P or its exchange
+          // slots (this loop keeps the one-buffer order for either type)
+          if (!wait_o_upto(h - 1)) { ok = false; break; }
           if (h + 1 < h1) {
             // head h+1's Q, K (their buffers' reader S_h is done) and V (its
             // buffer's reader P_{h-1} V_{h-1} was just waited for), so that
@@ -1151,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lw[w] = (b0 & 0xFFFFu) | (b1 << 16);
               }
               int ho, lo;
-              p_slot(r, 8 * (g + 4 * m), ho, lo);
+              p_slot<T>(r, 8 * (g + 4 * m), h & 1, ho, lo);
               *reinterpret_cast<uint4*>(sm + ho) = hv;
               *reinterpret_cast<uint4*>(sm + lo) = lv;
             }
@@ -1176,7 +1210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lt += s[8 * m + e];
               }
               int ho, lo;
-              p_slot(r, 8 * (g + 4 * m), ho, lo);
+              p_slot<T>(r, 8 * (g + 4 * m), h & 1, ho, lo);
               if constexpr (p_hi_only<T>())
                 *reinterpret_cast<uint4*>(sm + ho) = pack8_hi(s + 8 * m, T());
               else
@@ -1196,12 +1230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           l_s[(h * 4 + g) * 128 + r] = lt;
-          arrive(B_P_READY);
+          arrive(B_P_READY + (h & 1));
         }
         if (!ok) break;
         // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
         // sequence s are in TMEM columns 96g + 32s
-        if (!wait(B_O_DONE, c_o)) { ok = false; break; }
+        if (!wait_o_upto(h1 - 1)) { ok = false; break; }
         // assisted R: its P and V buffers are free, H may send its context
         if (ASSIST && !helper && elected) signal_peer(B_PEER_PBFREE);
         if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
