@@ -24,7 +24,7 @@
 //
 // Per layer (TMEM columns in brackets):
 //   QKV   acc[0, 384) = X . W_qkv^T      X = (hi, lo) of the layer input
-//   per head h: Q_h, K_h, V_h^T -> shared memory as (hi, lo);
+//   per head h: Q_h, K_h, V_h -> shared memory as (hi, lo);
 //         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
 //         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32).
 //         Head h+1's Q, K, V are written as soon as S_h has been read, so
@@ -110,8 +110,8 @@ constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/
 constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16-bit
 constexpr int kXA = 0;                                // [part][khalf] x 16 KB = 64 KB
 constexpr int kPB = kXA + 4 * kTile16;                // attention: P [part] 128 x 64 (own keys), then
-                                                      // V^T [buffer][part] 64 x 64; afterwards ctx [part][khalf]
-constexpr int kPV = kPB + 2 * kTile16;                // the two V^T buffers, 16 KB each (hi, lo 8 KB)
+                                                      // V [buffer][part] 64 x 64; afterwards ctx [part][khalf]
+constexpr int kPV = kPB + 2 * kTile16;                // the two V buffers, 16 KB each (hi, lo 8 KB)
 constexpr int kQB = kPB + 4 * kTile16;                // [part] 128 x 32, 8 KB each
 constexpr int kKB = kQB + 2 * 8192;                   // [part] 128 x 32
 constexpr int kVB = kKB + 2 * 8192;                   // spare during attention; a weight slot in the FFN
@@ -166,6 +166,20 @@ __device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
   d |= (uint64_t)(512 >> 4) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)4 << 61;
+  return d;
+}
+
+// Matrix descriptor of an MN-major operand in the 128-byte swizzle: each
+// 128-byte row holds 64 16-bit elements along MN (one swizzle atom wide) for
+// one K index, and 8-row K groups are 1024 bytes apart (stride byte offset).
+// The leading byte offset (between atoms along MN) is never used by an
+// operand 64 elements wide; it is set to the same 1024.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 
@@ -510,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par = 0;            // per-slot phase parity
     const uint32_t id128 = idesc_f16(128, 128, kBf);
     const uint32_t id64 = idesc_f16(128, 64, kBf);
+    const uint32_t id64_bmn = id64 | (1u << 16);  // B MN-major (bit 16)
     const uint32_t id32 = idesc_f16(128, 32, kBf);
     bool ok = true;
     const uint32_t xa = smem_u32(sm + kXA), pb = smem_u32(sm + kPB);
@@ -639,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = issue_s(h0);
         for (int h = h0; h < h1 && ok; ++h) {
           if (h + 1 < h1 && !(ok = issue_s(h + 1))) break;
-          // P_h, and V_h^T (published after Q_h, K_h: S_h does not wait for
+          // P_h, and V_h (published after Q_h, K_h: S_h does not wait for
           // it), on one of two barriers by head parity: a barrier serves
           // every other head, so it is never two phases ahead of this wait
           ok = ((h & 1) ? wait(B_P_READY1, c_p1) : wait(B_P_READY, c_p0)) &&
@@ -649,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_h = Ph.Vh + Ph.Vl (+ Pl.Vh with bf16) over the row's own 64
             // keys (4 steps): B holds both sequences' V side by side (N = 64),
             // so row r's result is in columns [96h + 32 s, +32) of its sequence s.
+            // B is MN-major: a 16-key step is 16 rows of 128 bytes further.
             const uint32_t vbuf = pv + (uint32_t)((h & 1) * kTile16);
             const uint32_t pbh = pb + (uint32_t)((p_bufs<T>() == 2 ? h & 1 : 0) * kTile16);
             const uint32_t as[3] = {pbh, pbh, pb + kTile16};
@@ -658,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kProducts; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c]) + 2 * k, sdesc_sw128(bs[c]) + 2 * k,
-                              id64, (c | k) != 0);
+                mma_f16_elect(tmem + 96 * h, sdesc_sw128(as[c]) + 2 * k, sdesc_mn_sw128(bs[c]) + 128 * k,
+                              id64_bmn, (c | k) != 0);
           }
           commit(B_O_DONE + (h & 1));
         }
@@ -825,26 +841,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) atomicMax(kmax_s + 2 * h + part, __float_as_int(kn));
       }
     };
-    // V_h^T (hi, lo) into buffer h % 2: the two sequences side by side, row
-    // n = 32 s + dim, column = key position in sequence s.  This thread: key
-    // r (sequence r / 64, position r % 64), dims [8 vp, 8 vp + 8).
+    // V_h (hi, lo) into buffer h % 2, the B operand of P V read MN-major:
+    // row = key position k, its 64 columns [V_s0[k] | V_s1[k]] (the two
+    // sequences side by side).  This thread: key r (sequence r / 64,
+    // position r % 64), dims [8 vp, 8 vp + 8) -- one 16-byte chunk per plane.
     auto convert_v = [&](int h, int vp) {
       float v[8];
       tmem_ld8_nw(trow + 96 * h + 64 + 8 * vp, v);
       tmem_wait_ld();
       add_vec<8>(v, vec_s + 96 * h + 64 + 8 * vp);
-      const int sv = r >> 6, kc = r & 63;
       unsigned char* vh = sm + kPV + (h & 1) * kTile16;
-      unsigned char* vlo = vh + kTile16 / 2;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int dim = 32 * sv + 8 * vp + c;
-        const int off = dim * 128 + (((kc >> 3) ^ (dim & 7)) << 4) + (kc & 7) * 2;
-        T hv, lv;
-        Split<T>::go(v[c], hv, lv);
-        *reinterpret_cast<T*>(vh + off) = hv;
-        *reinterpret_cast<T*>(vlo + off) = lv;
-      }
+      put8<T>(vh, vh + kTile16 / 2, sw128(r & 63, 4 * (r >> 6) + vp), v);
     };
     // LayerNorm of acc (TMEM columns tcol + [32g, +32)) + bias + residual
     // (the X buffer): per-group (mean, M2) over 32 columns, merged through
@@ -979,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait(B_S_DONE, c_s)) { ok = false; break; }
             if (!smx) {
               // S_h has read the Q, K buffers: head h + 1's Q, K first, so
-              // that S_{h+1} can start; then its V^T, once P_{h-1} V_{h-1}
+              // that S_{h+1} can start; then its V, once P_{h-1} V_{h-1}
               // (waited from the second head on) has read that V buffer.
               // That wait also means the MMA thread has taken the previous
               // phase of this head parity's V barrier (V_{h-1}).
