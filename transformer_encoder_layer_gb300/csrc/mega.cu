@@ -943,6 +943,30 @@ __global__ void __launch_bounds__(kThreads, 1)
              v[4 * c4 + 2], v[4 * c4 + 3]);
       }
     };
+    // A layer's b_qkv (head-grouped order) and b_1 in shared memory, with the
+    // per-head |k| maxima reset: layer 0's here, every next layer's (the next
+    // tile's layer 0 after the last) at the previous layer's FFN2 completion,
+    // from values loaded into registers after its last GELU.  Every reader of
+    // the old values is done by then, and the barrier of LayerNorm 2 (or of
+    // the helper's partial sum) publishes the new ones before the next QKV
+    // product completes.
+    // this thread's entries: cv, cv + 512 (cv = threadIdx.x - 128, recomputed
+    // where used rather than held in a register)
+#define TL_CV ((int)threadIdx.x - kCtrlWarps * 32)
+    auto vec_val = [&](const MegaLayer& Q, int k) -> float {
+      if (k >= 384 + a.dff) return 0.f;
+      return k < 384 ? __ldg(Q.b_qkv + ((k % 96) >> 5) * 128 + (k / 96) * 32 + (k & 31))
+                     : __ldg(Q.b_1 + (k - 384));
+    };
+    auto stage_vec = [&](float v0, float v1) {
+      float* vs = reinterpret_cast<float*>(sm + kVec);
+      if (TL_CV < 384 + a.dff) vs[TL_CV] = v0;
+      if (TL_CV + kCompute < 384 + a.dff) vs[TL_CV + kCompute] = v1;
+      if (threadIdx.x == kCtrlWarps * 32)
+        for (int k = 0; k < 2 * kH; ++k) kmax_s[k] = 0;
+    };
+    stage_vec(vec_val(a.layers[0], TL_CV), vec_val(a.layers[0], TL_CV + kCompute));
+    bar_compute();
     for (int t = TL_T0; t < n_tiles && ok; t += TL_TSTEP) {
       const int seq = t * S + sq;
       const bool row_valid = seq < a.B;
@@ -958,17 +982,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool first = l == 0;
         o_next = h0;
         if (!wait(B_QKV_DONE, c_qkv)) { ok = false; break; }
-        // Every reader of the previous layer's maxima finished before the
-        // QKV product could start.
-        if (threadIdx.x == kCtrlWarps * 32) {
-          for (int k = 0; k < 2 * kH; ++k) kmax_s[k] = 0;
-        }
-        // Stage this layer's b_qkv and b_1 (the previous layer's readers are done).
-        for (int k = threadIdx.x - kCtrlWarps * 32; k < 384 + a.dff; k += kCompute)
-          reinterpret_cast<float*>(sm + kVec)[k] =
-              k < 384 ? P.b_qkv[((k % 96) >> 5) * 128 + (k / 96) * 32 + (k & 31)]  // head-grouped order
-                      : P.b_1[k - 384];
-        bar_compute();
         // the first head's Q, K, V: every group (groups 0, 1 Q, groups 2, 3 K)
         convert_qk(h0, g < 2, g & 1);
         convert_v(h0, g);
@@ -1360,11 +1373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           arrive(B_H_READY);
         }
         if (!ok) break;
+        // the next layer's vectors, staged once FFN2 is done
+        const MegaLayer& Pn = a.layers[l + 1 < a.n_layers ? l + 1 : 0];
+        const float nv0 = vec_val(Pn, TL_CV), nv1 = vec_val(Pn, TL_CV + kCompute);
         // assisted H: every FFN1 product of its chunks is done, so y in its X
         // buffer is no longer read; R may write the next layer's input there
         if (helper && elected) signal_peer(B_PEER_XFREE);
         // ---- FFN2 + b_2 + residual y, LayerNorm 2
         if (!wait(B_F2_DONE, c_f2)) { ok = false; break; }
+        stage_vec(nv0, nv1);
         if (helper) {
           // the partial FFN2 sum over this CTA's chunks -> R's P/ctx area
           // (fp32 [row][128 columns]); R adds it before LayerNorm 2
