@@ -739,7 +739,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(bar + B_MMA_DONE, 0, status);
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
+    // the assisted kernel's compute code needs the 104; the plain kernel's
+    // fits 96 without spills and runs faster compiled to that budget
+    if constexpr (ASSIST) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
     // ======================================================== compute warps
     const int cw = warp - kCtrlWarps;      // 0..15
     const int g = cw >> 2;                 // column group
