@@ -14,7 +14,8 @@
 //   control  warp 0  TMA: the input tile (once per tile) and weight boxes
 //                    from L2 into a 2-deep ring, in the order the MMAs use them
 //            warp 1  TMEM (all 512 columns); one thread issues every MMA
-//            warps 2, 3 idle (they lend their registers: setmaxnreg)
+//            warps 2, 3 idle (they lend their registers: setmaxnreg, in the
+//                    assisted kernel)
 //   compute  16 warps in four column groups g = 0..3 of four warps; the four
 //            warps of a group cover the 128 rows (TMEM lane quarters), and
 //            group g takes columns [32g, 32g + 32) of a 128-wide row, head
@@ -407,9 +408,11 @@ __device__ __noinline__ float fixup_row(unsigned char* sm, const MegaLayer& P, i
 }
 
 // Registers: 96 per thread at launch (an SM sub-partition holds five warps
-// of 16384 / 5 / 32 registers); setmaxnreg then moves them from the control
-// warpgroup (64 each) to the compute warps (104 each): 128 x 64 + 512 x 104
-// = 61440 = 640 x 96, and per sub-partition 32 x (64 + 4 x 104) <= 16384.
+// of 16384 / 5 / 32 registers).  The control warpgroup drops to 64; in the
+// assisted kernel setmaxnreg gives those to the compute warps (104 each):
+// 128 x 64 + 512 x 104 = 61440 = 640 x 96, and per sub-partition
+// 32 x (64 + 4 x 104) <= 16384.  The plain kernel's compute code fits 96
+// without spills and is faster compiled to that budget.
 template <typename T, int L, bool ASSIST>
 __global__ void __launch_bounds__(kThreads, 1)
     mega_kernel(const __grid_constant__ CUtensorMap map_x, const MegaArgs a) {
