@@ -19,19 +19,23 @@
 //   compute  16 warps in four column groups g = 0..3 of four warps; the four
 //            warps of a group cover the 128 rows (TMEM lane quarters), and
 //            group g takes columns [32g, 32g + 32) of a 128-wide row, head
-//            g for the context, 32 of a 128-wide FFN chunk, and every 4th
-//            8-key chunk of the attention scores.  Four warps per SM
-//            sub-partition hide the latency of the CUDA-core phases.
+//            g for the context, 32 of a 128-wide FFN chunk, and a share of
+//            each row's 8-key chunks of the attention scores.  Four warps
+//            per SM sub-partition hide the latency of the CUDA-core phases.
 //
 // Per layer (TMEM columns in brackets):
 //   QKV   acc[0, 384) = X . W_qkv^T      X = (hi, lo) of the layer input
 //   per head h: Q_h, K_h, V_h -> shared memory as (hi, lo);
 //         S = Q_h K_h^T [384, 512); softmax with the causal + key-padding +
-//         own-sequence mask -> P (hi, lo); O_h = P V_h into [32h, 32h + 32).
+//         own-sequence mask -> P; O_h = P V_h into [96h, 96h + 64) (row r's
+//         result in [96h + 32 s, +32) for its sequence s).
 //         Head h+1's Q, K, V are written as soon as S_h has been read, so
 //         S_{h+1} runs during the softmax of head h (P V issued after it).
-//         The row maximum (and the second best score) is merged across the
-//         four groups through shared memory.
+//         Plain kernel: groups 0, 1 run the softmax (every 2nd 8-key chunk)
+//         while groups 2, 3 convert head h+1; assisted kernel: all four
+//         groups do both in turn (every 4th chunk).  The row maximum (and
+//         the second best score) is merged across the softmax groups
+//         through shared memory.
 //   ctx = O / l -> shared memory (hi, lo)
 //   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> TMEM
 //         [128, 256) as (hi, lo) 16-bit pairs, the A operand of FFN1 read
