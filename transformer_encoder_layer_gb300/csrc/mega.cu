@@ -485,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int reg_it = 0, ffn_it = 0;
       uint32_t par = 0, used = 0, out_par = 0;  // per-slot phase parity, slots ever loaded
       bool ok = true;
-      auto wload = [&](const CUtensorMap* m, int x, int y, uint32_t bytes, bool ffn) -> bool {
-        const int idx = ffn ? ffn_it++ : reg_it++;
-        const int st = ffn ? idx % kNSlot : idx % kNW;
-        if (ffn && idx == kNW) {
+      auto wload = [&](const CUtensorMap* m, int x, int y, uint32_t bytes, bool ffn, int slot = -1) -> bool {
+        const int idx = slot >= 0 ? 0 : ffn ? ffn_it++ : reg_it++;
+        const int st = slot >= 0 ? slot : ffn ? idx % kNSlot : idx % kNW;
+        if (slot < 0 && ffn && idx == kNW) {
           // the layer's first borrowed slot: its attention must be over
           if (!mbar_wait(bar + B_OUT_DONE, out_par, abort, status)) return false;
           out_par ^= 1;
@@ -507,10 +507,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sm + kXA + kTile16, &map_x, bar + B_X_FULL, 64, t * 128);
         for (int l = 0; l < a.n_layers && ok; ++l) {
           const MegaLayer& P = a.layers[l];
-          for (int nb = nb0; nb < nb1 && ok; ++nb)
-            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16, false);
-          if (!helper)
-            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
+          if constexpr (!ASSIST) {
+            // QKV: N blocks 0, 1 of K half 0 into slots 0, 1 and of K half 1
+            // into slots 2, 3 (adjacent pairs: two N = 256 operands), N block
+            // 2 into slots 4 and 0; the out-projection into slots 1, 0.  The
+            // borrowed slots 2-4 are free from the previous FFN's products to
+            // the end of this QKV product (the conversions write there after).
+            ok = wload(P.map_qkv, 0, 0, kTile16, false, 0) && wload(P.map_qkv, 0, 128, kTile16, false, 1) &&
+                 wload(P.map_qkv, 64, 0, kTile16, false, 2) && wload(P.map_qkv, 64, 128, kTile16, false, 3) &&
+                 wload(P.map_qkv, 0, 256, kTile16, false, 4) && wload(P.map_qkv, 64, 256, kTile16, false, 0);
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false, kh == 0 ? 1 : 0);
+          } else {
+            for (int nb = nb0; nb < nb1 && ok; ++nb)
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_qkv, 64 * kh, 128 * nb, kTile16, false);
+            if (!helper)
+              for (int kh = 0; kh < 2 && ok; ++kh) ok = wload(P.map_o, 64 * kh, 0, kTile16, false);
+          }
           ffn_it = 0;  // at least three FFN boxes per layer: slot 2 is used, OUT_DONE waited once
           for (int c = c0; c <= c1 && ok; ++c) {
             if (c < c1)  // W_1 rows [128c, 128c + 128): two 128 x 64 boxes
@@ -529,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ MMA
     int reg_it = 0, ffn_it = 0;  // the same slot sequence as the TMA thread
     uint32_t par = 0;            // per-slot phase parity
+    const uint32_t id256 = idesc_f16(128, 256, kBf);
     const uint32_t id128 = idesc_f16(128, 128, kBf);
     const uint32_t id64 = idesc_f16(128, 64, kBf);
     const uint32_t id64_bmn = id64 | (1u << 16);  // B MN-major (bit 16)
@@ -540,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A is a 128 x 64 tile at a_base; its lo plane is part_stride further on
     // (part_stride 0: the hi plane only).
     auto wbox = [&](uint32_t d, uint32_t a_base, uint32_t part_stride, uint32_t idesc, bool first,
-                    bool ffn) -> bool {
-      const int st = ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
+                    bool ffn, int slot = -1) -> bool {
+      const int st = slot >= 0 ? slot : ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
       if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
       par ^= 1u << st;
       tc_fence_after();
@@ -566,8 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The same with A in tensor memory: columns a_col + 8 k (k16 step k) of
     // the hi part, part_cols further on for the lo part.
     auto wbox_ta = [&](uint32_t d, uint32_t a_col, uint32_t part_cols, uint32_t idesc, bool first,
-                       bool ffn, int parts = 2) -> bool {
-      const int st = ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
+                       bool ffn, int parts = 2, int slot = -1) -> bool {
+      const int st = slot >= 0 ? slot : ffn ? ffn_it++ % kNSlot : reg_it++ % kNW;
       if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
       par ^= 1u << st;
       tc_fence_after();
@@ -608,6 +621,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
+    // QKV N blocks 0 and 1 of K half kh against A (layer 0: the input's hi
+    // plane in the X buffer; later layers: the (hi, lo) input in TMEM) into
+    // columns [0, 256): one N = 256 product per k16 step, its B operand the
+    // adjacent slots s0, s0 + 1 (rows 0-127, 128-255).
+    auto wpair = [&](bool from_x, int kh, int s0) -> bool {
+      const int s1 = s0 + 1;
+      if (!mbar_wait(bar + B_W_FULL + s0, (par >> s0) & 1, abort, status)) return false;
+      par ^= 1u << s0;
+      if (!mbar_wait(bar + B_W_FULL + s1, (par >> s1) & 1, abort, status)) return false;
+      par ^= 1u << s1;
+      tc_fence_after();
+      const uint64_t dw = sdesc_sw128(smem_u32(sm + wslot_off(s0)));
+      if (from_x) {
+        const uint64_t da = sdesc_sw128(xa + kh * kTile16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16_elect(tmem, da + ((k * 32) >> 4), dw + 2 * k, id256, (kh == 0 && k == 0) ? 0u : 1u);
+      } else {
+        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16_ta_elect(tmem, tmem + kTX + 32 * kh + p * 64 + 8 * k, dw + 2 * k, id256,
+                             (kh == 0 && p == 0 && k == 0) ? 0u : 1u);
+        }
+      }
+      mma_commit_elect(bar + B_W_EMPTY + s0);
+      mma_commit_elect(bar + B_W_EMPTY + s1);
+      __syncwarp();
+      return true;
+    };
     auto commit = [&](int b) {
       mma_commit_elect(bar + b);
       __syncwarp();
@@ -629,11 +672,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // layer 0: x from shared memory (exact in its hi plane); later layers:
         // the (hi, lo) input LayerNorm 2 also left in TMEM [384, 512) (the
         // helper has it in its X buffer, written by R)
-        for (int nb = nb0; nb < nb1 && ok; ++nb)
+        if constexpr (!ASSIST) {
+          // the loader's slots: N blocks 0, 1 as one N = 256 product per K
+          // half (slots 0-1, 2-3), then N block 2 (slots 4, 0)
+          ok = wpair(l == 0, 0, 0) && wpair(l == 0, 1, 2);
           for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = l == 0 ? wbox(tmem + 128 * nb, xa + kh * kTile16, 0u, id128, kh == 0, false)
-                 : helper ? wbox(tmem + 128 * nb, xa + kh * kTile16, 2u * kTile16, id128, kh == 0, false)
-                          : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
+            ok = l == 0 ? wbox(tmem + 256, xa + kh * kTile16, 0u, id128, kh == 0, false, kh == 0 ? 4 : 0)
+                        : wbox_ta(tmem + 256, kTX + 32 * kh, 64, id128, kh == 0, false, 2, kh == 0 ? 4 : 0);
+        } else {
+          for (int nb = nb0; nb < nb1 && ok; ++nb)
+            for (int kh = 0; kh < 2 && ok; ++kh)
+              ok = l == 0 ? wbox(tmem + 128 * nb, xa + kh * kTile16, 0u, id128, kh == 0, false)
+                   : helper ? wbox(tmem + 128 * nb, xa + kh * kTile16, 2u * kTile16, id128, kh == 0, false)
+                            : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
+        }
         if (!ok) break;
         commit(B_QKV_DONE);
         // ---- attention: S_0, then per head h: S_{h+1} as soon as head h+1's
@@ -703,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
+            ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false,
+                      ASSIST ? -1 : (kh == 0 ? 1 : 0));
           if (!ok) break;
           commit(B_OUT_DONE);
         }
