@@ -108,6 +108,11 @@ constexpr int kD = 128, kDH = 32, kH = 4;
 constexpr int kTY = 128;   // TMEM columns of y (hi [128, 192), lo [192, 256))
 constexpr int kTF = 256;   // TMEM FFN buffers b = 0, 1 at 256 + 128 b: FFN1 accumulator, then h (hi, lo)
 constexpr int kTX = 384;   // TMEM columns of the next layer's input (hi [384, 448), lo [448, 512))
+// plain kernel: the context of head h as (hi, lo) words in TMEM over its O
+// columns: dims [16j, 16j + 16) have their hi words at 96h + 16j + [0, 8)
+// and their lo words at 96h + 16j + [8, 16); the out-projection reads A
+// there and accumulates into [384, 512) (the score columns, free by then)
+constexpr int kTOut = 384;
 constexpr int kNW = 2;     // regular weight ring slots
 constexpr int kNSlot = 5;  // during the FFN: three more, borrowed from the Q/K/V buffers
 
@@ -651,6 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
+    // Plain kernel: one out-projection box (K half kh: heads 2 kh, 2 kh + 1)
+    // against the context words in TMEM (hi part, then lo part) into d.
+    auto wbox_o = [&](uint32_t d, int kh, int st) -> bool {
+      if (!mbar_wait(bar + B_W_FULL + st, (par >> st) & 1, abort, status)) return false;
+      par ^= 1u << st;
+      tc_fence_after();
+      const uint64_t dw = sdesc_sw128(smem_u32(sm + wslot_off(st)));
+      for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16_ta_elect(d, tmem + 96 * (2 * kh + k / 2) + 16 * (k % 2) + 8 * p, dw + 2 * k, id128,
+                           (kh == 0 && p == 0 && k == 0) ? 0u : 1u);
+      }
+      mma_commit_elect(bar + B_W_EMPTY + st);
+      __syncwarp();
+      return true;
+    };
     auto commit = [&](int b) {
       mma_commit_elect(bar + b);
       __syncwarp();
@@ -754,9 +776,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++c_pctx;
             tc_fence_after();
           }
-          for (int kh = 0; kh < 2 && ok; ++kh)
-            ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false,
-                      ASSIST ? -1 : (kh == 0 ? 1 : 0));
+          if constexpr (!ASSIST) {
+            for (int kh = 0; kh < 2 && ok; ++kh) ok = wbox_o(tmem + kTOut, kh, kh == 0 ? 1 : 0);
+          } else {
+            for (int kh = 0; kh < 2 && ok; ++kh)
+              ok = wbox(tmem + 128, pb + kh * kTile16, 2u * kTile16, id128, kh == 0, false);
+          }
           if (!ok) break;
           commit(B_OUT_DONE);
         }
@@ -914,6 +939,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       add_vec<8>(v, vec_s + 96 * h + 64 + 8 * vp);
       unsigned char* vh = sm + kPV + (h & 1) * kTile16;
       put8<T>(vh, vh + kTile16 / 2, sw128(r & 63, 4 * (r >> 6) + vp), v);
+    };
+    // Plain kernel: the context of head hh for this thread's row, dims
+    // [16j, 16j + 16): O / l as (hi, lo) words over TMEM columns 96 hh + 16j
+    // + [0, 16), which hold this row's own O values for sequence 0 and
+    // unused ones for sequence 1 -- no other thread reads or writes them.
+    // The stores are waited for before CTX_READY.
+    auto ctx_tmem = [&](int hh, int j) {
+      float o[16];
+      tmem_ld16_nw(trow + 96 * hh + 32 * sq + 16 * j, o);
+      const float lsum = l_s[(hh * 4) * 128 + r] + l_s[(hh * 4 + 1) * 128 + r] +
+                         l_s[(hh * 4 + 2) * 128 + r] + l_s[(hh * 4 + 3) * 128 + r];
+      tmem_wait_ld();
+      const float inv = 1.f / lsum;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) o[c] *= inv;
+      uint32_t w[16];
+      split8(o, *reinterpret_cast<uint4*>(w), *reinterpret_cast<uint4*>(w + 8), T());
+      split8(o + 8, *reinterpret_cast<uint4*>(w + 4), *reinterpret_cast<uint4*>(w + 12), T());
+      tmem_st16(trow + 96 * hh + 16 * j, w);
     };
     // LayerNorm of acc (TMEM columns tcol + [32g, +32)) + bias + residual
     // (the X buffer): per-group (mean, M2) over 32 columns, merged through
@@ -1080,6 +1124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive_n(bar + B_VH_READY + ((h + 1) & 1), 2);
               }
+              // the context of head h - 1, whose P V was just waited for
+              if (h > h0) ctx_tmem(h - 1, gs);
               continue;
             }
             float s[8 * NS];
@@ -1320,7 +1366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_o_upto(h1 - 1)) { ok = false; break; }
         // assisted R: its P and V buffers are free, H may send its context
         if (ASSIST && !helper && elected) signal_peer(B_PEER_PBFREE);
-        if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
+        if constexpr (!ASSIST) {
+          // the last head's context (the conversion warps wrote the others
+          // during the heads); every context store lands before CTX_READY
+          if (g >= 2) ctx_tmem(h1 - 1, g & 1);
+          tmem_wait_st();
+        } else if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
           float o[32];
           tmem_ld32_nw(trow + 96 * g + 32 * sq, o);
           tmem_wait_ld();
@@ -1371,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ct < 256) l_s[ct + 512] = lv1;
           bar_compute();
           float y[32];
-          layernorm(128, l_s, l_s + 128, l_s + 256, !first, false, y);
+          layernorm(ASSIST ? 128 : kTOut, l_s, l_s + 128, l_s + 256, !first, false, y);
           // y -> TMEM [128, 256) as (hi, lo) words: group g holds K columns
           // [32g, 32g + 32).  Every group read its out-projection accumulator
           // (the same columns) before the LayerNorm's exchange barrier.
