@@ -136,13 +136,13 @@ constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max pa
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
 constexpr int kBars = kVec + (384 + kMaxDff) * 4;
-constexpr int kNumBars = 43;
+constexpr int kNumBars = 44;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
 // mbarrier indices
 enum {
   B_X_FULL = 0, B_W_FULL, B_W_EMPTY = B_W_FULL + kNSlot, B_A_READY = B_W_EMPTY + kNSlot,
-  B_QKV_DONE, B_QKVH_READY, B_VH_READY, B_VH_READY1,
+  B_QKV_DONE, B_QKV_DONE2, B_QKVH_READY, B_VH_READY, B_VH_READY1,
   B_S_DONE, B_S_FREE, B_P_READY, B_P_READY1, B_O_DONE, B_O_DONE1, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
   B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC, B_SYNC_SM,
@@ -697,19 +697,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!ASSIST) {
           // the loader's slots: N blocks 0, 1 as one N = 256 product per K
           // half (slots 0-1, 2-3), then N block 2 (slots 4, 0)
+          // columns [0, 256) (heads 0, 1 and head 2's q, k) are released
+          // first, so the first head's conversion overlaps N block 2
           ok = wpair(l == 0, 0, 0) && wpair(l == 0, 1, 2);
+          if (!ok) break;
+          commit(B_QKV_DONE);
           for (int kh = 0; kh < 2 && ok; ++kh)
             ok = l == 0 ? wbox(tmem + 256, xa + kh * kTile16, 0u, id128, kh == 0, false, kh == 0 ? 4 : 0)
                         : wbox_ta(tmem + 256, kTX + 32 * kh, 64, id128, kh == 0, false, 2, kh == 0 ? 4 : 0);
+          if (!ok) break;
+          commit(B_QKV_DONE2);
         } else {
           for (int nb = nb0; nb < nb1 && ok; ++nb)
             for (int kh = 0; kh < 2 && ok; ++kh)
               ok = l == 0 ? wbox(tmem + 128 * nb, xa + kh * kTile16, 0u, id128, kh == 0, false)
                    : helper ? wbox(tmem + 128 * nb, xa + kh * kTile16, 2u * kTile16, id128, kh == 0, false)
                             : wbox_ta(tmem + 128 * nb, kTX + 32 * kh, 64, id128, kh == 0, false);
+          if (!ok) break;
+          commit(B_QKV_DONE);
         }
-        if (!ok) break;
-        commit(B_QKV_DONE);
         // ---- attention: S_0, then per head h: S_{h+1} as soon as head h+1's
         // Q, K, V are in shared memory, then P_h V_h, so the next scores are
         // computed while the compute warps run the softmax of head h.
@@ -1117,6 +1123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_n(bar + B_QKVH_READY, 2);
               }
               if (!wait_o_upto(h - 1)) { ok = false; break; }
+              // head 2's V is the first conversion from QKV columns [256, 384),
+              // completed once a layer like QKV_DONE (so the same parity)
+              if (h + 1 == 2) {
+                if (!mbar_wait(bar + B_QKV_DONE2, (uint32_t)((c_qkv - 1) & 1), abort, status)) { ok = false; break; }
+                tc_fence_after();
+              }
               if (h + 1 < h1) {
                 convert_v(h + 1, 2 * gs);
                 convert_v(h + 1, 2 * gs + 1);
