@@ -36,10 +36,12 @@
 //         groups do both in turn (every 4th chunk).  The row maximum (and
 //         the second best score) is merged across the softmax groups
 //         through shared memory.
-//   ctx = O / l -> shared memory (hi, lo)
-//   out   acc[128, 256) = ctx . W_o^T;  y = LN1(acc + b_o + x) -> TMEM
-//         [128, 256) as (hi, lo) 16-bit pairs, the A operand of FFN1 read
-//         straight from tensor memory
+//   ctx = O / l as (hi, lo): plain kernel, TMEM words over each head's O
+//         columns (written by the conversion warps as soon as that head's
+//         P V is done); assisted kernel, shared memory
+//   out   acc[384, 512) (assisted: [128, 256)) = ctx . W_o^T;
+//         y = LN1(acc + b_o + x) -> TMEM [128, 256) as (hi, lo) 16-bit
+//         pairs, the A operand of FFN1 read straight from tensor memory
 //   FFN   per 128-wide chunk c of d_ff: acc1[256 + 128 (c % 2), +128) =
 //         y . W_1c^T; h_c = gelu(acc1 + b_1c) replaces acc1 in the same TMEM
 //         columns as (hi, lo) words; acc2[0, 128) += h_c . W_2c^T (A from
