@@ -138,7 +138,7 @@ constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max pa
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
 constexpr int kBars = kVec + (384 + kMaxDff) * 4;
-constexpr int kNumBars = 44;
+constexpr int kNumBars = 42;
 constexpr int kSmemBytes = kBars + kNumBars * 8 + 16;
 
 // mbarrier indices
@@ -146,7 +146,7 @@ enum {
   B_X_FULL = 0, B_W_FULL, B_W_EMPTY = B_W_FULL + kNSlot, B_A_READY = B_W_EMPTY + kNSlot,
   B_QKV_DONE, B_QKV_DONE2, B_QKVH_READY, B_VH_READY, B_VH_READY1,
   B_S_DONE, B_S_FREE, B_P_READY, B_P_READY1, B_O_DONE, B_O_DONE1, B_CTX_READY, B_OUT_DONE, B_Y_READY, B_F1_DONE,
-  B_F1_DONE1, B_F1_FREE, B_F1_FREE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
+  B_F1_DONE1, B_H_READY, B_H_FREE, B_H_FREE1, B_F2_DONE, B_XA_FREE,
   B_MMA_DONE, B_SYNC, B_SYNC_SM,
   // assisted mode (a resident CTA R and a helper CTA H per tile, one cluster);
   // data hand-overs are bulk copies completing on the receiver's barrier
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         case B_A_READY: case B_QKVH_READY: case B_VH_READY: case B_VH_READY1: case B_S_FREE:
         case B_P_READY: case B_P_READY1:
         case B_CTX_READY:
-        case B_Y_READY: case B_F1_FREE: case B_F1_FREE1: case B_H_READY: case B_XA_FREE:
+        case B_Y_READY: case B_H_READY: case B_XA_FREE:
         case B_SYNC:
           cnt = kCompute;
           break;
