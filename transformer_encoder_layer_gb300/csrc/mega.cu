@@ -846,6 +846,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* qn2_s = reinterpret_cast<float*>(sm + kQn2);
     float* ex = reinterpret_cast<float*>(sm + kEx);
     float* l_s = reinterpret_cast<float*>(sm + kLs);
+    // the layer's LayerNorm vectors: the P area (plain kernel), the softmax
+    // sums' area (assisted kernel, whose P area holds the context)
+#define TL_LNV (ASSIST ? l_s : reinterpret_cast<float*>(sm + kPB))
     int* kmax_s = reinterpret_cast<int*>(sm + kKmax);
     const float* vec_s = reinterpret_cast<const float*>(sm + kVec);  // b_qkv, then b_1 at 384
     unsigned char* xa = sm + kXA;
@@ -1377,12 +1380,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // ---- ctx = O / l -> PB (hi, lo); group g takes head g, whose rows of
         // sequence s are in TMEM columns 96g + 32s
+        // The layer's six LayerNorm vectors (b_o, ln1 gamma, beta, b_2, ln2
+        // gamma, beta; 768 floats).  Plain kernel: loaded now, while the last
+        // P V completes, and stored into the P area (unused from then on in
+        // this layer) before CTX_READY, which with OUT_DONE orders them before
+        // every LayerNorm read.  Assisted kernel: see below.
+        const int ct = threadIdx.x - kCtrlWarps * 32;
+        auto ln_vec = [&](int k) -> float {
+          const int v6 = k >> 7, e = k & 127;
+          const float* src = v6 == 0 ? P.b_o : v6 == 1 ? P.ln1_g : v6 == 2 ? P.ln1_b
+                           : v6 == 3 ? P.b_2 : v6 == 4 ? P.ln2_g : P.ln2_b;
+          return __ldg(src + e);
+        };
+        float lv0 = 0.f, lv1 = 0.f;
+        if constexpr (!ASSIST) {
+          lv0 = ln_vec(ct);
+          lv1 = ct < 256 ? ln_vec(ct + 512) : 0.f;
+        }
         if (!wait_o_upto(h1 - 1)) { ok = false; break; }
         // assisted R: its P and V buffers are free, H may send its context
         if (ASSIST && !helper && elected) signal_peer(B_PEER_PBFREE);
         if constexpr (!ASSIST) {
           // the last head's context (the conversion warps wrote the others
           // during the heads); every context store lands before CTX_READY
+          TL_LNV[ct] = lv0;
+          if (ct < 256) TL_LNV[ct + 512] = lv1;
           if (g >= 2) ctx_tmem(h1 - 1, g & 1);
           tmem_wait_st();
         } else if (g >= h0 && g < h1) {  // this group's head is one of this CTA's
@@ -1417,26 +1439,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!wait_peer(B_PEER_Y, c_py)) { ok = false; break; }
         } else {
-          // The layer's six LayerNorm vectors (b_o, ln1 gamma, beta, b_2, ln2
-          // gamma, beta; 768 floats) go to the softmax-sum area, free once
+          // Assisted kernel: the vectors go to the softmax-sum area, free once
           // every thread has read its sums (CTX_READY precedes OUT_DONE): the
           // global loads are issued now and land during the out-projection.
-          const int ct = threadIdx.x - kCtrlWarps * 32;
-          auto ln_vec = [&](int k) -> float {
-            const int v6 = k >> 7, e = k & 127;
-            const float* src = v6 == 0 ? P.b_o : v6 == 1 ? P.ln1_g : v6 == 2 ? P.ln1_b
-                             : v6 == 3 ? P.b_2 : v6 == 4 ? P.ln2_g : P.ln2_b;
-            return __ldg(src + e);
-          };
-          const float lv0 = ln_vec(ct), lv1 = ct < 256 ? ln_vec(ct + 512) : 0.f;
+          if constexpr (ASSIST) {
+            lv0 = ln_vec(ct);
+            lv1 = ct < 256 ? ln_vec(ct + 512) : 0.f;
+          }
           arrive(B_CTX_READY);
           // ---- out-projection + b_o + residual x, LayerNorm 1 -> y in XA
           if (!wait(B_OUT_DONE, c_out)) { ok = false; break; }
-          l_s[ct] = lv0;
-          if (ct < 256) l_s[ct + 512] = lv1;
-          bar_compute();
+          if constexpr (ASSIST) {
+            l_s[ct] = lv0;
+            if (ct < 256) l_s[ct + 512] = lv1;
+            bar_compute();
+          }
           float y[32];
-          layernorm(ASSIST ? 128 : kTOut, l_s, l_s + 128, l_s + 256, !first, false, y);
+          layernorm(ASSIST ? 128 : kTOut, TL_LNV, TL_LNV + 128, TL_LNV + 256, !first, false, y);
           // y -> TMEM [128, 256) as (hi, lo) words: group g holds K columns
           // [32g, 32g + 32).  Every group read its out-projection accumulator
           // (the same columns) before the LayerNorm's exchange barrier.
@@ -1538,7 +1557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_peer(B_PEER_PART, c_part)) { ok = false; break; }
           }
           float xo[32];
-          layernorm(0, l_s + 384, l_s + 512, l_s + 640, true, true, xo,
+          layernorm(0, TL_LNV + 384, TL_LNV + 512, TL_LNV + 640, true, true, xo,
                     ASSIST ? reinterpret_cast<const float*>(pbuf) : nullptr);
           const int kh = g >> 1;
           // assisted: H's FFN1 no longer reads y -- so the copy of y out of
@@ -1589,6 +1608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 #undef TL_T0
 #undef TL_TSTEP
+#undef TL_LNV
 }
 
 template <typename T, int L, bool ASSIST>
