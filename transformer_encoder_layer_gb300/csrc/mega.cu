@@ -123,6 +123,7 @@ constexpr int kTile16 = 128 * 64 * 2;                 // 16 KB: 128 rows x 64 16
 constexpr int kXA = 0;                                // [part][khalf] x 16 KB = 64 KB
 constexpr int kPB = kXA + 4 * kTile16;                // attention: P [part] 128 x 64 (own keys), then
                                                       // V [buffer][part] 64 x 64; afterwards ctx [part][khalf]
+                                                      // (assisted) or the LayerNorm vectors (plain)
 constexpr int kPV = kPB + 2 * kTile16;                // the two V buffers, 16 KB each (hi, lo 8 KB)
 constexpr int kQB = kPB + 4 * kTile16;                // [part] 128 x 32, 8 KB each
 constexpr int kKB = kQB + 2 * 8192;                   // [part] 128 x 32
@@ -133,7 +134,8 @@ constexpr int kMisc = kWR + kNW * kTile16;
 constexpr int kQn2 = kMisc;                           // [2 head parity][2 group][128] partial |q_r|^2
 constexpr int kEx = kQn2 + 2 * 2 * 128 * 4;           // [2][4 group][128] exchange: (m1, m2) or (mean, M2)
 constexpr int kLs = kEx + 2 * 4 * 128 * 4;            // [4 head][4 group][128] partial softmax sums;
-                                                      // from the out-projection on: b_o, ln1 g, b, b_2, ln2 g, b
+                                                      // assisted kernel, from the out-projection on: b_o,
+                                                      // ln1 g, b, b_2, ln2 g, b (plain kernel: in the P area)
 constexpr int kKmax = kLs + 4 * 4 * 128 * 4;          // [4 head][2] int: max partial |k|^2 (float bits)
 constexpr int kMaxDff = 512;
 constexpr int kVec = kKmax + 64;                      // the layer's b_qkv [384] then b_1 [d_ff]
